@@ -1,0 +1,221 @@
+"""Python binding of libqx, the GB300 block-quantised GEMV library.
+
+Argument marshalling only: every function here checks Python-side types,
+allocates outputs with torch when the caller passes none, and calls the C ABI
+of ``include/qx.h`` with raw device pointers and the current CUDA stream.  All
+arithmetic runs in the CUDA kernels.  There is no fallback: if ``libqx.so`` is
+missing or the device is not a GB300, calls raise ``QxError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+QX_Q8_0, QX_Q4_K, QX_Q6_K = 8, 12, 14
+QX_MODE_F32, QX_MODE_W4A8 = 0, 1
+QX_OK = 0
+QX_ERR_ARG, QX_ERR_FMT, QX_ERR_SHAPE, QX_ERR_ALIGN = -1, -2, -3, -4
+QX_ERR_MODE, QX_ERR_CUDA, QX_ERR_DEVICE_TIMEOUT, QX_ERR_UNSUPPORTED_DEVICE = -5, -6, -7, -8
+QX_MAX_MULTI = 8
+QX_MAX_COLS = 32768
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libqx.so")
+
+EXPORTS = ["qx_quantize_act_q8", "qx_gemv", "qx_gemv_multi", "qx_gemm_prefill", "qx_gemm_prefill_ex",
+           "qx_gemv_partials", "qx_row_bytes", "qx_device_check", "qx_debug_timeout_probe",
+           "qx_status_string", "qx_version"]
+
+
+class QxError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {qx_status_string(status)} ({status})")
+
+
+class _Act(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("d", ctypes.c_void_p), ("sum", ctypes.c_void_p),
+                ("m", ctypes.c_int64), ("cols", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libqx.so (built by ``build()``); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libqx.so not found at {LIB_PATH}: build it with "
+                               "`python -m block_quantized_gemv_q8_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.qx_quantize_act_q8.argtypes = [P, I64, I64, ctypes.POINTER(_Act), P]
+        L.qx_gemv.argtypes = [I, P, I64, I64, P, P, I, P]
+        L.qx_gemv_multi.argtypes = [I, P, P, P, I64, P, P, I, P]
+        L.qx_gemm_prefill.argtypes = [I, P, I64, I64, ctypes.POINTER(_Act), P, P]
+        L.qx_gemm_prefill_ex.argtypes = [I, P, I64, I64, ctypes.POINTER(_Act), P, I, P]
+        L.qx_gemv_partials.argtypes = [I, P, I64, I64, ctypes.POINTER(_Act), P, P]
+        L.qx_row_bytes.argtypes = [I, I64]
+        L.qx_row_bytes.restype = ctypes.c_size_t
+        L.qx_device_check.argtypes = [P]
+        L.qx_debug_timeout_probe.argtypes = [ctypes.c_uint64, P]
+        L.qx_status_string.argtypes = [I]
+        L.qx_status_string.restype = ctypes.c_char_p
+        L.qx_version.argtypes = []
+        L.qx_version.restype = ctypes.c_char_p
+        for n in ("qx_quantize_act_q8", "qx_gemv", "qx_gemv_multi", "qx_gemm_prefill", "qx_gemm_prefill_ex",
+                  "qx_gemv_partials", "qx_device_check", "qx_debug_timeout_probe"):
+            getattr(L, n).restype = I
+        _lib = L
+    return _lib
+
+
+def build_library(force: bool = False) -> str:
+    """Compile libqx.so in-tree (nvcc, sm_103a)."""
+    import importlib
+    return importlib.import_module(__name__ + ".build").build(force=force)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t: torch.Tensor) -> ctypes.c_void_p:
+    if not t.is_cuda:
+        raise ValueError("qx operates on CUDA tensors only")
+    if not t.is_contiguous():
+        raise ValueError("qx needs contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check(st: int, what: str):
+    if st != QX_OK:
+        raise QxError(st, what)
+
+
+@dataclass
+class ActQ8:
+    """An int8-quantised activation: q [m, cols] int8, d and sum [m, cols/32]."""
+    q: torch.Tensor
+    d: torch.Tensor
+    sum: torch.Tensor
+
+    @property
+    def m(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def cols(self) -> int:
+        return self.q.shape[1]
+
+    @staticmethod
+    def empty(m: int, cols: int, device=None) -> "ActQ8":
+        device = device or torch.device("cuda")
+        return ActQ8(torch.empty((m, cols), dtype=torch.int8, device=device),
+                     torch.empty((m, cols // 32), dtype=torch.float32, device=device),
+                     torch.empty((m, cols // 32), dtype=torch.int32, device=device))
+
+    def c_struct(self) -> _Act:
+        return _Act(_ptr(self.q).value, _ptr(self.d).value, _ptr(self.sum).value, self.m, self.cols)
+
+    def row(self, i: int) -> "ActQ8":
+        return ActQ8(self.q[i:i + 1], self.d[i:i + 1], self.sum[i:i + 1])
+
+
+def qx_row_bytes(fmt: int, cols: int) -> int:
+    return int(lib().qx_row_bytes(fmt, cols))
+
+
+def qx_status_string(st: int) -> str:
+    return lib().qx_status_string(st).decode()
+
+
+def qx_version() -> str:
+    return lib().qx_version().decode()
+
+
+def qx_quantize_act_q8(x: torch.Tensor, out: ActQ8 | None = None, stream=None) -> ActQ8:
+    """x f32 [m, cols] (or [cols]) -> ActQ8 (int8 per block of 32 with an f32 absmax scale)."""
+    if x.dtype != torch.float32:
+        raise TypeError("qx_quantize_act_q8 takes float32 activations")
+    x2 = x.reshape(1, -1) if x.dim() == 1 else x
+    m, cols = x2.shape
+    out = out or ActQ8.empty(m, cols, x.device)
+    a = out.c_struct()
+    _check(lib().qx_quantize_act_q8(_ptr(x2), m, cols, ctypes.byref(a), _stream(stream)), "qx_quantize_act_q8")
+    return out
+
+
+def _x_arg(x, mode):
+    if mode == QX_MODE_F32:
+        if not isinstance(x, torch.Tensor) or x.dtype != torch.float32:
+            raise TypeError("f32 mode takes a float32 activation tensor")
+        return _ptr(x), None
+    if not isinstance(x, ActQ8):
+        raise TypeError("W4A8 mode takes an ActQ8 (from qx_quantize_act_q8)")
+    a = x.c_struct()
+    return ctypes.cast(ctypes.pointer(a), ctypes.c_void_p), a
+
+
+def qx_gemv(fmt: int, W: torch.Tensor, rows: int, cols: int, x, y: torch.Tensor | None = None,
+            mode: int = QX_MODE_W4A8, stream=None) -> torch.Tensor:
+    """y[rows] = W . x for block-quantised W (uint8 bytes) in f32 or W4A8 mode."""
+    y = y if y is not None else torch.empty(rows, dtype=torch.float32, device=W.device)
+    xp, keep = _x_arg(x, mode)
+    _check(lib().qx_gemv(fmt, _ptr(W), rows, cols, xp, _ptr(y), mode, _stream(stream)), "qx_gemv")
+    return y
+
+
+def qx_gemv_multi(fmts, Ws, rows, cols: int, x, ys=None, mode: int = QX_MODE_W4A8, stream=None):
+    """Several GEMVs over one activation in one launch per format."""
+    n = len(Ws)
+    ys = ys if ys is not None else [torch.empty(r, dtype=torch.float32, device=Ws[0].device) for r in rows]
+    F = (ctypes.c_int * n)(*fmts)
+    Wp = (ctypes.c_void_p * n)(*[_ptr(w).value for w in Ws])
+    R = (ctypes.c_int64 * n)(*rows)
+    Yp = (ctypes.c_void_p * n)(*[_ptr(t).value for t in ys])
+    xp, keep = _x_arg(x, mode)
+    _check(lib().qx_gemv_multi(n, F, Wp, R, cols, xp, Yp, mode, _stream(stream)), "qx_gemv_multi")
+    return ys
+
+
+def qx_gemv_partials(fmt: int, W: torch.Tensor, rows: int, cols: int, x: ActQ8, P: torch.Tensor | None = None,
+                     stream=None) -> torch.Tensor:
+    """Exact int32 partial sums [rows, cols/32] (Q4_K, Q8_0) or [rows, cols/16] (Q6_K)."""
+    g = 16 if fmt == QX_Q6_K else 32
+    P = P if P is not None else torch.empty((rows, cols // g), dtype=torch.int32, device=W.device)
+    a = x.c_struct()
+    _check(lib().qx_gemv_partials(fmt, _ptr(W), rows, cols, ctypes.byref(a), _ptr(P), _stream(stream)),
+           "qx_gemv_partials")
+    return P
+
+
+def qx_gemm_prefill(fmt: int, W: torch.Tensor, rows: int, cols: int, X: ActQ8, Y: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """Y [X.m, rows] = X' . W^T for a quantised activation batch X."""
+    return qx_gemm_prefill_ex(fmt, W, rows, cols, X, Y, 0, stream)
+
+
+def qx_gemm_prefill_ex(fmt: int, W: torch.Tensor, rows: int, cols: int, X: ActQ8, Y: torch.Tensor | None = None,
+                       path: int = 0, stream=None) -> torch.Tensor:
+    Y = Y if Y is not None else torch.empty((X.m, rows), dtype=torch.float32, device=W.device)
+    a = X.c_struct()
+    _check(lib().qx_gemm_prefill_ex(fmt, _ptr(W), rows, cols, ctypes.byref(a), _ptr(Y), path, _stream(stream)),
+           "qx_gemm_prefill_ex")
+    return Y
+
+
+def qx_device_check(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    return int(lib().qx_device_check(_stream(stream)))
+
+
+def qx_debug_timeout_probe(limit_ns: int, stream=None):
+    _check(lib().qx_debug_timeout_probe(limit_ns, _stream(stream)), "qx_debug_timeout_probe")

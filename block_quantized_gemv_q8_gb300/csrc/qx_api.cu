@@ -1,0 +1,353 @@
+// qx_api.cu -- the C ABI declared in include/qx.h: argument validation,
+// per-device set-up and launch geometry.  All arithmetic of the method runs
+// in the kernels (qx_actq8.cu, qx_gemv.cu, qx_prefill.cu).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/qx.h"
+#include "qx_internal.h"
+
+namespace qx {
+
+// Device error word: kernels OR a code in when a bounded wait runs out.
+__device__ unsigned g_err_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s bound on every pipeline wait
+constexpr size_t kStageTargetBytes = 24 * 1024;
+constexpr int kMaxStageRows = 256;
+
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int sm_count = 0;
+    unsigned* err_word = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// Query the current device once: capability, SM count, error word address.
+qx_status device_info(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QX_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return QX_ERR_CUDA;
+        d.supported = (major == 10 && minor == 3);
+        if (d.supported) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return QX_ERR_CUDA;
+            d.err_word = static_cast<unsigned*>(p);
+        }
+        d.ready = true;
+    }
+    if (!d.supported) return QX_ERR_UNSUPPORTED_DEVICE;
+    *out = &d;
+    return QX_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// Outputs are written one 32-bit element at a time.
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int block_weights(int fmt) {
+    switch (fmt) {
+        case QX_Q8_0: return 32;
+        case QX_Q4_K: return 256;
+        case QX_Q6_K: return 256;
+        default: return 0;
+    }
+}
+
+int block_bytes(int fmt) {
+    switch (fmt) {
+        case QX_Q8_0: return 34;
+        case QX_Q4_K: return 144;
+        case QX_Q6_K: return 210;
+        default: return 0;
+    }
+}
+
+int64_t gcd64(int64_t a, int64_t b) {
+    while (b) {
+        const int64_t t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+qx_status check_shape(int fmt, int64_t rows, int64_t cols) {
+    if (block_weights(fmt) == 0) return QX_ERR_FMT;
+    if (rows < 1 || cols < 1 || cols % block_weights(fmt) != 0 || cols > QX_MAX_COLS) return QX_ERR_SHAPE;
+    if (rows > (int64_t(1) << 40) / (cols / block_weights(fmt) * block_bytes(fmt))) return QX_ERR_SHAPE;
+    return QX_OK;
+}
+
+qx_status check_act(const qx_act_q8* a, int64_t m, int64_t cols) {
+    if (!a || !a->q || !a->d || !a->sum) return QX_ERR_ARG;
+    if (a->cols != cols || a->m < 1 || (m > 0 && a->m != m)) return QX_ERR_SHAPE;
+    if (!aligned16(a->q) || !aligned16(a->d) || !aligned16(a->sum)) return QX_ERR_ALIGN;
+    return QX_OK;
+}
+
+// Launch geometry of the streaming GEMV for one format/mode over a row space.
+qx_status gemv_geometry(int fmt, int mode, bool partials, int64_t cols, const DeviceInfo& dev, GemvParams& p,
+                        size_t& smem) {
+    const int C = gemv_cols_per_lane(fmt, mode);
+    if (cols % C) return QX_ERR_SHAPE;
+    const int L = static_cast<int>(cols / C);
+    int team_lanes, team_warps, nteams;
+    if (L <= 32) {
+        team_lanes = 1;
+        while (team_lanes < L) team_lanes <<= 1;
+        team_warps = 1;
+        nteams = kGemvConsumerWarps * (32 / team_lanes);
+    } else {
+        team_warps = (L + 31) / 32;
+        if (team_warps > kGemvConsumerWarps) return QX_ERR_SHAPE;
+        nteams = kGemvConsumerWarps / team_warps;
+        team_lanes = 32 * team_warps;
+    }
+    const int64_t rb = cols / block_weights(fmt) * block_bytes(fmt);
+    const int quantum = static_cast<int>(16 / gcd64(rb, 16));
+    const int64_t base = int64_t(nteams) / gcd64(nteams, quantum) * quantum;  // lcm
+    int64_t G = base;
+    while (G + base <= kMaxStageRows && size_t((G + base) * rb) <= kStageTargetBytes) G += base;
+    if (G > kMaxStageRows) G = base;  // very wide teams with tiny rows: keep one base group
+    const size_t slot = (size_t(G * rb) + kSlotPad + 127) / 128 * 128;
+    const bool one_cta = (mode == QX_MODE_F32 && fmt != QX_Q8_0);
+    const size_t budget = one_cta ? 200 * 1024 : 96 * 1024;
+    int stages = static_cast<int>(budget / slot);
+    if (stages > 8) stages = 8;
+    if (stages < 2) stages = 2;
+    const size_t red = team_warps > 1 ? size_t(stages) * G * (1 + team_warps) * 4 : 0;
+    smem = size_t(stages) * slot + size_t(stages) * 16 + red;
+    if (smem > 227 * 1024) return QX_ERR_SHAPE;
+
+    int per_sm = 0;
+    if (gemv_max_ctas_per_sm(fmt, mode, partials, smem, &per_sm) != cudaSuccess || per_sm < 1) return QX_ERR_CUDA;
+    const int64_t max_cta = int64_t(dev.sm_count) * per_sm;
+    const int64_t groups = (p.total_rows + quantum - 1) / quantum;
+    p.cols = cols;
+    p.row_bytes = rb;
+    p.quantum = quantum;
+    p.G = static_cast<int>(G);
+    p.stages = stages;
+    p.slot_bytes = static_cast<int>(slot);
+    p.team_lanes = team_lanes;
+    p.team_warps = team_warps;
+    p.nteams = nteams;
+    p.L = L;
+    p.n_cta = static_cast<int>(groups < max_cta ? groups : max_cta);
+    p.err = dev.err_word;
+    p.wait_ns = kDefaultWaitNs;
+    return QX_OK;
+}
+
+// One streaming-GEMV launch over `n` matrices of the same format.
+qx_status run_gemv(int fmt, int n, const void* const* W, const int64_t* rows, int64_t cols, const void* x,
+                   float* const* y, int32_t* P, qx_mode mode, cudaStream_t s) {
+    DeviceInfo* dev = nullptr;
+    qx_status st = device_info(&dev);
+    if (st != QX_OK) return st;
+    GemvParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.n_entries = n;
+    int64_t total = 0;
+    for (int k = 0; k < n; ++k) {
+        p.e[k].W = static_cast<const uint8_t*>(W[k]);
+        p.e[k].y = y ? y[k] : nullptr;
+        p.e[k].P = P;
+        p.e[k].rows = rows[k];
+        p.e[k].row0 = total;
+        total += rows[k];
+    }
+    p.total_rows = total;
+    if (mode == QX_MODE_F32) {
+        p.x = static_cast<const float*>(x);
+    } else {
+        const qx_act_q8* a = static_cast<const qx_act_q8*>(x);
+        p.xq = a->q;
+        p.xd = a->d;
+        p.xs = a->sum;
+    }
+    size_t smem = 0;
+    st = gemv_geometry(fmt, mode, P != nullptr, cols, *dev, p, smem);
+    if (st != QX_OK) return st;
+    if (launch_gemv(fmt, mode, P != nullptr, p, smem, s) != cudaSuccess) return QX_ERR_CUDA;
+    return QX_OK;
+}
+
+qx_status check_x(qx_mode mode, const void* x, int64_t cols) {
+    if (!x) return QX_ERR_ARG;
+    if (mode == QX_MODE_F32) return aligned16(x) ? QX_OK : QX_ERR_ALIGN;
+    if (mode == QX_MODE_W4A8) return check_act(static_cast<const qx_act_q8*>(x), 1, cols);
+    return QX_ERR_MODE;
+}
+
+}  // namespace
+}  // namespace qx
+
+using namespace qx;
+
+extern "C" {
+
+size_t qx_row_bytes(qx_fmt fmt, int64_t cols) {
+    const int bw = block_weights(fmt);
+    if (bw == 0 || cols < 1 || cols % bw) return 0;
+    return size_t(cols / bw) * block_bytes(fmt);
+}
+
+qx_status qx_quantize_act_q8(const float* x, int64_t m, int64_t cols, qx_act_q8* out, qx_stream_t s) {
+    if (!x || !out || !out->q || !out->d || !out->sum) return QX_ERR_ARG;
+    if (m < 1 || cols < 32 || cols % 32 || cols > (int64_t(1) << 30) || m > (int64_t(1) << 40) / cols)
+        return QX_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(out->q) || !aligned16(out->d) || !aligned16(out->sum)) return QX_ERR_ALIGN;
+    DeviceInfo* dev = nullptr;
+    const qx_status st = device_info(&dev);
+    if (st != QX_OK) return st;
+    if (launch_actq8(x, m * cols / 32, out->q, out->d, out->sum, dev->sm_count, reinterpret_cast<cudaStream_t>(s)) !=
+        cudaSuccess)
+        return QX_ERR_CUDA;
+    out->m = m;
+    out->cols = cols;
+    return QX_OK;
+}
+
+qx_status qx_gemv(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const void* x, float* y, qx_mode mode,
+                  qx_stream_t s) {
+    if (mode != QX_MODE_F32 && mode != QX_MODE_W4A8) return QX_ERR_MODE;
+    qx_status st = check_shape(fmt, rows, cols);
+    if (st != QX_OK) return st;
+    if (!W || !y) return QX_ERR_ARG;
+    if (!aligned16(W) || !aligned4(y)) return QX_ERR_ALIGN;
+    if ((st = check_x(mode, x, cols)) != QX_OK) return st;
+    return run_gemv(fmt, 1, &W, &rows, cols, x, &y, nullptr, mode, reinterpret_cast<cudaStream_t>(s));
+}
+
+qx_status qx_gemv_multi(int n, const qx_fmt* fmt, const void* const* W, const int64_t* rows, int64_t cols,
+                        const void* x, float* const* y, qx_mode mode, qx_stream_t s) {
+    if (n < 1 || n > QX_MAX_MULTI || !fmt || !W || !rows || !y) return QX_ERR_ARG;
+    if (mode != QX_MODE_F32 && mode != QX_MODE_W4A8) return QX_ERR_MODE;
+    qx_status st;
+    for (int k = 0; k < n; ++k) {
+        if ((st = check_shape(fmt[k], rows[k], cols)) != QX_OK) return st;
+        if (!W[k] || !y[k]) return QX_ERR_ARG;
+        if (!aligned16(W[k]) || !aligned4(y[k])) return QX_ERR_ALIGN;
+    }
+    if ((st = check_x(mode, x, cols)) != QX_OK) return st;
+    // One launch per distinct format, entries kept in call order.
+    const int fmts[3] = {QX_Q4_K, QX_Q6_K, QX_Q8_0};
+    for (int f : fmts) {
+        const void* Wf[QX_MAX_MULTI];
+        int64_t rf[QX_MAX_MULTI];
+        float* yf[QX_MAX_MULTI];
+        int nf = 0;
+        for (int k = 0; k < n; ++k)
+            if (fmt[k] == f) {
+                Wf[nf] = W[k];
+                rf[nf] = rows[k];
+                yf[nf] = y[k];
+                ++nf;
+            }
+        if (nf == 0) continue;
+        if ((st = run_gemv(f, nf, Wf, rf, cols, x, yf, nullptr, mode, reinterpret_cast<cudaStream_t>(s))) != QX_OK)
+            return st;
+    }
+    return QX_OK;
+}
+
+qx_status qx_gemv_partials(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* x, int32_t* P,
+                           qx_stream_t s) {
+    qx_status st = check_shape(fmt, rows, cols);
+    if (st != QX_OK) return st;
+    if (!W || !P) return QX_ERR_ARG;
+    if (!aligned16(W) || !aligned4(P)) return QX_ERR_ALIGN;
+    if ((st = check_act(x, 1, cols)) != QX_OK) return st;
+    return run_gemv(fmt, 1, &W, &rows, cols, x, nullptr, P, QX_MODE_W4A8, reinterpret_cast<cudaStream_t>(s));
+}
+
+qx_status qx_gemm_prefill_ex(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, float* Y,
+                             int path, qx_stream_t s) {
+    qx_status st = check_shape(fmt, rows, cols);
+    if (st != QX_OK) return st;
+    if (!W || !Y) return QX_ERR_ARG;
+    if (!aligned16(W) || !aligned4(Y)) return QX_ERR_ALIGN;
+    if ((st = check_act(X, 0, cols)) != QX_OK) return st;
+    if (path < 0 || path > 2) return QX_ERR_ARG;
+    if (path == 2) return QX_ERR_SHAPE;  // tensor-core path not built for this format/shape
+    // Row-by-row: each row of X is an independent W4A8 GEMV.
+    for (int64_t m = 0; m < X->m; ++m) {
+        qx_act_q8 row{X->q + m * cols, X->d + m * (cols / 32), X->sum + m * (cols / 32), 1, cols};
+        if (!aligned16(row.q) || !aligned16(row.d) || !aligned16(row.sum)) return QX_ERR_ALIGN;
+        float* ym = Y + m * rows;
+        if ((st = run_gemv(fmt, 1, &W, &rows, cols, &row, &ym, nullptr, QX_MODE_W4A8,
+                           reinterpret_cast<cudaStream_t>(s))) != QX_OK)
+            return st;
+    }
+    return QX_OK;
+}
+
+qx_status qx_gemm_prefill(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, float* Y,
+                          qx_stream_t s) {
+    return qx_gemm_prefill_ex(fmt, W, rows, cols, X, Y, 0, s);
+}
+
+qx_status qx_device_check(qx_stream_t s) {
+    DeviceInfo* dev = nullptr;
+    const qx_status st = device_info(&dev);
+    if (st != QX_OK) return st;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(s)) != cudaSuccess) return QX_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_err_word, sizeof(word)) != cudaSuccess) return QX_ERR_CUDA;
+    if (word) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof(zero)) != cudaSuccess) return QX_ERR_CUDA;
+        return QX_ERR_DEVICE_TIMEOUT;
+    }
+    return QX_OK;
+}
+
+qx_status qx_debug_timeout_probe(uint64_t limit_ns, qx_stream_t s) {
+    if (limit_ns < 1000000ull || limit_ns > 10000000000ull) return QX_ERR_ARG;
+    DeviceInfo* dev = nullptr;
+    const qx_status st = device_info(&dev);
+    if (st != QX_OK) return st;
+    return launch_timeout_probe(dev->err_word, limit_ns, reinterpret_cast<cudaStream_t>(s)) == cudaSuccess
+               ? QX_OK
+               : QX_ERR_CUDA;
+}
+
+const char* qx_status_string(qx_status st) {
+    switch (st) {
+        case QX_OK: return "QX_OK";
+        case QX_ERR_ARG: return "QX_ERR_ARG: null pointer or invalid argument";
+        case QX_ERR_FMT: return "QX_ERR_FMT: unknown block format";
+        case QX_ERR_SHAPE: return "QX_ERR_SHAPE: shape not served (cols must be whole blocks, within limits)";
+        case QX_ERR_ALIGN: return "QX_ERR_ALIGN: a pointer is not 16-byte aligned";
+        case QX_ERR_MODE: return "QX_ERR_MODE: unknown mode";
+        case QX_ERR_CUDA: return "QX_ERR_CUDA: a CUDA call or kernel launch failed";
+        case QX_ERR_DEVICE_TIMEOUT: return "QX_ERR_DEVICE_TIMEOUT: a kernel's bounded wait ran out";
+        case QX_ERR_UNSUPPORTED_DEVICE:
+            return "QX_ERR_UNSUPPORTED_DEVICE: the current device is not compute capability 10.3 (GB300)";
+        default: return "unknown qx status";
+    }
+}
+
+const char* qx_version(void) {
+    return "qx 0.1 sm_103a: actq8; gemv {q4_k,q6_k,q8_0} x {f32,w4a8} (bulk-copy stream); partials; multi";
+}
+
+}  // extern "C"

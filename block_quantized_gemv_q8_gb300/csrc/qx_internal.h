@@ -1,0 +1,62 @@
+// qx_internal.h -- launch descriptors shared by the C-ABI layer (qx_api.cu)
+// and the kernel translation units.  Host and device code; no CUDA types in
+// the public header depend on it.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/qx.h"
+
+namespace qx {
+
+// Consumer warps per GEMV CTA (one more warp issues the bulk copies).
+constexpr int kGemvConsumerWarps = 8;
+constexpr int kGemvThreads = 32 * (kGemvConsumerWarps + 1);
+// Bytes read past the end of a shared-memory slot by the unaligned-word loads.
+constexpr int kSlotPad = 16;
+
+struct GemvEntry {
+    const uint8_t* W;  // device, rows * row_bytes
+    float* y;          // device, [rows]      (y output)
+    int32_t* P;        // device, [rows, ng]  (partials output)
+    int64_t rows;
+    int64_t row0;      // first row of this entry in the concatenated row space
+};
+
+struct GemvParams {
+    GemvEntry e[QX_MAX_MULTI];
+    int n_entries;
+    int64_t total_rows;
+    int64_t cols;
+    int64_t row_bytes;
+    int quantum;      // rows per 16-byte-aligned row group
+    int G;            // rows per pipeline stage
+    int stages;       // pipeline depth (shared-memory slots)
+    int slot_bytes;   // bytes per slot, including kSlotPad
+    int team_lanes;   // lanes per team: a power of two <= 32, or 32 * team_warps
+    int team_warps;   // warps per team (1 for sub-warp teams)
+    int nteams;       // teams per CTA
+    int L;            // lanes with work per row (cols / columns-per-lane)
+    int n_cta;
+    const float* x;    // f32 mode activation [cols]
+    const int8_t* xq;  // W4A8 activation quants [cols]
+    const float* xd;   // W4A8 activation scales [cols/32]
+    const int32_t* xs; // W4A8 activation block sums [cols/32]
+    unsigned* err;     // device error word
+    uint64_t wait_ns;  // bound on every wait
+};
+
+// Columns owned by one lane, per (format, mode).
+constexpr int gemv_cols_per_lane(int fmt, int mode) {
+    return fmt == QX_Q8_0 ? 32 : (mode == QX_MODE_W4A8 ? 128 : 64);
+}
+
+// Launchers (defined in the kernel translation units).
+cudaError_t launch_actq8(const float* x, int64_t nblocks, int8_t* q, float* d, int32_t* sum, int sm_count,
+                         cudaStream_t s);
+cudaError_t launch_gemv(int fmt, int mode, bool partials, const GemvParams& p, size_t smem, cudaStream_t s);
+cudaError_t gemv_max_ctas_per_sm(int fmt, int mode, bool partials, size_t smem, int* out);
+cudaError_t launch_timeout_probe(unsigned* err, uint64_t limit_ns, cudaStream_t s);
+
+}  // namespace qx

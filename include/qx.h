@@ -1,0 +1,187 @@
+/*
+ * qx.h -- C ABI of the GB300 (sm_103a) block-quantised GEMV / GEMM library.
+ *
+ * The library computes the decode-time matrix-vector product of GGUF-style
+ * block-quantised weight rows (Q4_K, Q6_K, Q8_0) with one activation vector,
+ * in two methods (llamay docs, "Backends and hardware", section "Accelerate is
+ * not bit-identical": dequantising the weights to float and quantising the
+ * activation to int8 are two methods, not one method and its rounding error):
+ *
+ *   QX_MODE_F32  -- the weights are dequantised on the fly and dotted with an
+ *                   f32 activation (llambda.lisp README, "Features &
+ *                   Architecture": the f32 FMA GEMV over Q4_K_M / Q6_K).
+ *   QX_MODE_W4A8 -- the activation is quantised to int8 once per matmul and
+ *                   the weight rows are never materialised; per-block integer
+ *                   dot products are scaled per block (llamay, "Backends and
+ *                   hardware", section "CPU": the W4A8 fused dot product; and
+ *                   section "CUDA": an integer dot for the W4A8 inner product).
+ *
+ * It also runs the same contraction at prefill batch sizes on the tensor
+ * cores (llamay, section "CUDA": a tensor-core prefill kernel, whose missing
+ * piece was staging the next weight tile behind the current multiply).
+ *
+ * Conventions shared by every entry point:
+ *   - Weights are a row-major array of blocks; row r starts at byte
+ *     r * qx_row_bytes(fmt, cols).  Block layouts are the GGUF ones:
+ *       Q4_K 256 weights / 144 B: d f16, dmin f16, 12 B of packed 6-bit
+ *            scales and mins, 128 B of 4-bit quants; w = d*sc*q - dmin*m.
+ *       Q6_K 256 weights / 210 B: ql[128] (low 4 bits), qh[64] (high 2 bits),
+ *            scales[16] int8 (one per 16 weights), d f16 last;
+ *            w = d*sc*(q - 32).
+ *       Q8_0 32 weights / 34 B: d f16, 32 int8 quants; w = d*q.
+ *   - Every pointer named "device" is device memory owned by the caller.  The
+ *     library allocates nothing and keeps no per-call state; it caches one
+ *     device-property query per device.
+ *   - Calls are asynchronous on stream `s` (NULL = the legacy default stream)
+ *     and run on the current device.  Argument, shape and alignment errors
+ *     return before anything is launched or written; a failed launch returns
+ *     QX_ERR_CUDA.
+ *   - Alignment: W, the f32 activation x and the qx_act_q8 buffers must be
+ *     16-byte aligned; the outputs y, Y and P 4-byte aligned.
+ *   - Only compute capability 10.3 (GB300) is served.  Any other device is
+ *     declined with QX_ERR_UNSUPPORTED_DEVICE rather than run through another
+ *     kernel (llamay, section "CUDA": below its minimum capability the
+ *     backend declines at open with a message naming the reason).
+ *   - Kernels bound every wait.  A wait that runs out sets a device error
+ *     word and the kernel returns; qx_device_check() reports it.
+ */
+#ifndef QX_H
+#define QX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* qx_stream_t;
+
+/* Format tags (the GGML type ids, a naming convention only). */
+typedef enum { QX_Q8_0 = 8, QX_Q4_K = 12, QX_Q6_K = 14 } qx_fmt;
+
+typedef enum { QX_MODE_F32 = 0, QX_MODE_W4A8 = 1 } qx_mode;
+
+/* Status codes.  0 is success; every error is negative. */
+typedef int qx_status;
+#define QX_OK 0
+#define QX_ERR_ARG (-1)                /* null pointer, bad count, bad path       */
+#define QX_ERR_FMT (-2)                /* unknown format                          */
+#define QX_ERR_SHAPE (-3)              /* cols not whole blocks, size out of range */
+#define QX_ERR_ALIGN (-4)              /* a pointer is not 16-byte aligned        */
+#define QX_ERR_MODE (-5)               /* unknown mode, or mode/format mismatch   */
+#define QX_ERR_CUDA (-6)               /* a CUDA runtime call or launch failed    */
+#define QX_ERR_DEVICE_TIMEOUT (-7)     /* a kernel's bounded wait ran out         */
+#define QX_ERR_UNSUPPORTED_DEVICE (-8) /* current device is not compute 10.3      */
+
+/* Largest activation width served (columns per row). */
+#define QX_MAX_COLS 32768
+/* Largest number of matrices in one qx_gemv_multi call. */
+#define QX_MAX_MULTI 8
+
+/*
+ * An int8-quantised activation, m rows of `cols` values, in caller-owned
+ * device buffers (llamay, "Backends and hardware", section "CPU": the
+ * activation is quantised to int8 once per matmul):
+ *   q   [m, cols]      int8, row-major
+ *   d   [m, cols/32]   f32 scale of each block of 32
+ *   sum [m, cols/32]   int32 sum of the 32 quants of each block
+ * The struct itself lives in host memory.
+ */
+typedef struct {
+    int8_t* q;
+    float* d;
+    int32_t* sum;
+    int64_t m;
+    int64_t cols;
+} qx_act_q8;
+
+/*
+ * Quantise x (device, f32 [m, cols] row-major) per block of 32:
+ *   d = amax / 127 (f32, correctly rounded), q = round-half-even(x / d)
+ *   (correctly rounded f32 quotient) clamped to [-127, 127], q = 0 when
+ *   d == 0, sum = sum of q.
+ * Writes out->q, out->d, out->sum (device buffers sized for m x cols) and
+ * sets out->m = m, out->cols = cols.  cols must be a positive multiple of 32
+ * (QX_ERR_SHAPE), m >= 1.  Non-finite inputs are not checked; their outputs
+ * are unspecified.
+ */
+qx_status qx_quantize_act_q8(const float* x, int64_t m, int64_t cols, qx_act_q8* out, qx_stream_t s);
+
+/*
+ * y[r] = sum_i w[r, i] * x[i] for r in [0, rows)  (device y, f32 [rows]).
+ *   mode QX_MODE_F32 : x is `const float*`, device, f32 [cols].
+ *   mode QX_MODE_W4A8: x is `const qx_act_q8*` (host struct) with m == 1 and
+ *                      cols == cols, produced by qx_quantize_act_q8; y is the
+ *                      per-block-scaled sum of exact integer partial sums.
+ * cols must be a positive multiple of the block width (256 for Q4_K/Q6_K,
+ * 32 for Q8_0) and at most QX_MAX_COLS; rows >= 1.
+ */
+qx_status qx_gemv(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const void* x, float* y,
+                  qx_mode mode, qx_stream_t s);
+
+/*
+ * n independent GEMVs over one activation in a single launch, e.g. the Q, K
+ * and V projections, or gate and up: y[k] = W[k] . x for k in [0, n).
+ * fmt, W, rows and y are host arrays of n entries; W[k] and y[k] are device
+ * pointers.  All entries share cols, x and mode; 1 <= n <= QX_MAX_MULTI.
+ * Entries of different formats are run as one launch per format.
+ */
+qx_status qx_gemv_multi(int n, const qx_fmt* fmt, const void* const* W, const int64_t* rows, int64_t cols,
+                        const void* x, float* const* y, qx_mode mode, qx_stream_t s);
+
+/*
+ * Prefill: Y[m, r] = sum_i w[r, i] * x'[m, i] for every row m of the
+ * quantised activation X (X->m rows, X->cols == cols), with Y device f32
+ * [X->m, rows] row-major.  The rows of X are independent W4A8 GEMVs (colibri
+ * GPU_BACKENDS.md, XDNA lane: C = A x B is row-independent, so padding the
+ * batch to a tile is legitimate and padded rows are never written).
+ */
+qx_status qx_gemm_prefill(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, float* Y,
+                          qx_stream_t s);
+
+/*
+ * qx_gemm_prefill with a forced path: 0 = automatic, 1 = batched GEMV kernel
+ * (weights streamed once for all rows of X; X->m <= 8), 2 = tensor-core
+ * GEMM.  A path that cannot serve the call returns QX_ERR_SHAPE or
+ * QX_ERR_FMT rather than falling back.
+ */
+qx_status qx_gemm_prefill_ex(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X,
+                             float* Y, int path, qx_stream_t s);
+
+/*
+ * The exact integer partial sums of the W4A8 product, written instead of y:
+ * P[r, g] = sum over group g of q_w * q_x, with groups of 32 weights for Q4_K
+ * (q_w the unsigned 4-bit quant) and Q8_0 (q_w the int8 quant), and groups of
+ * 16 for Q6_K (q_w = q - 32).  P is device int32 [rows, cols/32] or
+ * [rows, cols/16].  Computed by the same kernel code as qx_gemv's W4A8 path
+ * (colibri GPU_BACKENDS.md: a numerics-matched integer GPU kernel).
+ */
+qx_status qx_gemv_partials(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* x,
+                           int32_t* P, qx_stream_t s);
+
+/* Bytes of one row of `cols` weights, or 0 if fmt is unknown or cols is not
+ * a positive multiple of the block width. */
+size_t qx_row_bytes(qx_fmt fmt, int64_t cols);
+
+/* Synchronise stream s, then read and clear the device error word of the
+ * current device: QX_OK, QX_ERR_DEVICE_TIMEOUT if a kernel's bounded wait ran
+ * out since the last check, or QX_ERR_CUDA if the synchronisation failed. */
+qx_status qx_device_check(qx_stream_t s);
+
+/* Test hook: launch one CTA that waits on a barrier nothing will complete,
+ * with a wait limit of `limit_ns` nanoseconds (1 ms .. 10 s), so that the
+ * bounded-wait path runs without any fault.  qx_device_check() then returns
+ * QX_ERR_DEVICE_TIMEOUT. */
+qx_status qx_debug_timeout_probe(uint64_t limit_ns, qx_stream_t s);
+
+/* Static, NUL-terminated strings. */
+const char* qx_status_string(qx_status st);
+const char* qx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QX_H */

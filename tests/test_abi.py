@@ -1,0 +1,100 @@
+"""The C-ABI library loads, exports every entry point declared in include/qx.h,
+and rejects bad arguments on the host before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_quantized_gemv_q8_gb300 as qx
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qx.build_library()
+    return qx.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "qx.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qx_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ["qx_quantize_act_q8", "qx_gemv", "qx_gemv_multi", "qx_gemm_prefill", "qx_gemv_partials"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} declared in qx.h but not exported by libqx.so"
+    assert set(qx.EXPORTS) <= set(declared_functions())
+
+
+def test_row_bytes(lib):
+    assert qx.qx_row_bytes(qx.QX_Q4_K, 4096) == 16 * 144
+    assert qx.qx_row_bytes(qx.QX_Q6_K, 14336) == 56 * 210
+    assert qx.qx_row_bytes(qx.QX_Q8_0, 896) == 28 * 34
+    assert qx.qx_row_bytes(qx.QX_Q4_K, 896) == 0
+    assert qx.qx_row_bytes(qx.QX_Q8_0, 0) == 0
+    assert qx.qx_row_bytes(7, 256) == 0
+
+
+def test_status_strings_and_version(lib):
+    for st in range(0, -9, -1):
+        assert qx.qx_status_string(st).startswith("QX_")
+    assert "sm_103a" in qx.qx_version()
+
+
+A16 = 1 << 20  # a fake but 16-byte aligned address; never dereferenced
+
+
+def test_host_validation_rejects_before_launch(lib):
+    P, s = ctypes.c_void_p, None
+    # unknown format / mode
+    assert lib.qx_gemv(99, P(A16), 4, 256, P(A16), P(A16), 0, s) == qx.QX_ERR_FMT
+    assert lib.qx_gemv(qx.QX_Q4_K, P(A16), 4, 256, P(A16), P(A16), 7, s) == qx.QX_ERR_MODE
+    # shape: cols not whole blocks, too wide, rows < 1
+    assert lib.qx_gemv(qx.QX_Q4_K, P(A16), 4, 896, P(A16), P(A16), 0, s) == qx.QX_ERR_SHAPE
+    assert lib.qx_gemv(qx.QX_Q8_0, P(A16), 4, 40, P(A16), P(A16), 0, s) == qx.QX_ERR_SHAPE
+    assert lib.qx_gemv(qx.QX_Q4_K, P(A16), 4, 65536, P(A16), P(A16), 0, s) == qx.QX_ERR_SHAPE
+    assert lib.qx_gemv(qx.QX_Q4_K, P(A16), 0, 256, P(A16), P(A16), 0, s) == qx.QX_ERR_SHAPE
+    # null pointers
+    assert lib.qx_gemv(qx.QX_Q4_K, None, 4, 256, P(A16), P(A16), 0, s) == qx.QX_ERR_ARG
+    assert lib.qx_gemv(qx.QX_Q4_K, P(A16), 4, 256, None, P(A16), 0, s) == qx.QX_ERR_ARG
+    # misaligned pointers
+    assert lib.qx_gemv(qx.QX_Q4_K, P(A16 + 2), 4, 256, P(A16), P(A16), 0, s) == qx.QX_ERR_ALIGN
+    assert lib.qx_gemv(qx.QX_Q4_K, P(A16), 4, 256, P(A16 + 4), P(A16), 0, s) == qx.QX_ERR_ALIGN
+    assert lib.qx_gemv(qx.QX_Q4_K, P(A16), 4, 256, P(A16), P(A16 + 2), 0, s) == qx.QX_ERR_ALIGN
+    # W4A8 activation descriptor checks
+    act = qx._Act(A16, A16, A16, 1, 512)
+    assert lib.qx_gemv(qx.QX_Q4_K, P(A16), 4, 256, ctypes.cast(ctypes.pointer(act), P), P(A16), 1, s) == \
+        qx.QX_ERR_SHAPE
+    act = qx._Act(A16, A16 + 4, A16, 1, 256)
+    assert lib.qx_gemv(qx.QX_Q4_K, P(A16), 4, 256, ctypes.cast(ctypes.pointer(act), P), P(A16), 1, s) == \
+        qx.QX_ERR_ALIGN
+    act = qx._Act(A16, None, A16, 1, 256)
+    assert lib.qx_gemv_partials(qx.QX_Q4_K, P(A16), 4, 256, ctypes.byref(act), P(A16), s) == qx.QX_ERR_ARG
+    # multi: bad counts
+    F = (ctypes.c_int * 9)(*([qx.QX_Q4_K] * 9))
+    assert lib.qx_gemv_multi(0, F, None, None, 256, P(A16), None, 0, s) == qx.QX_ERR_ARG
+    assert lib.qx_gemv_multi(9, F, None, None, 256, P(A16), None, 0, s) == qx.QX_ERR_ARG
+    # quantise: cols not a multiple of 32
+    act = qx._Act(A16, A16, A16, 0, 0)
+    assert lib.qx_quantize_act_q8(P(A16), 1, 48, ctypes.byref(act), s) == qx.QX_ERR_SHAPE
+    assert lib.qx_quantize_act_q8(P(A16 + 4), 1, 64, ctypes.byref(act), s) == qx.QX_ERR_ALIGN
+    # prefill: bad path
+    act = qx._Act(A16, A16, A16, 4, 256)
+    assert lib.qx_gemm_prefill_ex(qx.QX_Q4_K, P(A16), 4, 256, ctypes.byref(act), P(A16), 5, s) == qx.QX_ERR_ARG
+    # timeout probe limits
+    assert lib.qx_debug_timeout_probe(10, s) == qx.QX_ERR_ARG
+
+
+def test_python_binding_rejects_cpu_tensors(lib):
+    import torch
+    with pytest.raises((ValueError, TypeError)):
+        qx.qx_gemv(qx.QX_Q4_K, torch.zeros(144, dtype=torch.uint8), 1, 256, torch.zeros(256), mode=qx.QX_MODE_F32)

@@ -1,0 +1,199 @@
+"""GPU parity: the CUDA path against the CPU oracle on the same seeded inputs.
+
+Gates (the same in every test):
+  * activation quants, scales and block sums: bit-exact;
+  * integer partial sums of the W4A8 product: bit-exact;
+  * f32 outputs: |y - y_ref| <= 1e-4 * sum_i |w_i * x_i| per row, where x is
+    the f32 activation in f32 mode and the dequantised int8 activation in
+    W4A8 mode.
+"""
+import numpy as np
+import pytest
+import torch
+
+import block_quantized_gemv_q8_gb300 as qx
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    qx.build_library()
+    qx.lib()
+    assert qx.qx_device_check() == qx.QX_OK
+
+
+def dev(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t: torch.Tensor) -> np.ndarray:
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def assert_close(y, ref, absdot, what):
+    y = np.asarray(y, dtype=np.float64)
+    err = np.abs(y - ref)
+    bound = TOL * absdot
+    bad = np.nonzero(~(err <= bound))[0]
+    assert bad.size == 0, (f"{what}: {bad.size} rows out of tolerance, e.g. row {bad[0]}: "
+                           f"y={y[bad[0]]} ref={ref[bad[0]]} err={err[bad[0]]} bound={bound[bad[0]]}")
+
+
+def quantize_both(x: np.ndarray):
+    """GPU and oracle quantisation of the same activation; asserts bit-exactness."""
+    a = qx.qx_quantize_act_q8(dev(x))
+    q, d, s = oracle.quantize_act_q8(x)
+    assert np.array_equal(host(a.q), q), "activation quants differ"
+    assert np.array_equal(host(a.d).view(np.uint32), d.view(np.uint32)), "activation scales differ"
+    assert np.array_equal(host(a.sum), s), "activation block sums differ"
+    return a, q, d, s
+
+
+# -------------------------------------------------------- activation quant ----
+
+@pytest.mark.parametrize("m,cols", [(1, 32), (1, 896), (1, 4096), (3, 1024), (512, 4096), (1, 14336)])
+def test_actq8_bit_exact(m, cols):
+    x = synth.activation(m, cols, seed=100 + m + cols)
+    quantize_both(x)
+
+
+def test_actq8_special_values():
+    x = np.zeros((1, 256), np.float32)
+    x[0, 32] = 1e-44                      # block whose scale underflows to 0
+    x[0, 64:96] = np.linspace(-1e30, 1e30, 32)
+    x[0, 96] = 127 / 8                    # ties: x/d = k + 1/2 with d = 1/8
+    x[0, 97:103] = np.array([2.5, 3.5, -2.5, 0.5, 1.5, -126.5]) / 8
+    x[0, 128:160] = -3.0                  # constant block
+    x[0, 160:192] = np.float32(1e-30) * np.arange(32)
+    quantize_both(x)
+
+
+# ------------------------------------------------------------------ GEMV ----
+
+SHAPES = {
+    synth.Q4_K: [(1, 256), (7, 256), (37, 1024), (300, 4096), (129, 14336), (64, 32768), (1000, 1024)],
+    synth.Q6_K: [(1, 256), (5, 512), (37, 1024), (300, 4096), (65, 14336), (9, 2048)],
+    synth.Q8_0: [(1, 32), (7, 896), (33, 4096), (301, 896), (5, 8192), (3, 64)],
+}
+CASES = [(f, r, c) for f, shapes in SHAPES.items() for (r, c) in shapes]
+IDS = [f"{synth.NAMES[f]}-{r}x{c}" for f, r, c in CASES]
+
+
+@pytest.mark.parametrize("fmt,rows,cols", CASES, ids=IDS)
+def test_partials_bit_exact(fmt, rows, cols):
+    W = synth.weights(fmt, rows, cols, seed=rows * 7 + cols)
+    x = synth.activation(1, cols, seed=cols + 3)
+    a, q, d, s = quantize_both(x)
+    P = qx.qx_gemv_partials(fmt, dev(W), rows, cols, a)
+    ref = oracle.partials(fmt, W, rows, cols, q[0])
+    got = host(P)
+    assert got.shape == ref.shape
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, f"{bad.shape[0]} partials differ, first at {bad[0]}: {got[tuple(bad[0])]} vs {ref[tuple(bad[0])]}"
+
+
+@pytest.mark.parametrize("fmt,rows,cols", CASES, ids=IDS)
+def test_gemv_w4a8(fmt, rows, cols):
+    W = synth.weights(fmt, rows, cols, seed=rows * 11 + cols)
+    x = synth.activation(1, cols, seed=cols + 5)
+    a, q, d, s = quantize_both(x)
+    y = qx.qx_gemv(fmt, dev(W), rows, cols, a, mode=qx.QX_MODE_W4A8)
+    ref, absdot = oracle.gemv_w4a8(fmt, W, rows, cols, q[0], d[0])
+    assert_close(host(y), ref, absdot, f"w4a8 {synth.NAMES[fmt]} {rows}x{cols}")
+
+
+@pytest.mark.parametrize("fmt,rows,cols", [c for c in CASES if c[2] <= 16384],
+                         ids=[i for c, i in zip(CASES, IDS) if c[2] <= 16384])
+def test_gemv_f32(fmt, rows, cols):
+    W = synth.weights(fmt, rows, cols, seed=rows * 13 + cols)
+    x = synth.activation(1, cols, seed=cols + 7)[0]
+    y = qx.qx_gemv(fmt, dev(W), rows, cols, dev(x), mode=qx.QX_MODE_F32)
+    ref, absdot = oracle.gemv_f32(fmt, W, rows, cols, x)
+    assert_close(host(y), ref, absdot, f"f32 {synth.NAMES[fmt]} {rows}x{cols}")
+
+
+def test_gemv_zero_and_edge_values():
+    """All-zero weights, all-zero activation, a zero-scale super-block."""
+    rows, cols = 16, 1024
+    for fmt in (synth.Q4_K, synth.Q6_K, synth.Q8_0):
+        W = synth.weights(fmt, rows, cols, seed=3)
+        x = synth.activation(1, cols, seed=4)
+        Wz = np.zeros_like(W)
+        y = qx.qx_gemv(fmt, dev(Wz), rows, cols, dev(x[0]), mode=qx.QX_MODE_F32)
+        assert np.all(host(y) == 0)
+        a = qx.qx_quantize_act_q8(dev(np.zeros_like(x)))
+        y = qx.qx_gemv(fmt, dev(W), rows, cols, a, mode=qx.QX_MODE_W4A8)
+        assert np.all(host(y) == 0)
+
+
+def test_gemv_unaligned_base_offset():
+    """W and y at a 16-byte offset inside larger allocations; misaligned pointers are refused."""
+    fmt, rows, cols = synth.Q8_0, 9, 896
+    W = synth.weights(fmt, rows, cols, seed=8)
+    x = synth.activation(1, cols, seed=9)[0]
+    buf = torch.zeros(W.size + 48, dtype=torch.uint8, device="cuda")
+    buf[16:16 + W.size] = dev(W.reshape(-1))
+    y = torch.zeros(rows + 8, dtype=torch.float32, device="cuda")
+    qx.qx_gemv(fmt, buf[16:16 + W.size], rows, cols, dev(x), y=y[4:4 + rows], mode=qx.QX_MODE_F32)
+    ref, absdot = oracle.gemv_f32(fmt, W, rows, cols, x)
+    assert_close(host(y[4:4 + rows]), ref, absdot, "offset")
+    assert np.all(host(y[:4]) == 0) and np.all(host(y[4 + rows:]) == 0)
+    with pytest.raises(qx.QxError) as ei:
+        qx.qx_gemv(fmt, buf[8:8 + W.size], rows, cols, dev(x), mode=qx.QX_MODE_F32)
+    assert ei.value.status == qx.QX_ERR_ALIGN
+
+
+# ------------------------------------------------------------- multi GEMV ----
+
+@pytest.mark.parametrize("mode", [qx.QX_MODE_W4A8, qx.QX_MODE_F32])
+def test_gemv_multi_matches_separate(mode):
+    cols = 1024
+    shapes = [(synth.Q4_K, 200), (synth.Q4_K, 37), (synth.Q4_K, 64), (synth.Q8_0, 33), (synth.Q6_K, 5)]
+    Ws = [synth.weights(f, r, cols, seed=40 + i) for i, (f, r) in enumerate(shapes)]
+    x = synth.activation(1, cols, seed=41)
+    if mode == qx.QX_MODE_W4A8:
+        a, q, d, s = quantize_both(x)
+        xin = a
+    else:
+        xin = dev(x[0])
+    ys = qx.qx_gemv_multi([f for f, _ in shapes], [dev(W) for W in Ws], [r for _, r in shapes], cols, xin,
+                          mode=mode)
+    for (f, r), W, y in zip(shapes, Ws, ys):
+        if mode == qx.QX_MODE_W4A8:
+            ref, absdot = oracle.gemv_w4a8(f, W, r, cols, q[0], d[0])
+        else:
+            ref, absdot = oracle.gemv_f32(f, W, r, cols, x[0])
+        assert_close(host(y), ref, absdot, f"multi {synth.NAMES[f]} {r}")
+
+
+# ------------------------------------------------------------- prefill ----
+
+@pytest.mark.parametrize("m", [1, 3, 8])
+def test_prefill_small(m):
+    fmt, rows, cols = synth.Q4_K, 70, 1024
+    W = synth.weights(fmt, rows, cols, seed=50 + m)
+    X = synth.activation(m, cols, seed=51 + m)
+    a, q, d, s = quantize_both(X)
+    Y = qx.qx_gemm_prefill(fmt, dev(W), rows, cols, a)
+    ref, absdot = oracle.gemm_w4a8(fmt, W, rows, cols, q, d)
+    assert_close(host(Y).reshape(-1), ref.reshape(-1), absdot.reshape(-1), f"prefill m={m}")
+
+
+# ---------------------------------------------------- device error word ----
+
+def test_bounded_wait_reports_timeout_and_recovers():
+    assert qx.qx_device_check() == qx.QX_OK
+    qx.qx_debug_timeout_probe(5_000_000)  # 5 ms on a barrier nothing completes
+    assert qx.qx_device_check() == qx.QX_ERR_DEVICE_TIMEOUT
+    assert qx.qx_device_check() == qx.QX_OK  # cleared, context still usable
+    fmt, rows, cols = synth.Q4_K, 8, 256
+    W = synth.weights(fmt, rows, cols, seed=60)
+    x = synth.activation(1, cols, seed=61)[0]
+    y = qx.qx_gemv(fmt, dev(W), rows, cols, dev(x), mode=qx.QX_MODE_F32)
+    ref, absdot = oracle.gemv_f32(fmt, W, rows, cols, x)
+    assert_close(host(y), ref, absdot, "after probe")
