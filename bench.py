@@ -1,0 +1,411 @@
+"""Benchmark of the block-quantised GEMV library on one GB300 (or N replicas).
+
+Default workload: the GEMVs of a Llama-3.1-8B decode step at batch 1, Q4_K_M
+mix (Q4_K q/k/v/o/gate/up, Q6_K down), W4A8, 32 layers.  One step = for
+every layer: quantise the four activations, then q/k/v (one multi launch), o,
+gate/up (one multi launch), down.  Weights (4.41 GB per step) are resident in
+HBM and far larger than L2, so every step streams them from DRAM.
+
+Prints one JSON line:
+  value       weight-GB/s over the timed region (device-resident inputs)
+  e2e         the same metric through the public API with pinned host
+              activations copied in and all outputs copied back every step
+  roofline    the dominant kernel (gate/up Q4_K W4A8 multi-GEMV): algorithmic
+              bytes per launch / its mean CUDA-event duration vs measured HBM
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload
+
+`--impl reference` times the CPU oracle itself on the same metric.  Other
+workloads (`--workload`): q4k_1024 (Q4_K 1024x1024), lmhead_q6k (Q6_K
+128256x4096), qwen05b (Qwen2-0.5B decode step, 24 layers + Q8_0 lm_head),
+prefill (Q4_K 14336x4096, X[512, 4096]).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "quantized GEMV weight-GB/s & % of HBM peak (Llama-8B decode shapes, batch 1)"
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1916.5)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+KERNEL_SOURCES = ["qx_gemv.cu", "qx_device.cuh", "qx_api.cu", "qx_internal.h"]
+DOMINANT_PROFILE = os.path.join(ROOT, "profiles", "gemv_q4k_w4a8_gateup_llama8b.md")
+
+
+def dominant_traffic():
+    """DRAM bytes per launch of the dominant kernel from its committed ncu
+    summary, or None once the kernel sources differ from the captured ones."""
+    import hashlib
+    if not os.path.exists(DOMINANT_PROFILE):
+        return None
+    fields = {}
+    for line in open(DOMINANT_PROFILE):
+        if ":" in line and line.split(":", 1)[0] in ("traffic_bytes_per_launch", "source_sha256_16"):
+            k, v = line.split(":", 1)
+            fields[k] = v.strip()
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "block_quantized_gemv_q8_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    if fields.get("source_sha256_16") != h.hexdigest()[:16]:
+        return None
+    return int(fields["traffic_bytes_per_launch"])
+
+
+# ---------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.device_index = device_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- workloads ----
+
+class LlamaDecode:
+    """Llama-3.1-8B decode GEMVs at batch 1, W4A8, 32 layers (Q4_K_M mix)."""
+    name = "llama-3.1-8b decode GEMVs (q,k,v,o,gate,up Q4_K; down Q6_K), W4A8, batch 1, 32 layers"
+    unit = "GB/s"
+    higher_is_better = True
+
+    def __init__(self, layers: int = synth.LLAMA8B_LAYERS):
+        self.layers = layers
+        self.shapes = {n: (f, r, c) for n, f, r, c in synth.LLAMA8B_LAYER}
+        self.bytes_per_step = layers * sum(r * synth.row_bytes(f, c) for f, r, c in self.shapes.values())
+        self.launches_per_step = layers * 4
+        g, u = self.shapes["gate"], self.shapes["up"]
+        self.dominant = "q4_k w4a8 multi-GEMV (gate+up, 2 x 14336 x 4096)"
+        self.dominant_bytes = g[1] * synth.row_bytes(g[0], g[2]) + u[1] * synth.row_bytes(u[0], u[2])
+
+    def setup(self, qx, torch, seed_base: int = 0):
+        self.W, self.y = [], []
+        self.host_layer0 = None
+        for L in range(self.layers):
+            Wl, yl = {}, {}
+            for j, (n, (f, r, c)) in enumerate(self.shapes.items()):
+                Wh = synth.weights(f, r, c, seed=synth.seed_for(1, L + seed_base, j))
+                if L == 0:
+                    self.host_layer0 = self.host_layer0 or {}
+                    self.host_layer0[n] = Wh
+                Wl[n] = torch.from_numpy(Wh).cuda()
+                yl[n] = torch.empty(r, dtype=torch.float32, device="cuda")
+            self.W.append(Wl)
+            self.y.append(yl)
+        # activations: per layer x_qkv, x_o, x_ffn [4096] and x_down [14336], in one buffer
+        self.xcols = [4096, 4096, 4096, 14336]
+        per_layer = sum(self.xcols)
+        xs = np.concatenate([synth.activation(1, per_layer, seed=synth.seed_for(1, L + seed_base, 100))[0]
+                             for L in range(self.layers)])
+        self.x_host = xs
+        self.x_dev = torch.from_numpy(xs).cuda()
+        self.x_views, self.acts = [], []
+        off = 0
+        for L in range(self.layers):
+            views, acts = [], []
+            for c in self.xcols:
+                views.append(self.x_dev[off:off + c])
+                acts.append(qx.ActQ8.empty(1, c))
+                off += c
+            self.x_views.append(views)
+            self.acts.append(acts)
+        # one output buffer so that the e2e path copies it back in one piece
+        outs = [(L, n) for L in range(self.layers) for n in self.shapes]
+        total = sum(self.shapes[n][1] for _, n in outs)
+        self.y_all = torch.empty(total, dtype=torch.float32, device="cuda")
+        off = 0
+        for L, n in outs:
+            r = self.shapes[n][1]
+            self.y[L][n] = self.y_all[off:off + r]
+            off += r
+
+    def step(self, qx, stream, dom_events=None):
+        """One decode step: per layer q/k/v (one launch), o, gate/up (one launch), down.
+
+        Each launch quantises its f32 activation in-kernel (W4A8) and is
+        launched with programmatic dependent launch, so it streams its weights
+        while the previous launch finishes."""
+        F = qx.QX_Q4_K
+        mode = qx.QX_MODE_W4A8_FUSED | qx.QX_FLAG_PDL
+        for L in range(self.layers):
+            W, y, xv = self.W[L], self.y[L], self.x_views[L]
+            qx.qx_gemv_multi([F, F, F], [W["q"], W["k"], W["v"]], [4096, 1024, 1024], 4096, xv[0],
+                             ys=[y["q"], y["k"], y["v"]], mode=mode, stream=stream)
+            qx.qx_gemv(F, W["o"], 4096, 4096, xv[1], y=y["o"], mode=mode, stream=stream)
+            if dom_events is not None:
+                dom_events[L][0].record(stream)
+            qx.qx_gemv_multi([F, F], [W["gate"], W["up"]], [14336, 14336], 4096, xv[2],
+                             ys=[y["gate"], y["up"]], mode=mode, stream=stream)
+            if dom_events is not None:
+                dom_events[L][1].record(stream)
+            qx.qx_gemv(qx.QX_Q6_K, W["down"], 4096, 14336, xv[3], y=y["down"], mode=mode, stream=stream)
+
+    def cpu_sample(self, oracle, budget_s: float = 10.0):
+        """Oracle on layer 0 (quantise + 7 W4A8 GEMVs), repeated for ~budget_s."""
+        threads = oracle.default_threads()
+        x = self.x_host
+        acts = {}
+        nbytes, reps = 0, 0
+        t0 = time.perf_counter()
+        while True:
+            off = 0
+            for k, c in enumerate(self.xcols):
+                q, d, _ = oracle.quantize_act_q8(x[off:off + c][None])
+                acts[k] = (q[0], d[0])
+                off += c
+            which = {"q": 0, "k": 0, "v": 0, "o": 1, "gate": 2, "up": 2, "down": 3}
+            for n, (f, r, c) in self.shapes.items():
+                q, d = acts[which[n]]
+                oracle.gemv_w4a8(f, self.host_layer0[n], r, c, q, d, threads=threads, with_absdot=False)
+                nbytes += r * synth.row_bytes(f, c)
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                break
+        return {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                "sample": f"layer 0 of the same workload (7 W4A8 GEMVs + 4 activation quantisations, "
+                          f"{nbytes // reps} weight bytes) x {reps} repetitions, {el:.1f} s, OpenMP over rows"}
+
+
+# ------------------------------------------------------------------ main ----
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args):
+    """Time the CPU oracle itself on bounded samples of the workload (rank 0 only)."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    wl = LlamaDecode(layers=1)
+    # host-only set-up: layer 0 weights and activations
+    wl.shapes = {n: (f, r, c) for n, f, r, c in synth.LLAMA8B_LAYER}
+    wl.host_layer0 = {n: synth.weights(f, r, c, seed=synth.seed_for(1, 0, j))
+                      for j, (n, (f, r, c)) in enumerate(wl.shapes.items())}
+    wl.xcols = [4096, 4096, 4096, 14336]
+    wl.x_host = synth.activation(1, sum(wl.xcols), seed=synth.seed_for(1, 0, 100))[0]
+    per_step_budget = float(os.environ.get("QX_REF_STEP_S", "2.0"))
+    for _ in range(args.warmup):
+        wl.cpu_sample(oracle, budget_s=0.0)
+    vals, t0 = [], time.perf_counter()
+    cb = None
+    for _ in range(args.steps):
+        cb = wl.cpu_sample(oracle, budget_s=per_step_budget)
+        vals.append(cb["value"])
+    el = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    cb["value"] = value
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / max(1, args.steps) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64+f64",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "sample": "layer 0 per step (bounded, CPU oracle)"},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="qx", choices=["qx", "reference"])
+    ap.add_argument("--workload", default="llama8b", choices=["llama8b"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=synth.LLAMA8B_LAYERS)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import block_quantized_gemv_q8_gb300 as qx
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    qx.build_library()
+    qx.lib()
+
+    wl = LlamaDecode(layers=args.layers)
+    wl.setup(qx, torch, seed_base=0)
+    stream = torch.cuda.Stream()
+    # Timing events recorded inside the captured graph need external record nodes.
+    dom = [(torch.cuda.Event(enable_timing=True, external=True),
+            torch.cuda.Event(enable_timing=True, external=True)) for _ in range(wl.layers)]
+
+    # eager warm-up (first-call device set-up), then capture one step as a graph
+    with torch.cuda.stream(stream):
+        wl.step(qx, stream)
+    torch.cuda.synchronize()
+    assert qx.qx_device_check(stream) == qx.QX_OK
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        wl.step(qx, stream)
+    # the same step with timing events around every launch of the dominant kernel
+    g_dom = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_dom, stream=stream):
+        wl.step(qx, stream, dom_events=dom)
+
+    # e2e graph: pinned host activations in, step, all outputs back
+    x_pin = torch.from_numpy(wl.x_host).pin_memory()
+    y_pin = torch.empty(wl.y_all.numel(), dtype=torch.float32).pin_memory()
+    ge = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ge, stream=stream):
+        wl.x_dev.copy_(x_pin, non_blocking=True)
+        wl.step(qx, stream)
+        y_pin.copy_(wl.y_all, non_blocking=True)
+
+    def timed(graph, steps):
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if ws > 1:
+            t = torch.tensor([ms], device="cuda")
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g.replay()
+        with ClockSampler(local) as clk:
+            ms = timed(g, args.steps)
+            # dominant kernel: mean over its launches in the last of K instrumented steps
+            timed(g_dom, args.steps)
+            dom_ms = [a.elapsed_time(b) for a, b in dom]
+        for _ in range(args.warmup):
+            ge.replay()
+        ms_e2e = timed(ge, args.steps)
+    st = qx.qx_device_check(stream)
+    if st != qx.QX_OK:
+        raise RuntimeError(f"device error after the timed region: {qx.qx_status_string(st)}")
+
+    hbm, _, peak_kind = measured_peaks()
+    ms_step = ms / args.steps
+    value = ws * wl.bytes_per_step * args.steps / (ms * 1e-3) / 1e9
+    value_e2e = ws * wl.bytes_per_step * args.steps / (ms_e2e * 1e-3) / 1e9
+    dom_mean_ms = statistics.mean(dom_ms)
+    achieved = wl.dominant_bytes / (dom_mean_ms * 1e-3) / 1e9
+    traffic = dominant_traffic()
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        cpu = wl.cpu_sample(oracle, budget_s=10.0)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "s8xu4/u6->s32 (dp4a) + f32 scales", "data": "synthetic",
+            "config": {"workload": wl.name, "weight_bytes_per_step": wl.bytes_per_step,
+                       "layers": wl.layers, "batch": 1, "launches_per_step": wl.launches_per_step,
+                       "activation_quantisation": "in-kernel (same codes as qx_quantize_act_q8)",
+                       "launch_overlap": "programmatic dependent launch",
+                       "l2": "inputs larger than L2 (4.41 GB of weights streamed per step)",
+                       "launch": "one CUDA graph per step", "parallelism": "replicas" if ws > 1 else "single"},
+            "pct_of_hbm_peak": value / ws / hbm,
+            "us_per_token": ms_step * 1e3,
+            "roofline": {"bound": "hbm", "kernel": wl.dominant, "achieved": achieved, "peak": hbm,
+                         "unit": "GB/s", "frac": achieved / hbm, "peak_kind": peak_kind,
+                         "bytes_per_launch": wl.dominant_bytes, "mean_launch_ms": dom_mean_ms,
+                         "traffic": traffic,
+                         "traffic_source": "profiles/gemv_q4k_w4a8_gateup_llama8b.md" if traffic else None},
+            "e2e": {"value": value_e2e, "unit": "GB/s", "h2d_bytes_per_step": int(wl.x_host.nbytes),
+                    "d2h_bytes_per_step": int(wl.y_all.numel() * 4), "ms_per_step": ms_e2e / args.steps},
+            "gpu_launches": wl.launches_per_step * args.steps,
+            "roofline_note": "dominant-kernel events come from a second timed pass of K steps (graph with "
+                             "event nodes); value comes from the uninstrumented graph",
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

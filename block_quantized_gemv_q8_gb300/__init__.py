@@ -15,7 +15,8 @@ from dataclasses import dataclass
 import torch
 
 QX_Q8_0, QX_Q4_K, QX_Q6_K = 8, 12, 14
-QX_MODE_F32, QX_MODE_W4A8 = 0, 1
+QX_MODE_F32, QX_MODE_W4A8, QX_MODE_W4A8_FUSED = 0, 1, 2
+QX_FLAG_PDL = 0x100
 QX_OK = 0
 QX_ERR_ARG, QX_ERR_FMT, QX_ERR_SHAPE, QX_ERR_ALIGN = -1, -2, -3, -4
 QX_ERR_MODE, QX_ERR_CUDA, QX_ERR_DEVICE_TIMEOUT, QX_ERR_UNSUPPORTED_DEVICE = -5, -6, -7, -8
@@ -26,13 +27,14 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libqx.so")
 
 EXPORTS = ["qx_quantize_act_q8", "qx_gemv", "qx_gemv_multi", "qx_gemm_prefill", "qx_gemm_prefill_ex",
            "qx_gemv_partials", "qx_row_bytes", "qx_device_check", "qx_debug_timeout_probe",
-           "qx_status_string", "qx_version"]
+           "qx_status_string", "qx_last_error", "qx_version"]
 
 
 class QxError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
-        super().__init__(f"{what}: {qx_status_string(status)} ({status})")
+        detail = f" [{qx_last_error()}]" if status == QX_ERR_CUDA else ""
+        super().__init__(f"{what}: {qx_status_string(status)} ({status}){detail}")
 
 
 class _Act(ctypes.Structure):
@@ -64,6 +66,8 @@ def lib() -> ctypes.CDLL:
         L.qx_debug_timeout_probe.argtypes = [ctypes.c_uint64, P]
         L.qx_status_string.argtypes = [I]
         L.qx_status_string.restype = ctypes.c_char_p
+        L.qx_last_error.argtypes = []
+        L.qx_last_error.restype = ctypes.c_char_p
         L.qx_version.argtypes = []
         L.qx_version.restype = ctypes.c_char_p
         for n in ("qx_quantize_act_q8", "qx_gemv", "qx_gemv_multi", "qx_gemm_prefill", "qx_gemm_prefill_ex",
@@ -137,6 +141,10 @@ def qx_status_string(st: int) -> str:
     return lib().qx_status_string(st).decode()
 
 
+def qx_last_error() -> str:
+    return lib().qx_last_error().decode()
+
+
 def qx_version() -> str:
     return lib().qx_version().decode()
 
@@ -154,9 +162,9 @@ def qx_quantize_act_q8(x: torch.Tensor, out: ActQ8 | None = None, stream=None) -
 
 
 def _x_arg(x, mode):
-    if mode == QX_MODE_F32:
+    if (mode & 0xFF) in (QX_MODE_F32, QX_MODE_W4A8_FUSED):
         if not isinstance(x, torch.Tensor) or x.dtype != torch.float32:
-            raise TypeError("f32 mode takes a float32 activation tensor")
+            raise TypeError("f32 and fused-W4A8 modes take a float32 activation tensor")
         return _ptr(x), None
     if not isinstance(x, ActQ8):
         raise TypeError("W4A8 mode takes an ActQ8 (from qx_quantize_act_q8)")
@@ -166,7 +174,10 @@ def _x_arg(x, mode):
 
 def qx_gemv(fmt: int, W: torch.Tensor, rows: int, cols: int, x, y: torch.Tensor | None = None,
             mode: int = QX_MODE_W4A8, stream=None) -> torch.Tensor:
-    """y[rows] = W . x for block-quantised W (uint8 bytes) in f32 or W4A8 mode."""
+    """y[rows] = W . x for block-quantised W (uint8 bytes).
+
+    mode: QX_MODE_F32 (x f32), QX_MODE_W4A8 (x an ActQ8) or QX_MODE_W4A8_FUSED
+    (x f32, quantised inside the launch), optionally | QX_FLAG_PDL."""
     y = y if y is not None else torch.empty(rows, dtype=torch.float32, device=W.device)
     xp, keep = _x_arg(x, mode)
     _check(lib().qx_gemv(fmt, _ptr(W), rows, cols, xp, _ptr(y), mode, _stream(stream)), "qx_gemv")

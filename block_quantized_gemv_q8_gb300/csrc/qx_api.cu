@@ -4,8 +4,11 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "../../include/qx.h"
 #include "qx_internal.h"
@@ -19,7 +22,9 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s bound on every pipeline wait
-constexpr size_t kStageTargetBytes = 24 * 1024;
+constexpr size_t kStageTargetBytes = 48 * 1024;
+// Shared memory of a CTA that leaves room for a second one on the SM.
+constexpr size_t kHalfSmBytes = 110 * 1024;
 constexpr int kMaxStageRows = 256;
 
 struct DeviceInfo {
@@ -32,22 +37,58 @@ struct DeviceInfo {
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 
+// Text of the last CUDA failure on this thread (returned by qx_last_error).
+thread_local char g_last_error[256] = "";
+
+qx_status cuda_fail(cudaError_t e, const char* where) {
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(e), int(e));
+    cudaGetLastError();  // clear a non-sticky error so that it is not reported twice
+    return QX_ERR_CUDA;
+}
+// Resident CTAs per SM, keyed by (device, format, mode, partials, smem bytes).
+std::map<std::tuple<int, int, int, int, size_t>, int> g_occupancy;
+
+qx_status ctas_per_sm(int fmt, int mode, bool partials, size_t smem, int* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    const auto key = std::make_tuple(dev, fmt, mode, partials ? 1 : 0, smem);
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        auto it = g_occupancy.find(key);
+        if (it != g_occupancy.end()) {
+            *out = it->second;
+            return QX_OK;
+        }
+    }
+    int n = 0;
+    if ((e = gemv_max_ctas_per_sm(fmt, mode, partials, smem, &n)) != cudaSuccess)
+        return cuda_fail(e, "occupancy query");
+    if (n < 1) return cuda_fail(cudaErrorInvalidConfiguration, "no CTA fits on an SM");
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_occupancy[key] = n;
+    *out = n;
+    return QX_OK;
+}
+
 // Query the current device once: capability, SM count, error word address.
 qx_status device_info(DeviceInfo** out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QX_ERR_CUDA;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice, "device ordinal");
     std::lock_guard<std::mutex> lock(g_mu);
     DeviceInfo& d = g_dev[dev];
     if (!d.ready) {
         int major = 0, minor = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return QX_ERR_CUDA;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
         d.supported = (major == 10 && minor == 3);
         if (d.supported) {
             void* p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return QX_ERR_CUDA;
+            if ((e = cudaGetSymbolAddress(&p, g_err_word)) != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
             d.err_word = static_cast<unsigned*>(p);
         }
         d.ready = true;
@@ -103,9 +144,16 @@ qx_status check_act(const qx_act_q8* a, int64_t m, int64_t cols) {
 }
 
 // Launch geometry of the streaming GEMV for one format/mode over a row space.
-qx_status gemv_geometry(int fmt, int mode, bool partials, int64_t cols, const DeviceInfo& dev, GemvParams& p,
-                        size_t& smem) {
-    const int C = gemv_cols_per_lane(fmt, mode);
+//   * A lane owns C columns, a team of lanes owns a row (several warps when
+//     the row is wider than 32 lanes, several teams per warp when narrower).
+//   * A stage is G whole rows (a multiple of the team count and of the rows
+//     that make a 16-byte multiple), about kStageTargetBytes.
+//   * W4A8 and Q8_0 launches keep each CTA within half an SM (registers and
+//     shared memory) and run two CTAs per SM; under QX_FLAG_PDL the next
+//     launch's CTAs take each SM's slots as this launch's CTAs leave them.
+qx_status gemv_geometry(int fmt, int kmode, bool partials, bool fused, bool pdl, int64_t cols,
+                        const DeviceInfo& dev, GemvParams& p, size_t& smem) {
+    const int C = gemv_cols_per_lane(fmt, kmode);
     if (cols % C) return QX_ERR_SHAPE;
     const int L = static_cast<int>(cols / C);
     int team_lanes, team_warps, nteams;
@@ -122,23 +170,36 @@ qx_status gemv_geometry(int fmt, int mode, bool partials, int64_t cols, const De
     }
     const int64_t rb = cols / block_weights(fmt) * block_bytes(fmt);
     const int quantum = static_cast<int>(16 / gcd64(rb, 16));
-    const int64_t base = int64_t(nteams) / gcd64(nteams, quantum) * quantum;  // lcm
+    // every team gets the same number of whole row groups per stage
+    const int64_t team_rows = int64_t(nteams) * (partials ? 1 : gemv_rows_per_call(fmt, kmode));
+    const int64_t base = team_rows / gcd64(team_rows, quantum) * quantum;  // lcm
     int64_t G = base;
     while (G + base <= kMaxStageRows && size_t((G + base) * rb) <= kStageTargetBytes) G += base;
     if (G > kMaxStageRows) G = base;  // very wide teams with tiny rows: keep one base group
     const size_t slot = (size_t(G * rb) + kSlotPad + 127) / 128 * 128;
-    const bool one_cta = (mode == QX_MODE_F32 && fmt != QX_Q8_0);
-    const size_t budget = one_cta ? 200 * 1024 : 96 * 1024;
-    int stages = static_cast<int>(budget / slot);
-    if (stages > 8) stages = 8;
-    if (stages < 2) stages = 2;
+    const bool half_sm = (kmode == QX_MODE_W4A8 || fmt == QX_Q8_0);
+    const size_t budget = half_sm ? kHalfSmBytes : 200 * 1024;
+    const size_t act = fused ? (size_t(cols) + size_t(cols / 32) * 8 + 15) / 16 * 16 : 0;
+    int stages = 2;
+    while (stages < 8) {
+        const int s1 = stages + 1;
+        const size_t red = team_warps > 1 ? size_t(s1) * G * (1 + team_warps) * 4 : 0;
+        if (size_t(s1) * slot + size_t(s1) * 16 + red + act > budget) break;
+        stages = s1;
+    }
     const size_t red = team_warps > 1 ? size_t(stages) * G * (1 + team_warps) * 4 : 0;
-    smem = size_t(stages) * slot + size_t(stages) * 16 + red;
+    p.bar_off = static_cast<int>(size_t(stages) * slot);
+    p.red_off = p.bar_off + 16 * stages;
+    p.act_off = static_cast<int>((size_t(p.red_off) + red + 15) / 16 * 16);
+    smem = size_t(p.act_off) + act;
     if (smem > 227 * 1024) return QX_ERR_SHAPE;
 
     int per_sm = 0;
-    if (gemv_max_ctas_per_sm(fmt, mode, partials, smem, &per_sm) != cudaSuccess || per_sm < 1) return QX_ERR_CUDA;
-    const int64_t max_cta = int64_t(dev.sm_count) * per_sm;
+    const qx_status occ = ctas_per_sm(fmt, kmode, partials, smem, &per_sm);
+    if (occ != QX_OK) return occ;
+    const int want = 2;
+    const int64_t max_cta = int64_t(dev.sm_count) * (per_sm < want ? per_sm : want);
+    (void)pdl;
     const int64_t groups = (p.total_rows + quantum - 1) / quantum;
     p.cols = cols;
     p.row_bytes = rb;
@@ -156,9 +217,10 @@ qx_status gemv_geometry(int fmt, int mode, bool partials, int64_t cols, const De
     return QX_OK;
 }
 
-// One streaming-GEMV launch over `n` matrices of the same format.
+// One streaming-GEMV launch over `n` matrices of the same format.  `mode` is
+// the public mode (flags already removed).
 qx_status run_gemv(int fmt, int n, const void* const* W, const int64_t* rows, int64_t cols, const void* x,
-                   float* const* y, int32_t* P, qx_mode mode, cudaStream_t s) {
+                   float* const* y, int32_t* P, int mode, bool pdl, cudaStream_t s) {
     DeviceInfo* dev = nullptr;
     qx_status st = device_info(&dev);
     if (st != QX_OK) return st;
@@ -175,8 +237,12 @@ qx_status run_gemv(int fmt, int n, const void* const* W, const int64_t* rows, in
         total += rows[k];
     }
     p.total_rows = total;
+    int kmode = QX_MODE_W4A8;
     if (mode == QX_MODE_F32) {
         p.x = static_cast<const float*>(x);
+        kmode = QX_MODE_F32;
+    } else if (mode == QX_MODE_W4A8_FUSED) {
+        p.xf = static_cast<const float*>(x);
     } else {
         const qx_act_q8* a = static_cast<const qx_act_q8*>(x);
         p.xq = a->q;
@@ -184,15 +250,24 @@ qx_status run_gemv(int fmt, int n, const void* const* W, const int64_t* rows, in
         p.xs = a->sum;
     }
     size_t smem = 0;
-    st = gemv_geometry(fmt, mode, P != nullptr, cols, *dev, p, smem);
+    st = gemv_geometry(fmt, kmode, P != nullptr, p.xf != nullptr, pdl, cols, *dev, p, smem);
     if (st != QX_OK) return st;
-    if (launch_gemv(fmt, mode, P != nullptr, p, smem, s) != cudaSuccess) return QX_ERR_CUDA;
+    const cudaError_t e = launch_gemv(fmt, kmode, P != nullptr, p, smem, s, pdl);
+    return e == cudaSuccess ? QX_OK : cuda_fail(e, "gemv launch");
+}
+
+// Split a public mode argument into the mode and the PDL flag.
+qx_status parse_mode(int mode_arg, int* mode, bool* pdl) {
+    if (mode_arg & ~(0xFF | QX_FLAG_PDL)) return QX_ERR_MODE;
+    *mode = mode_arg & 0xFF;
+    *pdl = (mode_arg & QX_FLAG_PDL) != 0;
+    if (*mode != QX_MODE_F32 && *mode != QX_MODE_W4A8 && *mode != QX_MODE_W4A8_FUSED) return QX_ERR_MODE;
     return QX_OK;
 }
 
-qx_status check_x(qx_mode mode, const void* x, int64_t cols) {
+qx_status check_x(int mode, const void* x, int64_t cols) {
     if (!x) return QX_ERR_ARG;
-    if (mode == QX_MODE_F32) return aligned16(x) ? QX_OK : QX_ERR_ALIGN;
+    if (mode == QX_MODE_F32 || mode == QX_MODE_W4A8_FUSED) return aligned16(x) ? QX_OK : QX_ERR_ALIGN;
     if (mode == QX_MODE_W4A8) return check_act(static_cast<const qx_act_q8*>(x), 1, cols);
     return QX_ERR_MODE;
 }
@@ -218,30 +293,34 @@ qx_status qx_quantize_act_q8(const float* x, int64_t m, int64_t cols, qx_act_q8*
     DeviceInfo* dev = nullptr;
     const qx_status st = device_info(&dev);
     if (st != QX_OK) return st;
-    if (launch_actq8(x, m * cols / 32, out->q, out->d, out->sum, dev->sm_count, reinterpret_cast<cudaStream_t>(s)) !=
-        cudaSuccess)
-        return QX_ERR_CUDA;
+    const cudaError_t e =
+        launch_actq8(x, m * cols / 32, out->q, out->d, out->sum, dev->sm_count, reinterpret_cast<cudaStream_t>(s));
+    if (e != cudaSuccess) return cuda_fail(e, "actq8 launch");
     out->m = m;
     out->cols = cols;
     return QX_OK;
 }
 
-qx_status qx_gemv(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const void* x, float* y, qx_mode mode,
+qx_status qx_gemv(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const void* x, float* y, qx_mode mode_arg,
                   qx_stream_t s) {
-    if (mode != QX_MODE_F32 && mode != QX_MODE_W4A8) return QX_ERR_MODE;
-    qx_status st = check_shape(fmt, rows, cols);
+    int mode;
+    bool pdl;
+    qx_status st = parse_mode(mode_arg, &mode, &pdl);
     if (st != QX_OK) return st;
+    if ((st = check_shape(fmt, rows, cols)) != QX_OK) return st;
     if (!W || !y) return QX_ERR_ARG;
     if (!aligned16(W) || !aligned4(y)) return QX_ERR_ALIGN;
     if ((st = check_x(mode, x, cols)) != QX_OK) return st;
-    return run_gemv(fmt, 1, &W, &rows, cols, x, &y, nullptr, mode, reinterpret_cast<cudaStream_t>(s));
+    return run_gemv(fmt, 1, &W, &rows, cols, x, &y, nullptr, mode, pdl, reinterpret_cast<cudaStream_t>(s));
 }
 
 qx_status qx_gemv_multi(int n, const qx_fmt* fmt, const void* const* W, const int64_t* rows, int64_t cols,
-                        const void* x, float* const* y, qx_mode mode, qx_stream_t s) {
+                        const void* x, float* const* y, qx_mode mode_arg, qx_stream_t s) {
     if (n < 1 || n > QX_MAX_MULTI || !fmt || !W || !rows || !y) return QX_ERR_ARG;
-    if (mode != QX_MODE_F32 && mode != QX_MODE_W4A8) return QX_ERR_MODE;
-    qx_status st;
+    int mode;
+    bool pdl;
+    qx_status st = parse_mode(mode_arg, &mode, &pdl);
+    if (st != QX_OK) return st;
     for (int k = 0; k < n; ++k) {
         if ((st = check_shape(fmt[k], rows[k], cols)) != QX_OK) return st;
         if (!W[k] || !y[k]) return QX_ERR_ARG;
@@ -263,7 +342,8 @@ qx_status qx_gemv_multi(int n, const qx_fmt* fmt, const void* const* W, const in
                 ++nf;
             }
         if (nf == 0) continue;
-        if ((st = run_gemv(f, nf, Wf, rf, cols, x, yf, nullptr, mode, reinterpret_cast<cudaStream_t>(s))) != QX_OK)
+        if ((st = run_gemv(f, nf, Wf, rf, cols, x, yf, nullptr, mode, pdl, reinterpret_cast<cudaStream_t>(s))) !=
+            QX_OK)
             return st;
     }
     return QX_OK;
@@ -276,7 +356,7 @@ qx_status qx_gemv_partials(qx_fmt fmt, const void* W, int64_t rows, int64_t cols
     if (!W || !P) return QX_ERR_ARG;
     if (!aligned16(W) || !aligned4(P)) return QX_ERR_ALIGN;
     if ((st = check_act(x, 1, cols)) != QX_OK) return st;
-    return run_gemv(fmt, 1, &W, &rows, cols, x, nullptr, P, QX_MODE_W4A8, reinterpret_cast<cudaStream_t>(s));
+    return run_gemv(fmt, 1, &W, &rows, cols, x, nullptr, P, QX_MODE_W4A8, false, reinterpret_cast<cudaStream_t>(s));
 }
 
 qx_status qx_gemm_prefill_ex(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, float* Y,
@@ -293,7 +373,7 @@ qx_status qx_gemm_prefill_ex(qx_fmt fmt, const void* W, int64_t rows, int64_t co
         qx_act_q8 row{X->q + m * cols, X->d + m * (cols / 32), X->sum + m * (cols / 32), 1, cols};
         if (!aligned16(row.q) || !aligned16(row.d) || !aligned16(row.sum)) return QX_ERR_ALIGN;
         float* ym = Y + m * rows;
-        if ((st = run_gemv(fmt, 1, &W, &rows, cols, &row, &ym, nullptr, QX_MODE_W4A8,
+        if ((st = run_gemv(fmt, 1, &W, &rows, cols, &row, &ym, nullptr, QX_MODE_W4A8, false,
                            reinterpret_cast<cudaStream_t>(s))) != QX_OK)
             return st;
     }
@@ -309,12 +389,15 @@ qx_status qx_device_check(qx_stream_t s) {
     DeviceInfo* dev = nullptr;
     const qx_status st = device_info(&dev);
     if (st != QX_OK) return st;
-    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(s)) != cudaSuccess) return QX_ERR_CUDA;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(s));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     unsigned word = 0;
-    if (cudaMemcpyFromSymbol(&word, g_err_word, sizeof(word)) != cudaSuccess) return QX_ERR_CUDA;
+    if ((e = cudaMemcpyFromSymbol(&word, g_err_word, sizeof(word))) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpyFromSymbol");
     if (word) {
         const unsigned zero = 0;
-        if (cudaMemcpyToSymbol(g_err_word, &zero, sizeof(zero)) != cudaSuccess) return QX_ERR_CUDA;
+        if ((e = cudaMemcpyToSymbol(g_err_word, &zero, sizeof(zero))) != cudaSuccess)
+            return cuda_fail(e, "cudaMemcpyToSymbol");
         return QX_ERR_DEVICE_TIMEOUT;
     }
     return QX_OK;
@@ -325,9 +408,8 @@ qx_status qx_debug_timeout_probe(uint64_t limit_ns, qx_stream_t s) {
     DeviceInfo* dev = nullptr;
     const qx_status st = device_info(&dev);
     if (st != QX_OK) return st;
-    return launch_timeout_probe(dev->err_word, limit_ns, reinterpret_cast<cudaStream_t>(s)) == cudaSuccess
-               ? QX_OK
-               : QX_ERR_CUDA;
+    const cudaError_t e = launch_timeout_probe(dev->err_word, limit_ns, reinterpret_cast<cudaStream_t>(s));
+    return e == cudaSuccess ? QX_OK : cuda_fail(e, "probe launch");
 }
 
 const char* qx_status_string(qx_status st) {
@@ -345,6 +427,8 @@ const char* qx_status_string(qx_status st) {
         default: return "unknown qx status";
     }
 }
+
+const char* qx_last_error(void) { return g_last_error; }
 
 const char* qx_version(void) {
     return "qx 0.1 sm_103a: actq8; gemv {q4_k,q6_k,q8_0} x {f32,w4a8} (bulk-copy stream); partials; multi";

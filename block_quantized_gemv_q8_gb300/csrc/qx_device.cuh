@@ -110,6 +110,115 @@ __device__ __forceinline__ int dp4a(uint32_t a, uint32_t b, int c) {
     return __dp4a(static_cast<int>(a), static_cast<int>(b), c);
 }
 
+// dp4a with the bytes of `a` unsigned (0..255) and the bytes of `b` signed.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Quantisation of an activation to int8 per block of 32 (llamay docs,
+// "Backends and hardware", section "CPU": the activation is quantised to int8
+// once per matmul):
+//   d = amax / 127 (IEEE round-to-nearest f32 division),
+//   q = round-half-even(fl(x / d)) with fl(x / d) the correctly rounded f32
+//       quotient, clamped to [-127, 127]; q = 0 when d == 0;
+//   sum = sum of the 32 quants.
+// Every kernel that quantises an activation goes through the functions
+// below, so their codes are identical.
+//
+// Rounding fl(x / d) without dividing: t = fl(x * fl(1 / d)) differs from
+// fl(x / d) by at most 3 * 2^-24 * |x / d| (three roundings of relative size
+// <= 2^-24), below 2.3e-5 when |t| <= 128.  When t lies farther than 2^-14
+// from every half-integer, fl(x / d) rounds to the same integer as t does.
+// Values that fail this test (about one in 10^4, and all values when 1 / d
+// overflows) take the correctly rounded quotient from __fdiv_rn instead.
+__device__ __forceinline__ bool quotient_rounding_is_safe(float t, float k) {
+    return fabsf(t) <= 128.0f && 0.5f - fabsf(t - k) > 6.103515625e-05f;
+}
+
+// Quantise N consecutive values of one block (N = 32 / threads per block);
+// amax over the block and the block's quant sum are combined across the
+// THREADS adjacent lanes that share the block (THREADS a power of two <= 32,
+// all lanes of the warp taking part).  A lane with live == false takes part in
+// the shuffles only and stores nothing; the lane holding the block's first
+// values (first == true) stores d and sum.
+template <int N, int THREADS>
+__device__ __forceinline__ void quantize_block_part(const float* __restrict__ x, int8_t* __restrict__ q,
+                                                    float* d, int32_t* sum, bool live, bool first) {
+    static_assert(N * THREADS == 32 && N % 4 == 0, "a block is 32 values, stored in 4-byte groups");
+    float v[N];
+    const float4* src = reinterpret_cast<const float4*>(x);
+#pragma unroll
+    for (int k = 0; k < N / 4; ++k) {
+        const float4 f = src[k];
+        v[4 * k + 0] = f.x;
+        v[4 * k + 1] = f.y;
+        v[4 * k + 2] = f.z;
+        v[4 * k + 3] = f.w;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < N; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+    for (int o = 1; o < THREADS; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float db = __fdiv_rn(amax, 127.0f);
+    float r[N];
+    unsigned slow = 0;
+    if (db != 0.0f) {
+        const float rcp = __frcp_rn(db);
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const float t = v[i] * rcp;
+            r[i] = rintf(t);
+            slow |= quotient_rounding_is_safe(t, r[i]) ? 0u : (1u << i);
+        }
+        if (slow) {
+#pragma unroll
+            for (int i = 0; i < N; ++i)
+                if (slow & (1u << i)) r[i] = rintf(__fdiv_rn(v[i], db));
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) r[i] = 0.0f;
+    }
+    uint32_t packed[N / 4];
+    int s = 0;
+#pragma unroll
+    for (int j = 0; j < N / 4; ++j) {
+        uint32_t w = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int qi = static_cast<int>(fminf(fmaxf(r[4 * j + i], -127.0f), 127.0f));
+            s += qi;
+            w |= (static_cast<uint32_t>(qi) & 0xFFu) << (8 * i);
+        }
+        packed[j] = w;
+    }
+#pragma unroll
+    for (int o = 1; o < THREADS; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (live) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(q);
+#pragma unroll
+        for (int j = 0; j < N / 4; ++j) dst[j] = packed[j];
+        if (first) {
+            *d = db;
+            *sum = s;
+        }
+    }
+}
+
+// Quantise blocks [0, nblocks) with two adjacent lanes per block, 16 values
+// each: `task` runs over 2 * nblocks in rounds of `stride` (a multiple of 32),
+// and every lane calls this the same number of times.  x, q: 16-byte aligned.
+__device__ __forceinline__ void quantize_task(const float* __restrict__ x, int64_t nblocks, int64_t task,
+                                              int8_t* __restrict__ q, float* d, int32_t* sum) {
+    const bool live = task < 2 * nblocks;
+    const int64_t b = live ? task >> 1 : nblocks - 1;
+    const int half = static_cast<int>(task & 1);
+    quantize_block_part<16, 2>(x + b * 32 + half * 16, q + b * 32 + half * 16, d + b, sum + b, live, half == 0);
+}
+
 // fp16 bit pattern -> f32 (exact; subnormals kept).
 __device__ __forceinline__ float f16_bits_to_f32(uint32_t bits16) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xFFFFu)));

@@ -43,19 +43,29 @@ struct GemvParams {
     const int8_t* xq;  // W4A8 activation quants [cols]
     const float* xd;   // W4A8 activation scales [cols/32]
     const int32_t* xs; // W4A8 activation block sums [cols/32]
+    const float* xf;   // W4A8 with in-kernel quantisation: f32 activation [cols]
+    int bar_off;       // shared-memory byte offsets: mbarriers,
+    int red_off;       //   cross-warp row sums,
+    int act_off;       //   quantised activation (in-kernel quantisation)
     unsigned* err;     // device error word
     uint64_t wait_ns;  // bound on every wait
 };
 
 // Columns owned by one lane, per (format, mode).
-constexpr int gemv_cols_per_lane(int fmt, int mode) {
+__host__ __device__ constexpr int gemv_cols_per_lane(int fmt, int mode) {
     return fmt == QX_Q8_0 ? 32 : (mode == QX_MODE_W4A8 ? 128 : 64);
+}
+
+// Rows a team computes per call, per (format, mode) (must match the kernels).
+__host__ __device__ constexpr int gemv_rows_per_call(int fmt, int mode) {
+    return (fmt == QX_Q8_0 || (fmt == QX_Q4_K && mode == QX_MODE_W4A8)) ? 2 : 1;
 }
 
 // Launchers (defined in the kernel translation units).
 cudaError_t launch_actq8(const float* x, int64_t nblocks, int8_t* q, float* d, int32_t* sum, int sm_count,
                          cudaStream_t s);
-cudaError_t launch_gemv(int fmt, int mode, bool partials, const GemvParams& p, size_t smem, cudaStream_t s);
+cudaError_t launch_gemv(int fmt, int mode, bool partials, const GemvParams& p, size_t smem, cudaStream_t s,
+                        bool pdl);
 cudaError_t gemv_max_ctas_per_sm(int fmt, int mode, bool partials, size_t smem, int* out);
 cudaError_t launch_timeout_probe(unsigned* err, uint64_t limit_ns, cudaStream_t s);
 

@@ -61,7 +61,17 @@ typedef struct CUstream_st* qx_stream_t;
 /* Format tags (the GGML type ids, a naming convention only). */
 typedef enum { QX_Q8_0 = 8, QX_Q4_K = 12, QX_Q6_K = 14 } qx_fmt;
 
-typedef enum { QX_MODE_F32 = 0, QX_MODE_W4A8 = 1 } qx_mode;
+typedef enum { QX_MODE_F32 = 0, QX_MODE_W4A8 = 1, QX_MODE_W4A8_FUSED = 2 } qx_mode;
+
+/*
+ * Launch flag, OR'd into the mode argument of qx_gemv and qx_gemv_multi.
+ * QX_FLAG_PDL: programmatic dependent launch.  The launch may start while the
+ * previous kernel in the stream is still running: it begins streaming its
+ * weights at once and reads x (and writes y) only after that kernel has
+ * completed and its memory is visible.  The caller guarantees that the
+ * previous kernel in the stream does not write W.
+ */
+#define QX_FLAG_PDL 0x100
 
 /* Status codes.  0 is success; every error is negative. */
 typedef int qx_status;
@@ -115,6 +125,11 @@ qx_status qx_quantize_act_q8(const float* x, int64_t m, int64_t cols, qx_act_q8*
  *   mode QX_MODE_W4A8: x is `const qx_act_q8*` (host struct) with m == 1 and
  *                      cols == cols, produced by qx_quantize_act_q8; y is the
  *                      per-block-scaled sum of exact integer partial sums.
+ *   mode QX_MODE_W4A8_FUSED: x is `const float*`, device, f32 [cols]; the
+ *                      launch quantises it itself with the arithmetic of
+ *                      qx_quantize_act_q8 (identical int8 codes) and then
+ *                      computes exactly what QX_MODE_W4A8 computes.
+ * mode may carry QX_FLAG_PDL.
  * cols must be a positive multiple of the block width (256 for Q4_K/Q6_K,
  * 32 for Q8_0) and at most QX_MAX_COLS; rows >= 1.
  */
@@ -178,6 +193,9 @@ qx_status qx_debug_timeout_probe(uint64_t limit_ns, qx_stream_t s);
 
 /* Static, NUL-terminated strings. */
 const char* qx_status_string(qx_status st);
+/* The CUDA call and error text behind the most recent QX_ERR_CUDA returned
+ * on the calling thread ("" if none); valid until the next call on it. */
+const char* qx_last_error(void);
 const char* qx_version(void);
 
 #ifdef __cplusplus

@@ -117,13 +117,14 @@ def quantize_act_q8(x: np.ndarray):
     return q, d, s
 
 
-def gemv_f32(fmt: int, W: np.ndarray, rows: int, cols: int, x: np.ndarray, threads: int | None = None):
-    """f32 mode: (y float64 [rows], absdot float64 [rows])."""
+def gemv_f32(fmt: int, W: np.ndarray, rows: int, cols: int, x: np.ndarray, threads: int | None = None,
+             with_absdot: bool = True):
+    """f32 mode: (y float64 [rows], absdot float64 [rows] or None)."""
     W = np.ascontiguousarray(W, dtype=np.uint8)
     x = np.ascontiguousarray(x, dtype=np.float32).reshape(cols)
     y = np.empty(rows, dtype=np.float64)
-    a = np.empty(rows, dtype=np.float64)
-    _check(lib().orc_gemv_f32(fmt, _p(W), rows, cols, _p(x), _p(y), _p(a),
+    a = np.empty(rows, dtype=np.float64) if with_absdot else None
+    _check(lib().orc_gemv_f32(fmt, _p(W), rows, cols, _p(x), _p(y), _p(a) if with_absdot else None,
                               threads or default_threads()), "gemv_f32")
     return y, a
 
@@ -148,14 +149,16 @@ def partials(fmt: int, W: np.ndarray, rows: int, cols: int, qx: np.ndarray) -> n
 
 
 def gemv_w4a8(fmt: int, W: np.ndarray, rows: int, cols: int, qx: np.ndarray, dx: np.ndarray,
-              threads: int | None = None):
-    """W4A8 mode from an already quantised activation: (y, absdot) float64 [rows]."""
+              threads: int | None = None, with_absdot: bool = True):
+    """W4A8 mode from an already quantised activation: (y, absdot) float64 [rows].
+
+    with_absdot=False skips the tolerance scale (absdot is then None)."""
     W = np.ascontiguousarray(W, dtype=np.uint8)
     qx = np.ascontiguousarray(qx, dtype=np.int8).reshape(cols)
     dx = np.ascontiguousarray(dx, dtype=np.float32).reshape(cols // 32)
     y = np.empty(rows, dtype=np.float64)
-    a = np.empty(rows, dtype=np.float64)
-    _check(lib().orc_gemv_w4a8(fmt, _p(W), rows, cols, _p(qx), _p(dx), _p(y), _p(a),
+    a = np.empty(rows, dtype=np.float64) if with_absdot else None
+    _check(lib().orc_gemv_w4a8(fmt, _p(W), rows, cols, _p(qx), _p(dx), _p(y), _p(a) if with_absdot else None,
                                threads or default_threads()), "gemv_w4a8")
     return y, a
 

@@ -58,6 +58,8 @@ def test_host_validation_rejects_before_launch(lib):
     # unknown format / mode
     assert lib.qx_gemv(99, P(A16), 4, 256, P(A16), P(A16), 0, s) == qx.QX_ERR_FMT
     assert lib.qx_gemv(qx.QX_Q4_K, P(A16), 4, 256, P(A16), P(A16), 7, s) == qx.QX_ERR_MODE
+    assert lib.qx_gemv(qx.QX_Q4_K, P(A16), 4, 256, P(A16), P(A16), 0x200 | 1, s) == qx.QX_ERR_MODE
+    assert lib.qx_gemv(qx.QX_Q4_K, P(A16), 4, 256, P(A16 + 4), P(A16), qx.QX_MODE_W4A8_FUSED, s) == qx.QX_ERR_ALIGN
     # shape: cols not whole blocks, too wide, rows < 1
     assert lib.qx_gemv(qx.QX_Q4_K, P(A16), 4, 896, P(A16), P(A16), 0, s) == qx.QX_ERR_SHAPE
     assert lib.qx_gemv(qx.QX_Q8_0, P(A16), 4, 40, P(A16), P(A16), 0, s) == qx.QX_ERR_SHAPE

@@ -73,6 +73,39 @@ def test_actq8_special_values():
     quantize_both(x)
 
 
+def near_tie_activation(nblocks: int, seed: int) -> np.ndarray:
+    """Blocks whose every value sits within 4 ulps of a half-integer multiple of
+    the block's scale d = amax / 127: the hardest inputs for the rounding rule."""
+    rng = np.random.default_rng(seed)
+    x = np.zeros((nblocks, 32), np.float32)
+    for b in range(nblocks):
+        amax = np.float32(rng.uniform(1e-3, 1e3))
+        d = np.float32(amax / np.float32(127))
+        k = rng.integers(-127, 127, size=31).astype(np.float64)
+        v = ((k + 0.5) * np.float64(d)).astype(np.float32)
+        v = (v.view(np.int32) + rng.integers(-4, 5, size=31).astype(np.int32)).view(np.float32)
+        v = np.clip(v, -amax, amax)
+        x[b, 0] = amax
+        x[b, 1:] = v
+    return x.reshape(1, -1)
+
+
+def test_actq8_near_ties_bit_exact():
+    quantize_both(near_tie_activation(4096, seed=5))
+
+
+def test_fused_quantisation_near_ties():
+    """In-kernel quantisation of near-tie activations matches the standalone kernel."""
+    fmt, rows = synth.Q8_0, 64
+    x = near_tie_activation(128, seed=6)  # 4096 columns
+    cols = x.shape[1]
+    W = dev(synth.weights(fmt, rows, cols, seed=7))
+    a, q, d, s = quantize_both(x)
+    y_two_step = qx.qx_gemv(fmt, W, rows, cols, a, mode=qx.QX_MODE_W4A8)
+    y_fused = qx.qx_gemv(fmt, W, rows, cols, dev(x[0]), mode=qx.QX_MODE_W4A8_FUSED)
+    assert np.array_equal(host(y_fused).view(np.uint32), host(y_two_step).view(np.uint32))
+
+
 # ------------------------------------------------------------------ GEMV ----
 
 SHAPES = {
@@ -115,6 +148,38 @@ def test_gemv_f32(fmt, rows, cols):
     y = qx.qx_gemv(fmt, dev(W), rows, cols, dev(x), mode=qx.QX_MODE_F32)
     ref, absdot = oracle.gemv_f32(fmt, W, rows, cols, x)
     assert_close(host(y), ref, absdot, f"f32 {synth.NAMES[fmt]} {rows}x{cols}")
+
+
+@pytest.mark.parametrize("fmt,rows,cols", CASES, ids=IDS)
+def test_gemv_fused_quantisation_is_bit_identical(fmt, rows, cols):
+    """In-kernel quantisation gives the same int8 codes, hence the same y, bit for bit."""
+    W = dev(synth.weights(fmt, rows, cols, seed=rows * 17 + cols))
+    x = synth.activation(1, cols, seed=cols + 9)
+    a, q, d, s = quantize_both(x)
+    y_two_step = qx.qx_gemv(fmt, W, rows, cols, a, mode=qx.QX_MODE_W4A8)
+    y_fused = qx.qx_gemv(fmt, W, rows, cols, dev(x[0]), mode=qx.QX_MODE_W4A8_FUSED)
+    y_fused_pdl = qx.qx_gemv(fmt, W, rows, cols, dev(x[0]), mode=qx.QX_MODE_W4A8_FUSED | qx.QX_FLAG_PDL)
+    assert np.array_equal(host(y_fused).view(np.uint32), host(y_two_step).view(np.uint32))
+    assert np.array_equal(host(y_fused_pdl).view(np.uint32), host(y_two_step).view(np.uint32))
+
+
+def test_pdl_chain_matches_plain_launches():
+    """A chain of PDL launches where each activation is produced by the previous kernel."""
+    fmt, rows, cols = synth.Q4_K, 4096, 4096
+    Ws = [dev(synth.weights(fmt, rows, cols, seed=70 + i)) for i in range(4)]
+    x0 = dev(synth.activation(1, cols, seed=75)[0])
+    outs = {}
+    for flag in (0, qx.QX_FLAG_PDL):
+        x = x0.clone()
+        ys = []
+        for W in Ws:
+            y = qx.qx_gemv(fmt, W, rows, cols, x, mode=qx.QX_MODE_W4A8_FUSED | flag)
+            ys.append(y)
+            x = y  # the next launch reads what this one wrote
+        outs[flag] = [host(t).view(np.uint32) for t in ys]
+    for a, b in zip(outs[0], outs[qx.QX_FLAG_PDL]):
+        assert np.array_equal(a, b)
+    assert qx.qx_device_check() == qx.QX_OK
 
 
 def test_gemv_zero_and_edge_values():
