@@ -1,17 +1,20 @@
 """Benchmark of the block-quantised GEMV library on one GB300 (or N replicas).
 
 Default workload: the GEMVs of a Llama-3.1-8B decode step at batch 1, Q4_K_M
-mix (Q4_K q/k/v/o/gate/up, Q6_K down), W4A8, 32 layers.  One step = for
-every layer: quantise the four activations, then q/k/v (one multi launch), o,
-gate/up (one multi launch), down.  Weights (4.41 GB per step) are resident in
-HBM and far larger than L2, so every step streams them from DRAM.
+mix (Q4_K q/k/v/o/gate/up, Q6_K down), W4A8, 32 layers: per layer q/k/v (one
+job of three matrices), o, gate/up (one job of two), down, each GEMV after the
+previous one completes.  The step runs as one chain launch (qx_gemv_chain);
+the same step as 128 separate launches with programmatic dependent launch is
+reported beside it.  `value` is the faster of the two forms (named in
+config.launch); both are in the JSON line.  Weights (4.41 GB per step) are resident in HBM and far
+larger than L2, so every step streams them from DRAM.
 
 Prints one JSON line:
   value       weight-GB/s over the timed region (device-resident inputs)
   e2e         the same metric through the public API with pinned host
               activations copied in and all outputs copied back every step
-  roofline    the dominant kernel (gate/up Q4_K W4A8 multi-GEMV): algorithmic
-              bytes per launch / its mean CUDA-event duration vs measured HBM
+  roofline    the dominant (only) kernel, the chain: algorithmic bytes per
+              launch / its CUDA-event duration vs measured HBM bandwidth
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
 
 `--impl reference` times the CPU oracle itself on the same metric.  Other
@@ -49,28 +52,37 @@ def measured_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-KERNEL_SOURCES = ["qx_gemv.cu", "qx_device.cuh", "qx_api.cu", "qx_internal.h"]
-DOMINANT_PROFILE = os.path.join(ROOT, "profiles", "gemv_q4k_w4a8_gateup_llama8b.md")
+CHAIN_SOURCES = ["qx_chain.cu", "qx_lanes.cuh", "qx_device.cuh", "qx_api.cu", "qx_internal.h"]
+CHAIN_PROFILE_NAME = "profiles/gemv_chain_llama8b.md"
 
 
-def dominant_traffic():
-    """DRAM bytes per launch of the dominant kernel from its committed ncu
-    summary, or None once the kernel sources differ from the captured ones."""
+def kernel_sources_hash(files) -> str:
     import hashlib
-    if not os.path.exists(DOMINANT_PROFILE):
-        return None
-    fields = {}
-    for line in open(DOMINANT_PROFILE):
-        if ":" in line and line.split(":", 1)[0] in ("traffic_bytes_per_launch", "source_sha256_16"):
-            k, v = line.split(":", 1)
-            fields[k] = v.strip()
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in files:
         with open(os.path.join(ROOT, "block_quantized_gemv_q8_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
-    if fields.get("source_sha256_16") != h.hexdigest()[:16]:
+    return h.hexdigest()[:16]
+
+
+def profile_fields(path):
+    fields = {}
+    if os.path.exists(path):
+        for line in open(path):
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+    return fields
+
+
+def chain_traffic(layers: int):
+    """DRAM bytes of one chain launch of `layers` layers from the committed ncu
+    summary of a smaller chain (traffic grows with the layers streamed), or
+    None once the kernel sources differ from the captured ones."""
+    f = profile_fields(os.path.join(ROOT, CHAIN_PROFILE_NAME))
+    if "traffic_bytes_per_layer" not in f or f.get("source_sha256_16") != kernel_sources_hash(CHAIN_SOURCES):
         return None
-    return int(fields["traffic_bytes_per_launch"])
+    return int(f["traffic_bytes_per_layer"]) * layers
 
 
 # ---------------------------------------------------------------- clocks ----
@@ -140,9 +152,8 @@ class LlamaDecode:
         self.shapes = {n: (f, r, c) for n, f, r, c in synth.LLAMA8B_LAYER}
         self.bytes_per_step = layers * sum(r * synth.row_bytes(f, c) for f, r, c in self.shapes.values())
         self.launches_per_step = layers * 4
-        g, u = self.shapes["gate"], self.shapes["up"]
-        self.dominant = "q4_k w4a8 multi-GEMV (gate+up, 2 x 14336 x 4096)"
-        self.dominant_bytes = g[1] * synth.row_bytes(g[0], g[2]) + u[1] * synth.row_bytes(u[0], u[2])
+        self.dominant = "gemv_chain_kernel (the whole step: 128 dependent W4A8 GEMV jobs)"
+        self.dominant_bytes = self.bytes_per_step
 
     def setup(self, qx, torch, seed_base: int = 0):
         self.W, self.y = [], []
@@ -185,8 +196,30 @@ class LlamaDecode:
             self.y[L][n] = self.y_all[off:off + r]
             off += r
 
+    def make_chain(self, qx):
+        F = qx.QX_Q4_K
+        jobs = []
+        for L in range(self.layers):
+            W, y, xv = self.W[L], self.y[L], self.x_views[L]
+            jobs.append(qx.GemvJob(F, [W["q"], W["k"], W["v"]], [4096, 1024, 1024], 4096, xv[0],
+                                   [y["q"], y["k"], y["v"]]))
+            jobs.append(qx.GemvJob(F, [W["o"]], [4096], 4096, xv[1], [y["o"]]))
+            jobs.append(qx.GemvJob(F, [W["gate"], W["up"]], [14336, 14336], 4096, xv[2], [y["gate"], y["up"]]))
+            jobs.append(qx.GemvJob(qx.QX_Q6_K, [W["down"]], [4096], 14336, xv[3], [y["down"]]))
+        self.jobs = jobs
+        self.chain = qx.make_chain(jobs)
+        self.scratch = qx.chain_scratch(len(jobs))
+
+    def step_chain(self, qx, stream, events=None):
+        """One decode step as one chain launch."""
+        if events is not None:
+            events[0].record(stream)
+        qx.qx_gemv_chain(self.jobs, self.scratch, stream=stream, marshalled=self.chain)
+        if events is not None:
+            events[1].record(stream)
+
     def step(self, qx, stream, dom_events=None):
-        """One decode step: per layer q/k/v (one launch), o, gate/up (one launch), down.
+        """One decode step as 128 launches: per layer q/k/v (one launch), o, gate/up (one launch), down.
 
         Each launch quantises its f32 activation in-kernel (W4A8) and is
         launched with programmatic dependent launch, so it streams its weights
@@ -305,29 +338,36 @@ def main():
 
     wl = LlamaDecode(layers=args.layers)
     wl.setup(qx, torch, seed_base=0)
+    wl.make_chain(qx)
     stream = torch.cuda.Stream()
-    # Timing events recorded inside the captured graph need external record nodes.
-    dom = [(torch.cuda.Event(enable_timing=True, external=True),
-            torch.cuda.Event(enable_timing=True, external=True)) for _ in range(wl.layers)]
+    # Timing events recorded inside a captured graph need external record nodes.
+    ev = (torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
 
-    # eager warm-up (first-call device set-up), then capture one step as a graph
+    # eager warm-up (first-call device set-up) of both step forms, then graphs
     with torch.cuda.stream(stream):
+        wl.step_chain(qx, stream)
         wl.step(qx, stream)
     torch.cuda.synchronize()
     assert qx.qx_device_check(stream) == qx.QX_OK
-    g = torch.cuda.CUDAGraph()
+    g = torch.cuda.CUDAGraph()                 # the step: one chain launch
     with torch.cuda.graph(g, stream=stream):
+        wl.step_chain(qx, stream)
+    g_ev = torch.cuda.CUDAGraph()              # the same with events around the launch
+    with torch.cuda.graph(g_ev, stream=stream):
+        wl.step_chain(qx, stream, events=ev)
+    g_pdl = torch.cuda.CUDAGraph()             # the step as 128 PDL launches
+    with torch.cuda.graph(g_pdl, stream=stream):
         wl.step(qx, stream)
-    # the same step with timing events around every launch of the dominant kernel
-    g_dom = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_dom, stream=stream):
-        wl.step(qx, stream, dom_events=dom)
-
     # e2e graph: pinned host activations in, step, all outputs back
     x_pin = torch.from_numpy(wl.x_host).pin_memory()
     y_pin = torch.empty(wl.y_all.numel(), dtype=torch.float32).pin_memory()
     ge = torch.cuda.CUDAGraph()
     with torch.cuda.graph(ge, stream=stream):
+        wl.x_dev.copy_(x_pin, non_blocking=True)
+        wl.step_chain(qx, stream)
+        y_pin.copy_(wl.y_all, non_blocking=True)
+    ge_pdl = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ge_pdl, stream=stream):
         wl.x_dev.copy_(x_pin, non_blocking=True)
         wl.step(qx, stream)
         y_pin.copy_(wl.y_all, non_blocking=True)
@@ -354,23 +394,38 @@ def main():
             g.replay()
         with ClockSampler(local) as clk:
             ms = timed(g, args.steps)
-            # dominant kernel: mean over its launches in the last of K instrumented steps
-            timed(g_dom, args.steps)
-            dom_ms = [a.elapsed_time(b) for a, b in dom]
+            # the chain kernel's own duration: events around its launch, each
+            # of K instrumented steps read back one by one
+            dom_ms = []
+            for _ in range(args.steps):
+                g_ev.replay()
+                ev[1].synchronize()
+                dom_ms.append(ev[0].elapsed_time(ev[1]))
+        for _ in range(args.warmup):
+            g_pdl.replay()
+        ms_pdl = timed(g_pdl, args.steps)
         for _ in range(args.warmup):
             ge.replay()
-        ms_e2e = timed(ge, args.steps)
+        ms_e2e_chain = timed(ge, args.steps)
+        for _ in range(args.warmup):
+            ge_pdl.replay()
+        ms_e2e_pdl = timed(ge_pdl, args.steps)
     st = qx.qx_device_check(stream)
     if st != qx.QX_OK:
         raise RuntimeError(f"device error after the timed region: {qx.qx_status_string(st)}")
+    assert int(wl.scratch.sum()) == 0
 
     hbm, _, peak_kind = measured_peaks()
-    ms_step = ms / args.steps
-    value = ws * wl.bytes_per_step * args.steps / (ms * 1e-3) / 1e9
-    value_e2e = ws * wl.bytes_per_step * args.steps / (ms_e2e * 1e-3) / 1e9
+    per_s = lambda m: ws * wl.bytes_per_step * args.steps / (m * 1e-3) / 1e9  # noqa: E731
+    value_chain, value_pdl = per_s(ms), per_s(ms_pdl)
+    chain_is_faster = ms <= ms_pdl
+    ms_e2e = ms_e2e_chain if chain_is_faster else ms_e2e_pdl
+    value_e2e = per_s(ms_e2e)
+    ms_best = ms if chain_is_faster else ms_pdl
+    value, ms_step = per_s(ms_best), ms_best / args.steps
     dom_mean_ms = statistics.mean(dom_ms)
     achieved = wl.dominant_bytes / (dom_mean_ms * 1e-3) / 1e9
-    traffic = dominant_traffic()
+    traffic = chain_traffic(wl.layers)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
@@ -381,23 +436,28 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "s8xu4/u6->s32 (dp4a) + f32 scales", "data": "synthetic",
             "config": {"workload": wl.name, "weight_bytes_per_step": wl.bytes_per_step,
-                       "layers": wl.layers, "batch": 1, "launches_per_step": wl.launches_per_step,
+                       "layers": wl.layers, "batch": 1, "jobs_per_step": len(wl.jobs),
+                       "launch": ("one qx_gemv_chain launch per step" if chain_is_faster else
+                                  "128 qx_gemv / qx_gemv_multi launches per step with programmatic dependent "
+                                  "launch") + ", captured in a CUDA graph",
                        "activation_quantisation": "in-kernel (same codes as qx_quantize_act_q8)",
-                       "launch_overlap": "programmatic dependent launch",
                        "l2": "inputs larger than L2 (4.41 GB of weights streamed per step)",
-                       "launch": "one CUDA graph per step", "parallelism": "replicas" if ws > 1 else "single"},
+                       "parallelism": "replicas" if ws > 1 else "single"},
             "pct_of_hbm_peak": value / ws / hbm,
             "us_per_token": ms_step * 1e3,
             "roofline": {"bound": "hbm", "kernel": wl.dominant, "achieved": achieved, "peak": hbm,
+                         "note": "the chain kernel carries the whole step, so it is the dominant kernel of "
+                                 "the chain form",
                          "unit": "GB/s", "frac": achieved / hbm, "peak_kind": peak_kind,
                          "bytes_per_launch": wl.dominant_bytes, "mean_launch_ms": dom_mean_ms,
                          "traffic": traffic,
-                         "traffic_source": "profiles/gemv_q4k_w4a8_gateup_llama8b.md" if traffic else None},
+                         "traffic_source": CHAIN_PROFILE_NAME if traffic else None},
             "e2e": {"value": value_e2e, "unit": "GB/s", "h2d_bytes_per_step": int(wl.x_host.nbytes),
                     "d2h_bytes_per_step": int(wl.y_all.numel() * 4), "ms_per_step": ms_e2e / args.steps},
-            "gpu_launches": wl.launches_per_step * args.steps,
-            "roofline_note": "dominant-kernel events come from a second timed pass of K steps (graph with "
-                             "event nodes); value comes from the uninstrumented graph",
+            "per_launch_pdl": {"value": value_pdl, "unit": "GB/s", "ms_per_step": ms_pdl / args.steps,
+                               "launches_per_step": wl.launches_per_step},
+            "chain": {"value": value_chain, "unit": "GB/s", "ms_per_step": ms / args.steps, "launches_per_step": 1},
+            "gpu_launches": args.steps * (1 if chain_is_faster else wl.launches_per_step),
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
         }

@@ -22,11 +22,14 @@ QX_ERR_ARG, QX_ERR_FMT, QX_ERR_SHAPE, QX_ERR_ALIGN = -1, -2, -3, -4
 QX_ERR_MODE, QX_ERR_CUDA, QX_ERR_DEVICE_TIMEOUT, QX_ERR_UNSUPPORTED_DEVICE = -5, -6, -7, -8
 QX_MAX_MULTI = 8
 QX_MAX_COLS = 32768
+QX_CHAIN_MAX_JOBS = 128
+QX_CHAIN_MAX_ENTRIES = 4
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libqx.so")
 
 EXPORTS = ["qx_quantize_act_q8", "qx_gemv", "qx_gemv_multi", "qx_gemm_prefill", "qx_gemm_prefill_ex",
-           "qx_gemv_partials", "qx_row_bytes", "qx_device_check", "qx_debug_timeout_probe",
+           "qx_gemv_partials", "qx_gemv_chain", "qx_gemv_chain_scratch_bytes", "qx_row_bytes",
+           "qx_device_check", "qx_debug_timeout_probe",
            "qx_status_string", "qx_last_error", "qx_version"]
 
 
@@ -40,6 +43,12 @@ class QxError(RuntimeError):
 class _Act(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("d", ctypes.c_void_p), ("sum", ctypes.c_void_p),
                 ("m", ctypes.c_int64), ("cols", ctypes.c_int64)]
+
+
+class _Job(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int), ("n", ctypes.c_int), ("W", ctypes.c_void_p * 4),
+                ("rows", ctypes.c_int64 * 4), ("y", ctypes.c_void_p * 4), ("cols", ctypes.c_int64),
+                ("x", ctypes.c_void_p)]
 
 
 _lib = None
@@ -60,6 +69,9 @@ def lib() -> ctypes.CDLL:
         L.qx_gemm_prefill.argtypes = [I, P, I64, I64, ctypes.POINTER(_Act), P, P]
         L.qx_gemm_prefill_ex.argtypes = [I, P, I64, I64, ctypes.POINTER(_Act), P, I, P]
         L.qx_gemv_partials.argtypes = [I, P, I64, I64, ctypes.POINTER(_Act), P, P]
+        L.qx_gemv_chain.argtypes = [I, ctypes.POINTER(_Job), P, P]
+        L.qx_gemv_chain_scratch_bytes.argtypes = [I]
+        L.qx_gemv_chain_scratch_bytes.restype = ctypes.c_size_t
         L.qx_row_bytes.argtypes = [I, I64]
         L.qx_row_bytes.restype = ctypes.c_size_t
         L.qx_device_check.argtypes = [P]
@@ -71,7 +83,7 @@ def lib() -> ctypes.CDLL:
         L.qx_version.argtypes = []
         L.qx_version.restype = ctypes.c_char_p
         for n in ("qx_quantize_act_q8", "qx_gemv", "qx_gemv_multi", "qx_gemm_prefill", "qx_gemm_prefill_ex",
-                  "qx_gemv_partials", "qx_device_check", "qx_debug_timeout_probe"):
+                  "qx_gemv_partials", "qx_gemv_chain", "qx_device_check", "qx_debug_timeout_probe"):
             getattr(L, n).restype = I
         _lib = L
     return _lib
@@ -221,6 +233,49 @@ def qx_gemm_prefill_ex(fmt: int, W: torch.Tensor, rows: int, cols: int, X: ActQ8
     _check(lib().qx_gemm_prefill_ex(fmt, _ptr(W), rows, cols, ctypes.byref(a), _ptr(Y), path, _stream(stream)),
            "qx_gemm_prefill_ex")
     return Y
+
+
+@dataclass
+class GemvJob:
+    """One job of a chain: y[k] = W[k] . x for its entries (W4A8, in-kernel quantisation)."""
+    fmt: int
+    W: list
+    rows: list
+    cols: int
+    x: torch.Tensor
+    y: list | None = None
+
+
+def qx_gemv_chain_scratch_bytes(n_jobs: int) -> int:
+    return int(lib().qx_gemv_chain_scratch_bytes(n_jobs))
+
+
+def chain_scratch(n_jobs: int, device=None) -> torch.Tensor:
+    """Zero-filled scratch for a chain of n_jobs (reusable across calls)."""
+    return torch.zeros(qx_gemv_chain_scratch_bytes(n_jobs), dtype=torch.uint8, device=device or "cuda")
+
+
+def make_chain(jobs) -> ctypes.Array:
+    """Marshal a list of GemvJob into the C array (outputs allocated if missing)."""
+    arr = (_Job * len(jobs))()
+    for j, job in enumerate(jobs):
+        if job.y is None:
+            job.y = [torch.empty(r, dtype=torch.float32, device=job.W[0].device) for r in job.rows]
+        c = arr[j]
+        c.fmt, c.n, c.cols = job.fmt, len(job.W), job.cols
+        for k, (W, r, y) in enumerate(zip(job.W, job.rows, job.y)):
+            c.W[k] = _ptr(W).value
+            c.rows[k] = r
+            c.y[k] = _ptr(y).value
+        c.x = _ptr(job.x).value
+    return arr
+
+
+def qx_gemv_chain(jobs, scratch: torch.Tensor, stream=None, marshalled=None):
+    """Run a chain of dependent GEMVs in one launch; returns the jobs (with y)."""
+    arr = marshalled if marshalled is not None else make_chain(jobs)
+    _check(lib().qx_gemv_chain(len(arr), arr, _ptr(scratch), _stream(stream)), "qx_gemv_chain")
+    return jobs
 
 
 def qx_device_check(stream=None) -> int:

@@ -3,6 +3,7 @@
 // in the kernels (qx_actq8.cu, qx_gemv.cu, qx_prefill.cu).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -25,6 +26,8 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s bound on every pipeli
 constexpr size_t kStageTargetBytes = 48 * 1024;
 // Shared memory of a CTA that leaves room for a second one on the SM.
 constexpr size_t kHalfSmBytes = 110 * 1024;
+// Shared memory of a chain CTA (one per SM).
+constexpr size_t kChainSmBytes = 200 * 1024;
 constexpr int kMaxStageRows = 256;
 
 struct DeviceInfo {
@@ -151,43 +154,55 @@ qx_status check_act(const qx_act_q8* a, int64_t m, int64_t cols) {
 //   * W4A8 and Q8_0 launches keep each CTA within half an SM (registers and
 //     shared memory) and run two CTAs per SM; under QX_FLAG_PDL the next
 //     launch's CTAs take each SM's slots as this launch's CTAs leave them.
-qx_status gemv_geometry(int fmt, int kmode, bool partials, bool fused, bool pdl, int64_t cols,
-                        const DeviceInfo& dev, GemvParams& p, size_t& smem) {
+// Teams and stage rows for one format/mode/width (see gemv_geometry).
+struct TeamGeom {
+    int L, team_lanes, team_warps, nteams, quantum;
+    int64_t rb, G;
+};
+
+qx_status team_geometry(int fmt, int kmode, bool partials, int64_t cols, int consumer_warps, TeamGeom& g) {
     const int C = gemv_cols_per_lane(fmt, kmode);
     if (cols % C) return QX_ERR_SHAPE;
-    const int L = static_cast<int>(cols / C);
-    int team_lanes, team_warps, nteams;
-    if (L <= 32) {
-        team_lanes = 1;
-        while (team_lanes < L) team_lanes <<= 1;
-        team_warps = 1;
-        nteams = kGemvConsumerWarps * (32 / team_lanes);
+    g.L = static_cast<int>(cols / C);
+    if (g.L <= 32) {
+        g.team_lanes = 1;
+        while (g.team_lanes < g.L) g.team_lanes <<= 1;
+        g.team_warps = 1;
+        g.nteams = consumer_warps * (32 / g.team_lanes);
     } else {
-        team_warps = (L + 31) / 32;
-        if (team_warps > kGemvConsumerWarps) return QX_ERR_SHAPE;
-        nteams = kGemvConsumerWarps / team_warps;
-        team_lanes = 32 * team_warps;
+        g.team_warps = (g.L + 31) / 32;
+        if (g.team_warps > consumer_warps) return QX_ERR_SHAPE;
+        g.nteams = consumer_warps / g.team_warps;
+        g.team_lanes = 32 * g.team_warps;
     }
-    const int64_t rb = cols / block_weights(fmt) * block_bytes(fmt);
-    const int quantum = static_cast<int>(16 / gcd64(rb, 16));
+    g.rb = cols / block_weights(fmt) * block_bytes(fmt);
+    g.quantum = static_cast<int>(16 / gcd64(g.rb, 16));
     // every team gets the same number of whole row groups per stage
-    const int64_t team_rows = int64_t(nteams) * (partials ? 1 : gemv_rows_per_call(fmt, kmode));
-    const int64_t base = team_rows / gcd64(team_rows, quantum) * quantum;  // lcm
-    int64_t G = base;
-    while (G + base <= kMaxStageRows && size_t((G + base) * rb) <= kStageTargetBytes) G += base;
-    if (G > kMaxStageRows) G = base;  // very wide teams with tiny rows: keep one base group
-    const size_t slot = (size_t(G * rb) + kSlotPad + 127) / 128 * 128;
+    const int64_t team_rows = int64_t(g.nteams) * (partials ? 1 : gemv_rows_per_call(fmt, kmode));
+    const int64_t base = team_rows / gcd64(team_rows, g.quantum) * g.quantum;  // lcm
+    g.G = base;
+    while (g.G + base <= kMaxStageRows && size_t((g.G + base) * g.rb) <= kStageTargetBytes) g.G += base;
+    if (g.G > kMaxStageRows) g.G = base;  // very wide teams with tiny rows: keep one base group
+    return QX_OK;
+}
+
+qx_status gemv_geometry(int fmt, int kmode, bool partials, bool fused, bool pdl, int64_t cols,
+                        const DeviceInfo& dev, GemvParams& p, size_t& smem) {
+    TeamGeom g;
+    qx_status st = team_geometry(fmt, kmode, partials, cols, kGemvConsumerWarps, g);
+    if (st != QX_OK) return st;
+    const size_t slot = (size_t(g.G * g.rb) + kSlotPad + 127) / 128 * 128;
     const bool half_sm = (kmode == QX_MODE_W4A8 || fmt == QX_Q8_0);
     const size_t budget = half_sm ? kHalfSmBytes : 200 * 1024;
     const size_t act = fused ? (size_t(cols) + size_t(cols / 32) * 8 + 15) / 16 * 16 : 0;
     int stages = 2;
     while (stages < 8) {
         const int s1 = stages + 1;
-        const size_t red = team_warps > 1 ? size_t(s1) * G * (1 + team_warps) * 4 : 0;
+        const size_t red = g.team_warps > 1 ? size_t(s1) * g.G * (1 + g.team_warps) * 4 : 0;
         if (size_t(s1) * slot + size_t(s1) * 16 + red + act > budget) break;
         stages = s1;
     }
-    const size_t red = team_warps > 1 ? size_t(stages) * G * (1 + team_warps) * 4 : 0;
+    const size_t red = g.team_warps > 1 ? size_t(stages) * g.G * (1 + g.team_warps) * 4 : 0;
     p.bar_off = static_cast<int>(size_t(stages) * slot);
     p.red_off = p.bar_off + 16 * stages;
     p.act_off = static_cast<int>((size_t(p.red_off) + red + 15) / 16 * 16);
@@ -195,23 +210,76 @@ qx_status gemv_geometry(int fmt, int kmode, bool partials, bool fused, bool pdl,
     if (smem > 227 * 1024) return QX_ERR_SHAPE;
 
     int per_sm = 0;
-    const qx_status occ = ctas_per_sm(fmt, kmode, partials, smem, &per_sm);
-    if (occ != QX_OK) return occ;
+    st = ctas_per_sm(fmt, kmode, partials, smem, &per_sm);
+    if (st != QX_OK) return st;
     const int want = 2;
     const int64_t max_cta = int64_t(dev.sm_count) * (per_sm < want ? per_sm : want);
     (void)pdl;
-    const int64_t groups = (p.total_rows + quantum - 1) / quantum;
+    const int64_t groups = (p.total_rows + g.quantum - 1) / g.quantum;
     p.cols = cols;
-    p.row_bytes = rb;
-    p.quantum = quantum;
-    p.G = static_cast<int>(G);
+    p.row_bytes = g.rb;
+    p.quantum = g.quantum;
+    p.G = static_cast<int>(g.G);
     p.stages = stages;
     p.slot_bytes = static_cast<int>(slot);
-    p.team_lanes = team_lanes;
-    p.team_warps = team_warps;
-    p.nteams = nteams;
-    p.L = L;
+    p.team_lanes = g.team_lanes;
+    p.team_warps = g.team_warps;
+    p.nteams = g.nteams;
+    p.L = g.L;
     p.n_cta = static_cast<int>(groups < max_cta ? groups : max_cta);
+    p.err = dev.err_word;
+    p.wait_ns = kDefaultWaitNs;
+    return QX_OK;
+}
+
+// Geometry of a chain: per-job teams and stage rows, one slot size and ring
+// depth for all jobs, one CTA row split per job over the same grid.
+qx_status chain_geometry(const DeviceInfo& dev, ChainParams& p, size_t& smem) {
+    size_t max_stage = 0;
+    int64_t max_cols = 0;
+    int Gmax = 1, max_tw = 1;
+    for (int j = 0; j < p.n_jobs; ++j) {
+        ChainJob& jb = p.job[j];
+        TeamGeom g;
+        const qx_status st = team_geometry(jb.fmt, QX_MODE_W4A8, false, jb.cols, kChainConsumerWarps, g);
+        if (st != QX_OK) return st;
+        jb.row_bytes = g.rb;
+        jb.quantum = g.quantum;
+        jb.G = static_cast<int>(g.G);
+        jb.team_lanes = g.team_lanes;
+        jb.team_warps = g.team_warps;
+        jb.nteams = g.nteams;
+        jb.L = g.L;
+        max_stage = std::max(max_stage, size_t(g.G * g.rb));
+        max_cols = std::max(max_cols, jb.cols);
+        Gmax = std::max(Gmax, jb.G);
+        max_tw = std::max(max_tw, jb.team_warps);
+    }
+    const size_t slot = (max_stage + kSlotPad + 127) / 128 * 128;
+    const size_t act = (size_t(max_cols) + size_t(max_cols / 32) * 8 + 15) / 16 * 16;
+    int stages = 2;
+    while (stages < 8) {
+        const int s1 = stages + 1;
+        const size_t red = size_t(s1) * Gmax * (1 + max_tw) * 4;
+        if (size_t(s1) * slot + size_t(s1) * 16 + red + act > kChainSmBytes) break;
+        stages = s1;
+    }
+    const size_t red = size_t(stages) * Gmax * (1 + max_tw) * 4;
+    p.stages = stages;
+    p.slot_bytes = static_cast<int>(slot);
+    p.Gmax = Gmax;
+    p.max_team_warps = max_tw;
+    p.max_cols = max_cols;
+    p.bar_off = static_cast<int>(size_t(stages) * slot);
+    p.red_off = p.bar_off + 16 * stages;
+    p.act_off = static_cast<int>((size_t(p.red_off) + red + 15) / 16 * 16);
+    smem = size_t(p.act_off) + act;
+    if (smem > 227 * 1024) return QX_ERR_SHAPE;
+    int per_sm = 0;
+    const cudaError_t e = chain_max_ctas_per_sm(smem, &per_sm);
+    if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+    if (per_sm < 1) return cuda_fail(cudaErrorInvalidConfiguration, "no CTA fits on an SM");
+    p.n_cta = dev.sm_count;  // one CTA per SM (the kernel is built for one)
     p.err = dev.err_word;
     p.wait_ns = kDefaultWaitNs;
     return QX_OK;
@@ -383,6 +451,50 @@ qx_status qx_gemm_prefill_ex(qx_fmt fmt, const void* W, int64_t rows, int64_t co
 qx_status qx_gemm_prefill(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, float* Y,
                           qx_stream_t s) {
     return qx_gemm_prefill_ex(fmt, W, rows, cols, X, Y, 0, s);
+}
+
+size_t qx_gemv_chain_scratch_bytes(int n_jobs) {
+    if (n_jobs < 1 || n_jobs > QX_CHAIN_MAX_JOBS) return 0;
+    return size_t(n_jobs + 1) * sizeof(unsigned);
+}
+
+qx_status qx_gemv_chain(int n_jobs, const qx_gemv_job* jobs, void* scratch, qx_stream_t s) {
+    if (n_jobs < 1 || n_jobs > QX_CHAIN_MAX_JOBS || !jobs || !scratch) return QX_ERR_ARG;
+    if (!aligned4(scratch)) return QX_ERR_ALIGN;
+    static thread_local ChainParams p;  // large (tens of KB): not on the stack
+    std::memset(&p, 0, sizeof(p));
+    p.n_jobs = n_jobs;
+    qx_status st;
+    for (int j = 0; j < n_jobs; ++j) {
+        const qx_gemv_job& in = jobs[j];
+        if (in.n < 1 || in.n > QX_CHAIN_MAX_ENTRIES) return QX_ERR_ARG;
+        if (!in.x) return QX_ERR_ARG;
+        if (!aligned16(in.x)) return QX_ERR_ALIGN;
+        ChainJob& jb = p.job[j];
+        jb.fmt = in.fmt;
+        jb.n_entries = in.n;
+        jb.cols = in.cols;
+        jb.x = in.x;
+        int64_t total = 0;
+        for (int k = 0; k < in.n; ++k) {
+            if ((st = check_shape(in.fmt, in.rows[k], in.cols)) != QX_OK) return st;
+            if (!in.W[k] || !in.y[k]) return QX_ERR_ARG;
+            if (!aligned16(in.W[k]) || !aligned4(in.y[k])) return QX_ERR_ALIGN;
+            jb.e[k].W = static_cast<const uint8_t*>(in.W[k]);
+            jb.e[k].y = in.y[k];
+            jb.e[k].rows = in.rows[k];
+            jb.e[k].row0 = total;
+            total += in.rows[k];
+        }
+        jb.total_rows = total;
+    }
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != QX_OK) return st;
+    size_t smem = 0;
+    if ((st = chain_geometry(*dev, p, smem)) != QX_OK) return st;
+    p.counters = static_cast<unsigned*>(scratch);
+    const cudaError_t e = launch_chain(p, smem, reinterpret_cast<cudaStream_t>(s));
+    return e == cudaSuccess ? QX_OK : cuda_fail(e, "chain launch");
 }
 
 qx_status qx_device_check(qx_stream_t s) {

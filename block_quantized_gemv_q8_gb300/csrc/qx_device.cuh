@@ -14,6 +14,7 @@ constexpr unsigned kErrTimeoutEmpty = 2u;  // producer waited too long for a fre
 constexpr unsigned kErrTimeoutDrain = 4u;  // copies still in flight at exit
 constexpr unsigned kErrTimeoutProbe = 8u;  // the test probe's wait ran out
 constexpr unsigned kErrTimeoutMma = 16u;   // tensor-core pipeline wait ran out
+constexpr unsigned kErrTimeoutChain = 32u; // a chain job waited too long for the previous job
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

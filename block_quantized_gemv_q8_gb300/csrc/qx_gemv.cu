@@ -27,414 +27,15 @@
 //     reassociated.
 #include "qx_device.cuh"
 #include "qx_internal.h"
+#include "qx_lanes.cuh"
 
 namespace qx {
 
 namespace {
 
+using namespace lanes;
 constexpr int NW = kGemvConsumerWarps;
 
-// Exact f32 value of a small non-negative integer n < 2^23, via the exponent
-// trick: the float with bits 0x4B000000 | n is 2^23 + n.
-__device__ __forceinline__ float small_uint_to_f32(uint32_t n) {
-    return __int_as_float(0x4B000000u | n) - 8388608.0f;
-}
-
-// N consecutive (possibly 2-byte aligned) little-endian words from shared
-// memory, read as N + 1 aligned words and funnel-shifted.
-template <int N>
-__device__ __forceinline__ void load_words(const uint8_t* p, uint32_t (&out)[N]) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-    const uint32_t sh = static_cast<uint32_t>(a & 3u) * 8u;
-    uint32_t prev = w[0];
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-        const uint32_t next = w[i + 1];
-        out[i] = __funnelshift_r(prev, next, sh);
-        prev = next;
-    }
-}
-
-__device__ __forceinline__ uint32_t byte_of(uint32_t w, int k) { return (w >> (8 * k)) & 0xFFu; }
-
-// Q4_K: the eight 6-bit scales and mins of a super-block, four per word.
-//   sc_lo / m_lo: sub-blocks 0..3,  sc_hi / m_hi: sub-blocks 4..7.
-struct Q4KScales {
-    uint32_t sc_lo, m_lo, sc_hi, m_hi;
-};
-
-__device__ __forceinline__ Q4KScales q4k_unpack_scales(uint32_t s0, uint32_t s1, uint32_t s2) {
-    Q4KScales r;
-    r.sc_lo = s0 & 0x3F3F3F3Fu;
-    r.m_lo = s1 & 0x3F3F3F3Fu;
-    r.sc_hi = (s2 & 0x0F0F0F0Fu) | ((s0 >> 2) & 0x30303030u);
-    r.m_hi = ((s2 >> 4) & 0x0F0F0F0Fu) | ((s1 >> 2) & 0x30303030u);
-    return r;
-}
-
-// ----------------------------------------------------------------------------
-// Per-(format, mode) lane work.  Each specialisation owns C columns per lane:
-//   load(): the activation slice into registers (once per kernel)
-//   row():  this lane's contribution to one row (or its integer partials)
-// ----------------------------------------------------------------------------
-template <int FMT, int MODE>
-struct Lane;
-
-// Q4_K, W4A8: 128 columns = half a super-block = sub-blocks 4h..4h+3.
-// Integer partials of the lane's four sub-blocks; the high-nibble ones are
-// formed as dot(16 * q, x) with the unsigned x signed dp4a and are exactly 16
-// times the partial.
-__device__ __forceinline__ void q4k_half_dots(const uint8_t* bp, int h, const uint32_t (&xq)[32], int (&P)[4]) {
-    const uint4* qsp = reinterpret_cast<const uint4*>(bp + 16 + 64 * h);
-#pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-        const uint4 a = qsp[2 * cc], b = qsp[2 * cc + 1];
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        int plo = 0, phi16 = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            plo = dp4a(w[i] & 0x0F0F0F0Fu, xq[16 * cc + i], plo);
-            phi16 = dp4a_us(w[i] & 0xF0F0F0F0u, xq[16 * cc + 8 + i], phi16);
-        }
-        P[2 * cc] = plo;
-        P[2 * cc + 1] = phi16;
-    }
-}
-
-template <>
-struct Lane<QX_Q4_K, QX_MODE_W4A8> {
-    static constexpr int C = 128;
-    static constexpr int kGroups = 4;  // partials per lane
-    static constexpr int kRows = 2;    // rows per call
-    uint32_t xq[32];
-    float dxs[4];  // dx of sub-block u; the odd (high-nibble) ones divided by 16
-    float t[4];    // dx * (sum of q_x) of sub-block u: weight of the min term
-    __device__ __forceinline__ void load(const int8_t* q, const float* d, const int32_t* s, int l) {
-        const uint4* src = reinterpret_cast<const uint4*>(q + int64_t(l) * C);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const uint4 v = src[k];
-            xq[4 * k + 0] = v.x;
-            xq[4 * k + 1] = v.y;
-            xq[4 * k + 2] = v.z;
-            xq[4 * k + 3] = v.w;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float dx = d[l * 4 + u];
-            dxs[u] = (u & 1) ? dx * 0.0625f : dx;
-            t[u] = dx * float(s[l * 4 + u]);
-        }
-    }
-    template <int R>
-    __device__ __forceinline__ void rows(const uint8_t* const (&rp)[R], int l, float (&out)[R]) const {
-        const int sb = l >> 1, h = l & 1;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const uint8_t* bp = rp[r] + sb * 144;
-            const uint4 hdr = *reinterpret_cast<const uint4*>(bp);
-            int P[4];
-            q4k_half_dots(bp, h, xq, P);
-            const Q4KScales S = q4k_unpack_scales(hdr.y, hdr.z, hdr.w);
-            const uint32_t scw = h ? S.sc_hi : S.sc_lo;
-            const uint32_t mw = h ? S.m_hi : S.m_lo;
-            float accd = 0.0f, accm = 0.0f;
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                accd = fmaf(float(P[u] * int(byte_of(scw, u))), dxs[u], accd);
-                accm = fmaf(float(int(byte_of(mw, u))), t[u], accm);
-            }
-            out[r] = f16_bits_to_f32(hdr.x) * accd - f16_bits_to_f32(hdr.x >> 16) * accm;
-        }
-    }
-    __device__ __forceinline__ void partials(const uint8_t* rowp, int l, int (&P)[kGroups]) const {
-        const int sb = l >> 1, h = l & 1;
-        q4k_half_dots(rowp + sb * 144, h, xq, P);
-        P[1] >>= 4;  // exact: the high-nibble dots are 16 x the partial
-        P[3] >>= 4;
-    }
-    __device__ __forceinline__ static int64_t part_index(int l, int g) { return int64_t(l) * 4 + g; }
-};
-
-// Q4_K, f32: 64 columns = one 32-byte chunk c of quants = sub-blocks 2c, 2c+1.
-template <>
-struct Lane<QX_Q4_K, QX_MODE_F32> {
-    static constexpr int C = 64;
-    static constexpr int kGroups = 1;
-    static constexpr int kRows = 1;
-    float x[64];
-    float xsum[2];
-    __device__ __forceinline__ void load(const float* xp, int l) {
-        const float4* src = reinterpret_cast<const float4*>(xp + int64_t(l) * C);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float4 v = src[k];
-            x[4 * k + 0] = v.x;
-            x[4 * k + 1] = v.y;
-            x[4 * k + 2] = v.z;
-            x[4 * k + 3] = v.w;
-        }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            float s = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) s += x[32 * u + i];
-            xsum[u] = s;
-        }
-    }
-    template <int R>
-    __device__ __forceinline__ void rows(const uint8_t* const (&rp)[R], int l, float (&out)[R]) const {
-        const int sb = l >> 2, c = l & 3;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const uint8_t* bp = rp[r] + sb * 144;
-            const uint4 hdr = *reinterpret_cast<const uint4*>(bp);
-            const uint4* qsp = reinterpret_cast<const uint4*>(bp + 16 + 32 * c);
-            const uint4 a = qsp[0], b = qsp[1];
-            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            float slo = 0.0f, shi = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    slo = fmaf(small_uint_to_f32((w[i] >> (8 * k)) & 15u), x[4 * i + k], slo);
-                    shi = fmaf(small_uint_to_f32((w[i] >> (8 * k + 4)) & 15u), x[32 + 4 * i + k], shi);
-                }
-            }
-            const Q4KScales S = q4k_unpack_scales(hdr.y, hdr.z, hdr.w);
-            const uint32_t scw = c < 2 ? S.sc_lo : S.sc_hi;
-            const uint32_t mw = c < 2 ? S.m_lo : S.m_hi;
-            const int k0 = 2 * (c & 1);
-            const float d = f16_bits_to_f32(hdr.x), dmin = f16_bits_to_f32(hdr.x >> 16);
-            float acc = d * float(byte_of(scw, k0)) * slo;
-            acc = fmaf(-dmin * float(byte_of(mw, k0)), xsum[0], acc);
-            acc = fmaf(d * float(byte_of(scw, k0 + 1)), shi, acc);
-            acc = fmaf(-dmin * float(byte_of(mw, k0 + 1)), xsum[1], acc);
-            out[r] = acc;
-        }
-    }
-};
-
-// Q6_K, W4A8: 128 columns = half h of a super-block = quarters t = 0..3 of
-// 32 columns, each made of two 16-weight scale groups.  The quants q are
-// dotted unsigned (0..63) and the -32 offset is applied as -32 * sum(q_x)
-// per group, which is the same integer.
-__device__ __forceinline__ void q6k_half_dots(const uint8_t* bp, int h, const uint32_t (&xq)[32],
-                                              const int (&s16)[8], int (&P)[8]) {
-    uint32_t ql[16], qh[8];
-    load_words<16>(bp + 64 * h, ql);
-    load_words<8>(bp + 128 + 32 * h, qh);
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        int pu[2] = {0, 0};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t src = ql[8 * (t & 1) + i];
-            const uint32_t lo4 = (t < 2 ? src : (src >> 4)) & 0x0F0F0F0Fu;
-            const uint32_t hi2 = ((qh[i] >> (2 * t)) & 0x03030303u) << 4;
-            pu[i >> 2] = dp4a_us(lo4 | hi2, xq[8 * t + i], pu[i >> 2]);
-        }
-        P[2 * t] = pu[0] - 32 * s16[2 * t];
-        P[2 * t + 1] = pu[1] - 32 * s16[2 * t + 1];
-    }
-}
-
-template <>
-struct Lane<QX_Q6_K, QX_MODE_W4A8> {
-    static constexpr int C = 128;
-    static constexpr int kGroups = 8;
-    static constexpr int kRows = 1;
-    uint32_t xq[32];
-    float dx[4];
-    int s16[8];  // sum of q_x over each 16-group
-    __device__ __forceinline__ void load(const int8_t* q, const float* d, const int32_t*, int l) {
-        const uint4* src = reinterpret_cast<const uint4*>(q + int64_t(l) * C);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const uint4 v = src[k];
-            xq[4 * k + 0] = v.x;
-            xq[4 * k + 1] = v.y;
-            xq[4 * k + 2] = v.z;
-            xq[4 * k + 3] = v.w;
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) dx[u] = d[l * 4 + u];
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-            int s = 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) s = dp4a(xq[4 * g + i], 0x01010101u, s);
-            s16[g] = s;
-        }
-    }
-    template <int R>
-    __device__ __forceinline__ void rows(const uint8_t* const (&rp)[R], int l, float (&out)[R]) const {
-        const int sb = l >> 1, h = l & 1;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const uint8_t* bp = rp[r] + sb * 210;
-            int P[8];
-            q6k_half_dots(bp, h, xq, s16, P);
-            uint32_t scw[2];
-            load_words<2>(bp + 192 + 8 * h, scw);
-            float acc = 0.0f;
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const int sc0 = int(int8_t(byte_of(scw[t >> 1], 2 * (t & 1))));
-                const int sc1 = int(int8_t(byte_of(scw[t >> 1], 2 * (t & 1) + 1)));
-                acc = fmaf(dx[t], float(sc0 * P[2 * t] + sc1 * P[2 * t + 1]), acc);
-            }
-            out[r] = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(bp + 208)) * acc;
-        }
-    }
-    __device__ __forceinline__ void partials(const uint8_t* rowp, int l, int (&P)[kGroups]) const {
-        const int sb = l >> 1, h = l & 1;
-        q6k_half_dots(rowp + sb * 210, h, xq, s16, P);
-    }
-    __device__ __forceinline__ static int64_t part_index(int l, int g) { return int64_t(l) * 8 + g; }
-};
-
-// Q6_K, f32: 64 columns = quarters t = tp and t = tp + 2 of half h (they
-// share the same ql bytes, low and high nibbles).
-template <>
-struct Lane<QX_Q6_K, QX_MODE_F32> {
-    static constexpr int C = 64;
-    static constexpr int kGroups = 1;
-    static constexpr int kRows = 1;
-    float x[64];
-    __device__ __forceinline__ void load(const float* xp, int l) {
-        const int sb = l >> 2, h = (l >> 1) & 1, tp = l & 1;
-        const int64_t c0 = int64_t(sb) * 256 + 128 * h + 32 * tp;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const float4* src = reinterpret_cast<const float4*>(xp + c0 + 64 * half);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float4 v = src[k];
-                x[32 * half + 4 * k + 0] = v.x;
-                x[32 * half + 4 * k + 1] = v.y;
-                x[32 * half + 4 * k + 2] = v.z;
-                x[32 * half + 4 * k + 3] = v.w;
-            }
-        }
-    }
-    template <int R>
-    __device__ __forceinline__ void rows(const uint8_t* const (&rp)[R], int l, float (&out)[R]) const {
-        const int sb = l >> 2, h = (l >> 1) & 1, tp = l & 1;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const uint8_t* bp = rp[r] + sb * 210;
-            uint32_t ql[8], qh[8], scw[2];
-            load_words<8>(bp + 64 * h + 32 * tp, ql);
-            load_words<8>(bp + 128 + 32 * h, qh);
-            load_words<2>(bp + 192 + 8 * h, scw);
-            float sg[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // lo g0, lo g1, hi g0, hi g1
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint32_t nlo = ((ql[i] >> (8 * k)) & 15u) | (((qh[i] >> (8 * k + 2 * tp)) & 3u) << 4);
-                    const uint32_t nhi =
-                        ((ql[i] >> (8 * k + 4)) & 15u) | (((qh[i] >> (8 * k + 2 * tp + 4)) & 3u) << 4);
-                    // exact q - 32 in f32: the float with bits 0x4B000000 | q is 2^23 + q
-                    sg[i >> 2] = fmaf(__int_as_float(0x4B000000u | nlo) - 8388640.0f, x[4 * i + k], sg[i >> 2]);
-                    sg[2 + (i >> 2)] =
-                        fmaf(__int_as_float(0x4B000000u | nhi) - 8388640.0f, x[32 + 4 * i + k], sg[2 + (i >> 2)]);
-                }
-            }
-            // scale bytes of this half: index 2t + g for t in {tp, tp + 2}
-            const int lo0 = 2 * tp, hi0 = 2 * tp + 4;
-            float acc = float(int(int8_t(byte_of(scw[lo0 >> 2], lo0 & 3)))) * sg[0];
-            acc = fmaf(float(int(int8_t(byte_of(scw[(lo0 + 1) >> 2], (lo0 + 1) & 3)))), sg[1], acc);
-            acc = fmaf(float(int(int8_t(byte_of(scw[hi0 >> 2], hi0 & 3)))), sg[2], acc);
-            acc = fmaf(float(int(int8_t(byte_of(scw[(hi0 + 1) >> 2], (hi0 + 1) & 3)))), sg[3], acc);
-            out[r] = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(bp + 208)) * acc;
-        }
-    }
-};
-
-// Q8_0, W4A8: 32 columns = one block.
-template <>
-struct Lane<QX_Q8_0, QX_MODE_W4A8> {
-    static constexpr int C = 32;
-    static constexpr int kGroups = 1;
-    static constexpr int kRows = 2;
-    uint32_t xq[8];
-    float dx;
-    __device__ __forceinline__ void load(const int8_t* q, const float* d, const int32_t*, int l) {
-        const uint4* src = reinterpret_cast<const uint4*>(q + int64_t(l) * C);
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const uint4 v = src[k];
-            xq[4 * k + 0] = v.x;
-            xq[4 * k + 1] = v.y;
-            xq[4 * k + 2] = v.z;
-            xq[4 * k + 3] = v.w;
-        }
-        dx = d[l];
-    }
-    __device__ __forceinline__ int dot(const uint8_t* bp) const {
-        uint32_t qs[8];
-        load_words<8>(bp + 2, qs);
-        int acc = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc = dp4a(qs[i], xq[i], acc);
-        return acc;
-    }
-    template <int R>
-    __device__ __forceinline__ void rows(const uint8_t* const (&rp)[R], int l, float (&out)[R]) const {
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const uint8_t* bp = rp[r] + l * 34;
-            out[r] = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(bp)) * dx * float(dot(bp));
-        }
-    }
-    __device__ __forceinline__ void partials(const uint8_t* rowp, int l, int (&P)[kGroups]) const {
-        P[0] = dot(rowp + l * 34);
-    }
-    __device__ __forceinline__ static int64_t part_index(int l, int) { return l; }
-};
-
-// Q8_0, f32: 32 columns = one block.
-template <>
-struct Lane<QX_Q8_0, QX_MODE_F32> {
-    static constexpr int C = 32;
-    static constexpr int kGroups = 1;
-    static constexpr int kRows = 2;
-    float x[32];
-    __device__ __forceinline__ void load(const float* xp, int l) {
-        const float4* src = reinterpret_cast<const float4*>(xp + int64_t(l) * C);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float4 v = src[k];
-            x[4 * k + 0] = v.x;
-            x[4 * k + 1] = v.y;
-            x[4 * k + 2] = v.z;
-            x[4 * k + 3] = v.w;
-        }
-    }
-    template <int R>
-    __device__ __forceinline__ void rows(const uint8_t* const (&rp)[R], int l, float (&out)[R]) const {
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const uint8_t* bp = rp[r] + l * 34;
-            uint32_t qs[8];
-            load_words<8>(bp + 2, qs);
-            float acc = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    // int8 -> f32 exactly: bias the byte by 128 into [0, 255].
-                    const uint32_t u = ((qs[i] >> (8 * k)) & 0xFFu) ^ 0x80u;
-                    acc = fmaf(__int_as_float(0x4B000000u | u) - 8388736.0f, x[4 * i + k], acc);
-                }
-            }
-            out[r] = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(bp)) * acc;
-        }
-    }
-};
 
 // ----------------------------------------------------------------------------
 // Work distribution
@@ -478,15 +79,11 @@ constexpr int gemv_min_blocks() {
     return (MODE == QX_MODE_W4A8 || FMT == QX_Q8_0) ? 2 : 1;
 }
 
-// Synchronise the consumer warps only (the producer warp never joins).
-__device__ __forceinline__ void consumer_barrier() {
-    asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory");
-}
-
 template <int FMT, int MODE, bool PART>
 __global__ void __launch_bounds__(kGemvThreads, gemv_min_blocks<FMT, MODE>())
     gemv_kernel(const __grid_constant__ GemvParams p) {
     using LaneT = Lane<FMT, MODE>;
+    static_assert(PART || LaneT::kRows == gemv_rows_per_call(FMT, MODE), "row count must match the host geometry");
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = p.stages;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
@@ -551,46 +148,34 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_min_blocks<FMT, MODE>())
     }
 
     // ---------------- consumers ----------------------------------------------
-    int team, slice;
-    if (p.team_warps == 1) {
-        team = warp * (32 / p.team_lanes) + lane / p.team_lanes;
-        slice = lane % p.team_lanes;
-    } else {
-        team = warp / p.team_warps;
-        slice = (warp % p.team_warps) * 32 + lane;
-    }
-    const bool in_team = team < p.nteams;
-    const bool active = in_team && slice < p.L;
+    const Team tm = make_team(warp, lane, p.team_lanes, p.team_warps, p.nteams, p.L);
 
     pdl_wait_prior_grid();  // the activation may come from the previous kernel
     LaneT X;
+    const int8_t* q = p.xq;
+    const float* d = p.xd;
+    const int32_t* s = p.xs;
     if constexpr (MODE == QX_MODE_W4A8) {
-        const int8_t* q = p.xq;
-        const float* d = p.xd;
-        const int32_t* s = p.xs;
         if (p.xf != nullptr) {
             // Quantise the f32 activation once per CTA into shared memory,
-            // with the same code as qx_quantize_act_q8.
+            // with the same code as qx_quantize_act_q8; two adjacent lanes
+            // per block of 32, all consumer lanes take part.
             int8_t* sq = reinterpret_cast<int8_t*>(smem + p.act_off);
             float* sd = reinterpret_cast<float*>(sq + p.cols);
             int32_t* ss = reinterpret_cast<int32_t*>(sd + p.cols / 32);
-            // two adjacent lanes per block of 32; all consumer lanes take part
             const int nblk = static_cast<int>(p.cols / 32);
             for (int base = 0; base < 2 * nblk; base += NW * 32)
                 quantize_task(p.xf, nblk, base + threadIdx.x, sq, sd, ss);
-            consumer_barrier();
+            consumer_barrier<NW>();
             q = sq;
             d = sd;
             s = ss;
         }
-        if (active) X.load(q, d, s, slice);
-    } else {
-        if (active) X.load(p.x, slice);
     }
+    if (tm.active) load_slice<MODE>(X, q, d, s, p.x, tm.slice);
 
-    constexpr int R = PART ? 1 : LaneT::kRows;
-    static_assert(PART || LaneT::kRows == gemv_rows_per_call(FMT, MODE), "row count must match the host geometry");
     const uint32_t rb = static_cast<uint32_t>(p.row_bytes);
+    const int64_t ng = p.cols / (FMT == QX_Q6_K ? 16 : 32);
     StageWalker wk{r0, r1, 0};
     int e, nrows;
     int64_t lrow;
@@ -598,81 +183,15 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_min_blocks<FMT, MODE>())
         const int slot = k % S;
         if (!mbar_wait_bounded(&full[slot], (k / S) & 1, p.wait_ns, p.err, kErrTimeoutFull)) break;
         const uint8_t* sbuf = smem + size_t(slot) * p.slot_bytes;
-        for (int ib = 0; ib < nrows; ib += p.nteams * R) {
-            int ir[R];
-            bool vr[R];
-            const uint8_t* rp[R];
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                ir[r] = ib + team + r * p.nteams;
-                vr[r] = in_team && ir[r] < nrows;
-                rp[r] = sbuf + (vr[r] ? uint32_t(ir[r]) : 0u) * rb;
-            }
-            if constexpr (PART) {
-                if (vr[0] && active) {
-                    int P[LaneT::kGroups];
-                    X.partials(rp[0], slice, P);
-                    const int64_t ng = p.cols / (FMT == QX_Q6_K ? 16 : 32);
-                    int32_t* dst = p.e[e].P + (lrow + ir[0]) * ng;
-#pragma unroll
-                    for (int g = 0; g < LaneT::kGroups; ++g) dst[LaneT::part_index(slice, g)] = P[g];
-                }
-                continue;
-            } else {
-                float v[R];
-                if (active) {
-                    X.template rows<R>(rp, slice, v);
-                } else {
-#pragma unroll
-                    for (int r = 0; r < R; ++r) v[r] = 0.0f;
-                }
-                float* yb = p.e[e].y + lrow;
-                if (p.team_warps == 1) {
-                    if (R == 2 && p.team_lanes == 32) {
-                        // two rows in one butterfly: lanes 0-15 end with row 0, 16-31 with row 1
-                        float a = (lane & 16) ? v[R - 1] : v[0];
-                        const float b = (lane & 16) ? v[0] : v[R - 1];
-                        a += __shfl_xor_sync(0xffffffffu, b, 16);
-#pragma unroll
-                        for (int o = 8; o >= 1; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-                        if (lane == 0 && vr[0]) yb[ir[0]] = a;
-                        if (lane == 16 && vr[R - 1]) yb[ir[R - 1]] = a;
-                    } else {
-#pragma unroll
-                        for (int r = 0; r < R; ++r) {
-                            for (int o = p.team_lanes >> 1; o >= 1; o >>= 1)
-                                v[r] += __shfl_xor_sync(0xffffffffu, v[r], o);
-                            if (vr[r] && slice == 0) yb[ir[r]] = v[r];
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-#pragma unroll
-                        for (int o = 16; o >= 1; o >>= 1) v[r] += __shfl_xor_sync(0xffffffffu, v[r], o);
-                        if (vr[r] && lane == 0) {
-                            const int ri = slot * p.G + ir[r];
-                            float* rbuf = red + ri * p.team_warps;
-                            rbuf[warp % p.team_warps] = v[r];
-                            __threadfence_block();
-                            if (atomicAdd(&red_cnt[ri], 1) == p.team_warps - 1) {
-                                __threadfence_block();
-                                float sum = 0.0f;
-                                for (int w = 0; w < p.team_warps; ++w) sum += rbuf[w];
-                                yb[ir[r]] = sum;
-                                red_cnt[ri] = 0;
-                            }
-                        }
-                    }
-                }
-            }
-        }
+        consume_stage<FMT, MODE, PART>(X, tm, sbuf, nrows, rb, warp, lane, PART ? nullptr : p.e[e].y + lrow,
+                                       PART ? p.e[e].P + lrow * ng : nullptr, ng, red_cnt + slot * p.G,
+                                       red + slot * p.G * p.team_warps);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
     }
 }
 
-// Largest dynamic shared memory a CTA may use on sm_103a.
+// Largest shared memory (static + dynamic) a CTA may use on sm_103a.
 constexpr int kMaxDynamicSmem = 227 * 1024;
 
 // Raise the kernel's dynamic shared-memory limit to the maximum, once per
@@ -686,8 +205,11 @@ cudaError_t configure_once() {
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (done[dev]) return cudaSuccess;
+    cudaFuncAttributes fa;
+    err = cudaFuncGetAttributes(&fa, gemv_kernel<FMT, MODE, PART>);
+    if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(gemv_kernel<FMT, MODE, PART>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kMaxDynamicSmem);
+                               kMaxDynamicSmem - static_cast<int>(fa.sharedSizeBytes));
     if (err == cudaSuccess) done[dev] = true;
     return err;
 }

@@ -13,6 +13,9 @@ namespace qx {
 // Consumer warps per GEMV CTA (one more warp issues the bulk copies).
 constexpr int kGemvConsumerWarps = 8;
 constexpr int kGemvThreads = 32 * (kGemvConsumerWarps + 1);
+// Consumer warps per chain CTA (one CTA per SM; one more warp issues copies).
+constexpr int kChainConsumerWarps = 12;
+constexpr int kChainThreads = 32 * (kChainConsumerWarps + 1);
 // Bytes read past the end of a shared-memory slot by the unaligned-word loads.
 constexpr int kSlotPad = 16;
 
@@ -56,6 +59,31 @@ __host__ __device__ constexpr int gemv_cols_per_lane(int fmt, int mode) {
     return fmt == QX_Q8_0 ? 32 : (mode == QX_MODE_W4A8 ? 128 : 64);
 }
 
+// A chain of dependent W4A8 GEMVs in one launch (qx_gemv_chain).
+struct ChainJob {
+    GemvEntry e[QX_CHAIN_MAX_ENTRIES];  // P unused
+    const float* x;                      // f32 activation [cols], quantised in-kernel
+    int64_t cols;
+    int64_t row_bytes;
+    int64_t total_rows;
+    int fmt, n_entries, team_lanes, team_warps, nteams, quantum, G, L;
+};
+
+struct ChainParams {
+    int n_jobs;
+    int n_cta;
+    int stages;
+    int slot_bytes;
+    int bar_off, red_off, act_off;
+    int Gmax;            // most rows of any job's stage
+    int max_team_warps;  // most warps of any job's team
+    int64_t max_cols;    // widest activation (size of the quantised-activation area)
+    unsigned* counters;  // caller scratch: [n_jobs + 1] arrival counters, zero on entry and exit
+    unsigned* err;
+    uint64_t wait_ns;
+    ChainJob job[QX_CHAIN_MAX_JOBS];
+};
+
 // Rows a team computes per call, per (format, mode) (must match the kernels).
 __host__ __device__ constexpr int gemv_rows_per_call(int fmt, int mode) {
     return (fmt == QX_Q8_0 || (fmt == QX_Q4_K && mode == QX_MODE_W4A8)) ? 2 : 1;
@@ -68,5 +96,7 @@ cudaError_t launch_gemv(int fmt, int mode, bool partials, const GemvParams& p, s
                         bool pdl);
 cudaError_t gemv_max_ctas_per_sm(int fmt, int mode, bool partials, size_t smem, int* out);
 cudaError_t launch_timeout_probe(unsigned* err, uint64_t limit_ns, cudaStream_t s);
+cudaError_t launch_chain(const ChainParams& p, size_t smem, cudaStream_t s);
+cudaError_t chain_max_ctas_per_sm(size_t smem, int* out);
 
 }  // namespace qx

@@ -176,6 +176,44 @@ qx_status qx_gemm_prefill_ex(qx_fmt fmt, const void* W, int64_t rows, int64_t co
 qx_status qx_gemv_partials(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* x,
                            int32_t* P, qx_stream_t s);
 
+/*
+ * A chain of dependent GEMVs in one launch.  Decode runs its GEMVs one after
+ * another, each reading what an earlier one wrote (llamay docs, "Backends and
+ * hardware": decode streams every weight once per token; VKNN wiki, "Running
+ * an LLM on VKNN", section "Performance": the decode step is
+ * weight-bandwidth-bound).  Separate launches pay a launch, a prologue and a
+ * tail each; a chain streams the weights of job j + 1 while job j finishes.
+ *
+ * Job j computes y[k] = W[k] . x for its n entries (one format, shared cols
+ * and x, like qx_gemv_multi) in W4A8 mode with the activation quantised
+ * inside the launch (QX_MODE_W4A8_FUSED).  Job j + 1 reads its x only after
+ * every write of job j has completed, so its x may be (part of) job j's y.
+ */
+#define QX_CHAIN_MAX_JOBS 128
+#define QX_CHAIN_MAX_ENTRIES 4
+typedef struct {
+    qx_fmt fmt;
+    int n;                                  /* entries, 1..QX_CHAIN_MAX_ENTRIES */
+    const void* W[QX_CHAIN_MAX_ENTRIES];    /* device, 16-byte aligned          */
+    int64_t rows[QX_CHAIN_MAX_ENTRIES];
+    float* y[QX_CHAIN_MAX_ENTRIES];         /* device, f32 [rows], 4-byte aligned */
+    int64_t cols;
+    const float* x;                         /* device, f32 [cols], 16-byte aligned */
+} qx_gemv_job;
+
+/* Device scratch bytes a chain of n_jobs needs (arrival counters). */
+size_t qx_gemv_chain_scratch_bytes(int n_jobs);
+
+/*
+ * Run jobs[0 .. n_jobs) in order as one cooperative launch (all CTAs
+ * resident).  `scratch` is caller-owned device memory of at least
+ * qx_gemv_chain_scratch_bytes(n_jobs) bytes, zero-filled before the first
+ * call; a call that completes leaves it zero-filled again.  Calls that may
+ * overlap on the GPU need separate scratch.  After QX_ERR_DEVICE_TIMEOUT the
+ * scratch must be zero-filled again.  1 <= n_jobs <= QX_CHAIN_MAX_JOBS.
+ */
+qx_status qx_gemv_chain(int n_jobs, const qx_gemv_job* jobs, void* scratch, qx_stream_t s);
+
 /* Bytes of one row of `cols` weights, or 0 if fmt is unknown or cols is not
  * a positive multiple of the block width. */
 size_t qx_row_bytes(qx_fmt fmt, int64_t cols);

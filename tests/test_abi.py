@@ -25,7 +25,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ["qx_quantize_act_q8", "qx_gemv", "qx_gemv_multi", "qx_gemm_prefill", "qx_gemv_partials"]:
+    for n in ["qx_quantize_act_q8", "qx_gemv", "qx_gemv_multi", "qx_gemm_prefill", "qx_gemv_partials",
+              "qx_gemv_chain"]:
         assert n in names
 
 
