@@ -546,4 +546,89 @@ const char* qx_version(void) {
     return "qx 0.1 sm_103a: actq8; gemv {q4_k,q6_k,q8_0} x {f32,w4a8} (bulk-copy stream); partials; multi";
 }
 
+// ----------------------------------------------------------------------------
+// qx_gemv_chain_noalloc: qx_gemv_chain with library-owned scratch.
+//
+// qx_gemv_chain needs a few hundred bytes of device scratch for its per-job
+// arrival counters, which its caller allocates.  Some callers cannot
+// allocate device memory at the point where they run a chain: code that
+// executes while a CUDA graph is being captured (cudaMalloc is not allowed
+// there), runtimes that hand out device memory only from a fixed pool set up
+// at start, or plug-ins that may not touch the process's allocator.  For
+// them the counters live in the array below, which every GPU that loads the
+// library holds until the process exits.
+// ----------------------------------------------------------------------------
+
+// Largest chain the array serves (one counter per job plus one exit counter).
+constexpr int kNoallocMaxJobs = QX_CHAIN_MAX_JOBS;
+static __device__ __align__(256) unsigned g_noalloc_counters[kNoallocMaxJobs + 1];
+
+namespace {
+std::mutex g_noalloc_mu;
+unsigned* g_noalloc_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the counter array on the current device, looked up once
+// per device (with that device current) and cached.
+qx_status noalloc_counters(unsigned** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice, "device ordinal");
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        unsigned* ptr = nullptr;
+        e = cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_counters);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return QX_OK;
+}
+}  // namespace
+
+qx_status qx_gemv_chain_noalloc(int n_jobs, const qx_gemv_job* jobs, qx_stream_t s) {
+    if (n_jobs < 1 || n_jobs > kNoallocMaxJobs || !jobs) return QX_ERR_ARG;
+    static thread_local ChainParams p;  // large (tens of KB): not on the stack
+    std::memset(&p, 0, sizeof(p));
+    p.n_jobs = n_jobs;
+    qx_status st;
+    for (int j = 0; j < n_jobs; ++j) {
+        const qx_gemv_job& in = jobs[j];
+        if (in.n < 1 || in.n > QX_CHAIN_MAX_ENTRIES) return QX_ERR_ARG;
+        if (!in.x) return QX_ERR_ARG;
+        if (!aligned16(in.x)) return QX_ERR_ALIGN;
+        ChainJob& jb = p.job[j];
+        jb.fmt = in.fmt;
+        jb.n_entries = in.n;
+        jb.cols = in.cols;
+        jb.x = in.x;
+        int64_t total = 0;
+        for (int k = 0; k < in.n; ++k) {
+            if ((st = check_shape(in.fmt, in.rows[k], in.cols)) != QX_OK) return st;
+            if (!in.W[k] || !in.y[k]) return QX_ERR_ARG;
+            if (!aligned16(in.W[k]) || !aligned4(in.y[k])) return QX_ERR_ALIGN;
+            jb.e[k].W = static_cast<const uint8_t*>(in.W[k]);
+            jb.e[k].y = in.y[k];
+            jb.e[k].rows = in.rows[k];
+            jb.e[k].row0 = total;
+            total += in.rows[k];
+        }
+        jb.total_rows = total;
+    }
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != QX_OK) return st;
+    size_t smem = 0;
+    if ((st = chain_geometry(*dev, p, smem)) != QX_OK) return st;
+    unsigned* counters = nullptr;
+    if ((st = noalloc_counters(&counters)) != QX_OK) return st;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+    // The array keeps whatever the previous call left; the counters must
+    // start at zero.
+    cudaError_t e = cudaMemsetAsync(counters, 0, size_t(n_jobs + 1) * sizeof(unsigned), cs);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    p.counters = counters;
+    e = launch_chain(p, smem, cs);
+    return e == cudaSuccess ? QX_OK : cuda_fail(e, "chain launch");
+}
+
 }  // extern "C"

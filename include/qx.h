@@ -214,6 +214,29 @@ size_t qx_gemv_chain_scratch_bytes(int n_jobs);
  */
 qx_status qx_gemv_chain(int n_jobs, const qx_gemv_job* jobs, void* scratch, qx_stream_t s);
 
+/*
+ * qx_gemv_chain without caller scratch: for callers that cannot allocate
+ * device memory where they run a chain -- code running during CUDA graph
+ * capture, where cudaMalloc is not allowed; runtimes that only hand out
+ * memory from a pool fixed at start-up; plug-ins that must not use the
+ * process's allocator.  (The pages have no counterpart: this is a library
+ * convenience, not part of the method.)
+ *
+ * Same jobs and results as qx_gemv_chain.  The arrival counters live in a
+ * fixed array inside the library (QX_CHAIN_MAX_JOBS + 1 words on every GPU
+ * that loads the library, held until the process exits); the call allocates
+ * nothing, and clears the counters on stream s before each launch.
+ *   - n_jobs above QX_CHAIN_MAX_JOBS (the array's capacity) returns
+ *     QX_ERR_ARG before anything is launched.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture on the device.
+ *   - Every call on a device shares the one array: calls that may overlap on
+ *     the GPU (different streams without ordering) race and give wrong
+ *     results.  Order them, or use qx_gemv_chain with separate scratch.
+ */
+qx_status qx_gemv_chain_noalloc(int n_jobs, const qx_gemv_job* jobs, qx_stream_t s);
+
 /* Bytes of one row of `cols` weights, or 0 if fmt is unknown or cols is not
  * a positive multiple of the block width. */
 size_t qx_row_bytes(qx_fmt fmt, int64_t cols);

@@ -1,0 +1,82 @@
+"""qx_gemv_chain_noalloc: the chain entry point that allocates nothing.
+
+Some callers cannot allocate device memory where they run a chain (during
+CUDA graph capture, in pool-only runtimes, in plug-ins barred from the
+process allocator); this entry point keeps the chain's arrival counters in a
+fixed array inside the library instead of caller scratch.  The test calls it
+through the C ABI twice in a row and checks each result against
+qx_gemv_chain (caller scratch) within the tolerance the parity tests use,
+1e-4 * sum_i |w_i * x_i| per row.  It runs last (file name) and also alone.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import block_quantized_gemv_q8_gb300 as qx
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qx.build_library()
+    L = qx.lib()
+    L.qx_gemv_chain_noalloc.argtypes = [ctypes.c_int, ctypes.POINTER(qx._Job), ctypes.c_void_p]
+    L.qx_gemv_chain_noalloc.restype = ctypes.c_int
+    return L
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def test_noalloc_chain_matches_chain_with_scratch(lib):
+    specs = [(synth.Q4_K, [300, 64], 4096), (synth.Q6_K, [129], 14336), (synth.Q8_0, [151, 33], 896),
+             (synth.Q4_K, [4096], 4096)]
+    host = []
+    jobs = []
+    for i, (fmt, rows, cols) in enumerate(specs):
+        Ws = [synth.weights(fmt, r, cols, seed=900 + 10 * i + k) for k, r in enumerate(rows)]
+        x = synth.activation(1, cols, seed=950 + i)
+        host.append((fmt, Ws, rows, cols, x))
+        jobs.append(qx.GemvJob(fmt, [dev(W) for W in Ws], rows, cols, dev(x[0])))
+
+    # the existing entry point, with caller-owned scratch
+    qx.qx_gemv_chain(jobs, qx.chain_scratch(len(jobs)))
+    torch.cuda.synchronize()
+    ref = [[y.cpu().numpy().astype(np.float64) for y in job.y] for job in jobs]
+
+    # tolerance scale per row from the oracle (inputs from the generators only)
+    absdot = []
+    for fmt, Ws, rows, cols, x in host:
+        q, d, _ = oracle.quantize_act_q8(x)
+        absdot.append([oracle.gemv_w4a8(fmt, W, r, cols, q[0], d[0])[1] for W, r in zip(Ws, rows)])
+
+    stream = torch.cuda.current_stream()
+    for call in range(2):
+        outs = []
+        for job in jobs:
+            job.y = [torch.full((r,), float("nan"), dtype=torch.float32, device="cuda") for r in job.rows]
+            outs.append(job.y)
+        arr = qx.make_chain(jobs)
+        st = lib.qx_gemv_chain_noalloc(len(arr), arr, ctypes.c_void_p(stream.cuda_stream))
+        assert st == qx.QX_OK, qx.qx_status_string(st)
+        assert qx.qx_device_check(stream) == qx.QX_OK
+        for j, ys in enumerate(outs):
+            for k, y in enumerate(ys):
+                got = y.cpu().numpy().astype(np.float64)
+                err = np.abs(got - ref[j][k])
+                assert np.all(err <= TOL * absdot[j][k]), f"call {call} job {j} entry {k}: max err {err.max()}"
+
+
+def test_noalloc_chain_rejects_too_many_jobs(lib):
+    W = torch.zeros(144 * 4, dtype=torch.uint8, device="cuda")
+    x = torch.zeros(256, dtype=torch.float32, device="cuda")
+    jobs = [qx.GemvJob(synth.Q4_K, [W], [4], 256, x) for _ in range(qx.QX_CHAIN_MAX_JOBS + 1)]
+    arr = qx.make_chain(jobs)
+    assert lib.qx_gemv_chain_noalloc(len(arr), arr, None) == qx.QX_ERR_ARG
