@@ -310,13 +310,147 @@ def run_reference(args):
     return 0
 
 
+# ---------------------------------------------------- secondary workloads ----
+
+def graph_time_ms(torch, fn, reps: int, stream):
+    """Mean device time of fn() captured once in a CUDA graph, replayed `reps` times."""
+    with torch.cuda.stream(stream):
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_extra(args):
+    """The other configurations, measured for the record (not the headline)."""
+    import torch
+    import block_quantized_gemv_q8_gb300 as qx
+    qx.build_library()
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream()
+    hbm, bf16, peak_kind = measured_peaks()
+    out = {"workload": args.workload, "peak_hbm_gbs": hbm, "peak_kind": peak_kind}
+    FUSED, F32, PDL = qx.QX_MODE_W4A8_FUSED, qx.QX_MODE_F32, qx.QX_FLAG_PDL
+    if args.workload == "q4k_1024":
+        fmt, rows, cols = synth.Q4_K, 1024, 1024
+        nbytes = rows * synth.row_bytes(fmt, cols)
+        copies = 512  # 302 MB rotating pool, larger than L2
+        pool = torch.from_numpy(np.concatenate([synth.weights(fmt, rows, cols, seed=i) for i in range(8)])).cuda()
+        pool = pool.repeat(copies // 8, 1).reshape(copies, rows, -1)
+        x = torch.from_numpy(synth.activation(1, cols, seed=9)[0]).cuda()
+        y = torch.empty(rows, dtype=torch.float32, device="cuda")
+        for name, mode in (("w4a8", FUSED | PDL), ("f32", F32 | PDL)):
+            def rot():
+                for c in range(copies):
+                    qx.qx_gemv(fmt, pool[c], rows, cols, x, y=y, mode=mode, stream=stream)
+            ms = graph_time_ms(torch, rot, 5, stream) / copies
+            def hot():
+                for _ in range(64):
+                    qx.qx_gemv(fmt, pool[0], rows, cols, x, y=y, mode=mode & 0xFF, stream=stream)
+            ms_hot = graph_time_ms(torch, hot, 5, stream) / 64
+            out[name] = {"GB_per_s_rotating_pool": nbytes / (ms * 1e-3) / 1e9, "us_per_gemv_rotating": ms * 1e3,
+                         "us_per_gemv_l2_hot_serial": ms_hot * 1e3}
+    elif args.workload == "lmhead_q6k":
+        fmt, rows, cols = synth.LLAMA8B_LM_HEAD_Q6K[1:]
+        nbytes = rows * synth.row_bytes(fmt, cols)
+        W = torch.from_numpy(synth.weights(fmt, rows, cols, seed=20)).cuda()
+        x = torch.from_numpy(synth.activation(1, cols, seed=21)[0]).cuda()
+        y = torch.empty(rows, dtype=torch.float32, device="cuda")
+        for name, mode in (("w4a8", FUSED | PDL), ("f32", F32 | PDL)):
+            ms = graph_time_ms(torch, lambda: qx.qx_gemv(fmt, W, rows, cols, x, y=y, mode=mode, stream=stream),
+                               50, stream)
+            out[name] = {"GB_per_s": nbytes / (ms * 1e-3) / 1e9, "us": ms * 1e3, "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm}
+        out["weight_bytes"] = nbytes
+    elif args.workload == "qwen05b":
+        shapes = {n: (f, r, c) for n, f, r, c in synth.QWEN05B_LAYER}
+        L = synth.QWEN05B_LAYERS
+        Ws = [{n: torch.from_numpy(synth.weights(f, r, c, seed=synth.seed_for(3, l, j))).cuda()
+               for j, (n, (f, r, c)) in enumerate(shapes.items())} for l in range(L)]
+        lf, lr, lc = synth.QWEN05B_LM_HEAD[1:]
+        Wlm = torch.from_numpy(synth.weights(lf, lr, lc, seed=31)).cuda()
+        xs = [torch.from_numpy(synth.activation(1, 1024, seed=40 + k, valid_cols=896 if k == 2 else None)[0]).cuda()
+              for k in range(3)]
+        xd = torch.from_numpy(synth.activation(1, 4864, seed=44)[0]).cuda()
+        ys = {n: torch.empty(r, dtype=torch.float32, device="cuda") for n, (f, r, c) in shapes.items()}
+        ylm = torch.empty(lr, dtype=torch.float32, device="cuda")
+        nbytes = L * sum(r * synth.row_bytes(f, c) for f, r, c in shapes.values()) + lr * synth.row_bytes(lf, lc)
+        mode = FUSED | PDL
+        Q8, Q4 = synth.Q8_0, synth.Q4_K
+
+        def step():
+            for l in range(L):
+                W = Ws[l]
+                qx.qx_gemv_multi([Q8] * 3, [W["q"], W["k"], W["v"]], [896, 128, 128], 896, xs[0][:896],
+                                 ys=[ys["q"], ys["k"], ys["v"]], mode=mode, stream=stream)
+                qx.qx_gemv(Q8, W["o"], 896, 896, xs[1][:896], y=ys["o"], mode=mode, stream=stream)
+                qx.qx_gemv_multi([Q4, Q4], [W["gate"], W["up"]], [4864, 4864], 1024, xs[2],
+                                 ys=[ys["gate"], ys["up"]], mode=mode, stream=stream)
+                qx.qx_gemv(Q4, W["down"], 896, 4864, xd, y=ys["down"], mode=mode, stream=stream)
+            qx.qx_gemv(Q8, Wlm, lr, lc, xs[0][:896], y=ylm, mode=mode, stream=stream)
+        ms = graph_time_ms(torch, step, 50, stream)
+        jobs = []
+        for l in range(L):
+            W = Ws[l]
+            jobs += [qx.GemvJob(Q8, [W["q"], W["k"], W["v"]], [896, 128, 128], 896, xs[0][:896],
+                                [ys["q"], ys["k"], ys["v"]]),
+                     qx.GemvJob(Q8, [W["o"]], [896], 896, xs[1][:896], [ys["o"]]),
+                     qx.GemvJob(Q4, [W["gate"], W["up"]], [4864, 4864], 1024, xs[2], [ys["gate"], ys["up"]]),
+                     qx.GemvJob(Q4, [W["down"]], [896], 4864, xd, [ys["down"]])]
+        jobs.append(qx.GemvJob(Q8, [Wlm], [lr], lc, xs[0][:896], [ylm]))
+        arr, scratch = qx.make_chain(jobs), qx.chain_scratch(len(jobs))
+        ms_chain = graph_time_ms(torch, lambda: qx.qx_gemv_chain(jobs, scratch, stream=stream, marshalled=arr),
+                                 50, stream)
+        out.update({"weight_bytes_per_token": nbytes, "us_per_token_pdl_launches": ms * 1e3,
+                    "us_per_token_chain": ms_chain * 1e3, "GB_per_s_pdl": nbytes / (ms * 1e-3) / 1e9,
+                    "GB_per_s_chain": nbytes / (ms_chain * 1e-3) / 1e9,
+                    "launches_per_token_pdl": 4 * L + 1, "hbm_bound_us": nbytes / (hbm * 1e9) * 1e6})
+    elif args.workload == "prefill":
+        fmt, rows, cols = synth.PREFILL[1:]
+        W = torch.from_numpy(synth.weights(fmt, rows, cols, seed=70)).cuda()
+        X = torch.from_numpy(synth.activation(synth.PREFILL_M, cols, seed=71)).cuda()
+        act = qx.qx_quantize_act_q8(X)
+        torch.cuda.synchronize()
+        nbytes = rows * synth.row_bytes(fmt, cols)
+        sweep = []
+        for m in synth.PREFILL_SWEEP_M:
+            a = qx.ActQ8(act.q[:m], act.d[:m], act.sum[:m])
+            Y = torch.empty((m, rows), dtype=torch.float32, device="cuda")
+            rec = {"m": m}
+            for path in (1, 2):
+                if path == 1 and m > 64:
+                    continue
+                ms = graph_time_ms(torch, lambda: qx.qx_gemm_prefill_ex(fmt, W, rows, cols, a, Y=Y, path=path,
+                                                                        stream=stream), 10, stream)
+                rec[f"path{path}_us"] = ms * 1e3
+                rec[f"path{path}_tflops"] = 2.0 * m * rows * cols / (ms * 1e-3) / 1e12
+                rec[f"path{path}_weight_GB_per_s"] = nbytes / (ms * 1e-3) / 1e9
+            sweep.append(rec)
+        out.update({"sweep": sweep, "flops_per_row": 2 * rows * cols, "bf16_dense_peak_tflops": bf16,
+                    "note": "path 1 = one W4A8 GEMV launch per row; path 2 = tensor cores (mma.sync f16 with "
+                            "integer-valued operands); tflops count the int8-equivalent multiply-adds x2"})
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="qx", choices=["qx", "reference"])
-    ap.add_argument("--workload", default="llama8b", choices=["llama8b"])
+    ap.add_argument("--workload", default="llama8b", choices=["llama8b", "q4k_1024", "lmhead_q6k", "qwen05b",
+                                                               "prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=synth.LLAMA8B_LAYERS)
     args = ap.parse_args()
@@ -327,6 +461,9 @@ def main():
 
     import torch
     import block_quantized_gemv_q8_gb300 as qx
+
+    if args.workload != "llama8b":
+        return run_extra(args)
 
     ws, rank, local = dist_env()
     torch.cuda.set_device(local)

@@ -26,6 +26,8 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s bound on every pipeli
 constexpr size_t kStageTargetBytes = 48 * 1024;
 // Shared memory of a CTA that leaves room for a second one on the SM.
 constexpr size_t kHalfSmBytes = 110 * 1024;
+// Rows of X from which qx_gemm_prefill takes the tensor-core path.
+constexpr int64_t kPrefillTensorMinRows = 12;
 // Shared memory of a chain CTA (one per SM).
 constexpr size_t kChainSmBytes = 200 * 1024;
 constexpr int kMaxStageRows = 256;
@@ -435,7 +437,15 @@ qx_status qx_gemm_prefill_ex(qx_fmt fmt, const void* W, int64_t rows, int64_t co
     if (!aligned16(W) || !aligned4(Y)) return QX_ERR_ALIGN;
     if ((st = check_act(X, 0, cols)) != QX_OK) return st;
     if (path < 0 || path > 2) return QX_ERR_ARG;
-    if (path == 2) return QX_ERR_SHAPE;  // tensor-core path not built for this format/shape
+    const bool tensor = path == 2 || (path == 0 && fmt == QX_Q4_K && X->m >= kPrefillTensorMinRows);
+    if (tensor) {
+        if (fmt != QX_Q4_K) return QX_ERR_FMT;  // the tensor-core path serves Q4_K
+        DeviceInfo* dev = nullptr;
+        if ((st = device_info(&dev)) != QX_OK) return st;
+        const cudaError_t e = launch_prefill_q4k(static_cast<const uint8_t*>(W), rows, cols, X->q, X->d, X->sum,
+                                                 X->m, Y, reinterpret_cast<cudaStream_t>(s));
+        return e == cudaSuccess ? QX_OK : cuda_fail(e, "prefill launch");
+    }
     // Row-by-row: each row of X is an independent W4A8 GEMV.
     for (int64_t m = 0; m < X->m; ++m) {
         qx_act_q8 row{X->q + m * cols, X->d + m * (cols / 32), X->sum + m * (cols / 32), 1, cols};

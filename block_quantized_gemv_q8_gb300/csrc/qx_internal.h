@@ -97,6 +97,8 @@ cudaError_t launch_gemv(int fmt, int mode, bool partials, const GemvParams& p, s
 cudaError_t gemv_max_ctas_per_sm(int fmt, int mode, bool partials, size_t smem, int* out);
 cudaError_t launch_timeout_probe(unsigned* err, uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_chain(const ChainParams& p, size_t smem, cudaStream_t s);
+cudaError_t launch_prefill_q4k(const uint8_t* W, int64_t N, int64_t K, const int8_t* xq, const float* xd,
+                               const int32_t* xs, int64_t M, float* Y, cudaStream_t s);
 cudaError_t chain_max_ctas_per_sm(size_t smem, int* out);
 
 }  // namespace qx

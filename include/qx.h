@@ -157,10 +157,11 @@ qx_status qx_gemm_prefill(qx_fmt fmt, const void* W, int64_t rows, int64_t cols,
                           qx_stream_t s);
 
 /*
- * qx_gemm_prefill with a forced path: 0 = automatic, 1 = batched GEMV kernel
- * (weights streamed once for all rows of X; X->m <= 8), 2 = tensor-core
- * GEMM.  A path that cannot serve the call returns QX_ERR_SHAPE or
- * QX_ERR_FMT rather than falling back.
+ * qx_gemm_prefill with a forced path: 0 = automatic (tensor cores for Q4_K
+ * with X->m >= 12, else path 1), 1 = one W4A8 GEMV launch per row of X,
+ * 2 = tensor-core GEMM (Q4_K only: integer-valued f16 operands, exact
+ * per-sub-block sums, scales applied per sub-block).  A path that cannot serve
+ * the call returns QX_ERR_FMT rather than falling back.
  */
 qx_status qx_gemm_prefill_ex(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X,
                              float* Y, int path, qx_stream_t s);

@@ -238,15 +238,44 @@ def test_gemv_multi_matches_separate(mode):
 
 # ------------------------------------------------------------- prefill ----
 
-@pytest.mark.parametrize("m", [1, 3, 8])
-def test_prefill_small(m):
-    fmt, rows, cols = synth.Q4_K, 70, 1024
-    W = synth.weights(fmt, rows, cols, seed=50 + m)
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("m,rows,cols", [(1, 70, 1024), (3, 128, 256), (8, 300, 1024), (64, 129, 512),
+                                         (65, 256, 4096), (130, 70, 2048)])
+def test_prefill_paths(path, m, rows, cols):
+    fmt = synth.Q4_K
+    W = synth.weights(fmt, rows, cols, seed=50 + m + rows)
     X = synth.activation(m, cols, seed=51 + m)
     a, q, d, s = quantize_both(X)
-    Y = qx.qx_gemm_prefill(fmt, dev(W), rows, cols, a)
+    Y = qx.qx_gemm_prefill_ex(fmt, dev(W), rows, cols, a, path=path)
     ref, absdot = oracle.gemm_w4a8(fmt, W, rows, cols, q, d)
-    assert_close(host(Y).reshape(-1), ref.reshape(-1), absdot.reshape(-1), f"prefill m={m}")
+    assert_close(host(Y).reshape(-1), ref.reshape(-1), absdot.reshape(-1), f"prefill path {path} m={m}")
+
+
+def test_prefill_auto_and_refusals():
+    fmt, rows, cols, m = synth.Q4_K, 96, 1024, 16  # automatic path: tensor cores from 12 rows
+    W = dev(synth.weights(fmt, rows, cols, seed=60))
+    a, q, d, s = quantize_both(synth.activation(m, cols, seed=61))
+    y_auto = host(qx.qx_gemm_prefill(fmt, W, rows, cols, a))
+    y_tc = host(qx.qx_gemm_prefill_ex(fmt, W, rows, cols, a, path=2))
+    assert np.array_equal(y_auto.view(np.uint32), y_tc.view(np.uint32))
+    W6 = dev(synth.weights(synth.Q6_K, rows, cols, seed=62))
+    with pytest.raises(qx.QxError) as ei:
+        qx.qx_gemm_prefill_ex(synth.Q6_K, W6, rows, cols, a, path=2)
+    assert ei.value.status == qx.QX_ERR_FMT
+
+
+def test_prefill_full_size_sampled():
+    """X [512, 4096] against Q4_K [14336, 4096]: sampled rows of X and of W against the oracle."""
+    fmt, rows, cols, m = synth.Q4_K, 14336, 4096, 512
+    W = synth.weights(fmt, rows, cols, seed=63)
+    X = synth.activation(m, cols, seed=64)
+    a, q, d, s = quantize_both(X)
+    Y = host(qx.qx_gemm_prefill_ex(fmt, dev(W), rows, cols, a, path=2))
+    rng = np.random.default_rng(65)
+    xr = np.sort(rng.choice(m, 6, replace=False))
+    wr = np.sort(np.concatenate([rng.choice(rows, 250, replace=False), [0, rows - 1]]))
+    ref, absdot = oracle.gemm_w4a8(fmt, np.ascontiguousarray(W[wr]), len(wr), cols, q[xr], d[xr])
+    assert_close(Y[np.ix_(xr, wr)].reshape(-1), ref.reshape(-1), absdot.reshape(-1), "prefill full size")
 
 
 # ---------------------------------------------------- device error word ----
