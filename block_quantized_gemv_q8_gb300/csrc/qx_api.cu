@@ -197,17 +197,16 @@ qx_status gemv_geometry(int fmt, int kmode, bool partials, bool fused, bool pdl,
     const bool half_sm = (kmode == QX_MODE_W4A8 || fmt == QX_Q8_0);
     const size_t budget = half_sm ? kHalfSmBytes : 200 * 1024;
     const size_t act = fused ? (size_t(cols) + size_t(cols / 32) * 8 + 15) / 16 * 16 : 0;
+    // per stage: the slot, three mbarriers and (for y outputs) the per-lane partial sums
+    const int RS = partial_stride(g.L);
+    const size_t red_stage = partials ? 0 : size_t(g.G) * RS * 4;
+    const auto bytes_for = [&](int st) { return size_t(st) * (slot + 24 + red_stage) + 16 + act; };
     int stages = 2;
-    while (stages < 8) {
-        const int s1 = stages + 1;
-        const size_t red = g.team_warps > 1 ? size_t(s1) * g.G * (1 + g.team_warps) * 4 : 0;
-        if (size_t(s1) * slot + size_t(s1) * 16 + red + act > budget) break;
-        stages = s1;
-    }
-    const size_t red = g.team_warps > 1 ? size_t(stages) * g.G * (1 + g.team_warps) * 4 : 0;
+    while (stages < 8 && bytes_for(stages + 1) <= budget) ++stages;
     p.bar_off = static_cast<int>(size_t(stages) * slot);
-    p.red_off = p.bar_off + 16 * stages;
-    p.act_off = static_cast<int>((size_t(p.red_off) + red + 15) / 16 * 16);
+    p.red_off = static_cast<int>((size_t(p.bar_off) + 24 * size_t(stages) + 15) / 16 * 16);
+    p.act_off = static_cast<int>((size_t(p.red_off) + size_t(stages) * red_stage + 15) / 16 * 16);
+    p.RS = RS;
     smem = size_t(p.act_off) + act;
     if (smem > 227 * 1024) return QX_ERR_SHAPE;
 
@@ -237,9 +236,8 @@ qx_status gemv_geometry(int fmt, int kmode, bool partials, bool fused, bool pdl,
 // Geometry of a chain: per-job teams and stage rows, one slot size and ring
 // depth for all jobs, one CTA row split per job over the same grid.
 qx_status chain_geometry(const DeviceInfo& dev, ChainParams& p, size_t& smem) {
-    size_t max_stage = 0;
+    size_t max_stage = 0, red_slot = 4;
     int64_t max_cols = 0;
-    int Gmax = 1, max_tw = 1;
     for (int j = 0; j < p.n_jobs; ++j) {
         ChainJob& jb = p.job[j];
         TeamGeom g;
@@ -252,29 +250,23 @@ qx_status chain_geometry(const DeviceInfo& dev, ChainParams& p, size_t& smem) {
         jb.team_warps = g.team_warps;
         jb.nteams = g.nteams;
         jb.L = g.L;
+        jb.RS = partial_stride(g.L);
         max_stage = std::max(max_stage, size_t(g.G * g.rb));
         max_cols = std::max(max_cols, jb.cols);
-        Gmax = std::max(Gmax, jb.G);
-        max_tw = std::max(max_tw, jb.team_warps);
+        red_slot = std::max(red_slot, size_t(g.G) * jb.RS);
     }
     const size_t slot = (max_stage + kSlotPad + 127) / 128 * 128;
     const size_t act = (size_t(max_cols) + size_t(max_cols / 32) * 8 + 15) / 16 * 16;
+    const auto bytes_for = [&](int st) { return size_t(st) * (slot + 24 + red_slot * 4) + 16 + act; };
     int stages = 2;
-    while (stages < 8) {
-        const int s1 = stages + 1;
-        const size_t red = size_t(s1) * Gmax * (1 + max_tw) * 4;
-        if (size_t(s1) * slot + size_t(s1) * 16 + red + act > kChainSmBytes) break;
-        stages = s1;
-    }
-    const size_t red = size_t(stages) * Gmax * (1 + max_tw) * 4;
+    while (stages < 8 && bytes_for(stages + 1) <= kChainSmBytes) ++stages;
     p.stages = stages;
     p.slot_bytes = static_cast<int>(slot);
-    p.Gmax = Gmax;
-    p.max_team_warps = max_tw;
+    p.red_slot_floats = static_cast<int>(red_slot);
     p.max_cols = max_cols;
     p.bar_off = static_cast<int>(size_t(stages) * slot);
-    p.red_off = p.bar_off + 16 * stages;
-    p.act_off = static_cast<int>((size_t(p.red_off) + red + 15) / 16 * 16);
+    p.red_off = static_cast<int>((size_t(p.bar_off) + 24 * size_t(stages) + 15) / 16 * 16);
+    p.act_off = static_cast<int>((size_t(p.red_off) + size_t(stages) * red_slot * 4 + 15) / 16 * 16);
     smem = size_t(p.act_off) + act;
     if (smem > 227 * 1024) return QX_ERR_SHAPE;
     int per_sm = 0;

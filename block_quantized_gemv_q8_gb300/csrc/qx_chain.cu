@@ -9,13 +9,16 @@
 //   * the producer warp of every CTA streams its rows of job 0, job 1, ...
 //     into the shared-memory ring without pause -- weights never depend on
 //     earlier jobs;
+//   * the consumers store per-lane partial sums; the reducer warp of the CTA
+//     adds them per row, writes y and, after the CTA's last row of job j,
+//     counts the CTA on job j's arrival counter (caller scratch memory);
 //   * the consumers of job j + 1 first wait until every CTA has finished job
-//     j (a per-job arrival counter in caller scratch memory, bounded wait),
-//     then quantise job j + 1's activation (which may be job j's output),
-//     load their slices and consume the stages already in the ring.
+//     j (that counter, bounded wait), then quantise job j + 1's activation
+//     (which may be job j's output), load their slices and consume the
+//     stages already in the ring.
 // The ring keeps filling while the consumers wait, so the stream continues
-// across job boundaries.  The last CTA to leave resets the counters to zero
-// for the next call.
+// across job boundaries.  The last reducer to finish resets the counters to
+// zero for the next call.
 #include "qx_device.cuh"
 #include "qx_internal.h"
 #include "qx_lanes.cuh"
@@ -84,11 +87,11 @@ __device__ __forceinline__ bool wait_count(const unsigned* c, unsigned target, u
 
 struct Ring {
     uint8_t* smem;
-    uint64_t* full;
-    uint64_t* empty;
-    int* red_cnt;
-    float* red;
-    int S, slot_bytes, Gmax, max_tw;
+    uint64_t* full;   // the slot's bytes have landed
+    uint64_t* empty;  // consumers and reducer are done with the slot
+    uint64_t* part;   // the consumers' partials of the slot's rows are stored
+    float* red;       // per-lane partial sums, red_slot_floats per slot
+    int S, slot_bytes, red_slot_floats;
 };
 
 // Consume this CTA's stages of one job.  k counts stages across jobs (the
@@ -109,19 +112,22 @@ __device__ __forceinline__ bool run_job(const ChainParams& p, const ChainJob& jb
         const int slot = k % rg.S;
         if (!mbar_wait_bounded(&rg.full[slot], (k / rg.S) & 1, p.wait_ns, p.err, kErrTimeoutFull)) return false;
         const uint8_t* sbuf = rg.smem + size_t(slot) * rg.slot_bytes;
-        consume_stage<FMT, QX_MODE_W4A8, false>(X, tm, sbuf, nrows, rb, warp, lane, jb.e[e].y + lrow, nullptr, 0,
-                                                rg.red_cnt + slot * rg.Gmax, rg.red + slot * rg.Gmax * rg.max_tw);
+        consume_stage<FMT, QX_MODE_W4A8, false>(X, tm, sbuf, nrows, rb, rg.red + size_t(slot) * rg.red_slot_floats,
+                                                jb.RS, nullptr, 0);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&rg.empty[slot]);
+        if (lane == 0) {
+            mbar_arrive(&rg.part[slot]);
+            mbar_arrive(&rg.empty[slot]);
+        }
         ++k;
     }
     (void)jidx;
     return true;
 }
 
-// One CTA per SM: the ring can take most of the SM's shared memory, and 12
-// consumer warps (13 warps, at most 4 per SM partition) get up to 128
-// registers each.
+// One CTA per SM: the ring can take most of the SM's shared memory.  Twelve
+// warps in all (10 consumers, producer, reducer) are three per SM partition,
+// so each thread may use up to 168 registers.
 __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __grid_constant__ ChainParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int abort_flag;
@@ -129,20 +135,19 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
     rg.smem = smem;
     rg.S = p.stages;
     rg.slot_bytes = p.slot_bytes;
-    rg.Gmax = p.Gmax;
-    rg.max_tw = p.max_team_warps;
+    rg.red_slot_floats = p.red_slot_floats;
     rg.full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
     rg.empty = rg.full + rg.S;
-    rg.red_cnt = reinterpret_cast<int*>(smem + p.red_off);
-    rg.red = reinterpret_cast<float*>(rg.red_cnt + rg.S * rg.Gmax);
+    rg.part = rg.empty + rg.S;
+    rg.red = reinterpret_cast<float*>(smem + p.red_off);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < rg.S; ++s) {
             mbar_init(&rg.full[s], 1);
-            mbar_init(&rg.empty[s], NW);
+            mbar_init(&rg.empty[s], NW + 1);
+            mbar_init(&rg.part[s], NW);
         }
-        for (int i = 0; i < rg.S * rg.Gmax; ++i) rg.red_cnt[i] = 0;
         abort_flag = 0;
         fence_barrier_init();
     }
@@ -188,13 +193,50 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
         return;
     }
 
+    if (warp == NW + 1) {
+        // ---------------- reducer: row sums, then job completion -----------
+        int k = 0;
+        bool ok = true;
+        for (int j = 0; j < p.n_jobs && ok; ++j) {
+            const ChainJob& jb = p.job[j];
+            JobWalker wk{job_row_begin(jb, p.n_cta, blockIdx.x), job_row_begin(jb, p.n_cta, blockIdx.x + 1), 0};
+            int e, nrows;
+            int64_t lrow;
+            while (wk.next(jb, e, lrow, nrows)) {
+                const int slot = k % rg.S;
+                if (!mbar_wait_bounded(&rg.part[slot], (k / rg.S) & 1, p.wait_ns, p.err, kErrTimeoutFull)) {
+                    ok = false;
+                    break;
+                }
+                reduce_stage(rg.red + size_t(slot) * rg.red_slot_floats, jb.RS, jb.L, nrows, jb.e[e].y + lrow, lane);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&rg.empty[slot]);
+                ++k;
+            }
+            if (!ok) break;
+            // every y of job j from this CTA is written: count the CTA
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) arrive_release_gpu(&p.counters[j]);
+        }
+        if (ok && lane == 0) {
+            // the last CTA to finish the chain resets the counters for the next
+            // call; every arrival of every CTA precedes its final count here
+            __threadfence();
+            if (atomicAdd(&p.counters[p.n_jobs], 1u) == unsigned(p.n_cta) - 1u) {
+                for (int j = 0; j <= p.n_jobs; ++j) atomicExch(&p.counters[j], 0u);
+                __threadfence();
+            }
+        }
+        return;
+    }
+
     // ---------------- consumers ----------------------------------------------
     pdl_wait_prior_grid();
     int8_t* sq = reinterpret_cast<int8_t*>(smem + p.act_off);
     float* sd = reinterpret_cast<float*>(sq + p.max_cols);
     int32_t* ss = reinterpret_cast<int32_t*>(sd + p.max_cols / 32);
     int k = 0;
-    bool ok = true;
     for (int j = 0; j < p.n_jobs; ++j) {
         const ChainJob& jb = p.job[j];
         if (j > 0) {
@@ -202,10 +244,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
             if (threadIdx.x == 0 && !wait_count(&p.counters[j - 1], unsigned(p.n_cta), p.wait_ns, p.err))
                 abort_flag = 1;
             consumer_barrier<NW>();
-            if (abort_flag) {
-                ok = false;
-                break;
-            }
+            if (abort_flag) break;
         }
         const int nblk = static_cast<int>(jb.cols / 32);
         for (int base = 0; base < 2 * nblk; base += NW * 32) quantize_task(jb.x, nblk, base + threadIdx.x, sq, sd, ss);
@@ -217,20 +256,8 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
             default: jok = run_job<QX_Q8_0>(p, jb, j, k, rg, sq, sd, ss, warp, lane); break;
         }
         if (!jok) abort_flag = 1;
-        consumer_barrier<NW>();  // every consumer is done with job j (its y stores issued, x slices loaded)
-        if (abort_flag) {
-            ok = false;
-            break;
-        }
-        if (threadIdx.x == 0) arrive_release_gpu(&p.counters[j]);
-    }
-    if (ok && threadIdx.x == 0) {
-        // the last CTA to finish the chain resets the counters for the next call
-        __threadfence();
-        if (atomicAdd(&p.counters[p.n_jobs], 1u) == unsigned(p.n_cta) - 1u) {
-            for (int j = 0; j <= p.n_jobs; ++j) atomicExch(&p.counters[j], 0u);
-            __threadfence();
-        }
+        consumer_barrier<NW>();  // every consumer has loaded its slice: the activation area may be rewritten
+        if (abort_flag) break;
     }
 }
 

@@ -14,8 +14,10 @@
 //     whose bytes make a 16-byte multiple, so every copy is 16-byte aligned.
 //   * Consumer lanes own a fixed slice of columns for the whole kernel, so
 //     the activation slice stays in registers.  A "team" of lanes covers one
-//     row; teams take the rows of a stage in turn and reduce with warp
-//     shuffles (plus one shared-memory step when a row needs several warps).
+//     row; teams take the rows of a stage in turn.  Each lane stores its
+//     partial sum of a row to shared memory and moves on; a reducer warp adds
+//     the partials of each row in a fixed lane order and writes y, so no
+//     consumer ever waits on a cross-lane reduction.
 //   * W4A8 (llamay docs, "Backends and hardware", sections "CPU" and
 //     "CUDA"): per 32-weight sub-block (16 for Q6_K) the int8 x int4/int6/int8
 //     products are summed exactly with dp4a, and only then scaled; the weight
@@ -86,14 +88,13 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_min_blocks<FMT, MODE>())
     static_assert(PART || LaneT::kRows == gemv_rows_per_call(FMT, MODE), "row count must match the host geometry");
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = p.stages;
+    // full[s]: the slot's bytes have landed.  empty[s]: the consumers (and,
+    // for y outputs, the reducer) are done with the slot and its partials.
+    // part[s]: the consumers' partials of the slot's rows are stored.
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
     uint64_t* empty = full + S;
-    // Cross-warp row sums (rows wider than one warp): per (slot, row of
-    // stage) one partial per warp of the team and an arrival counter; the
-    // last warp to arrive adds them in warp order and writes y, so no warp
-    // ever waits on another.
-    int* red_cnt = reinterpret_cast<int*>(smem + p.red_off);  // [S][G]
-    float* red = reinterpret_cast<float*>(red_cnt + S * p.G);   // [S][G][team_warps]
+    uint64_t* part = empty + S;
+    float* red = reinterpret_cast<float*>(smem + p.red_off);  // [S][G][RS]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t r0 = cta_row_begin(p, blockIdx.x), r1 = cta_row_begin(p, blockIdx.x + 1);
@@ -101,10 +102,9 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_min_blocks<FMT, MODE>())
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], NW);
+            mbar_init(&empty[s], PART ? NW : NW + 1);
+            mbar_init(&part[s], NW);
         }
-        if (p.team_warps > 1)
-            for (int i = 0; i < S * p.G; ++i) red_cnt[i] = 0;
         fence_barrier_init();
     }
     __syncthreads();
@@ -147,6 +147,23 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_min_blocks<FMT, MODE>())
         return;
     }
 
+    if (warp == NW + 1) {
+        // ---------------- reducer: row sums of every stage, in order -------
+        if constexpr (!PART) {
+            StageWalker wk{r0, r1, 0};
+            int e, nrows;
+            int64_t lrow;
+            for (int k = 0; wk.next(p, e, lrow, nrows); ++k) {
+                const int slot = k % S;
+                if (!mbar_wait_bounded(&part[slot], (k / S) & 1, p.wait_ns, p.err, kErrTimeoutFull)) break;
+                reduce_stage(red + size_t(slot) * p.G * p.RS, p.RS, p.L, nrows, p.e[e].y + lrow, lane);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);
+            }
+        }
+        return;
+    }
+
     // ---------------- consumers ----------------------------------------------
     const Team tm = make_team(warp, lane, p.team_lanes, p.team_warps, p.nteams, p.L);
 
@@ -183,11 +200,13 @@ __global__ void __launch_bounds__(kGemvThreads, gemv_min_blocks<FMT, MODE>())
         const int slot = k % S;
         if (!mbar_wait_bounded(&full[slot], (k / S) & 1, p.wait_ns, p.err, kErrTimeoutFull)) break;
         const uint8_t* sbuf = smem + size_t(slot) * p.slot_bytes;
-        consume_stage<FMT, MODE, PART>(X, tm, sbuf, nrows, rb, warp, lane, PART ? nullptr : p.e[e].y + lrow,
-                                       PART ? p.e[e].P + lrow * ng : nullptr, ng, red_cnt + slot * p.G,
-                                       red + slot * p.G * p.team_warps);
+        consume_stage<FMT, MODE, PART>(X, tm, sbuf, nrows, rb, red + size_t(slot) * p.G * p.RS, p.RS,
+                                       PART ? p.e[e].P + lrow * ng : nullptr, ng);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
+        if (lane == 0) {
+            if constexpr (!PART) mbar_arrive(&part[slot]);
+            mbar_arrive(&empty[slot]);
+        }
     }
 }
 

@@ -10,12 +10,14 @@
 
 namespace qx {
 
-// Consumer warps per GEMV CTA (one more warp issues the bulk copies).
+// Warps of a GEMV CTA: the consumers, then one producer warp (issues the
+// bulk copies) and one reducer warp (sums the consumers' per-lane partials of
+// each row and writes y).
 constexpr int kGemvConsumerWarps = 8;
-constexpr int kGemvThreads = 32 * (kGemvConsumerWarps + 1);
-// Consumer warps per chain CTA (one CTA per SM; one more warp issues copies).
-constexpr int kChainConsumerWarps = 12;
-constexpr int kChainThreads = 32 * (kChainConsumerWarps + 1);
+constexpr int kGemvThreads = 32 * (kGemvConsumerWarps + 2);
+// Consumer warps per chain CTA (one CTA per SM), plus a producer and a reducer.
+constexpr int kChainConsumerWarps = 10;
+constexpr int kChainThreads = 32 * (kChainConsumerWarps + 2);
 // Bytes read past the end of a shared-memory slot by the unaligned-word loads.
 constexpr int kSlotPad = 16;
 
@@ -41,14 +43,15 @@ struct GemvParams {
     int team_warps;   // warps per team (1 for sub-warp teams)
     int nteams;       // teams per CTA
     int L;            // lanes with work per row (cols / columns-per-lane)
+    int RS;           // floats per row of the per-lane partial-sum area
     int n_cta;
     const float* x;    // f32 mode activation [cols]
     const int8_t* xq;  // W4A8 activation quants [cols]
     const float* xd;   // W4A8 activation scales [cols/32]
     const int32_t* xs; // W4A8 activation block sums [cols/32]
     const float* xf;   // W4A8 with in-kernel quantisation: f32 activation [cols]
-    int bar_off;       // shared-memory byte offsets: mbarriers,
-    int red_off;       //   cross-warp row sums,
+    int bar_off;       // shared-memory byte offsets: mbarriers (full, empty, part),
+    int red_off;       //   per-lane partial sums [stages][G][RS],
     int act_off;       //   quantised activation (in-kernel quantisation)
     unsigned* err;     // device error word
     uint64_t wait_ns;  // bound on every wait
@@ -66,7 +69,7 @@ struct ChainJob {
     int64_t cols;
     int64_t row_bytes;
     int64_t total_rows;
-    int fmt, n_entries, team_lanes, team_warps, nteams, quantum, G, L;
+    int fmt, n_entries, team_lanes, team_warps, nteams, quantum, G, L, RS;
 };
 
 struct ChainParams {
@@ -75,14 +78,20 @@ struct ChainParams {
     int stages;
     int slot_bytes;
     int bar_off, red_off, act_off;
-    int Gmax;            // most rows of any job's stage
-    int max_team_warps;  // most warps of any job's team
+    int red_slot_floats; // floats of the partial-sum area per slot (most G * RS of any job)
     int64_t max_cols;    // widest activation (size of the quantised-activation area)
     unsigned* counters;  // caller scratch: [n_jobs + 1] arrival counters, zero on entry and exit
     unsigned* err;
     uint64_t wait_ns;
     ChainJob job[QX_CHAIN_MAX_JOBS];
 };
+
+// Row stride (floats) of the per-lane partial sums of a row of L lanes: a
+// multiple of 4 (16-byte rows) with an odd number of 16-byte groups, so that
+// the reducer's lanes (one row each) read distinct banks.
+__host__ __device__ constexpr int partial_stride(int L) {
+    return ((L + 3) / 4 % 2 == 1) ? (L + 3) / 4 * 4 : (L + 3) / 4 * 4 + 4;
+}
 
 // Rows a team computes per call, per (format, mode) (must match the kernels).
 __host__ __device__ constexpr int gemv_rows_per_call(int fmt, int mode) {

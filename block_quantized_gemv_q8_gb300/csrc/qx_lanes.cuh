@@ -462,80 +462,73 @@ __device__ __forceinline__ Team make_team(int warp, int lane, int team_lanes, in
 }
 
 // All rows of one stage (rows [0, nrows) of `sbuf`, rb bytes each): team t
-// takes rows t, t + nteams, ... in calls of R rows.  y rows go to yb[i] (or
-// integer partials to Pb + i * ng).  Rows wider than a warp are summed
-// through red_cnt / red, this slot's [G] arrival counters and [G][team_warps]
-// partial sums: the last warp of a team to arrive adds the partials in warp
-// order and writes y, so no warp waits on another.
+// takes rows t, t + nteams, ... in calls of R rows.  Every lane stores its
+// partial sum of row i to red[i * RS + slice] (plain shared-memory stores, no
+// waiting); the reducer warp adds the L partials of each row later
+// (reduce_stage).  With PART, integer partials go to Pb + i * ng instead.
 template <int FMT, int MODE, bool PART, class LaneT>
 __device__ __forceinline__ void consume_stage(const LaneT& X, const Team& tm, const uint8_t* sbuf, int nrows,
-                                              uint32_t rb, int warp, int lane, float* yb, int32_t* Pb, int64_t ng,
-                                              int* red_cnt, float* red) {
+                                              uint32_t rb, float* red, int RS, int32_t* Pb, int64_t ng) {
+    if (!tm.active) return;
     constexpr int R = PART ? 1 : LaneT::kRows;
-    for (int ib = 0; ib < nrows; ib += tm.nteams * R) {
+    for (int ib = tm.team; ib < nrows; ib += tm.nteams * R) {
         int ir[R];
         bool vr[R];
         const uint8_t* rp[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            ir[r] = ib + tm.team + r * tm.nteams;
-            vr[r] = tm.in_team && ir[r] < nrows;
+            ir[r] = ib + r * tm.nteams;
+            vr[r] = ir[r] < nrows;
             rp[r] = sbuf + (vr[r] ? uint32_t(ir[r]) : 0u) * rb;
         }
         if constexpr (PART) {
-            if (vr[0] && tm.active) {
-                int P[LaneT::kGroups];
-                X.partials(rp[0], tm.slice, P);
-                int32_t* dst = Pb + int64_t(ir[0]) * ng;
+            int P[LaneT::kGroups];
+            X.partials(rp[0], tm.slice, P);
+            int32_t* dst = Pb + int64_t(ir[0]) * ng;
 #pragma unroll
-                for (int g = 0; g < LaneT::kGroups; ++g) dst[LaneT::part_index(tm.slice, g)] = P[g];
-            }
+            for (int g = 0; g < LaneT::kGroups; ++g) dst[LaneT::part_index(tm.slice, g)] = P[g];
         } else {
             float v[R];
-            if (tm.active) {
-                X.template rows<R>(rp, tm.slice, v);
-            } else {
+            X.template rows<R>(rp, tm.slice, v);
 #pragma unroll
-                for (int r = 0; r < R; ++r) v[r] = 0.0f;
-            }
-            if (tm.team_warps == 1) {
-                if (R == 2 && tm.team_lanes == 32) {
-                    // two rows in one butterfly: lanes 0-15 end with row 0, 16-31 with row 1
-                    float a = (lane & 16) ? v[R - 1] : v[0];
-                    const float b = (lane & 16) ? v[0] : v[R - 1];
-                    a += __shfl_xor_sync(0xffffffffu, b, 16);
+            for (int r = 0; r < R; ++r)
+                if (vr[r]) red[ir[r] * RS + tm.slice] = v[r];
+        }
+    }
+}
+
+// The reducer warp's share of one stage: y[i] = the L partials of row i
+// (red[i * RS + 0 .. L)) added in a fixed order -- four running sums over
+// slices s = 4k + c, then (c0 + c1) + (c2 + c3) -- one row per lane.
+__device__ __forceinline__ void reduce_stage(const float* red, int RS, int L, int nrows, float* y, int lane) {
+    for (int row = lane; row < nrows; row += 32) {
+        const float* pr = red + row * RS;
+        float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+        int s = 0;
+        for (; s + 16 <= L; s += 16) {
+            // four loads in flight, then the adds in slice order
+            float4 v[4];
 #pragma unroll
-                    for (int o = 8; o >= 1; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-                    if (lane == 0 && vr[0]) yb[ir[0]] = a;
-                    if (lane == 16 && vr[R - 1]) yb[ir[R - 1]] = a;
-                } else {
+            for (int u = 0; u < 4; ++u) v[u] = *reinterpret_cast<const float4*>(pr + s + 4 * u);
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        for (int o = tm.team_lanes >> 1; o >= 1; o >>= 1)
-                            v[r] += __shfl_xor_sync(0xffffffffu, v[r], o);
-                        if (vr[r] && tm.slice == 0) yb[ir[r]] = v[r];
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-#pragma unroll
-                    for (int o = 16; o >= 1; o >>= 1) v[r] += __shfl_xor_sync(0xffffffffu, v[r], o);
-                    if (vr[r] && lane == 0) {
-                        float* rbuf = red + ir[r] * tm.team_warps;
-                        rbuf[warp % tm.team_warps] = v[r];
-                        __threadfence_block();
-                        if (atomicAdd(&red_cnt[ir[r]], 1) == tm.team_warps - 1) {
-                            __threadfence_block();
-                            float sum = 0.0f;
-                            for (int w = 0; w < tm.team_warps; ++w) sum += rbuf[w];
-                            yb[ir[r]] = sum;
-                            red_cnt[ir[r]] = 0;
-                        }
-                    }
-                }
+            for (int u = 0; u < 4; ++u) {
+                a0 += v[u].x;
+                a1 += v[u].y;
+                a2 += v[u].z;
+                a3 += v[u].w;
             }
         }
+        for (; s + 4 <= L; s += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(pr + s);
+            a0 += v.x;
+            a1 += v.y;
+            a2 += v.z;
+            a3 += v.w;
+        }
+        if (s < L) a0 += pr[s];
+        if (s + 1 < L) a1 += pr[s + 1];
+        if (s + 2 < L) a2 += pr[s + 2];
+        y[row] = (a0 + a1) + (a2 + a3);
     }
 }
 
