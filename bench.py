@@ -427,7 +427,7 @@ def run_extra(args):
             a = qx.ActQ8(act.q[:m], act.d[:m], act.sum[:m])
             Y = torch.empty((m, rows), dtype=torch.float32, device="cuda")
             rec = {"m": m}
-            for path in (1, 2):
+            for path in (1, 2, 3):
                 if path == 1 and m > 64:
                     continue
                 ms = graph_time_ms(torch, lambda: qx.qx_gemm_prefill_ex(fmt, W, rows, cols, a, Y=Y, path=path,
@@ -435,10 +435,15 @@ def run_extra(args):
                 rec[f"path{path}_us"] = ms * 1e3
                 rec[f"path{path}_tflops"] = 2.0 * m * rows * cols / (ms * 1e-3) / 1e12
                 rec[f"path{path}_weight_GB_per_s"] = nbytes / (ms * 1e-3) / 1e9
+                if path == 3:  # three bf16 passes over K on tcgen05, whole call incl. the dequantise passes
+                    rec["path3_bf16_tflops"] = 3 * 2.0 * m * rows * cols / (ms * 1e-3) / 1e12
+                    rec["path3_frac_of_bf16_peak"] = rec["path3_bf16_tflops"] / bf16
             sweep.append(rec)
         out.update({"sweep": sweep, "flops_per_row": 2 * rows * cols, "bf16_dense_peak_tflops": bf16,
                     "note": "path 1 = one W4A8 GEMV launch per row; path 2 = tensor cores (mma.sync f16 with "
-                            "integer-valued operands); tflops count the int8-equivalent multiply-adds x2"})
+                            "integer-valued operands); path 3 = tcgen05 bf16 GEMM over the split dequantised "
+                            "operands (3 passes of K), timed with its dequantise passes; tflops count the "
+                            "int8-equivalent multiply-adds x2"})
     print(json.dumps(out), flush=True)
     return 0
 

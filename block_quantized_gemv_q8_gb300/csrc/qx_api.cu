@@ -28,6 +28,10 @@ constexpr size_t kStageTargetBytes = 48 * 1024;
 constexpr size_t kHalfSmBytes = 110 * 1024;
 // Rows of X from which qx_gemm_prefill takes the tensor-core path.
 constexpr int64_t kPrefillTensorMinRows = 12;
+// Automatic prefill path: the tcgen05 GEMM from this many rows of X (from
+// kPrefillTcMinRowsQ4K for Q4_K, which has the mma.sync path below that).
+constexpr int64_t kPrefillTcMinRows = 16;
+constexpr int64_t kPrefillTcMinRowsQ4K = 192;
 // Shared memory of a chain CTA (one per SM).
 constexpr size_t kChainSmBytes = 200 * 1024;
 constexpr int kMaxStageRows = 256;
@@ -339,6 +343,101 @@ qx_status check_x(int mode, const void* x, int64_t cols) {
 
 using namespace qx;
 
+namespace {
+
+// The library's own prefill workspace, one per device, grown on demand (never
+// while the stream is being captured into a graph).
+struct PrefillWorkspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+PrefillWorkspace g_prefill_ws[kMaxDevices];
+
+qx_status prefill_workspace(size_t need, cudaStream_t s, void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice, "device index");
+    std::lock_guard<std::mutex> lock(g_mu);
+    PrefillWorkspace& w = g_prefill_ws[dev];
+    if (w.bytes < need) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if ((e = cudaStreamIsCapturing(s, &cs)) != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+        if (cs != cudaStreamCaptureStatusNone) {
+            snprintf(g_last_error, sizeof(g_last_error),
+                     "prefill workspace of %zu bytes must be allocated before graph capture "
+                     "(run once uncaptured, or pass a workspace to qx_gemm_prefill_ws)",
+                     need);
+            return QX_ERR_ARG;
+        }
+        if (w.ptr) {
+            if ((e = cudaFree(w.ptr)) != cudaSuccess) return cuda_fail(e, "cudaFree");
+            w.ptr = nullptr;
+            w.bytes = 0;
+        }
+        if ((e = cudaMalloc(&w.ptr, need)) != cudaSuccess) {
+            w.ptr = nullptr;
+            return cuda_fail(e, "cudaMalloc (prefill workspace)");
+        }
+        w.bytes = need;
+    }
+    *out = w.ptr;
+    return QX_OK;
+}
+
+qx_status prefill_dispatch(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, float* Y,
+                           int path, void* ws, size_t ws_bytes, bool own_ws, qx_stream_t s) {
+    qx_status st = check_shape(fmt, rows, cols);
+    if (st != QX_OK) return st;
+    if (!W || !Y) return QX_ERR_ARG;
+    if (!aligned16(W) || !aligned4(Y)) return QX_ERR_ALIGN;
+    if ((st = check_act(X, 0, cols)) != QX_OK) return st;
+    if (path < 0 || path > 3) return QX_ERR_ARG;
+    if (path == 0) {
+        if (fmt == QX_Q4_K)
+            path = X->m >= kPrefillTcMinRowsQ4K ? 3 : (X->m >= kPrefillTensorMinRows ? 2 : 1);
+        else
+            path = X->m >= kPrefillTcMinRows ? 3 : 1;
+    }
+    if (path == 3) {
+        if (X->m > INT32_MAX || rows > INT32_MAX) return QX_ERR_SHAPE;
+        DeviceInfo* dev = nullptr;
+        if ((st = device_info(&dev)) != QX_OK) return st;
+        const size_t need = prefill_tc_workspace_bytes(rows, cols, X->m);
+        const cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
+        if (own_ws) {
+            if ((st = prefill_workspace(need, cs, &ws)) != QX_OK) return st;
+        } else {
+            if (!ws || ws_bytes < need) return QX_ERR_ARG;
+            if (!aligned16(ws)) return QX_ERR_ALIGN;
+        }
+        const cudaError_t e = launch_prefill_tc(fmt, static_cast<const uint8_t*>(W), rows, cols, int64_t(cols / block_weights(fmt)) * block_bytes(fmt),
+                                                X->q, X->d, X->m, Y, ws, dev->err_word, cs);
+        return e == cudaSuccess ? QX_OK : cuda_fail(e, "tcgen05 prefill launch");
+    }
+    const bool tensor = path == 2;
+    if (tensor) {
+        if (fmt != QX_Q4_K) return QX_ERR_FMT;  // the tensor-core path serves Q4_K
+        DeviceInfo* dev = nullptr;
+        if ((st = device_info(&dev)) != QX_OK) return st;
+        const cudaError_t e = launch_prefill_q4k(static_cast<const uint8_t*>(W), rows, cols, X->q, X->d, X->sum,
+                                                 X->m, Y, reinterpret_cast<cudaStream_t>(s));
+        return e == cudaSuccess ? QX_OK : cuda_fail(e, "prefill launch");
+    }
+    // Row-by-row: each row of X is an independent W4A8 GEMV.
+    for (int64_t m = 0; m < X->m; ++m) {
+        qx_act_q8 row{X->q + m * cols, X->d + m * (cols / 32), X->sum + m * (cols / 32), 1, cols};
+        if (!aligned16(row.q) || !aligned16(row.d) || !aligned16(row.sum)) return QX_ERR_ALIGN;
+        float* ym = Y + m * rows;
+        if ((st = run_gemv(fmt, 1, &W, &rows, cols, &row, &ym, nullptr, QX_MODE_W4A8, false,
+                           reinterpret_cast<cudaStream_t>(s))) != QX_OK)
+            return st;
+    }
+    return QX_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 size_t qx_row_bytes(qx_fmt fmt, int64_t cols) {
@@ -423,36 +522,22 @@ qx_status qx_gemv_partials(qx_fmt fmt, const void* W, int64_t rows, int64_t cols
 
 qx_status qx_gemm_prefill_ex(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, float* Y,
                              int path, qx_stream_t s) {
-    qx_status st = check_shape(fmt, rows, cols);
-    if (st != QX_OK) return st;
-    if (!W || !Y) return QX_ERR_ARG;
-    if (!aligned16(W) || !aligned4(Y)) return QX_ERR_ALIGN;
-    if ((st = check_act(X, 0, cols)) != QX_OK) return st;
-    if (path < 0 || path > 2) return QX_ERR_ARG;
-    const bool tensor = path == 2 || (path == 0 && fmt == QX_Q4_K && X->m >= kPrefillTensorMinRows);
-    if (tensor) {
-        if (fmt != QX_Q4_K) return QX_ERR_FMT;  // the tensor-core path serves Q4_K
-        DeviceInfo* dev = nullptr;
-        if ((st = device_info(&dev)) != QX_OK) return st;
-        const cudaError_t e = launch_prefill_q4k(static_cast<const uint8_t*>(W), rows, cols, X->q, X->d, X->sum,
-                                                 X->m, Y, reinterpret_cast<cudaStream_t>(s));
-        return e == cudaSuccess ? QX_OK : cuda_fail(e, "prefill launch");
-    }
-    // Row-by-row: each row of X is an independent W4A8 GEMV.
-    for (int64_t m = 0; m < X->m; ++m) {
-        qx_act_q8 row{X->q + m * cols, X->d + m * (cols / 32), X->sum + m * (cols / 32), 1, cols};
-        if (!aligned16(row.q) || !aligned16(row.d) || !aligned16(row.sum)) return QX_ERR_ALIGN;
-        float* ym = Y + m * rows;
-        if ((st = run_gemv(fmt, 1, &W, &rows, cols, &row, &ym, nullptr, QX_MODE_W4A8, false,
-                           reinterpret_cast<cudaStream_t>(s))) != QX_OK)
-            return st;
-    }
-    return QX_OK;
+    return prefill_dispatch(fmt, W, rows, cols, X, Y, path, nullptr, 0, true, s);
 }
 
 qx_status qx_gemm_prefill(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, float* Y,
                           qx_stream_t s) {
-    return qx_gemm_prefill_ex(fmt, W, rows, cols, X, Y, 0, s);
+    return prefill_dispatch(fmt, W, rows, cols, X, Y, 0, nullptr, 0, true, s);
+}
+
+size_t qx_gemm_prefill_workspace_bytes(qx_fmt fmt, int64_t rows, int64_t cols, int64_t m) {
+    if (check_shape(fmt, rows, cols) != QX_OK || m < 1) return 0;
+    return prefill_tc_workspace_bytes(rows, cols, m);
+}
+
+qx_status qx_gemm_prefill_ws(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, float* Y,
+                             int path, void* workspace, size_t workspace_bytes, qx_stream_t s) {
+    return prefill_dispatch(fmt, W, rows, cols, X, Y, path, workspace, workspace_bytes, false, s);
 }
 
 size_t qx_gemv_chain_scratch_bytes(int n_jobs) {

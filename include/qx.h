@@ -157,14 +157,45 @@ qx_status qx_gemm_prefill(qx_fmt fmt, const void* W, int64_t rows, int64_t cols,
                           qx_stream_t s);
 
 /*
- * qx_gemm_prefill with a forced path: 0 = automatic (tensor cores for Q4_K
- * with X->m >= 12, else path 1), 1 = one W4A8 GEMV launch per row of X,
- * 2 = tensor-core GEMM (Q4_K only: integer-valued f16 operands, exact
- * per-sub-block sums, scales applied per sub-block).  A path that cannot serve
- * the call returns QX_ERR_FMT rather than falling back.
+ * qx_gemm_prefill with a forced path:
+ *   0 = automatic (by measured time): Q4_K: path 1 below 12 rows of X,
+ *       path 2 below 192, path 3 from 192; other formats: path 1 below 16
+ *       rows, path 3 from 16;
+ *   1 = one W4A8 GEMV launch per row of X (bit-for-bit the qx_gemv result);
+ *   2 = mma.sync tensor-core GEMM, Q4_K only (integer-valued f16 operands,
+ *       exact per-sub-block integer sums, scales applied per sub-block);
+ *   3 = tcgen05 tensor-core GEMM, every format: the W4A8 product is the dot
+ *       product of the dequantised activation dx*q_x with the dequantised
+ *       weight (llamay docs, "Backends and hardware", sections "CPU" and
+ *       "CUDA"); both are written once as two bf16 terms (hi + lo, 16
+ *       significant bits) and Y = Xh Wh^T + Xh Wl^T + Xl Wh^T is accumulated
+ *       in f32 in tensor memory.  Each product's error is about 2^-15 of its
+ *       magnitude.  Paths 0 and 3 use a workspace of
+ *       qx_gemm_prefill_workspace_bytes bytes that the library allocates on
+ *       first use per device and keeps (growing it is refused with QX_ERR_ARG
+ *       while the stream is being captured into a graph); calls that may run
+ *       concurrently on different streams must use qx_gemm_prefill_ws.
+ * A path that cannot serve the call returns QX_ERR_FMT rather than falling
+ * back.
  */
 qx_status qx_gemm_prefill_ex(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X,
                              float* Y, int path, qx_stream_t s);
+
+/*
+ * Device bytes of the workspace that path 3 needs for this shape (two bf16
+ * copies of the weights and of the activation: 4 * cols * (rows + m) bytes,
+ * rounded up), or 0 for an invalid shape.
+ */
+size_t qx_gemm_prefill_workspace_bytes(qx_fmt fmt, int64_t rows, int64_t cols, int64_t m);
+
+/*
+ * qx_gemm_prefill_ex with caller-owned device workspace (16-byte aligned, at
+ * least qx_gemm_prefill_workspace_bytes bytes; used by paths 0 and 3, ignored
+ * by paths 1 and 2).  QX_ERR_ARG if it is missing or too small.  The
+ * workspace is overwritten; it must not be in use by another call.
+ */
+qx_status qx_gemm_prefill_ws(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, float* Y,
+                             int path, void* workspace, size_t workspace_bytes, qx_stream_t s);
 
 /*
  * The exact integer partial sums of the W4A8 product, written instead of y:

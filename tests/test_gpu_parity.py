@@ -238,7 +238,7 @@ def test_gemv_multi_matches_separate(mode):
 
 # ------------------------------------------------------------- prefill ----
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 2, 3])
 @pytest.mark.parametrize("m,rows,cols", [(1, 70, 1024), (3, 128, 256), (8, 300, 1024), (64, 129, 512),
                                          (65, 256, 4096), (130, 70, 2048)])
 def test_prefill_paths(path, m, rows, cols):
@@ -251,31 +251,91 @@ def test_prefill_paths(path, m, rows, cols):
     assert_close(host(Y).reshape(-1), ref.reshape(-1), absdot.reshape(-1), f"prefill path {path} m={m}")
 
 
+# The tcgen05 path serves every format; ragged M (partial 128-row tiles), N
+# (partial 256-column tiles) and K (a last 64-wide K tile read past the end,
+# zero-filled: Q8_0 with cols = 96 or 864).
+@pytest.mark.parametrize("fmt,m,rows,cols", [(synth.Q6_K, 16, 300, 1024), (synth.Q6_K, 129, 257, 256),
+                                             (synth.Q6_K, 33, 4096, 14336),
+                                             (synth.Q8_0, 16, 151, 896), (synth.Q8_0, 40, 33, 96),
+                                             (synth.Q8_0, 200, 513, 864),
+                                             (synth.Q4_K, 300, 1000, 4864)])
+def test_prefill_tcgen05_formats(fmt, m, rows, cols):
+    W = synth.weights(fmt, rows, cols, seed=70 + m + rows)
+    X = synth.activation(m, cols, seed=71 + m)
+    a, q, d, s = quantize_both(X)
+    Y = host(qx.qx_gemm_prefill_ex(fmt, dev(W), rows, cols, a, path=3))
+    assert np.all(np.isfinite(Y))
+    ref, absdot = oracle.gemm_w4a8(fmt, W, rows, cols, q, d)
+    assert_close(Y.reshape(-1), ref.reshape(-1), absdot.reshape(-1), f"tcgen05 prefill {synth.NAMES[fmt]} m={m}")
+
+
 def test_prefill_auto_and_refusals():
-    fmt, rows, cols, m = synth.Q4_K, 96, 1024, 16  # automatic path: tensor cores from 12 rows
+    fmt, rows, cols = synth.Q4_K, 96, 1024
     W = dev(synth.weights(fmt, rows, cols, seed=60))
-    a, q, d, s = quantize_both(synth.activation(m, cols, seed=61))
-    y_auto = host(qx.qx_gemm_prefill(fmt, W, rows, cols, a))
-    y_tc = host(qx.qx_gemm_prefill_ex(fmt, W, rows, cols, a, path=2))
-    assert np.array_equal(y_auto.view(np.uint32), y_tc.view(np.uint32))
+    # automatic path, Q4_K: GEMV per row below 12 rows, mma.sync below 192, tcgen05 from 192
     W6 = dev(synth.weights(synth.Q6_K, rows, cols, seed=62))
+    for Wm, f, m, forced in ((W, fmt, 11, 1), (W, fmt, 12, 2), (W, fmt, 191, 2), (W, fmt, 192, 3),
+                             (W6, synth.Q6_K, 15, 1), (W6, synth.Q6_K, 16, 3)):
+        a, q, d, s = quantize_both(synth.activation(m, cols, seed=61 + m))
+        y_auto = host(qx.qx_gemm_prefill(f, Wm, rows, cols, a))
+        y_forced = host(qx.qx_gemm_prefill_ex(f, Wm, rows, cols, a, path=forced))
+        assert np.array_equal(y_auto.view(np.uint32), y_forced.view(np.uint32)), f"m={m}"
     with pytest.raises(qx.QxError) as ei:
         qx.qx_gemm_prefill_ex(synth.Q6_K, W6, rows, cols, a, path=2)
     assert ei.value.status == qx.QX_ERR_FMT
+    with pytest.raises(qx.QxError) as ei:
+        qx.qx_gemm_prefill_ex(fmt, W, rows, cols, a, path=4)
+    assert ei.value.status == qx.QX_ERR_ARG
 
 
-def test_prefill_full_size_sampled():
+def test_prefill_caller_workspace_and_graph_capture():
+    fmt, rows, cols, m = synth.Q6_K, 200, 2048, 48
+    W = dev(synth.weights(fmt, rows, cols, seed=66))
+    a, q, d, s = quantize_both(synth.activation(m, cols, seed=67))
+    need = qx.qx_gemm_prefill_workspace_bytes(fmt, rows, cols, m)
+    assert need >= 4 * cols * (rows + m)
+    assert qx.qx_gemm_prefill_workspace_bytes(fmt, rows, cols + 1, m) == 0
+    y_lib = host(qx.qx_gemm_prefill_ex(fmt, W, rows, cols, a, path=3))
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    y_ws = host(qx.qx_gemm_prefill_ws(fmt, W, rows, cols, a, path=3, workspace=ws))
+    assert np.array_equal(y_lib.view(np.uint32), y_ws.view(np.uint32))
+    with pytest.raises(qx.QxError) as ei:
+        qx.qx_gemm_prefill_ws(fmt, W, rows, cols, a, path=3, workspace=ws[: need - 256])
+    assert ei.value.status == qx.QX_ERR_ARG
+    # caller workspace: the whole prefill is capturable and replays to the same bits
+    Y = torch.full((m, rows), float("nan"), device="cuda")
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        qx.qx_gemm_prefill_ws(fmt, W, rows, cols, a, Y=Y, path=3, workspace=ws, stream=stream)
+    g.replay()
+    assert np.array_equal(host(Y).view(np.uint32), y_lib.view(np.uint32))
+    # the library workspace cannot grow inside a capture: refused before any launch
+    big_rows = 1 << 17
+    Wbig = torch.zeros(big_rows * qx.qx_row_bytes(fmt, cols), dtype=torch.uint8, device="cuda")
+    Ybig = torch.empty((m, big_rows), device="cuda")
+    g2 = torch.cuda.CUDAGraph()
+    with pytest.raises(qx.QxError) as ei:
+        with torch.cuda.graph(g2, stream=stream):
+            qx.qx_gemm_prefill_ex(fmt, Wbig, big_rows, cols, a, Y=Ybig, path=3, stream=stream)
+    assert ei.value.status == qx.QX_ERR_ARG
+    torch.cuda.synchronize()
+    assert qx.qx_device_check() == qx.QX_OK
+
+
+@pytest.mark.parametrize("path", [2, 3])
+def test_prefill_full_size_sampled(path):
     """X [512, 4096] against Q4_K [14336, 4096]: sampled rows of X and of W against the oracle."""
     fmt, rows, cols, m = synth.Q4_K, 14336, 4096, 512
     W = synth.weights(fmt, rows, cols, seed=63)
     X = synth.activation(m, cols, seed=64)
     a, q, d, s = quantize_both(X)
-    Y = host(qx.qx_gemm_prefill_ex(fmt, dev(W), rows, cols, a, path=2))
+    Y = host(qx.qx_gemm_prefill_ex(fmt, dev(W), rows, cols, a, path=path))
     rng = np.random.default_rng(65)
     xr = np.sort(rng.choice(m, 6, replace=False))
     wr = np.sort(np.concatenate([rng.choice(rows, 250, replace=False), [0, rows - 1]]))
     ref, absdot = oracle.gemm_w4a8(fmt, np.ascontiguousarray(W[wr]), len(wr), cols, q[xr], d[xr])
-    assert_close(Y[np.ix_(xr, wr)].reshape(-1), ref.reshape(-1), absdot.reshape(-1), "prefill full size")
+    assert_close(Y[np.ix_(xr, wr)].reshape(-1), ref.reshape(-1), absdot.reshape(-1), f"prefill full size path {path}")
 
 
 # ---------------------------------------------------- device error word ----
