@@ -26,12 +26,12 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s bound on every pipeli
 constexpr size_t kStageTargetBytes = 48 * 1024;
 // Shared memory of a CTA that leaves room for a second one on the SM.
 constexpr size_t kHalfSmBytes = 110 * 1024;
-// Rows of X from which qx_gemm_prefill takes the tensor-core path.
-constexpr int64_t kPrefillTensorMinRows = 12;
-// Automatic prefill path: the tcgen05 GEMM from this many rows of X (from
-// kPrefillTcMinRowsQ4K for Q4_K, which has the mma.sync path below that).
+// Automatic prefill path (measured on GB300, X [m, 4096] x W [14336, 4096]):
+// the tcgen05 GEMM from this many rows of X, one GEMV per row below.  Q4_K
+// has the fused kernel (weights split in shared memory), the other formats
+// a dequantise pass first, hence the later crossover.
 constexpr int64_t kPrefillTcMinRows = 16;
-constexpr int64_t kPrefillTcMinRowsQ4K = 192;
+constexpr int64_t kPrefillTcMinRowsQ4K = 8;
 // Shared memory of a chain CTA (one per SM).
 constexpr size_t kChainSmBytes = 200 * 1024;
 constexpr int kMaxStageRows = 256;
@@ -394,16 +394,13 @@ qx_status prefill_dispatch(qx_fmt fmt, const void* W, int64_t rows, int64_t cols
     if ((st = check_act(X, 0, cols)) != QX_OK) return st;
     if (path < 0 || path > 3) return QX_ERR_ARG;
     if (path == 0) {
-        if (fmt == QX_Q4_K)
-            path = X->m >= kPrefillTcMinRowsQ4K ? 3 : (X->m >= kPrefillTensorMinRows ? 2 : 1);
-        else
-            path = X->m >= kPrefillTcMinRows ? 3 : 1;
+        path = X->m >= (fmt == QX_Q4_K ? kPrefillTcMinRowsQ4K : kPrefillTcMinRows) ? 3 : 1;
     }
     if (path == 3) {
         if (X->m > INT32_MAX || rows > INT32_MAX) return QX_ERR_SHAPE;
         DeviceInfo* dev = nullptr;
         if ((st = device_info(&dev)) != QX_OK) return st;
-        const size_t need = prefill_tc_workspace_bytes(rows, cols, X->m);
+        const size_t need = prefill_tc_workspace_bytes(fmt, rows, cols, X->m);
         const cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
         if (own_ws) {
             if ((st = prefill_workspace(need, cs, &ws)) != QX_OK) return st;
@@ -532,7 +529,7 @@ qx_status qx_gemm_prefill(qx_fmt fmt, const void* W, int64_t rows, int64_t cols,
 
 size_t qx_gemm_prefill_workspace_bytes(qx_fmt fmt, int64_t rows, int64_t cols, int64_t m) {
     if (check_shape(fmt, rows, cols) != QX_OK || m < 1) return 0;
-    return prefill_tc_workspace_bytes(rows, cols, m);
+    return prefill_tc_workspace_bytes(fmt, rows, cols, m);
 }
 
 qx_status qx_gemm_prefill_ws(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, float* Y,

@@ -158,9 +158,8 @@ qx_status qx_gemm_prefill(qx_fmt fmt, const void* W, int64_t rows, int64_t cols,
 
 /*
  * qx_gemm_prefill with a forced path:
- *   0 = automatic (by measured time): Q4_K: path 1 below 12 rows of X,
- *       path 2 below 192, path 3 from 192; other formats: path 1 below 16
- *       rows, path 3 from 16;
+ *   0 = automatic (by measured time): path 3 from 8 rows of X for Q4_K and
+ *       from 16 rows for the other formats, path 1 below;
  *   1 = one W4A8 GEMV launch per row of X (bit-for-bit the qx_gemv result);
  *   2 = mma.sync tensor-core GEMM, Q4_K only (integer-valued f16 operands,
  *       exact per-sub-block integer sums, scales applied per sub-block);
@@ -170,7 +169,9 @@ qx_status qx_gemm_prefill(qx_fmt fmt, const void* W, int64_t rows, int64_t cols,
  *       "CUDA"); both are written once as two bf16 terms (hi + lo, 16
  *       significant bits) and Y = Xh Wh^T + Xh Wl^T + Xl Wh^T is accumulated
  *       in f32 in tensor memory.  Each product's error is about 2^-15 of its
- *       magnitude.  Paths 0 and 3 use a workspace of
+ *       magnitude.  For Q4_K the weight terms are formed inside the GEMM
+ *       from the raw super-blocks; the other formats are dequantised into
+ *       the workspace first.  Paths 0 and 3 use a workspace of
  *       qx_gemm_prefill_workspace_bytes bytes that the library allocates on
  *       first use per device and keeps (growing it is refused with QX_ERR_ARG
  *       while the stream is being captured into a graph); calls that may run
@@ -183,8 +184,9 @@ qx_status qx_gemm_prefill_ex(qx_fmt fmt, const void* W, int64_t rows, int64_t co
 
 /*
  * Device bytes of the workspace that path 3 needs for this shape (two bf16
- * copies of the weights and of the activation: 4 * cols * (rows + m) bytes,
- * rounded up), or 0 for an invalid shape.
+ * copies of the activation, 4 * cols * m bytes, plus for Q6_K and Q8_0 two
+ * bf16 copies of the weights, 4 * cols * rows bytes; rounded up), or 0 for
+ * an invalid shape.
  */
 size_t qx_gemm_prefill_workspace_bytes(qx_fmt fmt, int64_t rows, int64_t cols, int64_t m);
 

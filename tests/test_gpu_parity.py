@@ -272,9 +272,9 @@ def test_prefill_tcgen05_formats(fmt, m, rows, cols):
 def test_prefill_auto_and_refusals():
     fmt, rows, cols = synth.Q4_K, 96, 1024
     W = dev(synth.weights(fmt, rows, cols, seed=60))
-    # automatic path, Q4_K: GEMV per row below 12 rows, mma.sync below 192, tcgen05 from 192
+    # automatic path: GEMV per row below 8 rows (Q4_K) or 16 rows (others), tcgen05 from there
     W6 = dev(synth.weights(synth.Q6_K, rows, cols, seed=62))
-    for Wm, f, m, forced in ((W, fmt, 11, 1), (W, fmt, 12, 2), (W, fmt, 191, 2), (W, fmt, 192, 3),
+    for Wm, f, m, forced in ((W, fmt, 7, 1), (W, fmt, 8, 3), (W, fmt, 200, 3),
                              (W6, synth.Q6_K, 15, 1), (W6, synth.Q6_K, 16, 3)):
         a, q, d, s = quantize_both(synth.activation(m, cols, seed=61 + m))
         y_auto = host(qx.qx_gemm_prefill(f, Wm, rows, cols, a))
@@ -294,6 +294,7 @@ def test_prefill_caller_workspace_and_graph_capture():
     a, q, d, s = quantize_both(synth.activation(m, cols, seed=67))
     need = qx.qx_gemm_prefill_workspace_bytes(fmt, rows, cols, m)
     assert need >= 4 * cols * (rows + m)
+    assert 4 * cols * m <= qx.qx_gemm_prefill_workspace_bytes(synth.Q4_K, rows, cols, m) < need
     assert qx.qx_gemm_prefill_workspace_bytes(fmt, rows, cols + 1, m) == 0
     y_lib = host(qx.qx_gemm_prefill_ex(fmt, W, rows, cols, a, path=3))
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
