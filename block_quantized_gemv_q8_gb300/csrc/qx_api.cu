@@ -195,7 +195,7 @@ qx_status team_geometry(int fmt, int kmode, bool partials, int64_t cols, int con
 qx_status gemv_geometry(int fmt, int kmode, bool partials, bool fused, bool pdl, int64_t cols,
                         const DeviceInfo& dev, GemvParams& p, size_t& smem) {
     TeamGeom g;
-    qx_status st = team_geometry(fmt, kmode, partials, cols, kGemvConsumerWarps, g);
+    qx_status st = team_geometry(fmt, kmode, partials, cols, gemv_consumer_warps(fmt, kmode), g);
     if (st != QX_OK) return st;
     const size_t slot = (size_t(g.G * g.rb) + kSlotPad + 127) / 128 * 128;
     const bool half_sm = (kmode == QX_MODE_W4A8 || fmt == QX_Q8_0);

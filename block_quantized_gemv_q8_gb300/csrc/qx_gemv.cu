@@ -36,7 +36,6 @@ namespace qx {
 namespace {
 
 using namespace lanes;
-constexpr int NW = kGemvConsumerWarps;
 
 
 // ----------------------------------------------------------------------------
@@ -82,9 +81,10 @@ constexpr int gemv_min_blocks() {
 }
 
 template <int FMT, int MODE, bool PART>
-__global__ void __launch_bounds__(kGemvThreads, gemv_min_blocks<FMT, MODE>())
+__global__ void __launch_bounds__(gemv_threads(FMT, MODE), gemv_min_blocks<FMT, MODE>())
     gemv_kernel(const __grid_constant__ GemvParams p) {
     using LaneT = Lane<FMT, MODE>;
+    constexpr int NW = gemv_consumer_warps(FMT, MODE);
     static_assert(PART || LaneT::kRows == gemv_rows_per_call(FMT, MODE), "row count must match the host geometry");
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = p.stages;
@@ -239,7 +239,7 @@ cudaError_t launch_one(const GemvParams& p, size_t smem, cudaStream_t s, bool pd
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.n_cta);
-    cfg.blockDim = dim3(kGemvThreads);
+    cfg.blockDim = dim3(gemv_threads(FMT, MODE));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -254,7 +254,8 @@ template <int FMT, int MODE, bool PART>
 cudaError_t occupancy_one(size_t smem, int* out) {
     cudaError_t err = configure_once<FMT, MODE, PART>();
     if (err != cudaSuccess) return err;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, gemv_kernel<FMT, MODE, PART>, kGemvThreads, smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, gemv_kernel<FMT, MODE, PART>, gemv_threads(FMT, MODE),
+                                                         smem);
 }
 
 }  // namespace

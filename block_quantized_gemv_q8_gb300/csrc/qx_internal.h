@@ -12,9 +12,13 @@ namespace qx {
 
 // Warps of a GEMV CTA: the consumers, then one producer warp (issues the
 // bulk copies) and one reducer warp (sums the consumers' per-lane partials of
-// each row and writes y).
-constexpr int kGemvConsumerWarps = 8;
-constexpr int kGemvThreads = 32 * (kGemvConsumerWarps + 2);
+// each row and writes y).  The f32-mode K-quant kernels run one CTA per SM
+// with 12 consumer warps (14 warps: at most 4 per SM partition, 128
+// registers each); the others two CTAs per SM with 8.
+__host__ __device__ constexpr int gemv_consumer_warps(int fmt, int mode) {
+    return (mode == QX_MODE_F32 && fmt != QX_Q8_0) ? 12 : 8;
+}
+__host__ __device__ constexpr int gemv_threads(int fmt, int mode) { return 32 * (gemv_consumer_warps(fmt, mode) + 2); }
 // Consumer warps per chain CTA (one CTA per SM), plus a producer and a reducer.
 constexpr int kChainConsumerWarps = 10;
 constexpr int kChainThreads = 32 * (kChainConsumerWarps + 2);

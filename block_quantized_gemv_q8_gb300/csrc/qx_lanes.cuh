@@ -28,6 +28,12 @@ __device__ __forceinline__ float small_uint_to_f32(uint32_t n) {
     return __int_as_float(0x4B000000u | n) - 8388608.0f;
 }
 
+// Byte k of w as the float 2^23 + byte (bits 0x4B0000bb), one byte-permute:
+// the caller subtracts 2^23 (plus any offset of the code) exactly.
+__device__ __forceinline__ float byte_biased_f32(uint32_t w, int k) {
+    return __int_as_float(__byte_perm(w, 0x4B000000u, 0x7540u + uint32_t(k)));
+}
+
 // N consecutive (possibly 2-byte aligned) little-endian words from shared
 // memory, read as N + 1 aligned words and funnel-shifted.
 template <int N>
@@ -184,10 +190,12 @@ struct Lane<QX_Q4_K, QX_MODE_F32> {
             float slo = 0.0f, shi = 0.0f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
+                // the low and the high nibbles, one per byte; each byte becomes an exact float
+                const uint32_t lo = w[i] & 0x0F0F0F0Fu, hi = (w[i] >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    slo = fmaf(small_uint_to_f32((w[i] >> (8 * k)) & 15u), x[4 * i + k], slo);
-                    shi = fmaf(small_uint_to_f32((w[i] >> (8 * k + 4)) & 15u), x[32 + 4 * i + k], shi);
+                    slo = fmaf(byte_biased_f32(lo, k) - 8388608.0f, x[4 * i + k], slo);
+                    shi = fmaf(byte_biased_f32(hi, k) - 8388608.0f, x[32 + 4 * i + k], shi);
                 }
             }
             const Q4KScales S = q4k_unpack_scales(hdr.y, hdr.z, hdr.w);
@@ -325,17 +333,18 @@ struct Lane<QX_Q6_K, QX_MODE_F32> {
             load_words<8>(bp + 128 + 32 * h, qh);
             load_words<2>(bp + 192 + 8 * h, scw);
             float sg[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // lo g0, lo g1, hi g0, hi g1
+            // qh bits 2 tp, 2 tp + 1 (quarter tp) and 2 tp + 4, 2 tp + 5 (quarter tp + 2) to bits 4, 5
+            const uint32_t sh_lo = 4u - 2u * uint32_t(tp), sh_hi = 2u * uint32_t(tp);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
+                // the 6-bit quants of both quarters, one per byte
+                const uint32_t wlo = (ql[i] & 0x0F0F0F0Fu) | ((qh[i] << sh_lo) & 0x30303030u);
+                const uint32_t whi = ((ql[i] >> 4) & 0x0F0F0F0Fu) | ((qh[i] >> sh_hi) & 0x30303030u);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const uint32_t nlo = ((ql[i] >> (8 * k)) & 15u) | (((qh[i] >> (8 * k + 2 * tp)) & 3u) << 4);
-                    const uint32_t nhi =
-                        ((ql[i] >> (8 * k + 4)) & 15u) | (((qh[i] >> (8 * k + 2 * tp + 4)) & 3u) << 4);
-                    // exact q - 32 in f32: the float with bits 0x4B000000 | q is 2^23 + q
-                    sg[i >> 2] = fmaf(__int_as_float(0x4B000000u | nlo) - 8388640.0f, x[4 * i + k], sg[i >> 2]);
-                    sg[2 + (i >> 2)] =
-                        fmaf(__int_as_float(0x4B000000u | nhi) - 8388640.0f, x[32 + 4 * i + k], sg[2 + (i >> 2)]);
+                    // exact q - 32 in f32: the float with bits 0x4B0000qq is 2^23 + q
+                    sg[i >> 2] = fmaf(byte_biased_f32(wlo, k) - 8388640.0f, x[4 * i + k], sg[i >> 2]);
+                    sg[2 + (i >> 2)] = fmaf(byte_biased_f32(whi, k) - 8388640.0f, x[32 + 4 * i + k], sg[2 + (i >> 2)]);
                 }
             }
             // scale bytes of this half: index 2t + g for t in {tp, tp + 2}
@@ -419,12 +428,10 @@ struct Lane<QX_Q8_0, QX_MODE_F32> {
             float acc = 0.0f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
+                // int8 -> f32 exactly: bias every byte by 128 into [0, 255]
+                const uint32_t u = qs[i] ^ 0x80808080u;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    // int8 -> f32 exactly: bias the byte by 128 into [0, 255].
-                    const uint32_t u = ((qs[i] >> (8 * k)) & 0xFFu) ^ 0x80u;
-                    acc = fmaf(__int_as_float(0x4B000000u | u) - 8388736.0f, x[4 * i + k], acc);
-                }
+                for (int k = 0; k < 4; ++k) acc = fmaf(byte_biased_f32(u, k) - 8388736.0f, x[4 * i + k], acc);
             }
             out[r] = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(bp)) * acc;
         }
