@@ -13,7 +13,8 @@ Prints one JSON line:
   value       weight-GB/s over the timed region (device-resident inputs)
   e2e         the same metric through the public API with pinned host
               activations copied in and all outputs copied back every step
-  roofline    the dominant (only) kernel, the chain: algorithmic bytes per
+  roofline    the dominant kernel of the faster form (the chain kernel, or the
+              gate/up GEMV launch of the per-launch form): algorithmic bytes per
               launch / its CUDA-event duration vs measured HBM bandwidth
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
 
@@ -54,6 +55,8 @@ def measured_peaks():
 
 CHAIN_SOURCES = ["qx_chain.cu", "qx_lanes.cuh", "qx_device.cuh", "qx_api.cu", "qx_internal.h"]
 CHAIN_PROFILE_NAME = "profiles/gemv_chain_llama8b.md"
+GEMV_SOURCES = ["qx_gemv.cu", "qx_lanes.cuh", "qx_device.cuh", "qx_api.cu", "qx_internal.h"]
+GATEUP_PROFILE_NAME = "profiles/gemv_q4k_w4a8_gateup_llama8b.md"
 
 
 def kernel_sources_hash(files) -> str:
@@ -83,6 +86,15 @@ def chain_traffic(layers: int):
     if "traffic_bytes_per_layer" not in f or f.get("source_sha256_16") != kernel_sources_hash(CHAIN_SOURCES):
         return None
     return int(f["traffic_bytes_per_layer"]) * layers
+
+
+def gateup_traffic():
+    """DRAM bytes of one gate/up GEMV launch from its committed ncu summary, or
+    None once the kernel sources differ from the captured ones."""
+    f = profile_fields(os.path.join(ROOT, GATEUP_PROFILE_NAME))
+    if "traffic_bytes_per_launch" not in f or f.get("source_sha256_16") != kernel_sources_hash(GEMV_SOURCES):
+        return None
+    return int(f["traffic_bytes_per_launch"])
 
 
 # ---------------------------------------------------------------- clocks ----
@@ -154,6 +166,9 @@ class LlamaDecode:
         self.launches_per_step = layers * 4
         self.dominant = "gemv_chain_kernel (the whole step: 128 dependent W4A8 GEMV jobs)"
         self.dominant_bytes = self.bytes_per_step
+        # dominant launch of the per-launch form: the Q4_K gate/up pair (2 x 14336 x 4096)
+        self.dominant_pdl = "gemv_kernel<Q4_K, W4A8> (gate/up: 2 x 14336 rows x 4096 cols, one launch)"
+        self.dominant_pdl_bytes = 2 * 14336 * synth.row_bytes(synth.Q4_K, 4096)
 
     def setup(self, qx, torch, seed_base: int = 0):
         self.W, self.y = [], []
@@ -500,6 +515,12 @@ def main():
     g_pdl = torch.cuda.CUDAGraph()             # the step as 128 PDL launches
     with torch.cuda.graph(g_pdl, stream=stream):
         wl.step(qx, stream)
+    # the same with events around every gate/up launch (the dominant launch)
+    dom_ev = [(torch.cuda.Event(enable_timing=True, external=True),
+               torch.cuda.Event(enable_timing=True, external=True)) for _ in range(wl.layers)]
+    g_pdl_ev = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_pdl_ev, stream=stream):
+        wl.step(qx, stream, dom_events=dom_ev)
     # e2e graph: pinned host activations in, step, all outputs back
     x_pin = torch.from_numpy(wl.x_host).pin_memory()
     y_pin = torch.empty(wl.y_all.numel(), dtype=torch.float32).pin_memory()
@@ -543,9 +564,15 @@ def main():
                 g_ev.replay()
                 ev[1].synchronize()
                 dom_ms.append(ev[0].elapsed_time(ev[1]))
-        for _ in range(args.warmup):
-            g_pdl.replay()
-        ms_pdl = timed(g_pdl, args.steps)
+            for _ in range(args.warmup):
+                g_pdl.replay()
+            ms_pdl = timed(g_pdl, args.steps)
+            # the gate/up launches' own durations, K instrumented steps read back one by one
+            dom_pdl_ms = []
+            for _ in range(args.steps):
+                g_pdl_ev.replay()
+                dom_ev[-1][1].synchronize()
+                dom_pdl_ms.extend(a.elapsed_time(b) for a, b in dom_ev)
         for _ in range(args.warmup):
             ge.replay()
         ms_e2e_chain = timed(ge, args.steps)
@@ -565,9 +592,21 @@ def main():
     value_e2e = per_s(ms_e2e)
     ms_best = ms if chain_is_faster else ms_pdl
     value, ms_step = per_s(ms_best), ms_best / args.steps
-    dom_mean_ms = statistics.mean(dom_ms)
-    achieved = wl.dominant_bytes / (dom_mean_ms * 1e-3) / 1e9
-    traffic = chain_traffic(wl.layers)
+    def roofline(kernel, nbytes, launch_ms, traffic, source, note):
+        achieved = nbytes / (launch_ms * 1e-3) / 1e9
+        return {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "peak_kind": peak_kind, "bytes_per_launch": nbytes,
+                "mean_launch_ms": launch_ms, "traffic": traffic, "traffic_source": source if traffic else None,
+                "note": note}
+    t_chain = chain_traffic(wl.layers)
+    roof_chain = roofline(wl.dominant, wl.dominant_bytes, statistics.mean(dom_ms), t_chain, CHAIN_PROFILE_NAME,
+                          "the chain kernel carries the whole step; timed with CUDA events around its launch")
+    t_gu = gateup_traffic()
+    roof_pdl = roofline(wl.dominant_pdl, wl.dominant_pdl_bytes, statistics.mean(dom_pdl_ms), t_gu,
+                        GATEUP_PROFILE_NAME,
+                        "61% of the per-launch form's device time (ncu launch list); timed with CUDA events "
+                        "around each of its 32 launches in an instrumented copy of the step graph; "
+                        "algorithmic bytes = the two Q4_K matrices (scales included)")
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
@@ -587,13 +626,8 @@ def main():
                        "parallelism": "replicas" if ws > 1 else "single"},
             "pct_of_hbm_peak": value / ws / hbm,
             "us_per_token": ms_step * 1e3,
-            "roofline": {"bound": "hbm", "kernel": wl.dominant, "achieved": achieved, "peak": hbm,
-                         "note": "the chain kernel carries the whole step, so it is the dominant kernel of "
-                                 "the chain form",
-                         "unit": "GB/s", "frac": achieved / hbm, "peak_kind": peak_kind,
-                         "bytes_per_launch": wl.dominant_bytes, "mean_launch_ms": dom_mean_ms,
-                         "traffic": traffic,
-                         "traffic_source": CHAIN_PROFILE_NAME if traffic else None},
+            "roofline": roof_chain if chain_is_faster else roof_pdl,
+            "roofline_other_form": roof_pdl if chain_is_faster else roof_chain,
             "e2e": {"value": value_e2e, "unit": "GB/s", "h2d_bytes_per_step": int(wl.x_host.nbytes),
                     "d2h_bytes_per_step": int(wl.y_all.numel() * 4), "ms_per_step": ms_e2e / args.steps},
             "per_launch_pdl": {"value": value_pdl, "unit": "GB/s", "ms_per_step": ms_pdl / args.steps,

@@ -35,6 +35,8 @@ constexpr int64_t kPrefillTcMinRowsQ4K = 8;
 // Shared memory of a chain CTA (one per SM).
 constexpr size_t kChainSmBytes = 200 * 1024;
 constexpr int kMaxStageRows = 256;
+// Launch bytes per SM up to which a PDL launch runs one CTA per SM.
+constexpr int64_t kOneCtaPerSmBytes = 192 * 1024;
 
 struct DeviceInfo {
     bool ready = false;
@@ -163,7 +165,7 @@ qx_status check_act(const qx_act_q8* a, int64_t m, int64_t cols) {
 // Teams and stage rows for one format/mode/width (see gemv_geometry).
 struct TeamGeom {
     int L, team_lanes, team_warps, nteams, quantum;
-    int64_t rb, G;
+    int64_t rb, G, base;  // base: the smallest stage (rows) that keeps teams and copies whole
 };
 
 qx_status team_geometry(int fmt, int kmode, bool partials, int64_t cols, int consumer_warps, TeamGeom& g) {
@@ -186,6 +188,7 @@ qx_status team_geometry(int fmt, int kmode, bool partials, int64_t cols, int con
     // every team gets the same number of whole row groups per stage
     const int64_t team_rows = int64_t(g.nteams) * (partials ? 1 : gemv_rows_per_call(fmt, kmode));
     const int64_t base = team_rows / gcd64(team_rows, g.quantum) * g.quantum;  // lcm
+    g.base = base;
     g.G = base;
     while (g.G + base <= kMaxStageRows && size_t((g.G + base) * g.rb) <= kStageTargetBytes) g.G += base;
     if (g.G > kMaxStageRows) g.G = base;  // very wide teams with tiny rows: keep one base group
@@ -197,29 +200,44 @@ qx_status gemv_geometry(int fmt, int kmode, bool partials, bool fused, bool pdl,
     TeamGeom g;
     qx_status st = team_geometry(fmt, kmode, partials, cols, gemv_consumer_warps(fmt, kmode), g);
     if (st != QX_OK) return st;
-    const size_t slot = (size_t(g.G * g.rb) + kSlotPad + 127) / 128 * 128;
     const bool half_sm = (kmode == QX_MODE_W4A8 || fmt == QX_Q8_0);
     const size_t budget = half_sm ? kHalfSmBytes : 200 * 1024;
     const size_t act = fused ? (size_t(cols) + size_t(cols / 32) * 8 + 15) / 16 * 16 : 0;
     // per stage: the slot, three mbarriers and (for y outputs) the per-lane partial sums
     const int RS = partial_stride(g.L);
+    const auto slot_of = [&](int64_t G) { return (size_t(G * g.rb) + kSlotPad + 127) / 128 * 128; };
+    // The quantised activation (fused mode) is dead once every lane has its
+    // slice in registers, before any partial sum is stored: the two share
+    // one area.
+    const auto bytes_for = [&](int64_t G, int st) {
+        const size_t red = partials ? 0 : size_t(st) * size_t(G) * RS * 4;
+        return size_t(st) * (slot_of(G) + 24) + 16 + (red > act ? red : act);
+    };
+    // Rows so wide that two stages exceed the budget: shrink the stage.
+    while (g.G > g.base && bytes_for(g.G, 2) > budget) g.G -= g.base;
+    const size_t slot = slot_of(g.G);
     const size_t red_stage = partials ? 0 : size_t(g.G) * RS * 4;
-    const auto bytes_for = [&](int st) { return size_t(st) * (slot + 24 + red_stage) + 16 + act; };
     int stages = 2;
-    while (stages < 8 && bytes_for(stages + 1) <= budget) ++stages;
+    while (stages < 8 && bytes_for(g.G, stages + 1) <= budget) ++stages;
     p.bar_off = static_cast<int>(size_t(stages) * slot);
     p.red_off = static_cast<int>((size_t(p.bar_off) + 24 * size_t(stages) + 15) / 16 * 16);
-    p.act_off = static_cast<int>((size_t(p.red_off) + size_t(stages) * red_stage + 15) / 16 * 16);
+    p.act_off = p.red_off;
     p.RS = RS;
-    smem = size_t(p.act_off) + act;
+    const size_t red_bytes = size_t(stages) * red_stage;
+    smem = size_t(p.red_off) + (red_bytes > act ? red_bytes : act);
     if (smem > 227 * 1024) return QX_ERR_SHAPE;
 
     int per_sm = 0;
     st = ctas_per_sm(fmt, kmode, partials, smem, &per_sm);
     if (st != QX_OK) return st;
-    const int want = 2;
+    // Under programmatic dependent launch, a launch that streams little per SM
+    // runs one CTA per SM: the rest of each SM then holds the next launch's
+    // CTA, which streams its weights during this launch's tail.  (GB300,
+    // Llama-3.1-8B decode step: q/k/v and o launches at one CTA per SM,
+    // gate/up and down at two, 1.38 ms per step; two everywhere, 1.47 ms.)
+    const bool small = p.total_rows * g.rb <= kOneCtaPerSmBytes * int64_t(dev.sm_count);
+    const int want = (pdl && small) ? 1 : 2;
     const int64_t max_cta = int64_t(dev.sm_count) * (per_sm < want ? per_sm : want);
-    (void)pdl;
     const int64_t groups = (p.total_rows + g.quantum - 1) / g.quantum;
     p.cols = cols;
     p.row_bytes = g.rb;

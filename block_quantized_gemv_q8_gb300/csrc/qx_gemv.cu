@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE), gemv_min_blocks<FMT, 
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
     uint64_t* empty = full + S;
     uint64_t* part = empty + S;
-    float* red = reinterpret_cast<float*>(smem + p.red_off);  // [S][G][RS]
+    float* red = reinterpret_cast<float*>(smem + p.red_off);  // [S][G][RS]; first the quantised activation
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t r0 = cta_row_begin(p, blockIdx.x), r1 = cta_row_begin(p, blockIdx.x + 1);
@@ -190,6 +190,10 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE), gemv_min_blocks<FMT, 
         }
     }
     if (tm.active) load_slice<MODE>(X, q, d, s, p.x, tm.slice);
+    if constexpr (MODE == QX_MODE_W4A8) {
+        // the quantised activation shares its area with the partial sums
+        if (p.xf != nullptr) consumer_barrier<NW>();
+    }
 
     const uint32_t rb = static_cast<uint32_t>(p.row_bytes);
     const int64_t ng = p.cols / (FMT == QX_Q6_K ? 16 : 32);

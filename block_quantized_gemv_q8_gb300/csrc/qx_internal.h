@@ -56,7 +56,8 @@ struct GemvParams {
     const float* xf;   // W4A8 with in-kernel quantisation: f32 activation [cols]
     int bar_off;       // shared-memory byte offsets: mbarriers (full, empty, part),
     int red_off;       //   per-lane partial sums [stages][G][RS],
-    int act_off;       //   quantised activation (in-kernel quantisation)
+    int act_off;       //   quantised activation (in-kernel quantisation; the same
+                       //   area as the partial sums, used before them)
     unsigned* err;     // device error word
     uint64_t wait_ns;  // bound on every wait
 };
