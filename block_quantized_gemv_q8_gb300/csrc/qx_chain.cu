@@ -103,7 +103,7 @@ __device__ __forceinline__ bool run_job(const ChainParams& p, const ChainJob& jb
     static_assert(LaneT::kRows == gemv_rows_per_call(FMT, QX_MODE_W4A8), "row count must match the host geometry");
     const Team tm = make_team(warp, lane, jb.team_lanes, jb.team_warps, jb.nteams, jb.L);
     LaneT X;
-    if (tm.active) X.load(q, d, s, tm.slice);
+    if (tm.active) X.load(q, d, s, tm.slice, FMT != QX_Q8_0);  // slices permuted in shared memory
     const uint32_t rb = static_cast<uint32_t>(jb.row_bytes);
     JobWalker wk{job_row_begin(jb, p.n_cta, blockIdx.x), job_row_begin(jb, p.n_cta, blockIdx.x + 1), 0};
     int e, nrows;
@@ -247,7 +247,8 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
             if (abort_flag) break;
         }
         const int nblk = static_cast<int>(jb.cols / 32);
-        for (int base = 0; base < 2 * nblk; base += NW * 32) quantize_task(jb.x, nblk, base + threadIdx.x, sq, sd, ss);
+        for (int base = 0; base < 2 * nblk; base += NW * 32)
+            quantize_task(jb.x, nblk, base + threadIdx.x, sq, sd, ss, jb.fmt != QX_Q8_0);
         consumer_barrier<NW>();
         bool jok;
         switch (jb.fmt) {

@@ -144,11 +144,8 @@ __device__ __forceinline__ bool quotient_rounding_is_safe(float t, float k) {
 // all lanes of the warp taking part).  A lane with live == false takes part in
 // the shuffles only and stores nothing; the lane holding the block's first
 // values (first == true) stores d and sum.
-template <int N, int THREADS>
-__device__ __forceinline__ void quantize_block_part(const float* __restrict__ x, int8_t* __restrict__ q,
-                                                    float* d, int32_t* sum, bool live, bool first) {
-    static_assert(N * THREADS == 32 && N % 4 == 0, "a block is 32 values, stored in 4-byte groups");
-    float v[N];
+template <int N>
+__device__ __forceinline__ void load_block_part(const float* __restrict__ x, float (&v)[N]) {
     const float4* src = reinterpret_cast<const float4*>(x);
 #pragma unroll
     for (int k = 0; k < N / 4; ++k) {
@@ -158,6 +155,12 @@ __device__ __forceinline__ void quantize_block_part(const float* __restrict__ x,
         v[4 * k + 2] = f.z;
         v[4 * k + 3] = f.w;
     }
+}
+
+template <int N, int THREADS>
+__device__ __forceinline__ void quantize_block_values(const float (&v)[N], int8_t* __restrict__ q, float* d,
+                                                      int32_t* sum, bool live, bool first) {
+    static_assert(N * THREADS == 32 && N % 4 == 0, "a block is 32 values, stored in 4-byte groups");
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < N; ++i) amax = fmaxf(amax, fabsf(v[i]));
@@ -165,36 +168,35 @@ __device__ __forceinline__ void quantize_block_part(const float* __restrict__ x,
     for (int o = 1; o < THREADS; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float db = __fdiv_rn(amax, 127.0f);
     float r[N];
-    unsigned slow = 0;
     if (db != 0.0f) {
         const float rcp = __frcp_rn(db);
+        bool safe = true;
 #pragma unroll
         for (int i = 0; i < N; ++i) {
             const float t = v[i] * rcp;
             r[i] = rintf(t);
-            slow |= quotient_rounding_is_safe(t, r[i]) ? 0u : (1u << i);
+            safe &= quotient_rounding_is_safe(t, r[i]);
         }
-        if (slow) {
+        if (!safe) {  // rare: some quotient lies too close to a rounding boundary
 #pragma unroll
-            for (int i = 0; i < N; ++i)
-                if (slow & (1u << i)) r[i] = rintf(__fdiv_rn(v[i], db));
+            for (int i = 0; i < N; ++i) r[i] = rintf(__fdiv_rn(v[i], db));
         }
     } else {
 #pragma unroll
         for (int i = 0; i < N; ++i) r[i] = 0.0f;
     }
+    // |x / d| <= 127 (1 + 2^-23) for every x of the block, so every code is
+    // already within [-127, 127]: the clamp of the definition never binds.
     uint32_t packed[N / 4];
     int s = 0;
 #pragma unroll
     for (int j = 0; j < N / 4; ++j) {
-        uint32_t w = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int qi = static_cast<int>(fminf(fmaxf(r[4 * j + i], -127.0f), 127.0f));
-            s += qi;
-            w |= (static_cast<uint32_t>(qi) & 0xFFu) << (8 * i);
-        }
-        packed[j] = w;
+        const int q0 = static_cast<int>(r[4 * j]), q1 = static_cast<int>(r[4 * j + 1]);
+        const int q2 = static_cast<int>(r[4 * j + 2]), q3 = static_cast<int>(r[4 * j + 3]);
+        const uint32_t lo = __byte_perm(uint32_t(q0), uint32_t(q1), 0x0040u);  // bytes q0, q1
+        const uint32_t hi = __byte_perm(uint32_t(q2), uint32_t(q3), 0x0040u);  // bytes q2, q3
+        packed[j] = __byte_perm(lo, hi, 0x5410u);
+        s = __dp4a(static_cast<int>(packed[j]), 0x01010101, s);  // + q0 + q1 + q2 + q3 (signed bytes)
     }
 #pragma unroll
     for (int o = 1; o < THREADS; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
@@ -209,15 +211,31 @@ __device__ __forceinline__ void quantize_block_part(const float* __restrict__ x,
     }
 }
 
+template <int N, int THREADS>
+__device__ __forceinline__ void quantize_block_part(const float* __restrict__ x, int8_t* __restrict__ q,
+                                                    float* d, int32_t* sum, bool live, bool first) {
+    float v[N];
+    load_block_part<N>(x, v);
+    quantize_block_values<N, THREADS>(v, q, d, sum, live, first);
+}
+
 // Quantise blocks [0, nblocks) with two adjacent lanes per block, 16 values
 // each: `task` runs over 2 * nblocks in rounds of `stride` (a multiple of 32),
 // and every lane calls this the same number of times.  x, q: 16-byte aligned.
+// With `swz`, the 16-byte chunk G of q is stored at chunk G ^ ((G / 8) % 8):
+// the chunks of each 128-byte slice are permuted by the slice's index, so
+// that 32 lanes reading their slices chunk by chunk hit distinct banks
+// (act_chunk_swizzle gives the inverse for the reader).
+__device__ __forceinline__ int64_t act_chunk_swizzle(int64_t chunk) { return chunk ^ ((chunk >> 3) & 7); }
+
 __device__ __forceinline__ void quantize_task(const float* __restrict__ x, int64_t nblocks, int64_t task,
-                                              int8_t* __restrict__ q, float* d, int32_t* sum) {
+                                              int8_t* __restrict__ q, float* d, int32_t* sum, bool swz = false) {
     const bool live = task < 2 * nblocks;
     const int64_t b = live ? task >> 1 : nblocks - 1;
     const int half = static_cast<int>(task & 1);
-    quantize_block_part<16, 2>(x + b * 32 + half * 16, q + b * 32 + half * 16, d + b, sum + b, live, half == 0);
+    const int64_t chunk = 2 * b + half;
+    quantize_block_part<16, 2>(x + b * 32 + half * 16, q + 16 * (swz ? act_chunk_swizzle(chunk) : chunk), d + b,
+                               sum + b, live, half == 0);
 }
 
 // fp16 bit pattern -> f32 (exact; subnormals kept).

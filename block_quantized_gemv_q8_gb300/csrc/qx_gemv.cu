@@ -123,6 +123,10 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE), gemv_min_blocks<FMT, 
         unsigned tail_slots = 0;  // slots whose bytes were last written by plain stores
         for (int k = 0; wk.next(p, e, lrow, nrows); ++k) {
             const int slot = k % S;
+            // Only the first stage streams ahead of the preceding kernel; the
+            // rest waits for it to complete, so a full ring of requests from
+            // every CTA does not land on top of its completion.
+            if (k == 1) pdl_wait_prior_grid();
             if (k >= S && !mbar_wait_bounded(&empty[slot], ((k / S) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty))
                 break;
             const uint8_t* src = p.e[e].W + lrow * p.row_bytes;
@@ -182,14 +186,15 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE), gemv_min_blocks<FMT, 
             int32_t* ss = reinterpret_cast<int32_t*>(sd + p.cols / 32);
             const int nblk = static_cast<int>(p.cols / 32);
             for (int base = 0; base < 2 * nblk; base += NW * 32)
-                quantize_task(p.xf, nblk, base + threadIdx.x, sq, sd, ss);
+                quantize_task(p.xf, nblk, base + threadIdx.x, sq, sd, ss, FMT != QX_Q8_0);
             consumer_barrier<NW>();
             q = sq;
             d = sd;
             s = ss;
         }
     }
-    if (tm.active) load_slice<MODE>(X, q, d, s, p.x, tm.slice);
+    // the quantised activation in shared memory has its 128-byte slices permuted
+    if (tm.active) load_slice<MODE>(X, q, d, s, p.x, tm.slice, FMT != QX_Q8_0 && p.xf != nullptr);
     if constexpr (MODE == QX_MODE_W4A8) {
         // the quantised activation shares its area with the partial sums
         if (p.xf != nullptr) consumer_barrier<NW>();

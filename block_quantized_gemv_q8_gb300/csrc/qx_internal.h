@@ -100,7 +100,7 @@ __host__ __device__ constexpr int partial_stride(int L) {
 
 // Rows a team computes per call, per (format, mode) (must match the kernels).
 __host__ __device__ constexpr int gemv_rows_per_call(int fmt, int mode) {
-    return (fmt == QX_Q8_0 || (fmt == QX_Q4_K && mode == QX_MODE_W4A8)) ? 2 : 1;
+    return fmt == QX_Q8_0 ? 2 : 1;
 }
 
 // Launchers (defined in the kernel translation units).

@@ -100,15 +100,17 @@ template <>
 struct Lane<QX_Q4_K, QX_MODE_W4A8> {
     static constexpr int C = 128;
     static constexpr int kGroups = 4;  // partials per lane
-    static constexpr int kRows = 2;    // rows per call
+    static constexpr int kRows = 1;    // rows per call
     uint32_t xq[32];
     float dxs[4];  // dx of sub-block u; the odd (high-nibble) ones divided by 16
     float t[4];    // dx * (sum of q_x) of sub-block u: weight of the min term
-    __device__ __forceinline__ void load(const int8_t* q, const float* d, const int32_t* s, int l) {
+    // swz: the slice's 16-byte chunks are stored permuted (act_chunk_swizzle)
+    __device__ __forceinline__ void load(const int8_t* q, const float* d, const int32_t* s, int l, bool swz) {
         const uint4* src = reinterpret_cast<const uint4*>(q + int64_t(l) * C);
+        const int sw = swz ? (l & 7) : 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            const uint4 v = src[k];
+            const uint4 v = src[k ^ sw];
             xq[4 * k + 0] = v.x;
             xq[4 * k + 1] = v.y;
             xq[4 * k + 2] = v.z;
@@ -251,11 +253,12 @@ struct Lane<QX_Q6_K, QX_MODE_W4A8> {
     uint32_t xq[32];
     float dx[4];
     int s16[8];  // sum of q_x over each 16-group
-    __device__ __forceinline__ void load(const int8_t* q, const float* d, const int32_t*, int l) {
+    __device__ __forceinline__ void load(const int8_t* q, const float* d, const int32_t*, int l, bool swz) {
         const uint4* src = reinterpret_cast<const uint4*>(q + int64_t(l) * C);
+        const int sw = swz ? (l & 7) : 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            const uint4 v = src[k];
+            const uint4 v = src[k ^ sw];
             xq[4 * k + 0] = v.x;
             xq[4 * k + 1] = v.y;
             xq[4 * k + 2] = v.z;
@@ -366,7 +369,7 @@ struct Lane<QX_Q8_0, QX_MODE_W4A8> {
     static constexpr int kRows = 2;
     uint32_t xq[8];
     float dx;
-    __device__ __forceinline__ void load(const int8_t* q, const float* d, const int32_t*, int l) {
+    __device__ __forceinline__ void load(const int8_t* q, const float* d, const int32_t*, int l, bool) {
         const uint4* src = reinterpret_cast<const uint4*>(q + int64_t(l) * C);
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
@@ -543,9 +546,9 @@ __device__ __forceinline__ void reduce_stage(const float* red, int RS, int L, in
 // the f32 activation.
 template <int MODE, class LaneT>
 __device__ __forceinline__ void load_slice(LaneT& X, const int8_t* q, const float* d, const int32_t* s,
-                                           const float* xf, int slice) {
+                                           const float* xf, int slice, bool swz) {
     if constexpr (MODE == QX_MODE_W4A8) {
-        X.load(q, d, s, slice);
+        X.load(q, d, s, slice, swz);
     } else {
         X.load(xf, slice);
     }
