@@ -34,6 +34,30 @@ __device__ __forceinline__ float byte_biased_f32(uint32_t w, int k) {
     return __int_as_float(__byte_perm(w, 0x4B000000u, 0x7540u + uint32_t(k)));
 }
 
+// Packed pairs of f32 (two lanes of one 64-bit register) and the sm_103a
+// two-wide f32 add and fused multiply-add on them (each element rounded as
+// its scalar counterpart).
+__device__ __forceinline__ uint64_t f32x2_pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float2 f32x2_unpack(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
 // N consecutive (possibly 2-byte aligned) little-endian words from shared
 // memory, read as N + 1 aligned words and funnel-shifted.
 template <int N>
@@ -308,7 +332,7 @@ struct Lane<QX_Q6_K, QX_MODE_F32> {
     static constexpr int C = 64;
     static constexpr int kGroups = 1;
     static constexpr int kRows = 1;
-    float x[64];
+    uint64_t x2[32];  // the 64 activation values as 32 packed pairs (x[2j], x[2j + 1])
     __device__ __forceinline__ void load(const float* xp, int l) {
         const int sb = l >> 2, h = (l >> 1) & 1, tp = l & 1;
         const int64_t c0 = int64_t(sb) * 256 + 128 * h + 32 * tp;
@@ -318,16 +342,16 @@ struct Lane<QX_Q6_K, QX_MODE_F32> {
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const float4 v = src[k];
-                x[32 * half + 4 * k + 0] = v.x;
-                x[32 * half + 4 * k + 1] = v.y;
-                x[32 * half + 4 * k + 2] = v.z;
-                x[32 * half + 4 * k + 3] = v.w;
+                x2[16 * half + 2 * k + 0] = f32x2_pack(v.x, v.y);
+                x2[16 * half + 2 * k + 1] = f32x2_pack(v.z, v.w);
             }
         }
     }
     template <int R>
     __device__ __forceinline__ void rows(const uint8_t* const (&rp)[R], int l, float (&out)[R]) const {
         const int sb = l >> 2, h = (l >> 1) & 1, tp = l & 1;
+        // 2^23 + q minus (2^23 + 32) = q - 32, exactly, two at a time
+        const uint64_t bias = f32x2_pack(-8388640.0f, -8388640.0f);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const uint8_t* bp = rp[r] + sb * 210;
@@ -335,7 +359,7 @@ struct Lane<QX_Q6_K, QX_MODE_F32> {
             load_words<8>(bp + 64 * h + 32 * tp, ql);
             load_words<8>(bp + 128 + 32 * h, qh);
             load_words<2>(bp + 192 + 8 * h, scw);
-            float sg[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // lo g0, lo g1, hi g0, hi g1
+            uint64_t sg2[4] = {0, 0, 0, 0};  // lo g0, lo g1, hi g0, hi g1; two running sums each
             // qh bits 2 tp, 2 tp + 1 (quarter tp) and 2 tp + 4, 2 tp + 5 (quarter tp + 2) to bits 4, 5
             const uint32_t sh_lo = 4u - 2u * uint32_t(tp), sh_hi = 2u * uint32_t(tp);
 #pragma unroll
@@ -344,11 +368,20 @@ struct Lane<QX_Q6_K, QX_MODE_F32> {
                 const uint32_t wlo = (ql[i] & 0x0F0F0F0Fu) | ((qh[i] << sh_lo) & 0x30303030u);
                 const uint32_t whi = ((ql[i] >> 4) & 0x0F0F0F0Fu) | ((qh[i] >> sh_hi) & 0x30303030u);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    // exact q - 32 in f32: the float with bits 0x4B0000qq is 2^23 + q
-                    sg[i >> 2] = fmaf(byte_biased_f32(wlo, k) - 8388640.0f, x[4 * i + k], sg[i >> 2]);
-                    sg[2 + (i >> 2)] = fmaf(byte_biased_f32(whi, k) - 8388640.0f, x[32 + 4 * i + k], sg[2 + (i >> 2)]);
+                for (int kp = 0; kp < 2; ++kp) {
+                    const uint64_t flo =
+                        f32x2_add(f32x2_pack(byte_biased_f32(wlo, 2 * kp), byte_biased_f32(wlo, 2 * kp + 1)), bias);
+                    const uint64_t fhi =
+                        f32x2_add(f32x2_pack(byte_biased_f32(whi, 2 * kp), byte_biased_f32(whi, 2 * kp + 1)), bias);
+                    sg2[i >> 2] = f32x2_fma(flo, x2[2 * i + kp], sg2[i >> 2]);
+                    sg2[2 + (i >> 2)] = f32x2_fma(fhi, x2[16 + 2 * i + kp], sg2[2 + (i >> 2)]);
                 }
+            }
+            float sg[4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const float2 v = f32x2_unpack(sg2[g]);
+                sg[g] = v.x + v.y;
             }
             // scale bytes of this half: index 2t + g for t in {tp, tp + 2}
             const int lo0 = 2 * tp, hi0 = 2 * tp + 4;
