@@ -37,6 +37,9 @@ constexpr size_t kChainSmBytes = 200 * 1024;
 constexpr int kMaxStageRows = 256;
 // Launch bytes per SM up to which a PDL launch runs one CTA per SM.
 constexpr int64_t kOneCtaPerSmBytes = 192 * 1024;
+// Launches streaming at least this many bytes take the merged variant where
+// one exists (gemv_has_merged).
+constexpr int64_t kMergedMinBytes = int64_t(128) << 20;
 
 struct DeviceInfo {
     bool ready = false;
@@ -57,13 +60,13 @@ qx_status cuda_fail(cudaError_t e, const char* where) {
     return QX_ERR_CUDA;
 }
 // Resident CTAs per SM, keyed by (device, format, mode, partials, smem bytes).
-std::map<std::tuple<int, int, int, int, size_t>, int> g_occupancy;
+std::map<std::tuple<int, int, int, int, int, size_t>, int> g_occupancy;
 
-qx_status ctas_per_sm(int fmt, int mode, bool partials, size_t smem, int* out) {
+qx_status ctas_per_sm(int fmt, int mode, bool partials, bool merged, size_t smem, int* out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    const auto key = std::make_tuple(dev, fmt, mode, partials ? 1 : 0, smem);
+    const auto key = std::make_tuple(dev, fmt, mode, partials ? 1 : 0, merged ? 1 : 0, smem);
     {
         std::lock_guard<std::mutex> lock(g_mu);
         auto it = g_occupancy.find(key);
@@ -73,7 +76,7 @@ qx_status ctas_per_sm(int fmt, int mode, bool partials, size_t smem, int* out) {
         }
     }
     int n = 0;
-    if ((e = gemv_max_ctas_per_sm(fmt, mode, partials, smem, &n)) != cudaSuccess)
+    if ((e = gemv_max_ctas_per_sm(fmt, mode, partials, merged, smem, &n)) != cudaSuccess)
         return cuda_fail(e, "occupancy query");
     if (n < 1) return cuda_fail(cudaErrorInvalidConfiguration, "no CTA fits on an SM");
     std::lock_guard<std::mutex> lock(g_mu);
@@ -178,10 +181,11 @@ qx_status team_geometry(int fmt, int kmode, bool partials, int64_t cols, int con
         g.team_warps = 1;
         g.nteams = consumer_warps * (32 / g.team_lanes);
     } else {
+        // teams of exactly L lanes, packed across warps
         g.team_warps = (g.L + 31) / 32;
         if (g.team_warps > consumer_warps) return QX_ERR_SHAPE;
-        g.nteams = consumer_warps / g.team_warps;
-        g.team_lanes = 32 * g.team_warps;
+        g.nteams = consumer_warps * 32 / g.L;
+        g.team_lanes = g.L;
     }
     g.rb = cols / block_weights(fmt) * block_bytes(fmt);
     g.quantum = static_cast<int>(16 / gcd64(g.rb, 16));
@@ -197,8 +201,15 @@ qx_status team_geometry(int fmt, int kmode, bool partials, int64_t cols, int con
 
 qx_status gemv_geometry(int fmt, int kmode, bool partials, bool fused, bool pdl, int64_t cols,
                         const DeviceInfo& dev, GemvParams& p, size_t& smem) {
+    // The merged Q6_K W4A8 variant streams faster in steady state (lm_head
+    // class launches: 5.95 TB/s against 5.40) but, packed next to the
+    // following launches under PDL, costs the Llama-3.1-8B decode step more
+    // than it saves on its 48 MB down projections: long launches only.
+    const int64_t rb = cols / block_weights(fmt) * block_bytes(fmt);
+    const bool merged = gemv_has_merged(fmt, kmode, partials) && p.total_rows * rb >= kMergedMinBytes;
+    p.merged = merged ? 1 : 0;
     TeamGeom g;
-    qx_status st = team_geometry(fmt, kmode, partials, cols, gemv_consumer_warps(fmt, kmode), g);
+    qx_status st = team_geometry(fmt, kmode, partials, cols, gemv_consumer_warps(fmt, kmode, merged), g);
     if (st != QX_OK) return st;
     const bool half_sm = (kmode == QX_MODE_W4A8 || fmt == QX_Q8_0);
     const size_t budget = half_sm ? kHalfSmBytes : 200 * 1024;
@@ -228,7 +239,7 @@ qx_status gemv_geometry(int fmt, int kmode, bool partials, bool fused, bool pdl,
     if (smem > 227 * 1024) return QX_ERR_SHAPE;
 
     int per_sm = 0;
-    st = ctas_per_sm(fmt, kmode, partials, smem, &per_sm);
+    st = ctas_per_sm(fmt, kmode, partials, merged, smem, &per_sm);
     if (st != QX_OK) return st;
     // Under programmatic dependent launch, a launch that streams little per SM
     // runs one CTA per SM: the rest of each SM then holds the next launch's
@@ -237,6 +248,11 @@ qx_status gemv_geometry(int fmt, int kmode, bool partials, bool fused, bool pdl,
     // gate/up and down at two, 1.38 ms per step; two everywhere, 1.47 ms.)
     const bool small = p.total_rows * g.rb <= kOneCtaPerSmBytes * int64_t(dev.sm_count);
     const int want = (pdl && small) ? 1 : 2;
+    // A small launch fills its whole ring ahead of the preceding kernel's
+    // completion; a large one only its first stage (measured on the same
+    // step: 1.217 ms against 1.230 ms with one stage everywhere, 1.241 ms
+    // with the whole ring everywhere).
+    p.prewait = small ? stages : 1;
     const int64_t max_cta = int64_t(dev.sm_count) * (per_sm < want ? per_sm : want);
     const int64_t groups = (p.total_rows + g.quantum - 1) / g.quantum;
     p.cols = cols;

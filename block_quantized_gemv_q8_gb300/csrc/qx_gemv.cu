@@ -80,17 +80,23 @@ constexpr int gemv_min_blocks() {
     return (MODE == QX_MODE_W4A8 || FMT == QX_Q8_0) ? 2 : 1;
 }
 
-template <int FMT, int MODE, bool PART>
-__global__ void __launch_bounds__(gemv_threads(FMT, MODE), gemv_min_blocks<FMT, MODE>())
+template <int FMT, int MODE, bool PART, bool MERGED>
+__global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_min_blocks<FMT, MODE>())
     gemv_kernel(const __grid_constant__ GemvParams p) {
     using LaneT = Lane<FMT, MODE>;
-    constexpr int NW = gemv_consumer_warps(FMT, MODE);
+    constexpr int NW = gemv_consumer_warps(FMT, MODE, MERGED);
+    constexpr bool kMerged = MERGED;
+    static_assert(!MERGED || gemv_has_merged(FMT, MODE, PART), "no merged variant of this kernel");
+    // warps that quantise an f32 activation in-kernel: the consumers, and a
+    // merged producer/reducer warp (it has nothing to reduce before then)
+    constexpr int QW = NW + (kMerged ? 1 : 0);
     static_assert(PART || LaneT::kRows == gemv_rows_per_call(FMT, MODE), "row count must match the host geometry");
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = p.stages;
     // full[s]: the slot's bytes have landed.  empty[s]: the consumers (and,
-    // for y outputs, the reducer) are done with the slot and its partials.
-    // part[s]: the consumers' partials of the slot's rows are stored.
+    // with a separate reducer warp, the reducer) are done with the slot and
+    // its partials.  part[s] (y outputs): the consumers' partials of the
+    // slot's rows are stored, and they are done with its bytes.
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
     uint64_t* empty = full + S;
     uint64_t* part = empty + S;
@@ -102,7 +108,7 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE), gemv_min_blocks<FMT, 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], PART ? NW : NW + 1);
+            mbar_init(&empty[s], (PART || kMerged) ? NW : NW + 1);
             mbar_init(&part[s], NW);
         }
         fence_barrier_init();
@@ -111,24 +117,24 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE), gemv_min_blocks<FMT, 
     pdl_launch_dependents();
 
     if (warp == NW) {
-        // ---------------- producer: one lane issues every bulk copy ----------
-        // Weights are never written by the preceding kernel, so they are
-        // fetched before the programmatic dependency on it is resolved.
-        if (lane != 0) return;
-        StageWalker wk{r0, r1, 0};
+        // ---------------- producer (and, merged, reducer) ---------------------
+        // Lane 0 issues every bulk copy.  Weights are never written by the
+        // preceding kernel, so the first p.prewait stages are fetched before
+        // the programmatic dependency on it is resolved.  Then lane 0 refills
+        // each slot once `empty` says its previous stage is done with -- or,
+        // when this warp is also the reducer, right after the warp has reduced
+        // that stage (the reducer is a slot's last user: the consumers are
+        // done with its bytes once their partials are stored).
         const uint64_t policy = policy_evict_first();
-        int e, nrows;
-        int64_t lrow;
+        StageWalker wk{r0, r1, 0};
         int issued = 0;
         unsigned tail_slots = 0;  // slots whose bytes were last written by plain stores
-        for (int k = 0; wk.next(p, e, lrow, nrows); ++k) {
-            const int slot = k % S;
-            // Only the first stage streams ahead of the preceding kernel; the
-            // rest waits for it to complete, so a full ring of requests from
-            // every CTA does not land on top of its completion.
-            if (k == 1) pdl_wait_prior_grid();
-            if (k >= S && !mbar_wait_bounded(&empty[slot], ((k / S) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty))
-                break;
+        // Copies the next stage into its slot; false once the CTA's rows are exhausted.
+        const auto issue_next = [&]() -> bool {
+            int e, nrows;
+            int64_t lrow;
+            if (!wk.next(p, e, lrow, nrows)) return false;
+            const int k = issued, slot = k % S;
             const uint8_t* src = p.e[e].W + lrow * p.row_bytes;
             const uint32_t bytes = static_cast<uint32_t>(int64_t(nrows) * p.row_bytes);
             const uint32_t abytes = bytes & ~15u;
@@ -144,16 +150,86 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE), gemv_min_blocks<FMT, 
             mbar_arrive_expect_tx(&full[slot], abytes);
             if (abytes) bulk_g2s_evict_first(dst, src, abytes, &full[slot], policy);
             issued = k + 1;
+            return true;
+        };
+        const auto issue_first_stages = [&]() {
+            for (int k = 0; k < S; ++k) {
+                if (k == p.prewait) pdl_wait_prior_grid();
+                if (!issue_next()) break;
+            }
+        };
+        // Keep the CTA alive until every copy it issued has landed (bounded;
+        // on the normal path each wait returns at once or shortly).
+        const auto drain = [&]() {
+            for (int k = issued > S ? issued - S : 0; k < issued; ++k)
+                mbar_wait_bounded(&full[k % S], (k / S) & 1, p.wait_ns, p.err, kErrTimeoutDrain);
+        };
+        if constexpr (!kMerged) {
+            if (lane != 0) return;
+            int e, nrows;
+            int64_t lrow;
+            StageWalker pw{r0, r1, 0};
+            for (int k = 0; pw.next(p, e, lrow, nrows); ++k) {
+                const int slot = k % S;
+                if (k == p.prewait) pdl_wait_prior_grid();
+                if (k >= S && !mbar_wait_bounded(&empty[slot], ((k / S) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty))
+                    break;
+                const uint8_t* src = p.e[e].W + lrow * p.row_bytes;
+                const uint32_t bytes = static_cast<uint32_t>(int64_t(nrows) * p.row_bytes);
+                const uint32_t abytes = bytes & ~15u;
+                uint8_t* dst = smem + size_t(slot) * p.slot_bytes;
+                if (bytes != abytes) {
+                    for (uint32_t t = abytes; t < bytes; ++t) dst[t] = src[t];
+                    tail_slots |= 1u << slot;
+                } else if (tail_slots & (1u << slot)) {
+                    fence_proxy_async_smem();
+                    tail_slots &= ~(1u << slot);
+                }
+                mbar_arrive_expect_tx(&full[slot], abytes);
+                if (abytes) bulk_g2s_evict_first(dst, src, abytes, &full[slot], policy);
+                issued = k + 1;
+            }
+            drain();
+        } else {
+            if (lane == 0) issue_first_stages();
+            // The other lanes wait here for lane 0, and below for each refill,
+            // so that the warp never sits in two different waits at once.
+            __syncwarp();
+            if constexpr (MODE == QX_MODE_W4A8) {
+                if (p.xf != nullptr) {
+                    // this warp's share of the in-kernel quantisation, and the
+                    // consumers' two barriers around it (see below)
+                    pdl_wait_prior_grid();
+                    int8_t* sq = reinterpret_cast<int8_t*>(smem + p.act_off);
+                    float* sd = reinterpret_cast<float*>(sq + p.cols);
+                    int32_t* ss = reinterpret_cast<int32_t*>(sd + p.cols / 32);
+                    const int nblk = static_cast<int>(p.cols / 32);
+                    for (int base = 0; base < 2 * nblk; base += QW * 32)
+                        quantize_task(p.xf, nblk, base + threadIdx.x, sq, sd, ss, FMT != QX_Q8_0);
+                    consumer_barrier<QW>();
+                    consumer_barrier<QW>();
+                }
+            }
+            StageWalker rw{r0, r1, 0};
+            int e, nrows;
+            int64_t lrow;
+            for (int k = 0; rw.next(p, e, lrow, nrows); ++k) {
+                const int slot = k % S;
+                const bool landed = mbar_wait_bounded(&part[slot], (k / S) & 1, p.wait_ns, p.err, kErrTimeoutFull);
+                if (!__all_sync(0xffffffffu, landed)) break;  // the whole warp leaves together
+                reduce_stage(red + size_t(slot) * p.G * p.RS, p.RS, p.L, nrows, p.e[e].y + lrow, lane);
+                __syncwarp();
+                if (lane == 0) issue_next();
+                __syncwarp();
+            }
+            if (lane == 0) drain();
         }
-        // Keep the CTA alive until every copy it issued has landed.
-        for (int k = issued > S ? issued - S : 0; k < issued; ++k)
-            mbar_wait_bounded(&full[k % S], (k / S) & 1, p.wait_ns, p.err, kErrTimeoutDrain);
         return;
     }
 
-    if (warp == NW + 1) {
-        // ---------------- reducer: row sums of every stage, in order -------
-        if constexpr (!PART) {
+    if constexpr (!PART && !kMerged) {
+        if (warp == NW + 1) {
+            // ---------------- reducer: row sums of every stage, in order -----
             StageWalker wk{r0, r1, 0};
             int e, nrows;
             int64_t lrow;
@@ -164,8 +240,8 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE), gemv_min_blocks<FMT, 
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[slot]);
             }
+            return;
         }
-        return;
     }
 
     // ---------------- consumers ----------------------------------------------
@@ -180,14 +256,15 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE), gemv_min_blocks<FMT, 
         if (p.xf != nullptr) {
             // Quantise the f32 activation once per CTA into shared memory,
             // with the same code as qx_quantize_act_q8; two adjacent lanes
-            // per block of 32, all consumer lanes take part.
+            // per block of 32; all consumer lanes (and a merged
+            // producer/reducer warp) take part.
             int8_t* sq = reinterpret_cast<int8_t*>(smem + p.act_off);
             float* sd = reinterpret_cast<float*>(sq + p.cols);
             int32_t* ss = reinterpret_cast<int32_t*>(sd + p.cols / 32);
             const int nblk = static_cast<int>(p.cols / 32);
-            for (int base = 0; base < 2 * nblk; base += NW * 32)
+            for (int base = 0; base < 2 * nblk; base += QW * 32)
                 quantize_task(p.xf, nblk, base + threadIdx.x, sq, sd, ss, FMT != QX_Q8_0);
-            consumer_barrier<NW>();
+            consumer_barrier<QW>();
             q = sq;
             d = sd;
             s = ss;
@@ -197,7 +274,7 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE), gemv_min_blocks<FMT, 
     if (tm.active) load_slice<MODE>(X, q, d, s, p.x, tm.slice, FMT != QX_Q8_0 && p.xf != nullptr);
     if constexpr (MODE == QX_MODE_W4A8) {
         // the quantised activation shares its area with the partial sums
-        if (p.xf != nullptr) consumer_barrier<NW>();
+        if (p.xf != nullptr) consumer_barrier<QW>();
     }
 
     const uint32_t rb = static_cast<uint32_t>(p.row_bytes);
@@ -214,7 +291,7 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE), gemv_min_blocks<FMT, 
         __syncwarp();
         if (lane == 0) {
             if constexpr (!PART) mbar_arrive(&part[slot]);
-            mbar_arrive(&empty[slot]);
+            if constexpr (!kMerged) mbar_arrive(&empty[slot]);
         }
     }
 }
@@ -225,7 +302,7 @@ constexpr int kMaxDynamicSmem = 227 * 1024;
 // Raise the kernel's dynamic shared-memory limit to the maximum, once per
 // kernel and device.  Occupancy and launches then depend only on the bytes
 // each launch asks for.
-template <int FMT, int MODE, bool PART>
+template <int FMT, int MODE, bool PART, bool MERGED>
 cudaError_t configure_once() {
     static bool done[64] = {false};
     int dev = 0;
@@ -234,21 +311,21 @@ cudaError_t configure_once() {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (done[dev]) return cudaSuccess;
     cudaFuncAttributes fa;
-    err = cudaFuncGetAttributes(&fa, gemv_kernel<FMT, MODE, PART>);
+    err = cudaFuncGetAttributes(&fa, gemv_kernel<FMT, MODE, PART, MERGED>);
     if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(gemv_kernel<FMT, MODE, PART>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(gemv_kernel<FMT, MODE, PART, MERGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kMaxDynamicSmem - static_cast<int>(fa.sharedSizeBytes));
     if (err == cudaSuccess) done[dev] = true;
     return err;
 }
 
-template <int FMT, int MODE, bool PART>
+template <int FMT, int MODE, bool PART, bool MERGED>
 cudaError_t launch_one(const GemvParams& p, size_t smem, cudaStream_t s, bool pdl) {
-    cudaError_t err = configure_once<FMT, MODE, PART>();
+    cudaError_t err = configure_once<FMT, MODE, PART, MERGED>();
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.n_cta);
-    cfg.blockDim = dim3(gemv_threads(FMT, MODE));
+    cfg.blockDim = dim3(gemv_threads(FMT, MODE, PART, MERGED));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -256,46 +333,56 @@ cudaError_t launch_one(const GemvParams& p, size_t smem, cudaStream_t s, bool pd
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<FMT, MODE, PART>, p);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<FMT, MODE, PART, MERGED>, p);
 }
 
-template <int FMT, int MODE, bool PART>
+template <int FMT, int MODE, bool PART, bool MERGED>
 cudaError_t occupancy_one(size_t smem, int* out) {
-    cudaError_t err = configure_once<FMT, MODE, PART>();
+    cudaError_t err = configure_once<FMT, MODE, PART, MERGED>();
     if (err != cudaSuccess) return err;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, gemv_kernel<FMT, MODE, PART>, gemv_threads(FMT, MODE),
-                                                         smem);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, gemv_kernel<FMT, MODE, PART, MERGED>,
+                                                         gemv_threads(FMT, MODE, PART, MERGED), smem);
 }
 
 }  // namespace
 
 cudaError_t launch_gemv(int fmt, int mode, bool partials, const GemvParams& p, size_t smem, cudaStream_t s,
                         bool pdl) {
+    if (p.merged) {
+        if (fmt == QX_Q6_K && mode == QX_MODE_W4A8 && !partials)
+            return launch_one<QX_Q6_K, QX_MODE_W4A8, false, true>(p, smem, s, pdl);
+        return cudaErrorInvalidValue;
+    }
     switch (fmt * 4 + mode * 2 + (partials ? 1 : 0)) {
-        case QX_Q4_K * 4 + 0: return launch_one<QX_Q4_K, QX_MODE_F32, false>(p, smem, s, pdl);
-        case QX_Q4_K * 4 + 2: return launch_one<QX_Q4_K, QX_MODE_W4A8, false>(p, smem, s, pdl);
-        case QX_Q4_K * 4 + 3: return launch_one<QX_Q4_K, QX_MODE_W4A8, true>(p, smem, s, pdl);
-        case QX_Q6_K * 4 + 0: return launch_one<QX_Q6_K, QX_MODE_F32, false>(p, smem, s, pdl);
-        case QX_Q6_K * 4 + 2: return launch_one<QX_Q6_K, QX_MODE_W4A8, false>(p, smem, s, pdl);
-        case QX_Q6_K * 4 + 3: return launch_one<QX_Q6_K, QX_MODE_W4A8, true>(p, smem, s, pdl);
-        case QX_Q8_0 * 4 + 0: return launch_one<QX_Q8_0, QX_MODE_F32, false>(p, smem, s, pdl);
-        case QX_Q8_0 * 4 + 2: return launch_one<QX_Q8_0, QX_MODE_W4A8, false>(p, smem, s, pdl);
-        case QX_Q8_0 * 4 + 3: return launch_one<QX_Q8_0, QX_MODE_W4A8, true>(p, smem, s, pdl);
+        case QX_Q4_K * 4 + 0: return launch_one<QX_Q4_K, QX_MODE_F32, false, false>(p, smem, s, pdl);
+        case QX_Q4_K * 4 + 2: return launch_one<QX_Q4_K, QX_MODE_W4A8, false, false>(p, smem, s, pdl);
+        case QX_Q4_K * 4 + 3: return launch_one<QX_Q4_K, QX_MODE_W4A8, true, false>(p, smem, s, pdl);
+        case QX_Q6_K * 4 + 0: return launch_one<QX_Q6_K, QX_MODE_F32, false, false>(p, smem, s, pdl);
+        case QX_Q6_K * 4 + 2: return launch_one<QX_Q6_K, QX_MODE_W4A8, false, false>(p, smem, s, pdl);
+        case QX_Q6_K * 4 + 3: return launch_one<QX_Q6_K, QX_MODE_W4A8, true, false>(p, smem, s, pdl);
+        case QX_Q8_0 * 4 + 0: return launch_one<QX_Q8_0, QX_MODE_F32, false, false>(p, smem, s, pdl);
+        case QX_Q8_0 * 4 + 2: return launch_one<QX_Q8_0, QX_MODE_W4A8, false, false>(p, smem, s, pdl);
+        case QX_Q8_0 * 4 + 3: return launch_one<QX_Q8_0, QX_MODE_W4A8, true, false>(p, smem, s, pdl);
         default: return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t gemv_max_ctas_per_sm(int fmt, int mode, bool partials, size_t smem, int* out) {
+cudaError_t gemv_max_ctas_per_sm(int fmt, int mode, bool partials, bool merged, size_t smem, int* out) {
+    if (merged) {
+        if (fmt == QX_Q6_K && mode == QX_MODE_W4A8 && !partials)
+            return occupancy_one<QX_Q6_K, QX_MODE_W4A8, false, true>(smem, out);
+        return cudaErrorInvalidValue;
+    }
     switch (fmt * 4 + mode * 2 + (partials ? 1 : 0)) {
-        case QX_Q4_K * 4 + 0: return occupancy_one<QX_Q4_K, QX_MODE_F32, false>(smem, out);
-        case QX_Q4_K * 4 + 2: return occupancy_one<QX_Q4_K, QX_MODE_W4A8, false>(smem, out);
-        case QX_Q4_K * 4 + 3: return occupancy_one<QX_Q4_K, QX_MODE_W4A8, true>(smem, out);
-        case QX_Q6_K * 4 + 0: return occupancy_one<QX_Q6_K, QX_MODE_F32, false>(smem, out);
-        case QX_Q6_K * 4 + 2: return occupancy_one<QX_Q6_K, QX_MODE_W4A8, false>(smem, out);
-        case QX_Q6_K * 4 + 3: return occupancy_one<QX_Q6_K, QX_MODE_W4A8, true>(smem, out);
-        case QX_Q8_0 * 4 + 0: return occupancy_one<QX_Q8_0, QX_MODE_F32, false>(smem, out);
-        case QX_Q8_0 * 4 + 2: return occupancy_one<QX_Q8_0, QX_MODE_W4A8, false>(smem, out);
-        case QX_Q8_0 * 4 + 3: return occupancy_one<QX_Q8_0, QX_MODE_W4A8, true>(smem, out);
+        case QX_Q4_K * 4 + 0: return occupancy_one<QX_Q4_K, QX_MODE_F32, false, false>(smem, out);
+        case QX_Q4_K * 4 + 2: return occupancy_one<QX_Q4_K, QX_MODE_W4A8, false, false>(smem, out);
+        case QX_Q4_K * 4 + 3: return occupancy_one<QX_Q4_K, QX_MODE_W4A8, true, false>(smem, out);
+        case QX_Q6_K * 4 + 0: return occupancy_one<QX_Q6_K, QX_MODE_F32, false, false>(smem, out);
+        case QX_Q6_K * 4 + 2: return occupancy_one<QX_Q6_K, QX_MODE_W4A8, false, false>(smem, out);
+        case QX_Q6_K * 4 + 3: return occupancy_one<QX_Q6_K, QX_MODE_W4A8, true, false>(smem, out);
+        case QX_Q8_0 * 4 + 0: return occupancy_one<QX_Q8_0, QX_MODE_F32, false, false>(smem, out);
+        case QX_Q8_0 * 4 + 2: return occupancy_one<QX_Q8_0, QX_MODE_W4A8, false, false>(smem, out);
+        case QX_Q8_0 * 4 + 3: return occupancy_one<QX_Q8_0, QX_MODE_W4A8, true, false>(smem, out);
         default: return cudaErrorInvalidValue;
     }
 }

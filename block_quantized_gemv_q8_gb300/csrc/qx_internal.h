@@ -10,15 +10,29 @@
 
 namespace qx {
 
-// Warps of a GEMV CTA: the consumers, then one producer warp (issues the
-// bulk copies) and one reducer warp (sums the consumers' per-lane partials of
-// each row and writes y).  The f32-mode K-quant kernels run one CTA per SM
-// with 12 consumer warps (14 warps: at most 4 per SM partition, 128
-// registers each); the others two CTAs per SM with 8.
-__host__ __device__ constexpr int gemv_consumer_warps(int fmt, int mode) {
-    return (mode == QX_MODE_F32 && fmt != QX_Q8_0) ? 12 : 8;
+// Warps of a GEMV CTA: the consumers, then a producer warp whose lane 0
+// issues the bulk copies, then (y outputs) a reducer warp that sums the
+// consumers' per-lane partials of each row and writes y.  An SM partition
+// holds 16K registers, so a kernel with up to 16 warps per SM (4 per
+// partition) gets 128 registers a thread, one with 17 to 20 warps 96.  The
+// f32-mode K-quant kernels run one CTA per SM with 12 consumer warps, the
+// others two per SM with 8.
+//
+// The merged variant (Q6_K W4A8 with y outputs; taken for long launches, see
+// gemv_geometry): 7 consumer warps and one warp that both produces and
+// reduces, 16 warps per SM and so 128 registers (the standard Q6_K W4A8
+// kernel is held to 96 and spills); rows of 14336 columns are then exactly
+// two teams of 112 lanes.
+__host__ __device__ constexpr bool gemv_has_merged(int fmt, int mode, bool partials) {
+    return !partials && mode == QX_MODE_W4A8 && fmt == QX_Q6_K;
 }
-__host__ __device__ constexpr int gemv_threads(int fmt, int mode) { return 32 * (gemv_consumer_warps(fmt, mode) + 2); }
+__host__ __device__ constexpr int gemv_consumer_warps(int fmt, int mode, bool merged) {
+    return (mode == QX_MODE_F32 && fmt != QX_Q8_0) ? 12 : (merged ? 7 : 8);
+}
+// Integer partials need no reducer warp; the merged variant has none either.
+__host__ __device__ constexpr int gemv_threads(int fmt, int mode, bool partials, bool merged) {
+    return 32 * (gemv_consumer_warps(fmt, mode, merged) + ((partials || merged) ? 1 : 2));
+}
 // Consumer warps per chain CTA (one CTA per SM), plus a producer and a reducer.
 constexpr int kChainConsumerWarps = 10;
 constexpr int kChainThreads = 32 * (kChainConsumerWarps + 2);
@@ -43,12 +57,14 @@ struct GemvParams {
     int G;            // rows per pipeline stage
     int stages;       // pipeline depth (shared-memory slots)
     int slot_bytes;   // bytes per slot, including kSlotPad
-    int team_lanes;   // lanes per team: a power of two <= 32, or 32 * team_warps
-    int team_warps;   // warps per team (1 for sub-warp teams)
+    int team_lanes;   // lanes per team: a power of two <= 32, or L (teams packed across warps)
+    int team_warps;   // 1 for sub-warp teams, else the warps a team touches (> 1)
     int nteams;       // teams per CTA
     int L;            // lanes with work per row (cols / columns-per-lane)
     int RS;           // floats per row of the per-lane partial-sum area
     int n_cta;
+    int prewait;       // stages the producer issues before waiting on the preceding kernel
+    int merged;        // 1: the merged producer/reducer variant (gemv_has_merged)
     const float* x;    // f32 mode activation [cols]
     const int8_t* xq;  // W4A8 activation quants [cols]
     const float* xd;   // W4A8 activation scales [cols/32]
@@ -108,7 +124,7 @@ cudaError_t launch_actq8(const float* x, int64_t nblocks, int8_t* q, float* d, i
                          cudaStream_t s);
 cudaError_t launch_gemv(int fmt, int mode, bool partials, const GemvParams& p, size_t smem, cudaStream_t s,
                         bool pdl);
-cudaError_t gemv_max_ctas_per_sm(int fmt, int mode, bool partials, size_t smem, int* out);
+cudaError_t gemv_max_ctas_per_sm(int fmt, int mode, bool partials, bool merged, size_t smem, int* out);
 cudaError_t launch_timeout_probe(unsigned* err, uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_chain(const ChainParams& p, size_t smem, cudaStream_t s);
 cudaError_t launch_prefill_q4k(const uint8_t* W, int64_t N, int64_t K, const int8_t* xq, const float* xd,

@@ -183,29 +183,31 @@ struct Lane<QX_Q4_K, QX_MODE_F32> {
     static constexpr int C = 64;
     static constexpr int kGroups = 1;
     static constexpr int kRows = 1;
-    float x[64];
+    uint64_t x2[32];  // the 64 activation values as 32 packed pairs (x[2j], x[2j + 1])
     float xsum[2];
     __device__ __forceinline__ void load(const float* xp, int l) {
         const float4* src = reinterpret_cast<const float4*>(xp + int64_t(l) * C);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float4 v = src[k];
-            x[4 * k + 0] = v.x;
-            x[4 * k + 1] = v.y;
-            x[4 * k + 2] = v.z;
-            x[4 * k + 3] = v.w;
-        }
-#pragma unroll
         for (int u = 0; u < 2; ++u) {
             float s = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) s += x[32 * u + i];
+            for (int k = 0; k < 8; ++k) {
+                const float4 v = src[8 * u + k];
+                x2[16 * u + 2 * k + 0] = f32x2_pack(v.x, v.y);
+                x2[16 * u + 2 * k + 1] = f32x2_pack(v.z, v.w);
+                s += v.x;
+                s += v.y;
+                s += v.z;
+                s += v.w;
+            }
             xsum[u] = s;
         }
     }
     template <int R>
     __device__ __forceinline__ void rows(const uint8_t* const (&rp)[R], int l, float (&out)[R]) const {
         const int sb = l >> 2, c = l & 3;
+        // 2^23 + q minus 2^23 = q, exactly, two at a time
+        const uint64_t bias = f32x2_pack(-8388608.0f, -8388608.0f);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const uint8_t* bp = rp[r] + sb * 144;
@@ -213,16 +215,27 @@ struct Lane<QX_Q4_K, QX_MODE_F32> {
             const uint4* qsp = reinterpret_cast<const uint4*>(bp + 16 + 32 * c);
             const uint4 a = qsp[0], b = qsp[1];
             const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            float slo = 0.0f, shi = 0.0f;
+            uint64_t s2[4] = {0, 0, 0, 0};  // low nibbles (two sums), high nibbles (two sums)
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 // the low and the high nibbles, one per byte; each byte becomes an exact float
                 const uint32_t lo = w[i] & 0x0F0F0F0Fu, hi = (w[i] >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    slo = fmaf(byte_biased_f32(lo, k) - 8388608.0f, x[4 * i + k], slo);
-                    shi = fmaf(byte_biased_f32(hi, k) - 8388608.0f, x[32 + 4 * i + k], shi);
+                for (int kp = 0; kp < 2; ++kp) {
+                    const uint64_t flo =
+                        f32x2_add(f32x2_pack(byte_biased_f32(lo, 2 * kp), byte_biased_f32(lo, 2 * kp + 1)), bias);
+                    const uint64_t fhi =
+                        f32x2_add(f32x2_pack(byte_biased_f32(hi, 2 * kp), byte_biased_f32(hi, 2 * kp + 1)), bias);
+                    s2[i & 1] = f32x2_fma(flo, x2[2 * i + kp], s2[i & 1]);
+                    s2[2 + (i & 1)] = f32x2_fma(fhi, x2[16 + 2 * i + kp], s2[2 + (i & 1)]);
                 }
+            }
+            float slo, shi;
+            {
+                const float2 a0 = f32x2_unpack(s2[0]), a1 = f32x2_unpack(s2[1]);
+                const float2 b0 = f32x2_unpack(s2[2]), b1 = f32x2_unpack(s2[3]);
+                slo = (a0.x + a0.y) + (a1.x + a1.y);
+                shi = (b0.x + b0.y) + (b1.x + b1.y);
             }
             const Q4KScales S = q4k_unpack_scales(hdr.y, hdr.z, hdr.w);
             const uint32_t scw = c < 2 ? S.sc_lo : S.sc_hi;
@@ -442,34 +455,38 @@ struct Lane<QX_Q8_0, QX_MODE_F32> {
     static constexpr int C = 32;
     static constexpr int kGroups = 1;
     static constexpr int kRows = 2;
-    float x[32];
+    uint64_t x2[16];  // the 32 activation values as 16 packed pairs
     __device__ __forceinline__ void load(const float* xp, int l) {
         const float4* src = reinterpret_cast<const float4*>(xp + int64_t(l) * C);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const float4 v = src[k];
-            x[4 * k + 0] = v.x;
-            x[4 * k + 1] = v.y;
-            x[4 * k + 2] = v.z;
-            x[4 * k + 3] = v.w;
+            x2[2 * k + 0] = f32x2_pack(v.x, v.y);
+            x2[2 * k + 1] = f32x2_pack(v.z, v.w);
         }
     }
     template <int R>
     __device__ __forceinline__ void rows(const uint8_t* const (&rp)[R], int l, float (&out)[R]) const {
+        // int8 -> f32 exactly: every byte biased by 128 into [0, 255], then 2^23 + 128 taken off
+        const uint64_t bias = f32x2_pack(-8388736.0f, -8388736.0f);
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const uint8_t* bp = rp[r] + l * 34;
             uint32_t qs[8];
             load_words<8>(bp + 2, qs);
-            float acc = 0.0f;
+            uint64_t s2[2] = {0, 0};
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                // int8 -> f32 exactly: bias every byte by 128 into [0, 255]
                 const uint32_t u = qs[i] ^ 0x80808080u;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) acc = fmaf(byte_biased_f32(u, k) - 8388736.0f, x[4 * i + k], acc);
+                for (int kp = 0; kp < 2; ++kp) {
+                    const uint64_t f =
+                        f32x2_add(f32x2_pack(byte_biased_f32(u, 2 * kp), byte_biased_f32(u, 2 * kp + 1)), bias);
+                    s2[i & 1] = f32x2_fma(f, x2[2 * i + kp], s2[i & 1]);
+                }
             }
-            out[r] = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(bp)) * acc;
+            const float2 a0 = f32x2_unpack(s2[0]), a1 = f32x2_unpack(s2[1]);
+            out[r] = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(bp)) * ((a0.x + a0.y) + (a1.x + a1.y));
         }
     }
 };
@@ -493,8 +510,11 @@ __device__ __forceinline__ Team make_team(int warp, int lane, int team_lanes, in
         t.team = warp * (32 / team_lanes) + lane / team_lanes;
         t.slice = lane % team_lanes;
     } else {
-        t.team = warp / team_warps;
-        t.slice = (warp % team_warps) * 32 + lane;
+        // teams of exactly L lanes packed across warp boundaries: the per-lane
+        // partials meet only in shared memory, so a team need not be whole warps
+        const int flat = warp * 32 + lane;
+        t.team = flat / team_lanes;
+        t.slice = flat % team_lanes;
     }
     t.in_team = t.team < nteams;
     t.active = t.in_team && t.slice < L;
@@ -587,11 +607,12 @@ __device__ __forceinline__ void load_slice(LaneT& X, const int8_t* q, const floa
     }
 }
 
-// Synchronise the CONSUMER_WARPS consumer warps only (the producer warp never
-// joins).
-template <int CONSUMER_WARPS>
+// Synchronise warps 0 .. WARPS - 1 only (the consumers, and in the GEMV
+// kernel a merged producer/reducer warp; a separate producer or reducer warp
+// never joins).
+template <int WARPS>
 __device__ __forceinline__ void consumer_barrier() {
-    asm volatile("bar.sync 1, %0;" ::"n"(CONSUMER_WARPS * 32) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(WARPS * 32) : "memory");
 }
 
 }  // namespace lanes
