@@ -87,9 +87,21 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
     constexpr int NW = gemv_consumer_warps(FMT, MODE, MERGED);
     constexpr bool kMerged = MERGED;
     static_assert(!MERGED || gemv_has_merged(FMT, MODE, PART), "no merged variant of this kernel");
-    // warps that quantise an f32 activation in-kernel: the consumers, and a
-    // merged producer/reducer warp (it has nothing to reduce before then)
-    constexpr int QW = NW + (kMerged ? 1 : 0);
+    // Warps that may quantise an f32 activation in-kernel: all of them -- the
+    // producer and the reducer have nothing else to do until the consumers
+    // finish their first stage, which needs the quantised activation.  They
+    // join only when that takes fewer rounds of two-lane block tasks than the
+    // consumers alone (each round waits on its loads: the 14336-column
+    // activation of a Llama-3.1-8B down projection, 4 rounds -> 3); a merged
+    // producer/reducer warp always joins.  The Q4_K and Q8_0 kernels are
+    // built without helpers: the extra code slowed their one-round launches
+    // measurably (GB300, Llama-3.1-8B q/k/v launch 5.24 -> 5.30 us).
+    constexpr int QW = NW + 1 + ((!PART && !kMerged) ? 1 : 0);
+    constexpr bool kMayHelp = kMerged || FMT == QX_Q6_K;
+    const int ntask = static_cast<int>(2 * (p.cols / 32));
+    const bool helpers =
+        kMerged || (kMayHelp && (ntask + NW * 32 - 1) / (NW * 32) > (ntask + QW * 32 - 1) / (QW * 32));
+    const int qthreads = helpers ? QW * 32 : NW * 32;  // threads that quantise (and sync around it)
     static_assert(PART || LaneT::kRows == gemv_rows_per_call(FMT, MODE), "row count must match the host geometry");
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = p.stages;
@@ -115,6 +127,21 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
     }
     __syncthreads();
     pdl_launch_dependents();
+
+    // A producer or reducer warp's share of the in-kernel quantisation (W4A8
+    // with an f32 activation), with the consumers' two barriers around it:
+    // the codes are complete / every consumer holds its slice (see below).
+    const auto quantise_share = [&]() {
+        pdl_wait_prior_grid();  // the activation may come from the previous kernel
+        int8_t* sq = reinterpret_cast<int8_t*>(smem + p.act_off);
+        float* sd = reinterpret_cast<float*>(sq + p.cols);
+        int32_t* ss = reinterpret_cast<int32_t*>(sd + p.cols / 32);
+        const int nblk = static_cast<int>(p.cols / 32);
+        for (int base = 0; base < 2 * nblk; base += qthreads)
+            quantize_task(p.xf, nblk, base + threadIdx.x, sq, sd, ss, FMT != QX_Q8_0);
+        quantiser_barrier(qthreads);
+        quantiser_barrier(qthreads);
+    };
 
     if (warp == NW) {
         // ---------------- producer (and, merged, reducer) ---------------------
@@ -165,15 +192,41 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
                 mbar_wait_bounded(&full[k % S], (k / S) & 1, p.wait_ns, p.err, kErrTimeoutDrain);
         };
         if constexpr (!kMerged) {
-            if (lane != 0) return;
-            int e, nrows;
-            int64_t lrow;
+            const bool helps = MODE == QX_MODE_W4A8 && p.xf != nullptr && helpers;
+            if (!helps) {
+                if (lane != 0) return;
+                int e, nrows;
+                int64_t lrow;
+                StageWalker pw{r0, r1, 0};
+                for (int k = 0; pw.next(p, e, lrow, nrows); ++k) {
+                    const int slot = k % S;
+                    if (k == p.prewait) pdl_wait_prior_grid();
+                    if (k >= S &&
+                        !mbar_wait_bounded(&empty[slot], ((k / S) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty))
+                        break;
+                    const uint8_t* src = p.e[e].W + lrow * p.row_bytes;
+                    const uint32_t bytes = static_cast<uint32_t>(int64_t(nrows) * p.row_bytes);
+                    const uint32_t abytes = bytes & ~15u;
+                    uint8_t* dst = smem + size_t(slot) * p.slot_bytes;
+                    if (bytes != abytes) {
+                        for (uint32_t t = abytes; t < bytes; ++t) dst[t] = src[t];
+                        tail_slots |= 1u << slot;
+                    } else if (tail_slots & (1u << slot)) {
+                        fence_proxy_async_smem();
+                        tail_slots &= ~(1u << slot);
+                    }
+                    mbar_arrive_expect_tx(&full[slot], abytes);
+                    if (abytes) bulk_g2s_evict_first(dst, src, abytes, &full[slot], policy);
+                    issued = k + 1;
+                }
+                drain();
+                return;
+            }
+            int e = 0, nrows = 0;
+            int64_t lrow = 0;
             StageWalker pw{r0, r1, 0};
-            for (int k = 0; pw.next(p, e, lrow, nrows); ++k) {
+            const auto issue_stage = [&](int k) {
                 const int slot = k % S;
-                if (k == p.prewait) pdl_wait_prior_grid();
-                if (k >= S && !mbar_wait_bounded(&empty[slot], ((k / S) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty))
-                    break;
                 const uint8_t* src = p.e[e].W + lrow * p.row_bytes;
                 const uint32_t bytes = static_cast<uint32_t>(int64_t(nrows) * p.row_bytes);
                 const uint32_t abytes = bytes & ~15u;
@@ -188,6 +241,26 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
                 mbar_arrive_expect_tx(&full[slot], abytes);
                 if (abytes) bulk_g2s_evict_first(dst, src, abytes, &full[slot], policy);
                 issued = k + 1;
+            };
+            // the first S stages (no slot to wait for), then the quantisation
+            // share, then every later stage once its slot is released
+            int k = 0;
+            bool more = true;
+            if (lane == 0) {
+                for (; k < S && (more = pw.next(p, e, lrow, nrows)); ++k) {
+                    if (k == p.prewait) pdl_wait_prior_grid();
+                    issue_stage(k);
+                }
+            }
+            __syncwarp();
+            quantise_share();
+            if (lane != 0) return;
+            if (more) {
+                for (; pw.next(p, e, lrow, nrows); ++k) {
+                    if (k == p.prewait) pdl_wait_prior_grid();
+                    if (!mbar_wait_bounded(&empty[k % S], ((k / S) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty)) break;
+                    issue_stage(k);
+                }
             }
             drain();
         } else {
@@ -195,21 +268,7 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
             // The other lanes wait here for lane 0, and below for each refill,
             // so that the warp never sits in two different waits at once.
             __syncwarp();
-            if constexpr (MODE == QX_MODE_W4A8) {
-                if (p.xf != nullptr) {
-                    // this warp's share of the in-kernel quantisation, and the
-                    // consumers' two barriers around it (see below)
-                    pdl_wait_prior_grid();
-                    int8_t* sq = reinterpret_cast<int8_t*>(smem + p.act_off);
-                    float* sd = reinterpret_cast<float*>(sq + p.cols);
-                    int32_t* ss = reinterpret_cast<int32_t*>(sd + p.cols / 32);
-                    const int nblk = static_cast<int>(p.cols / 32);
-                    for (int base = 0; base < 2 * nblk; base += QW * 32)
-                        quantize_task(p.xf, nblk, base + threadIdx.x, sq, sd, ss, FMT != QX_Q8_0);
-                    consumer_barrier<QW>();
-                    consumer_barrier<QW>();
-                }
-            }
+            if (MODE == QX_MODE_W4A8 && p.xf != nullptr) quantise_share();
             StageWalker rw{r0, r1, 0};
             int e, nrows;
             int64_t lrow;
@@ -230,6 +289,7 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
     if constexpr (!PART && !kMerged) {
         if (warp == NW + 1) {
             // ---------------- reducer: row sums of every stage, in order -----
+            if (MODE == QX_MODE_W4A8 && p.xf != nullptr && helpers) quantise_share();
             StageWalker wk{r0, r1, 0};
             int e, nrows;
             int64_t lrow;
@@ -262,9 +322,9 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
             float* sd = reinterpret_cast<float*>(sq + p.cols);
             int32_t* ss = reinterpret_cast<int32_t*>(sd + p.cols / 32);
             const int nblk = static_cast<int>(p.cols / 32);
-            for (int base = 0; base < 2 * nblk; base += QW * 32)
+            for (int base = 0; base < 2 * nblk; base += qthreads)
                 quantize_task(p.xf, nblk, base + threadIdx.x, sq, sd, ss, FMT != QX_Q8_0);
-            consumer_barrier<QW>();
+            quantiser_barrier(qthreads);
             q = sq;
             d = sd;
             s = ss;
@@ -274,7 +334,7 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
     if (tm.active) load_slice<MODE>(X, q, d, s, p.x, tm.slice, FMT != QX_Q8_0 && p.xf != nullptr);
     if constexpr (MODE == QX_MODE_W4A8) {
         // the quantised activation shares its area with the partial sums
-        if (p.xf != nullptr) consumer_barrier<QW>();
+        if (p.xf != nullptr) quantiser_barrier(qthreads);
     }
 
     const uint32_t rb = static_cast<uint32_t>(p.row_bytes);

@@ -607,12 +607,17 @@ __device__ __forceinline__ void load_slice(LaneT& X, const int8_t* q, const floa
     }
 }
 
-// Synchronise warps 0 .. WARPS - 1 only (the consumers, and in the GEMV
-// kernel a merged producer/reducer warp; a separate producer or reducer warp
-// never joins).
+// Synchronise warps 0 .. WARPS - 1 only (the consumers; the producer and
+// reducer warps never join).
 template <int WARPS>
 __device__ __forceinline__ void consumer_barrier() {
     asm volatile("bar.sync 1, %0;" ::"n"(WARPS * 32) : "memory");
+}
+
+// The same named barrier over the first `threads` threads (a multiple of 32,
+// uniform over the CTA): the warps that quantise the activation in-kernel.
+__device__ __forceinline__ void quantiser_barrier(int threads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
 }
 
 }  // namespace lanes
