@@ -247,8 +247,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
             if (abort_flag) break;
         }
         const int nblk = static_cast<int>(jb.cols / 32);
-        for (int base = 0; base < 2 * nblk; base += NW * 32)
-            quantize_task(jb.x, nblk, base + threadIdx.x, sq, sd, ss, jb.fmt != QX_Q8_0);
+        quantize_all<2>(jb.x, nblk, threadIdx.x, NW * 32, sq, sd, ss, jb.fmt != QX_Q8_0);
         consumer_barrier<NW>();
         bool jok;
         switch (jb.fmt) {

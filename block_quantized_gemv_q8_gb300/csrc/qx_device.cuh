@@ -96,10 +96,50 @@ __device__ __forceinline__ void bulk_g2s_evict_first(void* dst, const void* src,
         : "memory");
 }
 
+// 1-D bulk prefetch global -> L2 (no completion to wait for).  src and bytes
+// must be multiples of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
+}
+
+// Packed pairs of f32 (two lanes of one 64-bit register) and the sm_103a
+// two-wide f32 add and fused multiply-add on them (each element rounded as
+// its scalar counterpart).
+__device__ __forceinline__ uint64_t f32x2_pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ float2 f32x2_unpack(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
 }
 
 // Programmatic dependent launch: wait until the preceding grid in the stream
@@ -134,9 +174,16 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
 // from every half-integer, fl(x / d) rounds to the same integer as t does.
 // Values that fail this test (about one in 10^4, and all values when 1 / d
 // overflows) take the correctly rounded quotient from __fdiv_rn instead.
-__device__ __forceinline__ bool quotient_rounding_is_safe(float t, float k) {
-    return fabsf(t) <= 128.0f && 0.5f - fabsf(t - k) > 6.103515625e-05f;
-}
+//
+// The integer itself comes from the magic-number form of round-half-even:
+// for |t| < 2^22, fl(t + 1.5 * 2^23) = 1.5 * 2^23 + rne(t) exactly (the sum
+// lies in [2^23, 2^24), where the spacing of floats is 1), so subtracting
+// 1.5 * 2^23 again gives rne(t) and t - rne(t) exactly, and the low byte of
+// the sum's bit pattern is rne(t) as a two's-complement byte (the pattern of
+// 1.5 * 2^23 has a zero low byte).  |x| <= amax for every x of the block, so
+// the largest |t| is fl(amax * fl(1 / d)): one range check per block.
+constexpr float kMagicRne = 12582912.0f;            // 1.5 * 2^23
+constexpr float kTieMargin = 0.49993896484375f;     // 0.5 - 2^-14
 
 // Quantise N consecutive values of one block (N = 32 / threads per block);
 // amax over the block and the block's quant sum are combined across the
@@ -161,29 +208,40 @@ template <int N, int THREADS>
 __device__ __forceinline__ void quantize_block_values(const float (&v)[N], int8_t* __restrict__ q, float* d,
                                                       int32_t* sum, bool live, bool first) {
     static_assert(N * THREADS == 32 && N % 4 == 0, "a block is 32 values, stored in 4-byte groups");
-    float amax = 0.0f;
+    float m[N];
 #pragma unroll
-    for (int i = 0; i < N; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    for (int i = 0; i < N; ++i) m[i] = fabsf(v[i]);
+#pragma unroll
+    for (int w = N / 2; w >= 1; w >>= 1)  // max is exact: a tree gives the same amax
+#pragma unroll
+        for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+    float amax = m[0];
 #pragma unroll
     for (int o = 1; o < THREADS; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     const float db = __fdiv_rn(amax, 127.0f);
-    float r[N];
+    uint32_t bits[N];  // low byte: the code
     if (db != 0.0f) {
         const float rcp = __frcp_rn(db);
-        bool safe = true;
+        bool safe = amax * rcp <= 128.0f;
+        const uint64_t rcp2 = f32x2_pack(rcp, rcp);
+        const uint64_t magic2 = f32x2_pack(kMagicRne, kMagicRne), unmagic2 = f32x2_pack(-kMagicRne, -kMagicRne);
 #pragma unroll
-        for (int i = 0; i < N; ++i) {
-            const float t = v[i] * rcp;
-            r[i] = rintf(t);
-            safe &= quotient_rounding_is_safe(t, r[i]);
+        for (int i = 0; i < N; i += 2) {
+            const uint64_t t2 = f32x2_mul(f32x2_pack(v[i], v[i + 1]), rcp2);
+            const uint64_t m2 = f32x2_add(t2, magic2);           // 1.5 * 2^23 + rne(t)
+            const float2 e = f32x2_unpack(f32x2_sub(t2, f32x2_add(m2, unmagic2)));  // t - rne(t)
+            safe &= fabsf(e.x) < kTieMargin && fabsf(e.y) < kTieMargin;
+            const float2 mm = f32x2_unpack(m2);
+            bits[i] = __float_as_uint(mm.x);
+            bits[i + 1] = __float_as_uint(mm.y);
         }
         if (!safe) {  // rare: some quotient lies too close to a rounding boundary
 #pragma unroll
-            for (int i = 0; i < N; ++i) r[i] = rintf(__fdiv_rn(v[i], db));
+            for (int i = 0; i < N; ++i) bits[i] = __float_as_uint(rintf(__fdiv_rn(v[i], db)) + kMagicRne);
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < N; ++i) r[i] = 0.0f;
+        for (int i = 0; i < N; ++i) bits[i] = 0u;
     }
     // |x / d| <= 127 (1 + 2^-23) for every x of the block, so every code is
     // already within [-127, 127]: the clamp of the definition never binds.
@@ -191,10 +249,8 @@ __device__ __forceinline__ void quantize_block_values(const float (&v)[N], int8_
     int s = 0;
 #pragma unroll
     for (int j = 0; j < N / 4; ++j) {
-        const int q0 = static_cast<int>(r[4 * j]), q1 = static_cast<int>(r[4 * j + 1]);
-        const int q2 = static_cast<int>(r[4 * j + 2]), q3 = static_cast<int>(r[4 * j + 3]);
-        const uint32_t lo = __byte_perm(uint32_t(q0), uint32_t(q1), 0x0040u);  // bytes q0, q1
-        const uint32_t hi = __byte_perm(uint32_t(q2), uint32_t(q3), 0x0040u);  // bytes q2, q3
+        const uint32_t lo = __byte_perm(bits[4 * j], bits[4 * j + 1], 0x0040u);      // codes 0, 1
+        const uint32_t hi = __byte_perm(bits[4 * j + 2], bits[4 * j + 3], 0x0040u);  // codes 2, 3
         packed[j] = __byte_perm(lo, hi, 0x5410u);
         s = __dp4a(static_cast<int>(packed[j]), 0x01010101, s);  // + q0 + q1 + q2 + q3 (signed bytes)
     }
@@ -236,6 +292,53 @@ __device__ __forceinline__ void quantize_task(const float* __restrict__ x, int64
     const int64_t chunk = 2 * b + half;
     quantize_block_part<16, 2>(x + b * 32 + half * 16, q + 16 * (swz ? act_chunk_swizzle(chunk) : chunk), d + b,
                                sum + b, live, half == 0);
+}
+
+// Tasks task0 + r * stride (r < R) with every load issued before any
+// arithmetic, so that R rounds cost one memory round trip.  Same codes as
+// quantize_task.
+template <int R>
+__device__ __forceinline__ void quantize_tasks(const float* __restrict__ x, int64_t nblocks, int64_t task0,
+                                               int64_t stride, int8_t* __restrict__ q, float* d, int32_t* sum,
+                                               bool swz) {
+    float v[R][16];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t task = task0 + r * stride;
+        const int64_t b = task < 2 * nblocks ? task >> 1 : nblocks - 1;
+        load_block_part<16>(x + b * 32 + (task & 1) * 16, v[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int64_t task = task0 + r * stride;
+        const bool live = task < 2 * nblocks;
+        const int64_t b = live ? task >> 1 : nblocks - 1;
+        const int half = static_cast<int>(task & 1);
+        const int64_t chunk = 2 * b + half;
+        quantize_block_values<16, 2>(v[r], q + 16 * (swz ? act_chunk_swizzle(chunk) : chunk), d + b, sum + b, live,
+                                     half == 0);
+    }
+}
+
+// Every task of an activation of `nblocks` blocks over `threads` threads
+// (thread t takes tasks t, t + threads, ...; every thread of the group calls
+// this), the loads of up to RMAX rounds in flight at once (RMAX <= 4: each
+// round holds 16 values in registers).
+template <int RMAX>
+__device__ __forceinline__ void quantize_all(const float* __restrict__ x, int64_t nblocks, int t, int threads,
+                                             int8_t* __restrict__ q, float* d, int32_t* sum, bool swz) {
+    static_assert(RMAX >= 1 && RMAX <= 4, "one to four rounds per batch");
+    int rounds = static_cast<int>((2 * nblocks + threads - 1) / threads);
+    int64_t base = t;
+    while (rounds > 0) {
+        const int r = rounds < RMAX ? rounds : RMAX;
+        if (RMAX >= 4 && r == 4) quantize_tasks<(RMAX >= 4 ? 4 : 1)>(x, nblocks, base, threads, q, d, sum, swz);
+        else if (RMAX >= 3 && r == 3) quantize_tasks<(RMAX >= 3 ? 3 : 1)>(x, nblocks, base, threads, q, d, sum, swz);
+        else if (RMAX >= 2 && r == 2) quantize_tasks<(RMAX >= 2 ? 2 : 1)>(x, nblocks, base, threads, q, d, sum, swz);
+        else quantize_tasks<1>(x, nblocks, base, threads, q, d, sum, swz);
+        base += int64_t(r) * threads;
+        rounds -= r;
+    }
 }
 
 // fp16 bit pattern -> f32 (exact; subnormals kept).

@@ -34,30 +34,6 @@ __device__ __forceinline__ float byte_biased_f32(uint32_t w, int k) {
     return __int_as_float(__byte_perm(w, 0x4B000000u, 0x7540u + uint32_t(k)));
 }
 
-// Packed pairs of f32 (two lanes of one 64-bit register) and the sm_103a
-// two-wide f32 add and fused multiply-add on them (each element rounded as
-// its scalar counterpart).
-__device__ __forceinline__ uint64_t f32x2_pack(float a, float b) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ float2 f32x2_unpack(uint64_t v) {
-    float2 r;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-    return r;
-}
-__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-
 // N consecutive (possibly 2-byte aligned) little-endian words from shared
 // memory, read as N + 1 aligned words and funnel-shifted.
 template <int N>
