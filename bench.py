@@ -442,8 +442,8 @@ def run_extra(args):
             a = qx.ActQ8(act.q[:m], act.d[:m], act.sum[:m])
             Y = torch.empty((m, rows), dtype=torch.float32, device="cuda")
             rec = {"m": m}
-            for path in ((3,) if args.prefill_m else (1, 2, 3)):
-                if path == 1 and m > 64:
+            for path in ((3,) if args.prefill_m else (1, 2, 3, 4)):
+                if path in (1, 4) and m > 64:
                     continue
                 ms = graph_time_ms(torch, lambda: qx.qx_gemm_prefill_ex(fmt, W, rows, cols, a, Y=Y, path=path,
                                                                         stream=stream), 10, stream)
@@ -457,8 +457,9 @@ def run_extra(args):
         out.update({"sweep": sweep, "flops_per_row": 2 * rows * cols, "bf16_dense_peak_tflops": bf16,
                     "note": "path 1 = one W4A8 GEMV launch per row; path 2 = tensor cores (mma.sync f16 with "
                             "integer-valued operands); path 3 = tcgen05 bf16 GEMM over the split dequantised "
-                            "operands (3 passes of K), timed with its dequantise passes; tflops count the "
-                            "int8-equivalent multiply-adds x2"})
+                            "operands (3 passes of K), timed with its dequantise passes; path 4 = small-batch "
+                            "GEMV, one weight stream per 4 rows of X; tflops count the int8-equivalent "
+                            "multiply-adds x2"})
     print(json.dumps(out), flush=True)
     return 0
 

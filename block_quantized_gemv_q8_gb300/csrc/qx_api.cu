@@ -26,12 +26,12 @@ constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s bound on every pipeli
 constexpr size_t kStageTargetBytes = 48 * 1024;
 // Shared memory of a CTA that leaves room for a second one on the SM.
 constexpr size_t kHalfSmBytes = 110 * 1024;
-// Automatic prefill path (measured on GB300, X [m, 4096] x W [14336, 4096]):
-// the tcgen05 GEMM from this many rows of X, one GEMV per row below.  Q4_K
-// has the fused kernel (weights split in shared memory), the other formats
-// a dequantise pass first, hence the later crossover.
-constexpr int64_t kPrefillTcMinRows = 16;
-constexpr int64_t kPrefillTcMinRowsQ4K = 8;
+// Automatic prefill path (measured on GB300, X [m, 4096] x Q4_K [14336,
+// 4096]): one GEMV for a single row of X (10.9 us); the small-batch GEMV up
+// to kPrefillBatchMaxRows rows (m = 2, 4, 8, 16: 14.8, 14.8, 27.1, 51.6 us,
+// against 18.7, 33.0, 61.9, 121.4 us row by row and about 60 us on
+// tcgen05); the tcgen05 GEMM above (m = 64: 61.8 us against 197 us).
+constexpr int64_t kPrefillBatchMaxRows = 16;
 // Shared memory of a chain CTA (one per SM).
 constexpr size_t kChainSmBytes = 200 * 1024;
 constexpr int kMaxStageRows = 256;
@@ -174,8 +174,9 @@ struct TeamGeom {
     int64_t rb, G, base;  // base: the smallest stage (rows) that keeps teams and copies whole
 };
 
-qx_status team_geometry(int fmt, int kmode, bool partials, int64_t cols, int consumer_warps, TeamGeom& g) {
-    const int C = gemv_cols_per_lane(fmt, kmode);
+qx_status team_geometry(int fmt, int kmode, bool partials, int64_t cols, int consumer_warps, TeamGeom& g,
+                        bool batch = false) {
+    const int C = batch ? batch_cols_per_lane(fmt) : gemv_cols_per_lane(fmt, kmode);
     if (cols % C) return QX_ERR_SHAPE;
     g.L = static_cast<int>(cols / C);
     if (g.L <= 32) {
@@ -193,7 +194,7 @@ qx_status team_geometry(int fmt, int kmode, bool partials, int64_t cols, int con
     g.rb = cols / block_weights(fmt) * block_bytes(fmt);
     g.quantum = static_cast<int>(16 / gcd64(g.rb, 16));
     // every team gets the same number of whole row groups per stage
-    const int64_t team_rows = int64_t(g.nteams) * (partials ? 1 : gemv_rows_per_call(fmt, kmode));
+    const int64_t team_rows = int64_t(g.nteams) * ((partials || batch) ? 1 : gemv_rows_per_call(fmt, kmode));
     const int64_t base = team_rows / gcd64(team_rows, g.quantum) * g.quantum;  // lcm
     g.base = base;
     g.G = base;
@@ -366,6 +367,63 @@ qx_status run_gemv(int fmt, int n, const void* const* W, const int64_t* rows, in
     return e == cudaSuccess ? QX_OK : cuda_fail(e, "gemv launch");
 }
 
+// One small-batch launch (gemv_batch_kernel): rows m0 .. m0 + mvalid - 1 of
+// X (mvalid <= kBatchRows) against W [rows, cols], into Y [X->m, rows].
+qx_status run_gemv_batch(int fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, int64_t m0,
+                         int mvalid, float* Y, cudaStream_t s) {
+    DeviceInfo* dev = nullptr;
+    qx_status st = device_info(&dev);
+    if (st != QX_OK) return st;
+    GemvParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.n_entries = 1;
+    p.e[0].W = static_cast<const uint8_t*>(W);
+    p.e[0].y = Y + m0 * rows;
+    p.e[0].rows = rows;
+    p.e[0].row0 = 0;
+    p.total_rows = rows;
+    p.xq = X->q + m0 * cols;
+    p.xd = X->d + m0 * (cols / 32);
+    p.xs = X->sum + m0 * (cols / 32);
+    p.m_valid = mvalid;
+    p.y_stride = rows;
+    TeamGeom g;
+    if ((st = team_geometry(fmt, QX_MODE_W4A8, false, cols, kBatchConsumerWarps, g, true)) != QX_OK) return st;
+    const int RS = partial_stride(g.L);
+    const auto slot_of = [&](int64_t G) { return (size_t(G * g.rb) + kSlotPad + 127) / 128 * 128; };
+    const auto bytes_for = [&](int64_t G, int stg) {
+        return size_t(stg) * (slot_of(G) + 24 + size_t(G) * kBatchRows * RS * 4) + 32;
+    };
+    const size_t budget = 200 * 1024;
+    while (g.G > g.base && bytes_for(g.G, 2) > budget) g.G -= g.base;
+    int stages = 2;
+    while (stages < 8 && bytes_for(g.G, stages + 1) <= budget) ++stages;
+    const size_t slot = slot_of(g.G);
+    p.bar_off = static_cast<int>(size_t(stages) * slot);
+    p.red_off = static_cast<int>((size_t(p.bar_off) + 24 * size_t(stages) + 15) / 16 * 16);
+    p.act_off = p.red_off;
+    const size_t smem = size_t(p.red_off) + size_t(stages) * size_t(g.G) * kBatchRows * RS * 4;
+    if (smem > 227 * 1024) return QX_ERR_SHAPE;
+    p.RS = RS;
+    p.cols = cols;
+    p.row_bytes = g.rb;
+    p.quantum = g.quantum;
+    p.G = static_cast<int>(g.G);
+    p.stages = stages;
+    p.slot_bytes = static_cast<int>(slot);
+    p.team_lanes = g.team_lanes;
+    p.team_warps = g.team_warps;
+    p.nteams = g.nteams;
+    p.L = g.L;
+    const int64_t groups = (rows + g.quantum - 1) / g.quantum;
+    p.n_cta = static_cast<int>(groups < dev->sm_count ? groups : dev->sm_count);
+    p.prewait = stages;
+    p.err = dev->err_word;
+    p.wait_ns = kDefaultWaitNs;
+    const cudaError_t e = launch_gemv_batch(fmt, p, smem, s);
+    return e == cudaSuccess ? QX_OK : cuda_fail(e, "batched gemv launch");
+}
+
 // Split a public mode argument into the mode and the PDL flag.
 qx_status parse_mode(int mode_arg, int* mode, bool* pdl) {
     if (mode_arg & ~(0xFF | QX_FLAG_PDL)) return QX_ERR_MODE;
@@ -436,9 +494,19 @@ qx_status prefill_dispatch(qx_fmt fmt, const void* W, int64_t rows, int64_t cols
     if (!W || !Y) return QX_ERR_ARG;
     if (!aligned16(W) || !aligned4(Y)) return QX_ERR_ALIGN;
     if ((st = check_act(X, 0, cols)) != QX_OK) return st;
-    if (path < 0 || path > 3) return QX_ERR_ARG;
-    if (path == 0) {
-        path = X->m >= (fmt == QX_Q4_K ? kPrefillTcMinRowsQ4K : kPrefillTcMinRows) ? 3 : 1;
+    if (path < 0 || path > 4) return QX_ERR_ARG;
+    if (path == 0) path = X->m == 1 ? 1 : (X->m <= kPrefillBatchMaxRows ? 4 : 3);
+    if (path == 4) {
+        // kBatchRows rows of X per weight stream
+        for (int64_t m0 = 0; m0 < X->m; m0 += kBatchRows) {
+            const int mv = static_cast<int>(X->m - m0 < kBatchRows ? X->m - m0 : kBatchRows);
+            if (!aligned16(X->q + m0 * cols) || !aligned16(X->d + m0 * (cols / 32)) ||
+                !aligned16(X->sum + m0 * (cols / 32)))
+                return QX_ERR_ALIGN;
+            if ((st = run_gemv_batch(fmt, W, rows, cols, X, m0, mv, Y, reinterpret_cast<cudaStream_t>(s))) != QX_OK)
+                return st;
+        }
+        return QX_OK;
     }
     if (path == 3) {
         if (X->m > INT32_MAX || rows > INT32_MAX) return QX_ERR_SHAPE;

@@ -390,6 +390,108 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
     }
 }
 
+// ----------------------------------------------------------------------------
+// Small-batch GEMV: Y[m, r] for the kBatchRows rows of a quantised
+// activation X (qx_gemm_prefill path 4).  The same weight stream as
+// gemv_kernel (contiguous rows per CTA, bulk copies into a shared-memory
+// ring, a producer lane, a reducer warp), read once for all rows of X:
+// decode of several tokens at once (speculative or batched decode) is then
+// still bound by the weight bytes, not by one stream per token.  One CTA per
+// SM, 14 consumer warps.
+// ----------------------------------------------------------------------------
+template <int FMT>
+__global__ void __launch_bounds__(kBatchThreads, 1) gemv_batch_kernel(const __grid_constant__ GemvParams p) {
+    constexpr int NW = kBatchConsumerWarps;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int S = p.stages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
+    uint64_t* empty = full + S;
+    uint64_t* part = empty + S;
+    float* red = reinterpret_cast<float*>(smem + p.red_off);  // [S][G * kBatchRows][RS]
+    const size_t red_stage = size_t(p.G) * kBatchRows * p.RS;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t r0 = cta_row_begin(p, blockIdx.x), r1 = cta_row_begin(p, blockIdx.x + 1);
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < S; ++k) {
+            mbar_init(&full[k], 1);
+            mbar_init(&empty[k], NW + 1);
+            mbar_init(&part[k], NW);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    if (warp == NW) {
+        // ---------------- producer: lane 0 issues every bulk copy -----------
+        if (lane != 0) return;
+        const uint64_t policy = policy_evict_first();
+        unsigned tail_slots = 0;
+        StageWalker pw{r0, r1, 0};
+        int e, nrows, issued = 0;
+        int64_t lrow;
+        for (int k = 0; pw.next(p, e, lrow, nrows); ++k) {
+            const int slot = k % S;
+            if (k >= S && !mbar_wait_bounded(&empty[slot], ((k / S) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty))
+                break;
+            const uint8_t* src = p.e[e].W + lrow * p.row_bytes;
+            const uint32_t bytes = static_cast<uint32_t>(int64_t(nrows) * p.row_bytes);
+            const uint32_t abytes = bytes & ~15u;
+            uint8_t* dst = smem + size_t(slot) * p.slot_bytes;
+            if (bytes != abytes) {
+                // the last < 16 bytes of a matrix whose size is not a 16-byte multiple
+                for (uint32_t t = abytes; t < bytes; ++t) dst[t] = src[t];
+                tail_slots |= 1u << slot;
+            } else if (tail_slots & (1u << slot)) {
+                fence_proxy_async_smem();
+                tail_slots &= ~(1u << slot);
+            }
+            mbar_arrive_expect_tx(&full[slot], abytes);
+            if (abytes) bulk_g2s_evict_first(dst, src, abytes, &full[slot], policy);
+            issued = k + 1;
+        }
+        for (int k = issued > S ? issued - S : 0; k < issued; ++k)
+            mbar_wait_bounded(&full[k % S], (k / S) & 1, p.wait_ns, p.err, kErrTimeoutDrain);
+        return;
+    }
+    if (warp == NW + 1) {
+        // ---------------- reducer: (row, activation row) sums, in order -----
+        pdl_wait_prior_grid();  // y may be read by the previous kernel
+        StageWalker wk{r0, r1, 0};
+        int e, nrows;
+        int64_t lrow;
+        for (int k = 0; wk.next(p, e, lrow, nrows); ++k) {
+            const int slot = k % S;
+            if (!mbar_wait_bounded(&part[slot], (k / S) & 1, p.wait_ns, p.err, kErrTimeoutFull)) break;
+            reduce_stage_batch(red + slot * red_stage, p.RS, p.L, nrows, p.e[e].y + lrow, p.y_stride, p.m_valid,
+                               lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------------------------------------
+    const Team tm = make_team(warp, lane, p.team_lanes, p.team_warps, p.nteams, p.L);
+    pdl_wait_prior_grid();  // X may come from the previous kernel
+    BatchLane<FMT> X;
+    if (tm.active) X.load(p.xq, p.xd, p.xs, p.cols, p.m_valid, tm.slice);
+    const uint32_t rb = static_cast<uint32_t>(p.row_bytes);
+    StageWalker wk{r0, r1, 0};
+    int e, nrows;
+    int64_t lrow;
+    for (int k = 0; wk.next(p, e, lrow, nrows); ++k) {
+        const int slot = k % S;
+        if (!mbar_wait_bounded(&full[slot], (k / S) & 1, p.wait_ns, p.err, kErrTimeoutFull)) break;
+        consume_stage_batch<FMT>(X, tm, smem + size_t(slot) * p.slot_bytes, nrows, rb, red + slot * red_stage, p.RS);
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&part[slot]);
+            mbar_arrive(&empty[slot]);
+        }
+    }
+}
+
 // Largest shared memory (static + dynamic) a CTA may use on sm_103a.
 constexpr int kMaxDynamicSmem = 227 * 1024;
 
@@ -438,7 +540,35 @@ cudaError_t occupancy_one(size_t smem, int* out) {
                                                          gemv_threads(FMT, MODE, PART, MERGED), smem);
 }
 
+template <int FMT>
+cudaError_t launch_batch_one(const GemvParams& p, size_t smem, cudaStream_t s) {
+    static bool done[64] = {false};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!done[dev]) {
+        cudaFuncAttributes fa;
+        if ((err = cudaFuncGetAttributes(&fa, gemv_batch_kernel<FMT>)) != cudaSuccess) return err;
+        err = cudaFuncSetAttribute(gemv_batch_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   kMaxDynamicSmem - static_cast<int>(fa.sharedSizeBytes));
+        if (err != cudaSuccess) return err;
+        done[dev] = true;
+    }
+    gemv_batch_kernel<FMT><<<p.n_cta, kBatchThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_gemv_batch(int fmt, const GemvParams& p, size_t smem, cudaStream_t s) {
+    switch (fmt) {
+        case QX_Q4_K: return launch_batch_one<QX_Q4_K>(p, smem, s);
+        case QX_Q6_K: return launch_batch_one<QX_Q6_K>(p, smem, s);
+        case QX_Q8_0: return launch_batch_one<QX_Q8_0>(p, smem, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
 
 cudaError_t launch_gemv(int fmt, int mode, bool partials, const GemvParams& p, size_t smem, cudaStream_t s,
                         bool pdl) {

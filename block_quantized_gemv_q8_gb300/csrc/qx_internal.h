@@ -77,7 +77,21 @@ struct GemvParams {
                        //   area as the partial sums, used before them)
     unsigned* err;     // device error word
     uint64_t wait_ns;  // bound on every wait
+    // Batched launches (gemv_batch_kernel): rows m of a quantised activation
+    // X, y[m * y_stride + r] for m < m_valid; the lanes hold kBatchRows rows
+    // (rows m_valid .. kBatchRows - 1 repeat row m_valid - 1, unwritten).
+    int m_valid;
+    int64_t y_stride;
 };
+
+// Small-batch GEMV (one weight stream for several activation rows): rows of
+// X per launch, consumer warps (one CTA per SM: 16 warps of <= 128
+// registers), and columns per lane (half as many as the batch-1 W4A8 lanes,
+// so that four activation slices fit in registers).
+constexpr int kBatchRows = 4;
+constexpr int kBatchConsumerWarps = 14;
+constexpr int kBatchThreads = 32 * (kBatchConsumerWarps + 2);
+__host__ __device__ constexpr int batch_cols_per_lane(int fmt) { return fmt == QX_Q8_0 ? 32 : 64; }
 
 // Columns owned by one lane, per (format, mode).
 __host__ __device__ constexpr int gemv_cols_per_lane(int fmt, int mode) {
@@ -126,6 +140,7 @@ cudaError_t launch_actq8(const float* x, int64_t nblocks, int8_t* q, float* d, i
 cudaError_t launch_gemv(int fmt, int mode, bool partials, const GemvParams& p, size_t smem, cudaStream_t s,
                         bool pdl);
 cudaError_t gemv_max_ctas_per_sm(int fmt, int mode, bool partials, bool merged, size_t smem, int* out);
+cudaError_t launch_gemv_batch(int fmt, const GemvParams& p, size_t smem, cudaStream_t s);
 cudaError_t launch_timeout_probe(unsigned* err, uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_chain(const ChainParams& p, size_t smem, cudaStream_t s);
 cudaError_t launch_prefill_q4k(const uint8_t* W, int64_t N, int64_t K, const int8_t* xq, const float* xd,

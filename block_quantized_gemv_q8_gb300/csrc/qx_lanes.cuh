@@ -571,6 +571,256 @@ __device__ __forceinline__ void reduce_stage(const float* red, int RS, int L, in
     }
 }
 
+// ----------------------------------------------------------------------------
+// Small-batch lanes (gemv_batch_kernel): kBatchRows rows of a quantised
+// activation X share every weight row's bytes, so the weights stream once
+// for all of them.  A lane owns batch_cols_per_lane(fmt) columns and holds
+// the slices of every row of X in registers; the weight words are unpacked
+// once and dotted with each row's codes.  Same arithmetic per (row of X,
+// weight row) as the batch-1 W4A8 lanes.
+// ----------------------------------------------------------------------------
+template <int FMT>
+struct BatchLane;
+
+// Q4_K: 64 columns = the 32-byte quant chunk c of super-block sb: sub-block
+// 2c in the low nibbles, sub-block 2c + 1 in the high nibbles.
+template <>
+struct BatchLane<QX_Q4_K> {
+    static constexpr int C = 64;
+    static constexpr int MB = kBatchRows;
+    uint32_t xq[MB][16];
+    float dxs[MB][2];  // dx of sub-blocks 2c and 2c + 1, the second divided by 16
+    float t[MB][2];    // dx * (sum of q_x): weight of the min term
+    // row m of X (rows >= mvalid repeat row mvalid - 1); qstride: bytes per row of X's codes
+    __device__ __forceinline__ void load(const int8_t* q, const float* d, const int32_t* s, int64_t qstride,
+                                         int mvalid, int l) {
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+            const int64_t mm = m < mvalid ? m : mvalid - 1;
+            const uint4* src = reinterpret_cast<const uint4*>(q + mm * qstride + int64_t(l) * C);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint4 v = src[k];
+                xq[m][4 * k + 0] = v.x;
+                xq[m][4 * k + 1] = v.y;
+                xq[m][4 * k + 2] = v.z;
+                xq[m][4 * k + 3] = v.w;
+            }
+            const int64_t b = mm * (qstride / 32) + 2 * l;
+            const float d0 = d[b], d1 = d[b + 1];
+            dxs[m][0] = d0;
+            dxs[m][1] = d1 * 0.0625f;
+            t[m][0] = d0 * float(s[b]);
+            t[m][1] = d1 * float(s[b + 1]);
+        }
+    }
+    __device__ __forceinline__ void row(const uint8_t* rp, int l, float (&out)[MB]) const {
+        const int sb = l >> 2, c = l & 3;
+        const uint8_t* bp = rp + sb * 144;
+        const uint4 hdr = *reinterpret_cast<const uint4*>(bp);
+        const uint4* qsp = reinterpret_cast<const uint4*>(bp + 16 + 32 * c);
+        const uint4 a = qsp[0], b = qsp[1];
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        int plo[MB], phi16[MB];  // phi16: 16 x the high-nibble partial (unsigned x signed dp4a)
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+            plo[m] = 0;
+            phi16[m] = 0;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t lo = w[i] & 0x0F0F0F0Fu, hi = w[i] & 0xF0F0F0F0u;
+#pragma unroll
+            for (int m = 0; m < MB; ++m) {
+                plo[m] = dp4a(lo, xq[m][i], plo[m]);
+                phi16[m] = dp4a_us(hi, xq[m][8 + i], phi16[m]);
+            }
+        }
+        const Q4KScales S = q4k_unpack_scales(hdr.y, hdr.z, hdr.w);
+        const uint32_t scw = c < 2 ? S.sc_lo : S.sc_hi;
+        const uint32_t mw = c < 2 ? S.m_lo : S.m_hi;
+        const int k0 = 2 * (c & 1);
+        const int sc0 = int(byte_of(scw, k0)), sc1 = int(byte_of(scw, k0 + 1));
+        const float m0 = float(int(byte_of(mw, k0))), m1 = float(int(byte_of(mw, k0 + 1)));
+        const float dd = f16_bits_to_f32(hdr.x), dmin = f16_bits_to_f32(hdr.x >> 16);
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+            const float accd = fmaf(float(phi16[m] * sc1), dxs[m][1], float(plo[m] * sc0) * dxs[m][0]);
+            const float accm = fmaf(m1, t[m][1], m0 * t[m][0]);
+            out[m] = dd * accd - dmin * accm;
+        }
+    }
+};
+
+// Q6_K: 64 columns = quarters tp and tp + 2 of half h of super-block sb
+// (they share the same 32 ql bytes, low and high nibbles, and the same qh
+// bytes); four scale groups of 16.  The quants are dotted unsigned (0..63)
+// and the -32 offset is applied as -32 * sum(q_x) per group.
+template <>
+struct BatchLane<QX_Q6_K> {
+    static constexpr int C = 64;
+    static constexpr int MB = kBatchRows;
+    uint32_t xq[MB][16];  // quarter tp (words 0..7), quarter tp + 2 (words 8..15)
+    float dx[MB][2];
+    int s16[MB][4];
+    __device__ __forceinline__ void load(const int8_t* q, const float* d, const int32_t*, int64_t qstride,
+                                         int mvalid, int l) {
+        const int sb = l >> 2, h = (l >> 1) & 1, tp = l & 1;
+        const int64_t c0 = int64_t(sb) * 256 + 128 * h + 32 * tp;
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+            const int64_t mm = m < mvalid ? m : mvalid - 1;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const uint4* src = reinterpret_cast<const uint4*>(q + mm * qstride + c0 + 64 * half);
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const uint4 v = src[k];
+                    xq[m][8 * half + 4 * k + 0] = v.x;
+                    xq[m][8 * half + 4 * k + 1] = v.y;
+                    xq[m][8 * half + 4 * k + 2] = v.z;
+                    xq[m][8 * half + 4 * k + 3] = v.w;
+                }
+                dx[m][half] = d[mm * (qstride / 32) + (c0 + 64 * half) / 32];
+            }
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                int sg = 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sg = dp4a(xq[m][4 * g + i], 0x01010101u, sg);
+                s16[m][g] = sg;
+            }
+        }
+    }
+    __device__ __forceinline__ void row(const uint8_t* rp, int l, float (&out)[MB]) const {
+        const int sb = l >> 2, h = (l >> 1) & 1, tp = l & 1;
+        const uint8_t* bp = rp + sb * 210;
+        uint32_t ql[8], qh[8], scw[2];
+        load_words<8>(bp + 64 * h + 32 * tp, ql);
+        load_words<8>(bp + 128 + 32 * h, qh);
+        load_words<2>(bp + 192 + 8 * h, scw);
+        // qh bits 2 tp, 2 tp + 1 (quarter tp) and 2 tp + 4, 2 tp + 5 (quarter tp + 2) to bits 4, 5
+        const uint32_t sh_lo = 4u - 2u * uint32_t(tp), sh_hi = 2u * uint32_t(tp);
+        int P[MB][4];
+#pragma unroll
+        for (int m = 0; m < MB; ++m)
+#pragma unroll
+            for (int g = 0; g < 4; ++g) P[m][g] = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t wlo = (ql[i] & 0x0F0F0F0Fu) | ((qh[i] << sh_lo) & 0x30303030u);
+            const uint32_t whi = ((ql[i] >> 4) & 0x0F0F0F0Fu) | ((qh[i] >> sh_hi) & 0x30303030u);
+#pragma unroll
+            for (int m = 0; m < MB; ++m) {
+                P[m][i >> 2] = dp4a_us(wlo, xq[m][i], P[m][i >> 2]);
+                P[m][2 + (i >> 2)] = dp4a_us(whi, xq[m][8 + i], P[m][2 + (i >> 2)]);
+            }
+        }
+        // scale bytes of this half: 2 tp, 2 tp + 1 (quarter tp), 2 tp + 4, 2 tp + 5 (quarter tp + 2)
+        const int sa = int(int8_t(byte_of(scw[0], 2 * tp))), sbb = int(int8_t(byte_of(scw[0], 2 * tp + 1)));
+        const int sc = int(int8_t(byte_of(scw[1], 2 * tp))), sd = int(int8_t(byte_of(scw[1], 2 * tp + 1)));
+        const float dd = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(bp + 208));
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+            const int lo = sa * (P[m][0] - 32 * s16[m][0]) + sbb * (P[m][1] - 32 * s16[m][1]);
+            const int hi = sc * (P[m][2] - 32 * s16[m][2]) + sd * (P[m][3] - 32 * s16[m][3]);
+            out[m] = dd * fmaf(dx[m][1], float(hi), dx[m][0] * float(lo));
+        }
+    }
+};
+
+// Q8_0: 32 columns = one block.
+template <>
+struct BatchLane<QX_Q8_0> {
+    static constexpr int C = 32;
+    static constexpr int MB = kBatchRows;
+    uint32_t xq[MB][8];
+    float dx[MB];
+    __device__ __forceinline__ void load(const int8_t* q, const float* d, const int32_t*, int64_t qstride,
+                                         int mvalid, int l) {
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+            const int64_t mm = m < mvalid ? m : mvalid - 1;
+            const uint4* src = reinterpret_cast<const uint4*>(q + mm * qstride + int64_t(l) * C);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const uint4 v = src[k];
+                xq[m][4 * k + 0] = v.x;
+                xq[m][4 * k + 1] = v.y;
+                xq[m][4 * k + 2] = v.z;
+                xq[m][4 * k + 3] = v.w;
+            }
+            dx[m] = d[mm * (qstride / 32) + l];
+        }
+    }
+    __device__ __forceinline__ void row(const uint8_t* rp, int l, float (&out)[MB]) const {
+        const uint8_t* bp = rp + l * 34;
+        uint32_t qs[8];
+        load_words<8>(bp + 2, qs);
+        int P[MB];
+#pragma unroll
+        for (int m = 0; m < MB; ++m) P[m] = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int m = 0; m < MB; ++m) P[m] = dp4a(qs[i], xq[m][i], P[m]);
+        const float dd = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(bp));
+#pragma unroll
+        for (int m = 0; m < MB; ++m) out[m] = dd * dx[m] * float(P[m]);
+    }
+};
+
+// All rows of one stage for the batched lanes: team t takes rows t,
+// t + nteams, ...; the partial of (row i, activation row m) goes to
+// red[(i * kBatchRows + m) * RS + slice].
+template <int FMT>
+__device__ __forceinline__ void consume_stage_batch(const BatchLane<FMT>& X, const Team& tm, const uint8_t* sbuf,
+                                                    int nrows, uint32_t rb, float* red, int RS) {
+    if (!tm.active) return;
+    for (int i = tm.team; i < nrows; i += tm.nteams) {
+        float v[kBatchRows];
+        X.row(sbuf + uint32_t(i) * rb, tm.slice, v);
+#pragma unroll
+        for (int m = 0; m < kBatchRows; ++m) red[(i * kBatchRows + m) * RS + tm.slice] = v[m];
+    }
+}
+
+// The reducer's share of one batched stage: one (row, activation row) pair
+// per lane, its L partials added in the same fixed order as reduce_stage;
+// y[m * y_stride + row] for m < mvalid.
+__device__ __forceinline__ void reduce_stage_batch(const float* red, int RS, int L, int nrows, float* y,
+                                                   int64_t y_stride, int mvalid, int lane) {
+    for (int pair = lane; pair < nrows * kBatchRows; pair += 32) {
+        const int row = pair / kBatchRows, m = pair % kBatchRows;
+        const float* pr = red + pair * RS;
+        float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+        int s = 0;
+        for (; s + 16 <= L; s += 16) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = *reinterpret_cast<const float4*>(pr + s + 4 * u);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                a0 += v[u].x;
+                a1 += v[u].y;
+                a2 += v[u].z;
+                a3 += v[u].w;
+            }
+        }
+        for (; s + 4 <= L; s += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(pr + s);
+            a0 += v.x;
+            a1 += v.y;
+            a2 += v.z;
+            a3 += v.w;
+        }
+        if (s < L) a0 += pr[s];
+        if (s + 1 < L) a1 += pr[s + 1];
+        if (s + 2 < L) a2 += pr[s + 2];
+        if (m < mvalid) y[int64_t(m) * y_stride + row] = (a0 + a1) + (a2 + a3);
+    }
+}
+
 // Load a lane's activation slice: from the quantised activation (W4A8) or
 // the f32 activation.
 template <int MODE, class LaneT>

@@ -158,8 +158,8 @@ qx_status qx_gemm_prefill(qx_fmt fmt, const void* W, int64_t rows, int64_t cols,
 
 /*
  * qx_gemm_prefill with a forced path:
- *   0 = automatic (by measured time): path 3 from 8 rows of X for Q4_K and
- *       from 16 rows for the other formats, path 1 below;
+ *   0 = automatic (by measured time): path 1 for one row of X, path 4 for
+ *       2 to 16 rows, path 3 above;
  *   1 = one W4A8 GEMV launch per row of X (bit-for-bit the qx_gemv result);
  *   2 = mma.sync tensor-core GEMM, Q4_K only (integer-valued f16 operands,
  *       exact per-sub-block integer sums, scales applied per sub-block);
@@ -176,6 +176,13 @@ qx_status qx_gemm_prefill(qx_fmt fmt, const void* W, int64_t rows, int64_t cols,
  *       first use per device and keeps (growing it is refused with QX_ERR_ARG
  *       while the stream is being captured into a graph); calls that may run
  *       concurrently on different streams must use qx_gemm_prefill_ws.
+ *   4 = small-batch GEMV, every format: the weights are streamed once per
+ *       group of four rows of X (decode of several tokens at once:
+ *       speculative or batched decode), each lane holding its column slice
+ *       of the four rows' codes and dotting every weight word with each;
+ *       the same per-block integer dot products and scales as qx_gemv's
+ *       W4A8 path, in a different f32 summation order (within the same
+ *       tolerance, not bit-for-bit path 1).
  * A path that cannot serve the call returns QX_ERR_FMT rather than falling
  * back.
  */

@@ -1,0 +1,91 @@
+"""Small-batch GEMV (qx_gemm_prefill_ex path 4): several rows of a quantised
+activation against one stream of the weights, compared with the oracle.
+
+The rows of X are independent W4A8 GEMVs (colibri GPU_BACKENDS.md, XDNA
+lane: C = A x B is row-independent), so the oracle's prefill is one W4A8
+GEMV per row of X; every output must lie within 1e-4 * sum|w * x'| of it.
+"""
+import numpy as np
+import pytest
+import torch
+
+import block_quantized_gemv_q8_gb300 as qx
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    qx.build_library()
+    qx.lib()
+    assert qx.qx_device_check() == qx.QX_OK
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+def check(fmt, W, rows, cols, X, what, sample_rows=None):
+    a = qx.qx_quantize_act_q8(dev(X))
+    q, d, s = oracle.quantize_act_q8(X)
+    assert np.array_equal(host(a.q), q) and np.array_equal(host(a.d).view(np.uint32), d.view(np.uint32))
+    m = X.shape[0]
+    # one guard row after Y: the kernel must write exactly Y[m, rows]
+    Yg = torch.full((m + 1, rows), float("nan"), device="cuda")
+    qx.qx_gemm_prefill_ex(fmt, dev(W), rows, cols, a, Y=Yg[:m], path=4)
+    Yh = host(Yg)
+    assert np.all(np.isnan(Yh[m])), f"{what}: wrote past Y"
+    Y = Yh[:m]
+    assert np.all(np.isfinite(Y)), f"{what}: unwritten or non-finite outputs"
+    wr = np.arange(rows) if sample_rows is None else sample_rows
+    ref, absdot = oracle.gemm_w4a8(fmt, np.ascontiguousarray(W[wr]), len(wr), cols, q, d)
+    y = Y[:, wr].astype(np.float64)
+    err = np.abs(y - ref)
+    bad = np.argwhere(~(err <= TOL * absdot))
+    assert bad.size == 0, (f"{what}: {len(bad)} outputs out of tolerance, e.g. {tuple(bad[0])}: "
+                           f"y={y[tuple(bad[0])]} ref={ref[tuple(bad[0])]}")
+    return Y
+
+
+# ragged batches (1..9 rows of X: whole and partial groups of four), ragged
+# row counts (not multiples of the CTA split or of the stage), narrow and wide rows
+@pytest.mark.parametrize("fmt,m,rows,cols", [
+    (synth.Q4_K, 1, 70, 1024), (synth.Q4_K, 2, 300, 4096), (synth.Q4_K, 3, 129, 256),
+    (synth.Q4_K, 4, 1000, 4096), (synth.Q4_K, 5, 77, 14336), (synth.Q4_K, 8, 513, 1024),
+    (synth.Q6_K, 2, 300, 1024), (synth.Q6_K, 4, 129, 14336), (synth.Q6_K, 7, 33, 256),
+    (synth.Q8_0, 2, 151, 896), (synth.Q8_0, 4, 300, 32), (synth.Q8_0, 6, 513, 864), (synth.Q8_0, 9, 128, 4096),
+])
+def test_batch_matches_oracle(fmt, m, rows, cols):
+    W = synth.weights(fmt, rows, cols, seed=80 + m + rows)
+    X = synth.activation(m, cols, seed=81 + m)
+    check(fmt, W, rows, cols, X, f"batch {synth.NAMES[fmt]} m={m} rows={rows} cols={cols}")
+
+
+def test_batch_zero_rows_of_x_and_tail_bytes():
+    """A zero row of X gives exact zeros; a matrix whose size is not a
+    16-byte multiple (Q8_0, 3 rows of 34 bytes) takes its tail by plain loads."""
+    fmt, rows, cols = synth.Q8_0, 3, 32
+    W = synth.weights(fmt, rows, cols, seed=90)
+    X = synth.activation(3, cols, seed=91)
+    X[1] = 0.0
+    Y = check(fmt, W, rows, cols, X, "zero row / tail bytes")
+    assert np.all(Y[1] == 0.0)
+
+
+@pytest.mark.parametrize("m", [4, 8])
+def test_batch_full_size_sampled(m):
+    """Llama-3.1-8B gate projection shape, Q4_K [14336, 4096], sampled rows."""
+    fmt, rows, cols = synth.Q4_K, 14336, 4096
+    W = synth.weights(fmt, rows, cols, seed=92)
+    X = synth.activation(m, cols, seed=93 + m)
+    rng = np.random.default_rng(94)
+    wr = np.sort(np.concatenate([rng.choice(rows, 300, replace=False), [0, rows - 1]]))
+    check(fmt, W, rows, cols, X, f"full size m={m}", sample_rows=wr)

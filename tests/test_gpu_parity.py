@@ -272,10 +272,10 @@ def test_prefill_tcgen05_formats(fmt, m, rows, cols):
 def test_prefill_auto_and_refusals():
     fmt, rows, cols = synth.Q4_K, 96, 1024
     W = dev(synth.weights(fmt, rows, cols, seed=60))
-    # automatic path: GEMV per row below 8 rows (Q4_K) or 16 rows (others), tcgen05 from there
+    # automatic path: a GEMV for one row, the small-batch GEMV for 2..16 rows, tcgen05 above
     W6 = dev(synth.weights(synth.Q6_K, rows, cols, seed=62))
-    for Wm, f, m, forced in ((W, fmt, 7, 1), (W, fmt, 8, 3), (W, fmt, 200, 3),
-                             (W6, synth.Q6_K, 15, 1), (W6, synth.Q6_K, 16, 3)):
+    for Wm, f, m, forced in ((W, fmt, 1, 1), (W, fmt, 2, 4), (W, fmt, 16, 4), (W, fmt, 17, 3), (W, fmt, 200, 3),
+                             (W6, synth.Q6_K, 15, 4), (W6, synth.Q6_K, 17, 3)):
         a, q, d, s = quantize_both(synth.activation(m, cols, seed=61 + m))
         y_auto = host(qx.qx_gemm_prefill(f, Wm, rows, cols, a))
         y_forced = host(qx.qx_gemm_prefill_ex(f, Wm, rows, cols, a, path=forced))
@@ -284,7 +284,7 @@ def test_prefill_auto_and_refusals():
         qx.qx_gemm_prefill_ex(synth.Q6_K, W6, rows, cols, a, path=2)
     assert ei.value.status == qx.QX_ERR_FMT
     with pytest.raises(qx.QxError) as ei:
-        qx.qx_gemm_prefill_ex(fmt, W, rows, cols, a, path=4)
+        qx.qx_gemm_prefill_ex(fmt, W, rows, cols, a, path=5)
     assert ei.value.status == qx.QX_ERR_ARG
 
 
