@@ -442,7 +442,7 @@ def run_extra(args):
             a = qx.ActQ8(act.q[:m], act.d[:m], act.sum[:m])
             Y = torch.empty((m, rows), dtype=torch.float32, device="cuda")
             rec = {"m": m}
-            for path in ((3,) if args.prefill_m else (1, 2, 3, 4)):
+            for path in ((args.prefill_path,) if args.prefill_m else (1, 2, 3, 4)):
                 if path in (1, 4) and m > 64:
                     continue
                 ms = graph_time_ms(torch, lambda: qx.qx_gemm_prefill_ex(fmt, W, rows, cols, a, Y=Y, path=path,
@@ -471,7 +471,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="qx", choices=["qx", "reference"])
     ap.add_argument("--prefill-m", type=int, default=0,
-                    help="prefill workload: time only the tcgen05 path at this many rows of X")
+                    help="prefill workload: time only one path (--prefill-path) at this many rows of X")
+    ap.add_argument("--prefill-path", type=int, default=3, choices=[1, 2, 3, 4],
+                    help="prefill workload with --prefill-m: the path timed")
     ap.add_argument("--workload", default="llama8b", choices=["llama8b", "q4k_1024", "lmhead_q6k", "qwen05b",
                                                                "prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

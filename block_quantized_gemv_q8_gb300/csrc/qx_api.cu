@@ -257,13 +257,14 @@ qx_status gemv_geometry(int fmt, int kmode, bool partials, bool fused, bool pdl,
     // step: 1.217 ms against 1.230 ms with one stage everywhere, 1.241 ms
     // with the whole ring everywhere).
     p.prewait = small ? stages : 1;
-    // Under programmatic dependent launch, each CTA also prefetches into L2
-    // the next kL2AheadBytes of its rows after those stages, before waiting:
-    // HBM then keeps streaming while the preceding kernel drains and the
-    // activation is quantised (GB300, Llama-3.1-8B decode step: 1.218 ->
-    // 1.210 ms; 1.248 -> 1.212 ms on another box; deeper prefetches slow
-    // the preceding kernel's last CTAs more than they gain).
-    p.l2_ahead = pdl ? kL2AheadBytes : 0;
+    // A small launch whose rows overflow its ring also prefetches into L2
+    // the next kL2AheadBytes of its rows before waiting: HBM then keeps
+    // streaming while the preceding kernel drains and the activation is
+    // quantised (GB300, Llama-3.1-8B decode step, per-CTA timestamps: the
+    // q/k/v and o launches' last CTAs finish 0.8 us earlier).  Large
+    // launches do not: their CTAs start as the preceding kernel's leave, and
+    // the prefetch then queues ahead of their activation reads.
+    p.l2_ahead = (pdl && small) ? kL2AheadBytes : 0;
     const int64_t max_cta = int64_t(dev.sm_count) * (per_sm < want ? per_sm : want);
     const int64_t groups = (p.total_rows + g.quantum - 1) / g.quantum;
     p.cols = cols;
