@@ -174,9 +174,11 @@ struct TeamGeom {
     int64_t rb, G, base;  // base: the smallest stage (rows) that keeps teams and copies whole
 };
 
+// batch_rows > 0: the small-batch lanes for that many rows of X.
 qx_status team_geometry(int fmt, int kmode, bool partials, int64_t cols, int consumer_warps, TeamGeom& g,
-                        bool batch = false) {
-    const int C = batch ? batch_cols_per_lane(fmt) : gemv_cols_per_lane(fmt, kmode);
+                        int batch_rows = 0) {
+    const bool batch = batch_rows > 0;
+    const int C = batch ? batch_cols_per_lane(fmt, batch_rows) : gemv_cols_per_lane(fmt, kmode);
     if (cols % C) return QX_ERR_SHAPE;
     g.L = static_cast<int>(cols / C);
     if (g.L <= 32) {
@@ -369,9 +371,10 @@ qx_status run_gemv(int fmt, int n, const void* const* W, const int64_t* rows, in
 }
 
 // One small-batch launch (gemv_batch_kernel): rows m0 .. m0 + mvalid - 1 of
-// X (mvalid <= kBatchRows) against W [rows, cols], into Y [X->m, rows].
+// X (mvalid <= mb, mb = kBatchRows or kBatchRowsWide) against W [rows,
+// cols], into Y [X->m, rows].
 qx_status run_gemv_batch(int fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, int64_t m0,
-                         int mvalid, float* Y, cudaStream_t s) {
+                         int mvalid, int mb, float* Y, cudaStream_t s) {
     DeviceInfo* dev = nullptr;
     qx_status st = device_info(&dev);
     if (st != QX_OK) return st;
@@ -386,14 +389,15 @@ qx_status run_gemv_batch(int fmt, const void* W, int64_t rows, int64_t cols, con
     p.xq = X->q + m0 * cols;
     p.xd = X->d + m0 * (cols / 32);
     p.xs = X->sum + m0 * (cols / 32);
+    p.mb = mb;
     p.m_valid = mvalid;
     p.y_stride = rows;
     TeamGeom g;
-    if ((st = team_geometry(fmt, QX_MODE_W4A8, false, cols, kBatchConsumerWarps, g, true)) != QX_OK) return st;
+    if ((st = team_geometry(fmt, QX_MODE_W4A8, false, cols, kBatchConsumerWarps, g, mb)) != QX_OK) return st;
     const int RS = partial_stride(g.L);
     const auto slot_of = [&](int64_t G) { return (size_t(G * g.rb) + kSlotPad + 127) / 128 * 128; };
     const auto bytes_for = [&](int64_t G, int stg) {
-        return size_t(stg) * (slot_of(G) + 24 + size_t(G) * kBatchRows * RS * 4) + 32;
+        return size_t(stg) * (slot_of(G) + 24 + size_t(G) * mb * RS * 4) + 32;
     };
     const size_t budget = 200 * 1024;
     while (g.G > g.base && bytes_for(g.G, 2) > budget) g.G -= g.base;
@@ -403,7 +407,7 @@ qx_status run_gemv_batch(int fmt, const void* W, int64_t rows, int64_t cols, con
     p.bar_off = static_cast<int>(size_t(stages) * slot);
     p.red_off = static_cast<int>((size_t(p.bar_off) + 24 * size_t(stages) + 15) / 16 * 16);
     p.act_off = p.red_off;
-    const size_t smem = size_t(p.red_off) + size_t(stages) * size_t(g.G) * kBatchRows * RS * 4;
+    const size_t smem = size_t(p.red_off) + size_t(stages) * size_t(g.G) * mb * RS * 4;
     if (smem > 227 * 1024) return QX_ERR_SHAPE;
     p.RS = RS;
     p.cols = cols;
@@ -498,14 +502,18 @@ qx_status prefill_dispatch(qx_fmt fmt, const void* W, int64_t rows, int64_t cols
     if (path < 0 || path > 4) return QX_ERR_ARG;
     if (path == 0) path = X->m == 1 ? 1 : (X->m <= kPrefillBatchMaxRows ? 4 : 3);
     if (path == 4) {
-        // kBatchRows rows of X per weight stream
-        for (int64_t m0 = 0; m0 < X->m; m0 += kBatchRows) {
-            const int mv = static_cast<int>(X->m - m0 < kBatchRows ? X->m - m0 : kBatchRows);
+        // eight rows of X per weight stream while more than four remain, then four
+        for (int64_t m0 = 0; m0 < X->m;) {
+            const int64_t left = X->m - m0;
+            const int mb = left > kBatchRows ? kBatchRowsWide : kBatchRows;
+            const int mv = static_cast<int>(left < mb ? left : mb);
             if (!aligned16(X->q + m0 * cols) || !aligned16(X->d + m0 * (cols / 32)) ||
                 !aligned16(X->sum + m0 * (cols / 32)))
                 return QX_ERR_ALIGN;
-            if ((st = run_gemv_batch(fmt, W, rows, cols, X, m0, mv, Y, reinterpret_cast<cudaStream_t>(s))) != QX_OK)
+            if ((st = run_gemv_batch(fmt, W, rows, cols, X, m0, mv, mb, Y, reinterpret_cast<cudaStream_t>(s))) !=
+                QX_OK)
                 return st;
+            m0 += mv;
         }
         return QX_OK;
     }

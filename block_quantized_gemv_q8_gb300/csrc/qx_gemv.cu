@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
 }
 
 // ----------------------------------------------------------------------------
-// Small-batch GEMV: Y[m, r] for the kBatchRows rows of a quantised
+// Small-batch GEMV: Y[m, r] for MB (four or eight) rows of a quantised
 // activation X (qx_gemm_prefill path 4).  The same weight stream as
 // gemv_kernel (contiguous rows per CTA, bulk copies into a shared-memory
 // ring, a producer lane, a reducer warp), read once for all rows of X:
@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
 // still bound by the weight bytes, not by one stream per token.  One CTA per
 // SM, 14 consumer warps.
 // ----------------------------------------------------------------------------
-template <int FMT>
+template <int FMT, int MB>
 __global__ void __launch_bounds__(kBatchThreads, 1) gemv_batch_kernel(const __grid_constant__ GemvParams p) {
     constexpr int NW = kBatchConsumerWarps;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -407,8 +407,8 @@ __global__ void __launch_bounds__(kBatchThreads, 1) gemv_batch_kernel(const __gr
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
     uint64_t* empty = full + S;
     uint64_t* part = empty + S;
-    float* red = reinterpret_cast<float*>(smem + p.red_off);  // [S][G * kBatchRows][RS]
-    const size_t red_stage = size_t(p.G) * kBatchRows * p.RS;
+    float* red = reinterpret_cast<float*>(smem + p.red_off);  // [S][G * MB][RS]
+    const size_t red_stage = size_t(p.G) * MB * p.RS;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t r0 = cta_row_begin(p, blockIdx.x), r1 = cta_row_begin(p, blockIdx.x + 1);
     if (threadIdx.x == 0) {
@@ -463,8 +463,8 @@ __global__ void __launch_bounds__(kBatchThreads, 1) gemv_batch_kernel(const __gr
         for (int k = 0; wk.next(p, e, lrow, nrows); ++k) {
             const int slot = k % S;
             if (!mbar_wait_bounded(&part[slot], (k / S) & 1, p.wait_ns, p.err, kErrTimeoutFull)) break;
-            reduce_stage_batch(red + slot * red_stage, p.RS, p.L, nrows, p.e[e].y + lrow, p.y_stride, p.m_valid,
-                               lane);
+            reduce_stage_batch<MB>(red + slot * red_stage, p.RS, p.L, nrows, p.e[e].y + lrow, p.y_stride,
+                                   p.m_valid, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
         }
@@ -474,7 +474,7 @@ __global__ void __launch_bounds__(kBatchThreads, 1) gemv_batch_kernel(const __gr
     // ---------------- consumers ----------------------------------------------
     const Team tm = make_team(warp, lane, p.team_lanes, p.team_warps, p.nteams, p.L);
     pdl_wait_prior_grid();  // X may come from the previous kernel
-    BatchLane<FMT> X;
+    BatchLane<FMT, MB> X;
     if (tm.active) X.load(p.xq, p.xd, p.xs, p.cols, p.m_valid, tm.slice);
     const uint32_t rb = static_cast<uint32_t>(p.row_bytes);
     StageWalker wk{r0, r1, 0};
@@ -483,7 +483,8 @@ __global__ void __launch_bounds__(kBatchThreads, 1) gemv_batch_kernel(const __gr
     for (int k = 0; wk.next(p, e, lrow, nrows); ++k) {
         const int slot = k % S;
         if (!mbar_wait_bounded(&full[slot], (k / S) & 1, p.wait_ns, p.err, kErrTimeoutFull)) break;
-        consume_stage_batch<FMT>(X, tm, smem + size_t(slot) * p.slot_bytes, nrows, rb, red + slot * red_stage, p.RS);
+        consume_stage_batch<FMT, MB>(X, tm, smem + size_t(slot) * p.slot_bytes, nrows, rb, red + slot * red_stage,
+                                     p.RS);
         __syncwarp();
         if (lane == 0) {
             mbar_arrive(&part[slot]);
@@ -540,7 +541,7 @@ cudaError_t occupancy_one(size_t smem, int* out) {
                                                          gemv_threads(FMT, MODE, PART, MERGED), smem);
 }
 
-template <int FMT>
+template <int FMT, int MB>
 cudaError_t launch_batch_one(const GemvParams& p, size_t smem, cudaStream_t s) {
     static bool done[64] = {false};
     int dev = 0;
@@ -549,23 +550,28 @@ cudaError_t launch_batch_one(const GemvParams& p, size_t smem, cudaStream_t s) {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!done[dev]) {
         cudaFuncAttributes fa;
-        if ((err = cudaFuncGetAttributes(&fa, gemv_batch_kernel<FMT>)) != cudaSuccess) return err;
-        err = cudaFuncSetAttribute(gemv_batch_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if ((err = cudaFuncGetAttributes(&fa, gemv_batch_kernel<FMT, MB>)) != cudaSuccess) return err;
+        err = cudaFuncSetAttribute(gemv_batch_kernel<FMT, MB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    kMaxDynamicSmem - static_cast<int>(fa.sharedSizeBytes));
         if (err != cudaSuccess) return err;
         done[dev] = true;
     }
-    gemv_batch_kernel<FMT><<<p.n_cta, kBatchThreads, smem, s>>>(p);
+    gemv_batch_kernel<FMT, MB><<<p.n_cta, kBatchThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_gemv_batch(int fmt, const GemvParams& p, size_t smem, cudaStream_t s) {
+    const bool wide = p.mb == kBatchRowsWide;
+    if (!wide && p.mb != kBatchRows) return cudaErrorInvalidValue;
     switch (fmt) {
-        case QX_Q4_K: return launch_batch_one<QX_Q4_K>(p, smem, s);
-        case QX_Q6_K: return launch_batch_one<QX_Q6_K>(p, smem, s);
-        case QX_Q8_0: return launch_batch_one<QX_Q8_0>(p, smem, s);
+        case QX_Q4_K: return wide ? launch_batch_one<QX_Q4_K, kBatchRowsWide>(p, smem, s)
+                                  : launch_batch_one<QX_Q4_K, kBatchRows>(p, smem, s);
+        case QX_Q6_K: return wide ? launch_batch_one<QX_Q6_K, kBatchRowsWide>(p, smem, s)
+                                  : launch_batch_one<QX_Q6_K, kBatchRows>(p, smem, s);
+        case QX_Q8_0: return wide ? launch_batch_one<QX_Q8_0, kBatchRowsWide>(p, smem, s)
+                                  : launch_batch_one<QX_Q8_0, kBatchRows>(p, smem, s);
         default: return cudaErrorInvalidValue;
     }
 }

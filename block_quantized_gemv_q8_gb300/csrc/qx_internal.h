@@ -78,20 +78,25 @@ struct GemvParams {
     unsigned* err;     // device error word
     uint64_t wait_ns;  // bound on every wait
     // Batched launches (gemv_batch_kernel): rows m of a quantised activation
-    // X, y[m * y_stride + r] for m < m_valid; the lanes hold kBatchRows rows
-    // (rows m_valid .. kBatchRows - 1 repeat row m_valid - 1, unwritten).
+    // X, y[m * y_stride + r] for m < m_valid; the lanes hold mb rows (rows
+    // m_valid .. mb - 1 repeat row m_valid - 1, unwritten).
+    int mb;
     int m_valid;
     int64_t y_stride;
 };
 
 // Small-batch GEMV (one weight stream for several activation rows): rows of
-// X per launch, consumer warps (one CTA per SM: 16 warps of <= 128
-// registers), and columns per lane (half as many as the batch-1 W4A8 lanes,
-// so that four activation slices fit in registers).
+// X per launch (four, or eight for 5..8 remaining rows), consumer warps (one
+// CTA per SM: 16 warps of <= 128 registers), and columns per lane (64 for
+// the K-quants with four rows, 32 otherwise, so that the rows' activation
+// slices fit in registers).
 constexpr int kBatchRows = 4;
+constexpr int kBatchRowsWide = 8;
 constexpr int kBatchConsumerWarps = 14;
 constexpr int kBatchThreads = 32 * (kBatchConsumerWarps + 2);
-__host__ __device__ constexpr int batch_cols_per_lane(int fmt) { return fmt == QX_Q8_0 ? 32 : 64; }
+__host__ __device__ constexpr int batch_cols_per_lane(int fmt, int mb) {
+    return (fmt == QX_Q8_0 || mb > kBatchRows) ? 32 : 64;
+}
 
 // Columns owned by one lane, per (format, mode).
 __host__ __device__ constexpr int gemv_cols_per_lane(int fmt, int mode) {

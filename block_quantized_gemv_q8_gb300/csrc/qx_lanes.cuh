@@ -579,15 +579,16 @@ __device__ __forceinline__ void reduce_stage(const float* red, int RS, int L, in
 // once and dotted with each row's codes.  Same arithmetic per (row of X,
 // weight row) as the batch-1 W4A8 lanes.
 // ----------------------------------------------------------------------------
-template <int FMT>
+template <int FMT, int MB>
 struct BatchLane;
 
+// Four rows of X.
 // Q4_K: 64 columns = the 32-byte quant chunk c of super-block sb: sub-block
 // 2c in the low nibbles, sub-block 2c + 1 in the high nibbles.
 template <>
-struct BatchLane<QX_Q4_K> {
+struct BatchLane<QX_Q4_K, 4> {
     static constexpr int C = 64;
-    static constexpr int MB = kBatchRows;
+    static constexpr int MB = 4;
     uint32_t xq[MB][16];
     float dxs[MB][2];  // dx of sub-blocks 2c and 2c + 1, the second divided by 16
     float t[MB][2];    // dx * (sum of q_x): weight of the min term
@@ -657,9 +658,9 @@ struct BatchLane<QX_Q4_K> {
 // bytes); four scale groups of 16.  The quants are dotted unsigned (0..63)
 // and the -32 offset is applied as -32 * sum(q_x) per group.
 template <>
-struct BatchLane<QX_Q6_K> {
+struct BatchLane<QX_Q6_K, 4> {
     static constexpr int C = 64;
-    static constexpr int MB = kBatchRows;
+    static constexpr int MB = 4;
     uint32_t xq[MB][16];  // quarter tp (words 0..7), quarter tp + 2 (words 8..15)
     float dx[MB][2];
     int s16[MB][4];
@@ -729,11 +730,130 @@ struct BatchLane<QX_Q6_K> {
     }
 };
 
-// Q8_0: 32 columns = one block.
+// Eight rows of X: 32-column lanes, so that eight slices fit in registers.
+// Q4_K: 32 columns = sub-block j = 2c + hb of super-block sb: the low (hb =
+// 0) or high (hb = 1) nibbles of quant chunk c.  The high nibbles are dotted
+// in place (16 x q, the unsigned x signed dp4a) and the factor folded into dx.
 template <>
-struct BatchLane<QX_Q8_0> {
+struct BatchLane<QX_Q4_K, 8> {
     static constexpr int C = 32;
-    static constexpr int MB = kBatchRows;
+    static constexpr int MB = 8;
+    uint32_t xq[MB][8];
+    float dxs[MB];  // dx, divided by 16 for a high-nibble sub-block
+    float t[MB];    // dx * (sum of q_x)
+    __device__ __forceinline__ void load(const int8_t* q, const float* d, const int32_t* s, int64_t qstride,
+                                         int mvalid, int l) {
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+            const int64_t mm = m < mvalid ? m : mvalid - 1;
+            const uint4* src = reinterpret_cast<const uint4*>(q + mm * qstride + int64_t(l) * C);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const uint4 v = src[k];
+                xq[m][4 * k + 0] = v.x;
+                xq[m][4 * k + 1] = v.y;
+                xq[m][4 * k + 2] = v.z;
+                xq[m][4 * k + 3] = v.w;
+            }
+            const int64_t b = mm * (qstride / 32) + l;
+            const float dx = d[b];
+            dxs[m] = (l & 1) ? dx * 0.0625f : dx;
+            t[m] = dx * float(s[b]);
+        }
+    }
+    __device__ __forceinline__ void row(const uint8_t* rp, int l, float (&out)[MB]) const {
+        const int sb = l >> 3, j = l & 7;
+        const uint8_t* bp = rp + sb * 144;
+        const uint4 hdr = *reinterpret_cast<const uint4*>(bp);
+        const uint4* qsp = reinterpret_cast<const uint4*>(bp + 16 + 32 * (j >> 1));
+        const uint4 a = qsp[0], b = qsp[1];
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        const uint32_t mask = (j & 1) ? 0xF0F0F0F0u : 0x0F0F0F0Fu;
+        int P[MB];
+#pragma unroll
+        for (int m = 0; m < MB; ++m) P[m] = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t wq = w[i] & mask;
+#pragma unroll
+            for (int m = 0; m < MB; ++m) P[m] = dp4a_us(wq, xq[m][i], P[m]);
+        }
+        const Q4KScales S = q4k_unpack_scales(hdr.y, hdr.z, hdr.w);
+        const int sc = int(byte_of(j < 4 ? S.sc_lo : S.sc_hi, j & 3));
+        const float mn = float(int(byte_of(j < 4 ? S.m_lo : S.m_hi, j & 3)));
+        const float dd = f16_bits_to_f32(hdr.x), dmin = f16_bits_to_f32(hdr.x >> 16);
+#pragma unroll
+        for (int m = 0; m < MB; ++m) out[m] = dd * (float(P[m] * sc) * dxs[m]) - dmin * (mn * t[m]);
+    }
+};
+
+// Q6_K: 32 columns = quarter t of half h of super-block sb (ql bytes
+// 64h + 32 (t & 1), low nibbles for t < 2, high for t >= 2; qh bits 2t,
+// 2t + 1); two scale groups of 16.
+template <>
+struct BatchLane<QX_Q6_K, 8> {
+    static constexpr int C = 32;
+    static constexpr int MB = 8;
+    uint32_t xq[MB][8];
+    float dx[MB];
+    int s16[MB][2];
+    __device__ __forceinline__ void load(const int8_t* q, const float* d, const int32_t*, int64_t qstride,
+                                         int mvalid, int l) {
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+            const int64_t mm = m < mvalid ? m : mvalid - 1;
+            const uint4* src = reinterpret_cast<const uint4*>(q + mm * qstride + int64_t(l) * C);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const uint4 v = src[k];
+                xq[m][4 * k + 0] = v.x;
+                xq[m][4 * k + 1] = v.y;
+                xq[m][4 * k + 2] = v.z;
+                xq[m][4 * k + 3] = v.w;
+            }
+            dx[m] = d[mm * (qstride / 32) + l];
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                int sg = 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) sg = dp4a(xq[m][4 * g + i], 0x01010101u, sg);
+                s16[m][g] = sg;
+            }
+        }
+    }
+    __device__ __forceinline__ void row(const uint8_t* rp, int l, float (&out)[MB]) const {
+        const int sb = l >> 3, h = (l >> 2) & 1, tq = l & 3;
+        const uint8_t* bp = rp + sb * 210;
+        uint32_t ql[8], qh[8], scw;
+        load_words<8>(bp + 64 * h + 32 * (tq & 1), ql);
+        load_words<8>(bp + 128 + 32 * h, qh);
+        scw = lds_u32_a2(bp + 192 + 8 * h + 2 * tq);  // scale bytes 2t, 2t + 1 of this half
+        const uint32_t nib = (tq >> 1) * 4u, hsh = 2u * uint32_t(tq);
+        int P[MB][2];
+#pragma unroll
+        for (int m = 0; m < MB; ++m) P[m][0] = P[m][1] = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            // the 6-bit quants of quarter t, one per byte
+            const uint32_t wq = ((ql[i] >> nib) & 0x0F0F0F0Fu) | (((qh[i] >> hsh) & 0x03030303u) << 4);
+#pragma unroll
+            for (int m = 0; m < MB; ++m) P[m][i >> 2] = dp4a_us(wq, xq[m][i], P[m][i >> 2]);
+        }
+        const int s0 = int(int8_t(byte_of(scw, 0))), s1 = int(int8_t(byte_of(scw, 1)));
+        const float dd = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(bp + 208));
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+            const int acc = s0 * (P[m][0] - 32 * s16[m][0]) + s1 * (P[m][1] - 32 * s16[m][1]);
+            out[m] = dd * (dx[m] * float(acc));
+        }
+    }
+};
+
+// Q8_0: 32 columns = one block (four or eight rows of X).
+template <int MB_>
+struct BatchLane<QX_Q8_0, MB_> {
+    static constexpr int C = 32;
+    static constexpr int MB = MB_;
     uint32_t xq[MB][8];
     float dx[MB];
     __device__ __forceinline__ void load(const int8_t* q, const float* d, const int32_t*, int64_t qstride,
@@ -772,26 +892,27 @@ struct BatchLane<QX_Q8_0> {
 
 // All rows of one stage for the batched lanes: team t takes rows t,
 // t + nteams, ...; the partial of (row i, activation row m) goes to
-// red[(i * kBatchRows + m) * RS + slice].
-template <int FMT>
-__device__ __forceinline__ void consume_stage_batch(const BatchLane<FMT>& X, const Team& tm, const uint8_t* sbuf,
-                                                    int nrows, uint32_t rb, float* red, int RS) {
+// red[(i * MB + m) * RS + slice].
+template <int FMT, int MB>
+__device__ __forceinline__ void consume_stage_batch(const BatchLane<FMT, MB>& X, const Team& tm,
+                                                    const uint8_t* sbuf, int nrows, uint32_t rb, float* red, int RS) {
     if (!tm.active) return;
     for (int i = tm.team; i < nrows; i += tm.nteams) {
-        float v[kBatchRows];
+        float v[MB];
         X.row(sbuf + uint32_t(i) * rb, tm.slice, v);
 #pragma unroll
-        for (int m = 0; m < kBatchRows; ++m) red[(i * kBatchRows + m) * RS + tm.slice] = v[m];
+        for (int m = 0; m < MB; ++m) red[(i * MB + m) * RS + tm.slice] = v[m];
     }
 }
 
 // The reducer's share of one batched stage: one (row, activation row) pair
 // per lane, its L partials added in the same fixed order as reduce_stage;
 // y[m * y_stride + row] for m < mvalid.
+template <int MB>
 __device__ __forceinline__ void reduce_stage_batch(const float* red, int RS, int L, int nrows, float* y,
                                                    int64_t y_stride, int mvalid, int lane) {
-    for (int pair = lane; pair < nrows * kBatchRows; pair += 32) {
-        const int row = pair / kBatchRows, m = pair % kBatchRows;
+    for (int pair = lane; pair < nrows * MB; pair += 32) {
+        const int row = pair / MB, m = pair % MB;
         const float* pr = red + pair * RS;
         float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
         int s = 0;
