@@ -37,9 +37,6 @@ constexpr size_t kChainSmBytes = 200 * 1024;
 constexpr int kMaxStageRows = 256;
 // Launch bytes per SM up to which a PDL launch runs one CTA per SM.
 constexpr int64_t kOneCtaPerSmBytes = 192 * 1024;
-// Bytes of its later rows a PDL-launched CTA prefetches into L2 before
-// waiting on the preceding kernel.
-constexpr int64_t kL2AheadBytes = 128 * 1024;
 // Launches streaming at least this many bytes take the merged variant where
 // one exists (gemv_has_merged).
 constexpr int64_t kMergedMinBytes = int64_t(128) << 20;
@@ -259,14 +256,6 @@ qx_status gemv_geometry(int fmt, int kmode, bool partials, bool fused, bool pdl,
     // step: 1.217 ms against 1.230 ms with one stage everywhere, 1.241 ms
     // with the whole ring everywhere).
     p.prewait = small ? stages : 1;
-    // A small launch whose rows overflow its ring also prefetches into L2
-    // the next kL2AheadBytes of its rows before waiting: HBM then keeps
-    // streaming while the preceding kernel drains and the activation is
-    // quantised (GB300, Llama-3.1-8B decode step, per-CTA timestamps: the
-    // q/k/v and o launches' last CTAs finish 0.8 us earlier).  Large
-    // launches do not: their CTAs start as the preceding kernel's leave, and
-    // the prefetch then queues ahead of their activation reads.
-    p.l2_ahead = (pdl && small) ? kL2AheadBytes : 0;
     const int64_t max_cta = int64_t(dev.sm_count) * (per_sm < want ? per_sm : want);
     const int64_t groups = (p.total_rows + g.quantum - 1) / g.quantum;
     p.cols = cols;

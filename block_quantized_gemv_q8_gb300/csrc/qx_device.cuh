@@ -96,12 +96,6 @@ __device__ __forceinline__ void bulk_g2s_evict_first(void* dst, const void* src,
         : "memory");
 }
 
-// 1-D bulk prefetch global -> L2 (no completion to wait for).  src and bytes
-// must be multiples of 16.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

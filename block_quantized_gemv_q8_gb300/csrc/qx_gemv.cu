@@ -72,26 +72,6 @@ struct StageWalker {
     }
 };
 
-// Prefetches into L2 up to `limit` bytes of the rows [g, gend) (in the
-// concatenated row space), in row order.  Issued before waiting on the
-// preceding kernel, so that HBM keeps streaming this CTA's later rows while
-// that kernel drains; the bulk copies of those rows then hit L2.  Byte ranges
-// are trimmed inwards to 16-byte boundaries.
-__device__ __forceinline__ void prefetch_rows_l2(const GemvParams& p, int64_t g, int64_t gend, int64_t limit) {
-    constexpr int64_t kChunk = 32 * 1024;
-    for (int e = 0; e < p.n_entries && limit > 0; ++e) {
-        const int64_t er0 = p.e[e].row0, er1 = er0 + p.e[e].rows;
-        const int64_t a = g > er0 ? g : er0, b = gend < er1 ? gend : er1;
-        if (a >= b) continue;
-        int64_t lo = ((a - er0) * p.row_bytes + 15) & ~int64_t(15);
-        int64_t hi = ((b - er0) * p.row_bytes) & ~int64_t(15);
-        if (hi - lo > limit) hi = lo + (limit & ~int64_t(15));
-        for (int64_t o = lo; o < hi; o += kChunk)
-            bulk_prefetch_l2(p.e[e].W + o, static_cast<uint32_t>(hi - o < kChunk ? hi - o : kChunk));
-        if (hi > lo) limit -= hi - lo;
-    }
-}
-
 // W4A8 kernels and Q8_0 kernels fit two CTAs per SM (<= 112 registers), so
 // that with programmatic dependent launch the next GEMV's CTA can be resident
 // next to this one and stream its weights while this one finishes.
@@ -204,10 +184,7 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
         };
         const auto issue_first_stages = [&]() {
             for (int k = 0; k < S; ++k) {
-                if (k == p.prewait) {
-                    if (p.l2_ahead > 0) prefetch_rows_l2(p, wk.g, r1, p.l2_ahead);
-                    pdl_wait_prior_grid();
-                }
+                if (k == p.prewait) pdl_wait_prior_grid();
                 if (!issue_next()) break;
             }
         };
@@ -226,10 +203,7 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
                 StageWalker pw{r0, r1, 0};
                 for (int k = 0; pw.next(p, e, lrow, nrows); ++k) {
                     const int slot = k % S;
-                    if (k == p.prewait) {
-                        if (p.l2_ahead > 0) prefetch_rows_l2(p, p.e[e].row0 + lrow, r1, p.l2_ahead);
-                        pdl_wait_prior_grid();
-                    }
+                    if (k == p.prewait) pdl_wait_prior_grid();
                     if (k >= S &&
                         !mbar_wait_bounded(&empty[slot], ((k / S) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty))
                         break;
@@ -277,10 +251,7 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
             bool more = true;
             if (lane == 0) {
                 for (; k < S && (more = pw.next(p, e, lrow, nrows)); ++k) {
-                    if (k == p.prewait) {
-                        if (p.l2_ahead > 0) prefetch_rows_l2(p, p.e[e].row0 + lrow, r1, p.l2_ahead);
-                        pdl_wait_prior_grid();
-                    }
+                    if (k == p.prewait) pdl_wait_prior_grid();
                     issue_stage(k);
                 }
             }
@@ -289,10 +260,7 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
             if (lane != 0) return;
             if (more) {
                 for (; pw.next(p, e, lrow, nrows); ++k) {
-                    if (k == p.prewait) {
-                        if (p.l2_ahead > 0) prefetch_rows_l2(p, p.e[e].row0 + lrow, r1, p.l2_ahead);
-                        pdl_wait_prior_grid();
-                    }
+                    if (k == p.prewait) pdl_wait_prior_grid();
                     if (!mbar_wait_bounded(&empty[k % S], ((k / S) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty)) break;
                     issue_stage(k);
                 }

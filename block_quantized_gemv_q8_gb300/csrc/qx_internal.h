@@ -64,7 +64,6 @@ struct GemvParams {
     int RS;           // floats per row of the per-lane partial-sum area
     int n_cta;
     int prewait;       // stages the producer issues before waiting on the preceding kernel
-    int64_t l2_ahead;  // bytes of the CTA's later rows prefetched into L2 before that wait
     int merged;        // 1: the merged producer/reducer variant (gemv_has_merged)
     const float* x;    // f32 mode activation [cols]
     const int8_t* xq;  // W4A8 activation quants [cols]
