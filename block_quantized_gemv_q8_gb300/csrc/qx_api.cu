@@ -59,14 +59,14 @@ qx_status cuda_fail(cudaError_t e, const char* where) {
     cudaGetLastError();  // clear a non-sticky error so that it is not reported twice
     return QX_ERR_CUDA;
 }
-// Resident CTAs per SM, keyed by (device, format, mode, partials, smem bytes).
-std::map<std::tuple<int, int, int, int, int, size_t>, int> g_occupancy;
+// Resident CTAs per SM, keyed by (device, format, mode, partials, merged, fused, smem bytes).
+std::map<std::tuple<int, int, int, int, int, int, size_t>, int> g_occupancy;
 
-qx_status ctas_per_sm(int fmt, int mode, bool partials, bool merged, size_t smem, int* out) {
+qx_status ctas_per_sm(int fmt, int mode, bool partials, bool merged, bool fused, size_t smem, int* out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    const auto key = std::make_tuple(dev, fmt, mode, partials ? 1 : 0, merged ? 1 : 0, smem);
+    const auto key = std::make_tuple(dev, fmt, mode, partials ? 1 : 0, merged ? 1 : 0, fused ? 1 : 0, smem);
     {
         std::lock_guard<std::mutex> lock(g_mu);
         auto it = g_occupancy.find(key);
@@ -76,7 +76,7 @@ qx_status ctas_per_sm(int fmt, int mode, bool partials, bool merged, size_t smem
         }
     }
     int n = 0;
-    if ((e = gemv_max_ctas_per_sm(fmt, mode, partials, merged, smem, &n)) != cudaSuccess)
+    if ((e = gemv_max_ctas_per_sm(fmt, mode, partials, merged, fused, smem, &n)) != cudaSuccess)
         return cuda_fail(e, "occupancy query");
     if (n < 1) return cuda_fail(cudaErrorInvalidConfiguration, "no CTA fits on an SM");
     std::lock_guard<std::mutex> lock(g_mu);
@@ -242,7 +242,7 @@ qx_status gemv_geometry(int fmt, int kmode, bool partials, bool fused, bool pdl,
     if (smem > 227 * 1024) return QX_ERR_SHAPE;
 
     int per_sm = 0;
-    st = ctas_per_sm(fmt, kmode, partials, merged, smem, &per_sm);
+    st = ctas_per_sm(fmt, kmode, partials, merged, fused, smem, &per_sm);
     if (st != QX_OK) return st;
     // Under programmatic dependent launch, a launch that streams little per SM
     // runs one CTA per SM: the rest of each SM then holds the next launch's

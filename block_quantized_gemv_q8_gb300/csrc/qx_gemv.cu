@@ -80,13 +80,15 @@ constexpr int gemv_min_blocks() {
     return (MODE == QX_MODE_W4A8 || FMT == QX_Q8_0) ? 2 : 1;
 }
 
-template <int FMT, int MODE, bool PART, bool MERGED>
+// FUSED: W4A8 with the activation quantised in-kernel (p.xf set).
+template <int FMT, int MODE, bool PART, bool MERGED, bool FUSED>
 __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_min_blocks<FMT, MODE>())
     gemv_kernel(const __grid_constant__ GemvParams p) {
     using LaneT = Lane<FMT, MODE>;
     constexpr int NW = gemv_consumer_warps(FMT, MODE, MERGED);
     constexpr bool kMerged = MERGED;
     static_assert(!MERGED || gemv_has_merged(FMT, MODE, PART), "no merged variant of this kernel");
+    static_assert(!FUSED || (MODE == QX_MODE_W4A8 && !PART), "in-kernel quantisation is a W4A8 y-output variant");
     // Warps that may quantise an f32 activation in-kernel: all of them -- the
     // producer and the reducer have nothing else to do until the consumers
     // finish their first stage, which needs the quantised activation.  They
@@ -195,7 +197,7 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
                 mbar_wait_bounded(&full[k % S], (k / S) & 1, p.wait_ns, p.err, kErrTimeoutDrain);
         };
         if constexpr (!kMerged) {
-            const bool helps = MODE == QX_MODE_W4A8 && p.xf != nullptr && helpers;
+            const bool helps = FUSED && helpers;
             if (!helps) {
                 if (lane != 0) return;
                 int e, nrows;
@@ -271,7 +273,7 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
             // The other lanes wait here for lane 0, and below for each refill,
             // so that the warp never sits in two different waits at once.
             __syncwarp();
-            if (MODE == QX_MODE_W4A8 && p.xf != nullptr) quantise_share();
+            if constexpr (FUSED) quantise_share();
             StageWalker rw{r0, r1, 0};
             int e, nrows;
             int64_t lrow;
@@ -292,7 +294,7 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
     if constexpr (!PART && !kMerged) {
         if (warp == NW + 1) {
             // ---------------- reducer: row sums of every stage, in order -----
-            if (MODE == QX_MODE_W4A8 && p.xf != nullptr && helpers) quantise_share();
+            if (FUSED && helpers) quantise_share();
             StageWalker wk{r0, r1, 0};
             int e, nrows;
             int64_t lrow;
@@ -315,8 +317,8 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
     const float* d = p.xd;
     const int32_t* s = p.xs;
     pdl_wait_prior_grid();  // the activation may come from the previous kernel
-    if constexpr (MODE == QX_MODE_W4A8) {
-        if (p.xf != nullptr) {
+    if constexpr (FUSED) {
+        {
             // Quantise the f32 activation once per CTA into shared memory,
             // with the same code as qx_quantize_act_q8; two adjacent lanes
             // per block of 32; all consumer lanes (and a merged
@@ -333,10 +335,10 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
         }
     }
     // the quantised activation in shared memory has its 128-byte slices permuted
-    if (tm.active) load_slice<MODE>(X, q, d, s, p.x, tm.slice, FMT != QX_Q8_0 && p.xf != nullptr);
+    if (tm.active) load_slice<MODE>(X, q, d, s, p.x, tm.slice, FMT != QX_Q8_0 && FUSED);
     if constexpr (MODE == QX_MODE_W4A8) {
         // the quantised activation shares its area with the partial sums
-        if (p.xf != nullptr) quantiser_barrier(qthreads);
+        if constexpr (FUSED) quantiser_barrier(qthreads);
     }
 
     const uint32_t rb = static_cast<uint32_t>(p.row_bytes);
@@ -467,7 +469,7 @@ constexpr int kMaxDynamicSmem = 227 * 1024;
 // Raise the kernel's dynamic shared-memory limit to the maximum, once per
 // kernel and device.  Occupancy and launches then depend only on the bytes
 // each launch asks for.
-template <int FMT, int MODE, bool PART, bool MERGED>
+template <int FMT, int MODE, bool PART, bool MERGED, bool FUSED>
 cudaError_t configure_once() {
     static bool done[64] = {false};
     int dev = 0;
@@ -476,17 +478,17 @@ cudaError_t configure_once() {
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (done[dev]) return cudaSuccess;
     cudaFuncAttributes fa;
-    err = cudaFuncGetAttributes(&fa, gemv_kernel<FMT, MODE, PART, MERGED>);
+    err = cudaFuncGetAttributes(&fa, gemv_kernel<FMT, MODE, PART, MERGED, FUSED>);
     if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(gemv_kernel<FMT, MODE, PART, MERGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(gemv_kernel<FMT, MODE, PART, MERGED, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kMaxDynamicSmem - static_cast<int>(fa.sharedSizeBytes));
     if (err == cudaSuccess) done[dev] = true;
     return err;
 }
 
-template <int FMT, int MODE, bool PART, bool MERGED>
+template <int FMT, int MODE, bool PART, bool MERGED, bool FUSED>
 cudaError_t launch_one(const GemvParams& p, size_t smem, cudaStream_t s, bool pdl) {
-    cudaError_t err = configure_once<FMT, MODE, PART, MERGED>();
+    cudaError_t err = configure_once<FMT, MODE, PART, MERGED, FUSED>();
     if (err != cudaSuccess) return err;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.n_cta);
@@ -498,14 +500,14 @@ cudaError_t launch_one(const GemvParams& p, size_t smem, cudaStream_t s, bool pd
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<FMT, MODE, PART, MERGED>, p);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<FMT, MODE, PART, MERGED, FUSED>, p);
 }
 
-template <int FMT, int MODE, bool PART, bool MERGED>
+template <int FMT, int MODE, bool PART, bool MERGED, bool FUSED>
 cudaError_t occupancy_one(size_t smem, int* out) {
-    cudaError_t err = configure_once<FMT, MODE, PART, MERGED>();
+    cudaError_t err = configure_once<FMT, MODE, PART, MERGED, FUSED>();
     if (err != cudaSuccess) return err;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, gemv_kernel<FMT, MODE, PART, MERGED>,
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, gemv_kernel<FMT, MODE, PART, MERGED, FUSED>,
                                                          gemv_threads(FMT, MODE, PART, MERGED), smem);
 }
 
@@ -546,41 +548,52 @@ cudaError_t launch_gemv_batch(int fmt, const GemvParams& p, size_t smem, cudaStr
 
 cudaError_t launch_gemv(int fmt, int mode, bool partials, const GemvParams& p, size_t smem, cudaStream_t s,
                         bool pdl) {
+    const bool fused = p.xf != nullptr;
+    if (fused && (mode != QX_MODE_W4A8 || partials)) return cudaErrorInvalidValue;
     if (p.merged) {
         if (fmt == QX_Q6_K && mode == QX_MODE_W4A8 && !partials)
-            return launch_one<QX_Q6_K, QX_MODE_W4A8, false, true>(p, smem, s, pdl);
+            return fused ? launch_one<QX_Q6_K, QX_MODE_W4A8, false, true, true>(p, smem, s, pdl)
+                         : launch_one<QX_Q6_K, QX_MODE_W4A8, false, true, false>(p, smem, s, pdl);
         return cudaErrorInvalidValue;
     }
-    switch (fmt * 4 + mode * 2 + (partials ? 1 : 0)) {
-        case QX_Q4_K * 4 + 0: return launch_one<QX_Q4_K, QX_MODE_F32, false, false>(p, smem, s, pdl);
-        case QX_Q4_K * 4 + 2: return launch_one<QX_Q4_K, QX_MODE_W4A8, false, false>(p, smem, s, pdl);
-        case QX_Q4_K * 4 + 3: return launch_one<QX_Q4_K, QX_MODE_W4A8, true, false>(p, smem, s, pdl);
-        case QX_Q6_K * 4 + 0: return launch_one<QX_Q6_K, QX_MODE_F32, false, false>(p, smem, s, pdl);
-        case QX_Q6_K * 4 + 2: return launch_one<QX_Q6_K, QX_MODE_W4A8, false, false>(p, smem, s, pdl);
-        case QX_Q6_K * 4 + 3: return launch_one<QX_Q6_K, QX_MODE_W4A8, true, false>(p, smem, s, pdl);
-        case QX_Q8_0 * 4 + 0: return launch_one<QX_Q8_0, QX_MODE_F32, false, false>(p, smem, s, pdl);
-        case QX_Q8_0 * 4 + 2: return launch_one<QX_Q8_0, QX_MODE_W4A8, false, false>(p, smem, s, pdl);
-        case QX_Q8_0 * 4 + 3: return launch_one<QX_Q8_0, QX_MODE_W4A8, true, false>(p, smem, s, pdl);
+    switch (fmt * 8 + mode * 4 + (partials ? 2 : 0) + (fused ? 1 : 0)) {
+        case QX_Q4_K * 8 + 0: return launch_one<QX_Q4_K, QX_MODE_F32, false, false, false>(p, smem, s, pdl);
+        case QX_Q4_K * 8 + 4: return launch_one<QX_Q4_K, QX_MODE_W4A8, false, false, false>(p, smem, s, pdl);
+        case QX_Q4_K * 8 + 5: return launch_one<QX_Q4_K, QX_MODE_W4A8, false, false, true>(p, smem, s, pdl);
+        case QX_Q4_K * 8 + 6: return launch_one<QX_Q4_K, QX_MODE_W4A8, true, false, false>(p, smem, s, pdl);
+        case QX_Q6_K * 8 + 0: return launch_one<QX_Q6_K, QX_MODE_F32, false, false, false>(p, smem, s, pdl);
+        case QX_Q6_K * 8 + 4: return launch_one<QX_Q6_K, QX_MODE_W4A8, false, false, false>(p, smem, s, pdl);
+        case QX_Q6_K * 8 + 5: return launch_one<QX_Q6_K, QX_MODE_W4A8, false, false, true>(p, smem, s, pdl);
+        case QX_Q6_K * 8 + 6: return launch_one<QX_Q6_K, QX_MODE_W4A8, true, false, false>(p, smem, s, pdl);
+        case QX_Q8_0 * 8 + 0: return launch_one<QX_Q8_0, QX_MODE_F32, false, false, false>(p, smem, s, pdl);
+        case QX_Q8_0 * 8 + 4: return launch_one<QX_Q8_0, QX_MODE_W4A8, false, false, false>(p, smem, s, pdl);
+        case QX_Q8_0 * 8 + 5: return launch_one<QX_Q8_0, QX_MODE_W4A8, false, false, true>(p, smem, s, pdl);
+        case QX_Q8_0 * 8 + 6: return launch_one<QX_Q8_0, QX_MODE_W4A8, true, false, false>(p, smem, s, pdl);
         default: return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t gemv_max_ctas_per_sm(int fmt, int mode, bool partials, bool merged, size_t smem, int* out) {
+cudaError_t gemv_max_ctas_per_sm(int fmt, int mode, bool partials, bool merged, bool fused, size_t smem, int* out) {
+    if (fused && (mode != QX_MODE_W4A8 || partials)) return cudaErrorInvalidValue;
     if (merged) {
         if (fmt == QX_Q6_K && mode == QX_MODE_W4A8 && !partials)
-            return occupancy_one<QX_Q6_K, QX_MODE_W4A8, false, true>(smem, out);
+            return fused ? occupancy_one<QX_Q6_K, QX_MODE_W4A8, false, true, true>(smem, out)
+                         : occupancy_one<QX_Q6_K, QX_MODE_W4A8, false, true, false>(smem, out);
         return cudaErrorInvalidValue;
     }
-    switch (fmt * 4 + mode * 2 + (partials ? 1 : 0)) {
-        case QX_Q4_K * 4 + 0: return occupancy_one<QX_Q4_K, QX_MODE_F32, false, false>(smem, out);
-        case QX_Q4_K * 4 + 2: return occupancy_one<QX_Q4_K, QX_MODE_W4A8, false, false>(smem, out);
-        case QX_Q4_K * 4 + 3: return occupancy_one<QX_Q4_K, QX_MODE_W4A8, true, false>(smem, out);
-        case QX_Q6_K * 4 + 0: return occupancy_one<QX_Q6_K, QX_MODE_F32, false, false>(smem, out);
-        case QX_Q6_K * 4 + 2: return occupancy_one<QX_Q6_K, QX_MODE_W4A8, false, false>(smem, out);
-        case QX_Q6_K * 4 + 3: return occupancy_one<QX_Q6_K, QX_MODE_W4A8, true, false>(smem, out);
-        case QX_Q8_0 * 4 + 0: return occupancy_one<QX_Q8_0, QX_MODE_F32, false, false>(smem, out);
-        case QX_Q8_0 * 4 + 2: return occupancy_one<QX_Q8_0, QX_MODE_W4A8, false, false>(smem, out);
-        case QX_Q8_0 * 4 + 3: return occupancy_one<QX_Q8_0, QX_MODE_W4A8, true, false>(smem, out);
+    switch (fmt * 8 + mode * 4 + (partials ? 2 : 0) + (fused ? 1 : 0)) {
+        case QX_Q4_K * 8 + 0: return occupancy_one<QX_Q4_K, QX_MODE_F32, false, false, false>(smem, out);
+        case QX_Q4_K * 8 + 4: return occupancy_one<QX_Q4_K, QX_MODE_W4A8, false, false, false>(smem, out);
+        case QX_Q4_K * 8 + 5: return occupancy_one<QX_Q4_K, QX_MODE_W4A8, false, false, true>(smem, out);
+        case QX_Q4_K * 8 + 6: return occupancy_one<QX_Q4_K, QX_MODE_W4A8, true, false, false>(smem, out);
+        case QX_Q6_K * 8 + 0: return occupancy_one<QX_Q6_K, QX_MODE_F32, false, false, false>(smem, out);
+        case QX_Q6_K * 8 + 4: return occupancy_one<QX_Q6_K, QX_MODE_W4A8, false, false, false>(smem, out);
+        case QX_Q6_K * 8 + 5: return occupancy_one<QX_Q6_K, QX_MODE_W4A8, false, false, true>(smem, out);
+        case QX_Q6_K * 8 + 6: return occupancy_one<QX_Q6_K, QX_MODE_W4A8, true, false, false>(smem, out);
+        case QX_Q8_0 * 8 + 0: return occupancy_one<QX_Q8_0, QX_MODE_F32, false, false, false>(smem, out);
+        case QX_Q8_0 * 8 + 4: return occupancy_one<QX_Q8_0, QX_MODE_W4A8, false, false, false>(smem, out);
+        case QX_Q8_0 * 8 + 5: return occupancy_one<QX_Q8_0, QX_MODE_W4A8, false, false, true>(smem, out);
+        case QX_Q8_0 * 8 + 6: return occupancy_one<QX_Q8_0, QX_MODE_W4A8, true, false, false>(smem, out);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -143,7 +143,7 @@ cudaError_t launch_actq8(const float* x, int64_t nblocks, int8_t* q, float* d, i
                          cudaStream_t s);
 cudaError_t launch_gemv(int fmt, int mode, bool partials, const GemvParams& p, size_t smem, cudaStream_t s,
                         bool pdl);
-cudaError_t gemv_max_ctas_per_sm(int fmt, int mode, bool partials, bool merged, size_t smem, int* out);
+cudaError_t gemv_max_ctas_per_sm(int fmt, int mode, bool partials, bool merged, bool fused, size_t smem, int* out);
 cudaError_t launch_gemv_batch(int fmt, const GemvParams& p, size_t smem, cudaStream_t s);
 cudaError_t launch_timeout_probe(unsigned* err, uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_chain(const ChainParams& p, size_t smem, cudaStream_t s);
