@@ -159,8 +159,11 @@ class LlamaDecode:
     unit = "GB/s"
     higher_is_better = True
 
-    def __init__(self, layers: int = synth.LLAMA8B_LAYERS):
+    def __init__(self, layers: int = synth.LLAMA8B_LAYERS, down_layout: str = "soa"):
         self.layers = layers
+        # the Q6_K down projection as stored (GGUF blocks) or repacked at load time
+        # into QX_Q6_K_SOA (the same values and, for 14336 columns, the same bytes per row)
+        self.down_layout = down_layout
         self.shapes = {n: (f, r, c) for n, f, r, c in synth.LLAMA8B_LAYER}
         self.bytes_per_step = layers * sum(r * synth.row_bytes(f, c) for f, r, c in self.shapes.values())
         self.launches_per_step = layers * 4
@@ -181,6 +184,8 @@ class LlamaDecode:
                     self.host_layer0 = self.host_layer0 or {}
                     self.host_layer0[n] = Wh
                 Wl[n] = torch.from_numpy(Wh).cuda()
+                if n == "down" and self.down_layout == "soa":
+                    Wl["down_soa"] = qx.qx_repack(qx.QX_Q6_K, qx.QX_Q6_K_SOA, Wl[n], r, c)
                 yl[n] = torch.empty(r, dtype=torch.float32, device="cuda")
             self.W.append(Wl)
             self.y.append(yl)
@@ -252,7 +257,10 @@ class LlamaDecode:
                              ys=[y["gate"], y["up"]], mode=mode, stream=stream)
             if dom_events is not None:
                 dom_events[L][1].record(stream)
-            qx.qx_gemv(qx.QX_Q6_K, W["down"], 4096, 14336, xv[3], y=y["down"], mode=mode, stream=stream)
+            if self.down_layout == "soa":
+                qx.qx_gemv(qx.QX_Q6_K_SOA, W["down_soa"], 4096, 14336, xv[3], y=y["down"], mode=mode, stream=stream)
+            else:
+                qx.qx_gemv(qx.QX_Q6_K, W["down"], 4096, 14336, xv[3], y=y["down"], mode=mode, stream=stream)
 
     def cpu_sample(self, oracle, budget_s: float = 10.0):
         """Oracle on layer 0 (quantise + 7 W4A8 GEMVs), repeated for ~budget_s."""
@@ -382,8 +390,11 @@ def run_extra(args):
         W = torch.from_numpy(synth.weights(fmt, rows, cols, seed=20)).cuda()
         x = torch.from_numpy(synth.activation(1, cols, seed=21)[0]).cuda()
         y = torch.empty(rows, dtype=torch.float32, device="cuda")
-        for name, mode in (("w4a8", FUSED | PDL), ("f32", F32 | PDL)):
-            ms = graph_time_ms(torch, lambda: qx.qx_gemv(fmt, W, rows, cols, x, y=y, mode=mode, stream=stream),
+        # the GGUF layout, and the same weights repacked at load time into QX_Q6_K_SOA (same bytes per row)
+        Ws = qx.qx_repack(qx.QX_Q6_K, qx.QX_Q6_K_SOA, W, rows, cols)
+        for name, f, Wm, mode in (("w4a8", fmt, W, FUSED | PDL), ("f32", fmt, W, F32 | PDL),
+                                  ("w4a8_soa", qx.QX_Q6_K_SOA, Ws, FUSED | PDL), ("f32_soa", qx.QX_Q6_K_SOA, Ws, F32 | PDL)):
+            ms = graph_time_ms(torch, lambda: qx.qx_gemv(f, Wm, rows, cols, x, y=y, mode=mode, stream=stream),
                                50, stream)
             out[name] = {"GB_per_s": nbytes / (ms * 1e-3) / 1e9, "us": ms * 1e3, "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm}
         out["weight_bytes"] = nbytes
@@ -478,6 +489,8 @@ def main():
                                                                "prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=synth.LLAMA8B_LAYERS)
+    ap.add_argument("--down-layout", default="soa", choices=["soa", "gguf"],
+                    help="Llama step: the Q6_K down projection repacked at load time (QX_Q6_K_SOA) or as stored")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -498,7 +511,7 @@ def main():
     qx.build_library()
     qx.lib()
 
-    wl = LlamaDecode(layers=args.layers)
+    wl = LlamaDecode(layers=args.layers, down_layout=args.down_layout)
     wl.setup(qx, torch, seed_base=0)
     wl.make_chain(qx)
     stream = torch.cuda.Stream()
@@ -628,6 +641,9 @@ def main():
                                   "128 qx_gemv / qx_gemv_multi launches per step with programmatic dependent "
                                   "launch") + ", captured in a CUDA graph",
                        "activation_quantisation": "in-kernel (same codes as qx_quantize_act_q8)",
+                       "down_projection_layout": ("Q6_K repacked at load time into QX_Q6_K_SOA (qx_repack; same "
+                                                  "values, same 11760 bytes per row; the chain form reads the "
+                                                  "GGUF blocks)") if wl.down_layout == "soa" else "GGUF Q6_K blocks",
                        "l2": "inputs larger than L2 (4.41 GB of weights streamed per step)",
                        "parallelism": "replicas" if ws > 1 else "single"},
             "pct_of_hbm_peak": value / ws / hbm,

@@ -15,6 +15,7 @@ from dataclasses import dataclass
 import torch
 
 QX_Q8_0, QX_Q4_K, QX_Q6_K = 8, 12, 14
+QX_Q6_K_SOA = 142  # Q6_K repacked at load time (qx_repack)
 QX_MODE_F32, QX_MODE_W4A8, QX_MODE_W4A8_FUSED = 0, 1, 2
 QX_FLAG_PDL = 0x100
 QX_OK = 0
@@ -28,7 +29,7 @@ QX_CHAIN_MAX_ENTRIES = 4
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libqx.so")
 
 EXPORTS = ["qx_quantize_act_q8", "qx_gemv", "qx_gemv_multi", "qx_gemm_prefill", "qx_gemm_prefill_ex",
-           "qx_gemm_prefill_ws", "qx_gemm_prefill_workspace_bytes", "qx_gemv_partials", "qx_gemv_chain", "qx_gemv_chain_scratch_bytes", "qx_row_bytes",
+           "qx_gemm_prefill_ws", "qx_gemm_prefill_workspace_bytes", "qx_gemv_partials", "qx_gemv_chain", "qx_gemv_chain_scratch_bytes", "qx_row_bytes", "qx_repack",
            "qx_device_check", "qx_debug_timeout_probe",
            "qx_status_string", "qx_last_error", "qx_version"]
 
@@ -78,6 +79,7 @@ def lib() -> ctypes.CDLL:
         L.qx_row_bytes.argtypes = [I, I64]
         L.qx_row_bytes.restype = ctypes.c_size_t
         L.qx_device_check.argtypes = [P]
+        L.qx_repack.argtypes = [I, I, P, I64, I64, P, P]
         L.qx_debug_timeout_probe.argtypes = [ctypes.c_uint64, P]
         L.qx_status_string.argtypes = [I]
         L.qx_status_string.restype = ctypes.c_char_p
@@ -86,7 +88,8 @@ def lib() -> ctypes.CDLL:
         L.qx_version.argtypes = []
         L.qx_version.restype = ctypes.c_char_p
         for n in ("qx_quantize_act_q8", "qx_gemv", "qx_gemv_multi", "qx_gemm_prefill", "qx_gemm_prefill_ex",
-                  "qx_gemm_prefill_ws", "qx_gemv_partials", "qx_gemv_chain", "qx_device_check", "qx_debug_timeout_probe"):
+                  "qx_gemm_prefill_ws", "qx_gemv_partials", "qx_gemv_chain", "qx_device_check", "qx_debug_timeout_probe",
+                  "qx_repack"):
             getattr(L, n).restype = I
         _lib = L
     return _lib
@@ -152,6 +155,16 @@ def qx_row_bytes(fmt: int, cols: int) -> int:
     return int(lib().qx_row_bytes(fmt, cols))
 
 
+def qx_repack(from_fmt: int, to_fmt: int, W: torch.Tensor, rows: int, cols: int, out: torch.Tensor | None = None,
+              stream=None) -> torch.Tensor:
+    """Repack rows x cols weights between QX_Q6_K and QX_Q6_K_SOA (device to device)."""
+    nbytes = rows * qx_row_bytes(to_fmt, cols)
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
+    _check(lib().qx_repack(from_fmt, to_fmt, _ptr(W), rows, cols, _ptr(out), _stream(stream)), "qx_repack")
+    return out
+
+
 def qx_status_string(st: int) -> str:
     return lib().qx_status_string(st).decode()
 
@@ -214,8 +227,8 @@ def qx_gemv_multi(fmts, Ws, rows, cols: int, x, ys=None, mode: int = QX_MODE_W4A
 
 def qx_gemv_partials(fmt: int, W: torch.Tensor, rows: int, cols: int, x: ActQ8, P: torch.Tensor | None = None,
                      stream=None) -> torch.Tensor:
-    """Exact int32 partial sums [rows, cols/32] (Q4_K, Q8_0) or [rows, cols/16] (Q6_K)."""
-    g = 16 if fmt == QX_Q6_K else 32
+    """Exact int32 partial sums [rows, cols/32] (Q4_K, Q8_0) or [rows, cols/16] (Q6_K, QX_Q6_K_SOA)."""
+    g = 16 if fmt in (QX_Q6_K, QX_Q6_K_SOA) else 32
     P = P if P is not None else torch.empty((rows, cols // g), dtype=torch.int32, device=W.device)
     a = x.c_struct()
     _check(lib().qx_gemv_partials(fmt, _ptr(W), rows, cols, ctypes.byref(a), _ptr(P), _stream(stream)),

@@ -121,6 +121,7 @@ int block_weights(int fmt) {
         case QX_Q8_0: return 32;
         case QX_Q4_K: return 256;
         case QX_Q6_K: return 256;
+        case QX_Q6_K_SOA: return 256;
         default: return 0;
     }
 }
@@ -143,10 +144,21 @@ int64_t gcd64(int64_t a, int64_t b) {
     return a;
 }
 
+// Bytes of one row (cols a positive multiple of the block width).  A
+// QX_Q6_K_SOA row: 208 bytes per super-block, then the f16 d values padded to
+// a 16-byte multiple.
+int64_t row_bytes_of(int fmt, int64_t cols) {
+    if (fmt == QX_Q6_K_SOA) {
+        const int64_t nsb = cols / 256;
+        return 208 * nsb + (2 * nsb + 15) / 16 * 16;
+    }
+    return cols / block_weights(fmt) * block_bytes(fmt);
+}
+
 qx_status check_shape(int fmt, int64_t rows, int64_t cols) {
     if (block_weights(fmt) == 0) return QX_ERR_FMT;
     if (rows < 1 || cols < 1 || cols % block_weights(fmt) != 0 || cols > QX_MAX_COLS) return QX_ERR_SHAPE;
-    if (rows > (int64_t(1) << 40) / (cols / block_weights(fmt) * block_bytes(fmt))) return QX_ERR_SHAPE;
+    if (rows > (int64_t(1) << 40) / row_bytes_of(fmt, cols)) return QX_ERR_SHAPE;
     return QX_OK;
 }
 
@@ -190,7 +202,7 @@ qx_status team_geometry(int fmt, int kmode, bool partials, int64_t cols, int con
         g.nteams = consumer_warps * 32 / g.L;
         g.team_lanes = g.L;
     }
-    g.rb = cols / block_weights(fmt) * block_bytes(fmt);
+    g.rb = row_bytes_of(fmt, cols);
     g.quantum = static_cast<int>(16 / gcd64(g.rb, 16));
     // every team gets the same number of whole row groups per stage
     const int64_t team_rows = int64_t(g.nteams) * ((partials || batch) ? 1 : gemv_rows_per_call(fmt, kmode));
@@ -208,7 +220,7 @@ qx_status gemv_geometry(int fmt, int kmode, bool partials, bool fused, bool pdl,
     // class launches: 5.95 TB/s against 5.40) but, packed next to the
     // following launches under PDL, costs the Llama-3.1-8B decode step more
     // than it saves on its 48 MB down projections: long launches only.
-    const int64_t rb = cols / block_weights(fmt) * block_bytes(fmt);
+    const int64_t rb = row_bytes_of(fmt, cols);
     const bool merged = gemv_has_merged(fmt, kmode, partials) && p.total_rows * rb >= kMergedMinBytes;
     p.merged = merged ? 1 : 0;
     TeamGeom g;
@@ -489,6 +501,10 @@ qx_status prefill_dispatch(qx_fmt fmt, const void* W, int64_t rows, int64_t cols
     if (!aligned16(W) || !aligned4(Y)) return QX_ERR_ALIGN;
     if ((st = check_act(X, 0, cols)) != QX_OK) return st;
     if (path < 0 || path > 4) return QX_ERR_ARG;
+    if (fmt == QX_Q6_K_SOA) {
+        if (path != 0 && path != 1) return QX_ERR_FMT;  // the GEMM paths read the GGUF layouts
+        path = 1;
+    }
     if (path == 0) path = X->m == 1 ? 1 : (X->m <= kPrefillBatchMaxRows ? 4 : 3);
     if (path == 4) {
         // eight rows of X per weight stream while more than four remain, then four
@@ -550,7 +566,26 @@ extern "C" {
 size_t qx_row_bytes(qx_fmt fmt, int64_t cols) {
     const int bw = block_weights(fmt);
     if (bw == 0 || cols < 1 || cols % bw) return 0;
-    return size_t(cols / bw) * block_bytes(fmt);
+    return size_t(row_bytes_of(fmt, cols));
+}
+
+qx_status qx_repack(qx_fmt from, qx_fmt to, const void* src, int64_t rows, int64_t cols, void* dst,
+                    qx_stream_t s) {
+    const bool to_soa = from == QX_Q6_K && to == QX_Q6_K_SOA;
+    if (!to_soa && !(from == QX_Q6_K_SOA && to == QX_Q6_K)) return QX_ERR_FMT;
+    qx_status st = check_shape(from, rows, cols);
+    if (st != QX_OK) return st;
+    if ((st = check_shape(to, rows, cols)) != QX_OK) return st;
+    if (!src || !dst) return QX_ERR_ARG;
+    if (!aligned16(src) || !aligned16(dst)) return QX_ERR_ALIGN;
+    const int64_t sb = row_bytes_of(from, cols), db = row_bytes_of(to, cols);
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
+    if (s0 < d0 + uintptr_t(rows * db) && d0 < s0 + uintptr_t(rows * sb)) return QX_ERR_ARG;  // overlap
+    DeviceInfo* dev = nullptr;
+    if ((st = device_info(&dev)) != QX_OK) return st;
+    const cudaError_t e = launch_repack_q6k(to_soa, static_cast<const uint8_t*>(src), rows, cols / 256, sb,
+                                            static_cast<uint8_t*>(dst), db, reinterpret_cast<cudaStream_t>(s));
+    return e == cudaSuccess ? QX_OK : cuda_fail(e, "repack launch");
 }
 
 qx_status qx_quantize_act_q8(const float* x, int64_t m, int64_t cols, qx_act_q8* out, qx_stream_t s) {
@@ -595,9 +630,17 @@ qx_status qx_gemv_multi(int n, const qx_fmt* fmt, const void* const* W, const in
         if (!aligned16(W[k]) || !aligned4(y[k])) return QX_ERR_ALIGN;
     }
     if ((st = check_x(mode, x, cols)) != QX_OK) return st;
-    // One launch per distinct format, entries kept in call order.
-    const int fmts[3] = {QX_Q4_K, QX_Q6_K, QX_Q8_0};
-    for (int f : fmts) {
+    // One launch per distinct format (in order of first appearance), entries
+    // kept in call order; every entry's format passed check_shape above.
+    int fmts[QX_MAX_MULTI];
+    int nfmt = 0;
+    for (int k = 0; k < n; ++k) {
+        bool seen = false;
+        for (int i = 0; i < nfmt; ++i) seen |= fmts[i] == fmt[k];
+        if (!seen) fmts[nfmt++] = fmt[k];
+    }
+    for (int i = 0; i < nfmt; ++i) {
+        const int f = fmts[i];
         const void* Wf[QX_MAX_MULTI];
         int64_t rf[QX_MAX_MULTI];
         float* yf[QX_MAX_MULTI];
@@ -664,6 +707,7 @@ qx_status qx_gemv_chain(int n_jobs, const qx_gemv_job* jobs, void* scratch, qx_s
         if (in.n < 1 || in.n > QX_CHAIN_MAX_ENTRIES) return QX_ERR_ARG;
         if (!in.x) return QX_ERR_ARG;
         if (!aligned16(in.x)) return QX_ERR_ALIGN;
+        if (in.fmt == QX_Q6_K_SOA) return QX_ERR_FMT;  // the chain kernel reads the GGUF layouts
         ChainJob& jb = p.job[j];
         jb.fmt = in.fmt;
         jb.n_entries = in.n;
@@ -791,6 +835,7 @@ qx_status qx_gemv_chain_noalloc(int n_jobs, const qx_gemv_job* jobs, qx_stream_t
         if (in.n < 1 || in.n > QX_CHAIN_MAX_ENTRIES) return QX_ERR_ARG;
         if (!in.x) return QX_ERR_ARG;
         if (!aligned16(in.x)) return QX_ERR_ALIGN;
+        if (in.fmt == QX_Q6_K_SOA) return QX_ERR_FMT;  // the chain kernel reads the GGUF layouts
         ChainJob& jb = p.job[j];
         jb.fmt = in.fmt;
         jb.n_entries = in.n;

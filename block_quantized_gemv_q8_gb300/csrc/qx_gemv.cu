@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
     // built without helpers: the extra code slowed their one-round launches
     // measurably (GB300, Llama-3.1-8B q/k/v launch 5.24 -> 5.30 us).
     constexpr int QW = NW + 1 + ((!PART && !kMerged) ? 1 : 0);
-    constexpr bool kMayHelp = kMerged || FMT == QX_Q6_K;
+    constexpr bool kMayHelp = kMerged || FMT == QX_Q6_K || FMT == QX_Q6_K_SOA;
     const int ntask = static_cast<int>(2 * (p.cols / 32));
     const bool helpers =
         kMerged || (kMayHelp && (ntask + NW * 32 - 1) / (NW * 32) > (ntask + QW * 32 - 1) / (QW * 32));
@@ -336,13 +336,14 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
     }
     // the quantised activation in shared memory has its 128-byte slices permuted
     if (tm.active) load_slice<MODE>(X, q, d, s, p.x, tm.slice, FMT != QX_Q8_0 && FUSED);
+    if constexpr (FMT == QX_Q6_K_SOA) X.geometry(p.cols);
     if constexpr (MODE == QX_MODE_W4A8) {
         // the quantised activation shares its area with the partial sums
         if constexpr (FUSED) quantiser_barrier(qthreads);
     }
 
     const uint32_t rb = static_cast<uint32_t>(p.row_bytes);
-    const int64_t ng = p.cols / (FMT == QX_Q6_K ? 16 : 32);
+    const int64_t ng = p.cols / ((FMT == QX_Q6_K || FMT == QX_Q6_K_SOA) ? 16 : 32);
     StageWalker wk{r0, r1, 0};
     int e, nrows;
     int64_t lrow;
@@ -554,6 +555,9 @@ cudaError_t launch_gemv(int fmt, int mode, bool partials, const GemvParams& p, s
         if (fmt == QX_Q6_K && mode == QX_MODE_W4A8 && !partials)
             return fused ? launch_one<QX_Q6_K, QX_MODE_W4A8, false, true, true>(p, smem, s, pdl)
                          : launch_one<QX_Q6_K, QX_MODE_W4A8, false, true, false>(p, smem, s, pdl);
+        if (fmt == QX_Q6_K_SOA && mode == QX_MODE_W4A8 && !partials)
+            return fused ? launch_one<QX_Q6_K_SOA, QX_MODE_W4A8, false, true, true>(p, smem, s, pdl)
+                         : launch_one<QX_Q6_K_SOA, QX_MODE_W4A8, false, true, false>(p, smem, s, pdl);
         return cudaErrorInvalidValue;
     }
     switch (fmt * 8 + mode * 4 + (partials ? 2 : 0) + (fused ? 1 : 0)) {
@@ -569,6 +573,10 @@ cudaError_t launch_gemv(int fmt, int mode, bool partials, const GemvParams& p, s
         case QX_Q8_0 * 8 + 4: return launch_one<QX_Q8_0, QX_MODE_W4A8, false, false, false>(p, smem, s, pdl);
         case QX_Q8_0 * 8 + 5: return launch_one<QX_Q8_0, QX_MODE_W4A8, false, false, true>(p, smem, s, pdl);
         case QX_Q8_0 * 8 + 6: return launch_one<QX_Q8_0, QX_MODE_W4A8, true, false, false>(p, smem, s, pdl);
+        case QX_Q6_K_SOA * 8 + 0: return launch_one<QX_Q6_K_SOA, QX_MODE_F32, false, false, false>(p, smem, s, pdl);
+        case QX_Q6_K_SOA * 8 + 4: return launch_one<QX_Q6_K_SOA, QX_MODE_W4A8, false, false, false>(p, smem, s, pdl);
+        case QX_Q6_K_SOA * 8 + 5: return launch_one<QX_Q6_K_SOA, QX_MODE_W4A8, false, false, true>(p, smem, s, pdl);
+        case QX_Q6_K_SOA * 8 + 6: return launch_one<QX_Q6_K_SOA, QX_MODE_W4A8, true, false, false>(p, smem, s, pdl);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -579,6 +587,9 @@ cudaError_t gemv_max_ctas_per_sm(int fmt, int mode, bool partials, bool merged, 
         if (fmt == QX_Q6_K && mode == QX_MODE_W4A8 && !partials)
             return fused ? occupancy_one<QX_Q6_K, QX_MODE_W4A8, false, true, true>(smem, out)
                          : occupancy_one<QX_Q6_K, QX_MODE_W4A8, false, true, false>(smem, out);
+        if (fmt == QX_Q6_K_SOA && mode == QX_MODE_W4A8 && !partials)
+            return fused ? occupancy_one<QX_Q6_K_SOA, QX_MODE_W4A8, false, true, true>(smem, out)
+                         : occupancy_one<QX_Q6_K_SOA, QX_MODE_W4A8, false, true, false>(smem, out);
         return cudaErrorInvalidValue;
     }
     switch (fmt * 8 + mode * 4 + (partials ? 2 : 0) + (fused ? 1 : 0)) {
@@ -594,6 +605,10 @@ cudaError_t gemv_max_ctas_per_sm(int fmt, int mode, bool partials, bool merged, 
         case QX_Q8_0 * 8 + 4: return occupancy_one<QX_Q8_0, QX_MODE_W4A8, false, false, false>(smem, out);
         case QX_Q8_0 * 8 + 5: return occupancy_one<QX_Q8_0, QX_MODE_W4A8, false, false, true>(smem, out);
         case QX_Q8_0 * 8 + 6: return occupancy_one<QX_Q8_0, QX_MODE_W4A8, true, false, false>(smem, out);
+        case QX_Q6_K_SOA * 8 + 0: return occupancy_one<QX_Q6_K_SOA, QX_MODE_F32, false, false, false>(smem, out);
+        case QX_Q6_K_SOA * 8 + 4: return occupancy_one<QX_Q6_K_SOA, QX_MODE_W4A8, false, false, false>(smem, out);
+        case QX_Q6_K_SOA * 8 + 5: return occupancy_one<QX_Q6_K_SOA, QX_MODE_W4A8, false, false, true>(smem, out);
+        case QX_Q6_K_SOA * 8 + 6: return occupancy_one<QX_Q6_K_SOA, QX_MODE_W4A8, true, false, false>(smem, out);
         default: return cudaErrorInvalidValue;
     }
 }

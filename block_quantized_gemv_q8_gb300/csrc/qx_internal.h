@@ -24,7 +24,7 @@ namespace qx {
 // kernel is held to 96 and spills); rows of 14336 columns are then exactly
 // two teams of 112 lanes.
 __host__ __device__ constexpr bool gemv_has_merged(int fmt, int mode, bool partials) {
-    return !partials && mode == QX_MODE_W4A8 && fmt == QX_Q6_K;
+    return !partials && mode == QX_MODE_W4A8 && (fmt == QX_Q6_K || fmt == QX_Q6_K_SOA);
 }
 __host__ __device__ constexpr int gemv_consumer_warps(int fmt, int mode, bool merged) {
     return (mode == QX_MODE_F32 && fmt != QX_Q8_0) ? 12 : (merged ? 7 : 8);
@@ -145,6 +145,9 @@ cudaError_t launch_gemv(int fmt, int mode, bool partials, const GemvParams& p, s
                         bool pdl);
 cudaError_t gemv_max_ctas_per_sm(int fmt, int mode, bool partials, bool merged, bool fused, size_t smem, int* out);
 cudaError_t launch_gemv_batch(int fmt, const GemvParams& p, size_t smem, cudaStream_t s);
+// Q6_K <-> QX_Q6_K_SOA (qx_repack.cu); row bytes of each side.
+cudaError_t launch_repack_q6k(bool to_soa, const uint8_t* src, int64_t rows, int64_t nsb, int64_t src_row_bytes,
+                              uint8_t* dst, int64_t dst_row_bytes, cudaStream_t s);
 cudaError_t launch_timeout_probe(unsigned* err, uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_chain(const ChainParams& p, size_t smem, cudaStream_t s);
 cudaError_t launch_prefill_q4k(const uint8_t* W, int64_t N, int64_t K, const int8_t* xq, const float* xd,

@@ -383,6 +383,174 @@ struct Lane<QX_Q6_K, QX_MODE_F32> {
     }
 };
 
+// Q6_K repacked at load time (QX_Q6_K_SOA, qx_repack): per super-block 208
+// bytes -- ql[128], qh[64], scales[16], every field 16-byte aligned -- and
+// the row's d values gathered after its super-blocks, at byte d_off =
+// 208 * (super-blocks per row).  The same arithmetic as the Q6_K lanes above;
+// the fields are read with aligned vector loads instead of funnel-shifted
+// words.
+__device__ __forceinline__ void load8_al(const uint8_t* p, uint32_t (&w)[8]) {
+    const uint4* p4 = reinterpret_cast<const uint4*>(p);
+    const uint4 a = p4[0], b = p4[1];
+    w[0] = a.x;
+    w[1] = a.y;
+    w[2] = a.z;
+    w[3] = a.w;
+    w[4] = b.x;
+    w[5] = b.y;
+    w[6] = b.z;
+    w[7] = b.w;
+}
+
+__device__ __forceinline__ void q6k_half_dots_al(const uint8_t* bp, int h, const uint32_t (&xq)[32],
+                                                 const int (&s16)[8], int (&P)[8]) {
+    uint32_t qh[8];
+    load8_al(bp + 128 + 32 * h, qh);
+#pragma unroll
+    for (int tl = 0; tl < 2; ++tl) {
+        uint32_t ql[8];
+        load8_al(bp + 64 * h + 32 * tl, ql);
+#pragma unroll
+        for (int th = 0; th < 2; ++th) {
+            const int t = tl + 2 * th;
+            int pu[2] = {0, 0};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t lo4 = (th ? (ql[i] >> 4) : ql[i]) & 0x0F0F0F0Fu;
+                const uint32_t hsh = t < 2 ? (qh[i] << (4 - 2 * t)) : (qh[i] >> (2 * t - 4));
+                pu[i >> 2] = dp4a_us(lo4 | (hsh & 0x30303030u), xq[8 * t + i], pu[i >> 2]);
+            }
+            P[2 * t] = pu[0] - 32 * s16[2 * t];
+            P[2 * t + 1] = pu[1] - 32 * s16[2 * t + 1];
+        }
+    }
+}
+
+template <>
+struct Lane<QX_Q6_K_SOA, QX_MODE_W4A8> {
+    static constexpr int C = 128;
+    static constexpr int kGroups = 8;
+    static constexpr int kRows = 1;
+    uint32_t xq[32];
+    float dx[4];
+    int s16[8];
+    int d_off;
+    __device__ __forceinline__ void geometry(int64_t cols) { d_off = static_cast<int>(cols / 256) * 208; }
+    __device__ __forceinline__ void load(const int8_t* q, const float* d, const int32_t*, int l, bool swz) {
+        const uint4* src = reinterpret_cast<const uint4*>(q + int64_t(l) * C);
+        const int sw = swz ? (l & 7) : 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint4 v = src[k ^ sw];
+            xq[4 * k + 0] = v.x;
+            xq[4 * k + 1] = v.y;
+            xq[4 * k + 2] = v.z;
+            xq[4 * k + 3] = v.w;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dx[u] = d[l * 4 + u];
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+            int s = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) s = dp4a(xq[4 * g + i], 0x01010101u, s);
+            s16[g] = s;
+        }
+    }
+    template <int R>
+    __device__ __forceinline__ void rows(const uint8_t* const (&rp)[R], int l, float (&out)[R]) const {
+        const int sb = l >> 1, h = l & 1;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint8_t* bp = rp[r] + sb * 208;
+            int P[8];
+            q6k_half_dots_al(bp, h, xq, s16, P);
+            const uint2 sc2 = *reinterpret_cast<const uint2*>(bp + 192 + 8 * h);
+            const uint32_t scw[2] = {sc2.x, sc2.y};
+            float acc = 0.0f;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int sc0 = int(int8_t(byte_of(scw[t >> 1], 2 * (t & 1))));
+                const int sc1 = int(int8_t(byte_of(scw[t >> 1], 2 * (t & 1) + 1)));
+                acc = fmaf(dx[t], float(sc0 * P[2 * t] + sc1 * P[2 * t + 1]), acc);
+            }
+            out[r] = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(rp[r] + d_off + 2 * sb)) * acc;
+        }
+    }
+    __device__ __forceinline__ void partials(const uint8_t* rowp, int l, int (&P)[kGroups]) const {
+        const int sb = l >> 1, h = l & 1;
+        q6k_half_dots_al(rowp + sb * 208, h, xq, s16, P);
+    }
+    __device__ __forceinline__ static int64_t part_index(int l, int g) { return int64_t(l) * 8 + g; }
+};
+
+template <>
+struct Lane<QX_Q6_K_SOA, QX_MODE_F32> {
+    static constexpr int C = 64;
+    static constexpr int kGroups = 1;
+    static constexpr int kRows = 1;
+    uint64_t x2[32];  // the 64 activation values as 32 packed pairs (x[2j], x[2j + 1])
+    int d_off;
+    __device__ __forceinline__ void geometry(int64_t cols) { d_off = static_cast<int>(cols / 256) * 208; }
+    __device__ __forceinline__ void load(const float* xp, int l) {
+        const int sb = l >> 2, h = (l >> 1) & 1, tp = l & 1;
+        const int64_t c0 = int64_t(sb) * 256 + 128 * h + 32 * tp;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const float4* src = reinterpret_cast<const float4*>(xp + c0 + 64 * half);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float4 v = src[k];
+                x2[16 * half + 2 * k + 0] = f32x2_pack(v.x, v.y);
+                x2[16 * half + 2 * k + 1] = f32x2_pack(v.z, v.w);
+            }
+        }
+    }
+    template <int R>
+    __device__ __forceinline__ void rows(const uint8_t* const (&rp)[R], int l, float (&out)[R]) const {
+        const int sb = l >> 2, h = (l >> 1) & 1, tp = l & 1;
+        // 2^23 + q minus (2^23 + 32) = q - 32, exactly, two at a time
+        const uint64_t bias = f32x2_pack(-8388640.0f, -8388640.0f);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint8_t* bp = rp[r] + sb * 208;
+            uint32_t ql[8], qh[8];
+            load8_al(bp + 64 * h + 32 * tp, ql);
+            load8_al(bp + 128 + 32 * h, qh);
+            const uint2 sc2 = *reinterpret_cast<const uint2*>(bp + 192 + 8 * h);
+            const uint32_t scw[2] = {sc2.x, sc2.y};
+            uint64_t sg2[4] = {0, 0, 0, 0};  // lo g0, lo g1, hi g0, hi g1; two running sums each
+            const uint32_t sh_lo = 4u - 2u * uint32_t(tp), sh_hi = 2u * uint32_t(tp);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t wlo = (ql[i] & 0x0F0F0F0Fu) | ((qh[i] << sh_lo) & 0x30303030u);
+                const uint32_t whi = ((ql[i] >> 4) & 0x0F0F0F0Fu) | ((qh[i] >> sh_hi) & 0x30303030u);
+#pragma unroll
+                for (int kp = 0; kp < 2; ++kp) {
+                    const uint64_t flo =
+                        f32x2_add(f32x2_pack(byte_biased_f32(wlo, 2 * kp), byte_biased_f32(wlo, 2 * kp + 1)), bias);
+                    const uint64_t fhi =
+                        f32x2_add(f32x2_pack(byte_biased_f32(whi, 2 * kp), byte_biased_f32(whi, 2 * kp + 1)), bias);
+                    sg2[i >> 2] = f32x2_fma(flo, x2[2 * i + kp], sg2[i >> 2]);
+                    sg2[2 + (i >> 2)] = f32x2_fma(fhi, x2[16 + 2 * i + kp], sg2[2 + (i >> 2)]);
+                }
+            }
+            float sg[4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const float2 v = f32x2_unpack(sg2[g]);
+                sg[g] = v.x + v.y;
+            }
+            const int lo0 = 2 * tp, hi0 = 2 * tp + 4;
+            float acc = float(int(int8_t(byte_of(scw[lo0 >> 2], lo0 & 3)))) * sg[0];
+            acc = fmaf(float(int(int8_t(byte_of(scw[(lo0 + 1) >> 2], (lo0 + 1) & 3)))), sg[1], acc);
+            acc = fmaf(float(int(int8_t(byte_of(scw[hi0 >> 2], hi0 & 3)))), sg[2], acc);
+            acc = fmaf(float(int(int8_t(byte_of(scw[(hi0 + 1) >> 2], (hi0 + 1) & 3)))), sg[3], acc);
+            out[r] = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(rp[r] + d_off + 2 * sb)) * acc;
+        }
+    }
+};
+
 // Q8_0, W4A8: 32 columns = one block.
 template <>
 struct Lane<QX_Q8_0, QX_MODE_W4A8> {

@@ -58,8 +58,9 @@ extern "C" {
 /* Same type as cudaStream_t. */
 typedef struct CUstream_st* qx_stream_t;
 
-/* Format tags (the GGML type ids, a naming convention only). */
-typedef enum { QX_Q8_0 = 8, QX_Q4_K = 12, QX_Q6_K = 14 } qx_fmt;
+/* Format tags (the GGML type ids, a naming convention only), and
+ * QX_Q6_K_SOA: Q6_K repacked at load time by qx_repack (see there). */
+typedef enum { QX_Q8_0 = 8, QX_Q4_K = 12, QX_Q6_K = 14, QX_Q6_K_SOA = 142 } qx_fmt;
 
 typedef enum { QX_MODE_F32 = 0, QX_MODE_W4A8 = 1, QX_MODE_W4A8_FUSED = 2 } qx_mode;
 
@@ -210,8 +211,8 @@ qx_status qx_gemm_prefill_ws(qx_fmt fmt, const void* W, int64_t rows, int64_t co
  * The exact integer partial sums of the W4A8 product, written instead of y:
  * P[r, g] = sum over group g of q_w * q_x, with groups of 32 weights for Q4_K
  * (q_w the unsigned 4-bit quant) and Q8_0 (q_w the int8 quant), and groups of
- * 16 for Q6_K (q_w = q - 32).  P is device int32 [rows, cols/32] or
- * [rows, cols/16].  Computed by the same kernel code as qx_gemv's W4A8 path
+ * 16 for Q6_K and QX_Q6_K_SOA (q_w = q - 32).  P is device int32
+ * [rows, cols/32] or [rows, cols/16].  Computed by the same kernel code as qx_gemv's W4A8 path
  * (colibri GPU_BACKENDS.md: a numerics-matched integer GPU kernel).
  */
 qx_status qx_gemv_partials(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* x,
@@ -281,6 +282,30 @@ qx_status qx_gemv_chain_noalloc(int n_jobs, const qx_gemv_job* jobs, qx_stream_t
 /* Bytes of one row of `cols` weights, or 0 if fmt is unknown or cols is not
  * a positive multiple of the block width. */
 size_t qx_row_bytes(qx_fmt fmt, int64_t cols);
+
+/*
+ * Load-time repack between the GGUF Q6_K layout and QX_Q6_K_SOA (llamay
+ * docs, "Backends and hardware", section "Repacking is a per-device decision
+ * now": block layouts are rewritten once, at load, for the device that runs
+ * them).  A QX_Q6_K_SOA row of cols weights (nsb = cols / 256 super-blocks)
+ * holds, for each super-block j, the 208 bytes ql[128], qh[64], scales[16]
+ * of the GGUF block at bytes [208 j, 208 j + 208), then the nsb f16 d values
+ * at byte 208 nsb, padded with zero bytes to a 16-byte multiple:
+ * qx_row_bytes(QX_Q6_K_SOA, cols) = 208 nsb + 16 * ceil(2 nsb / 16) (the
+ * GGUF row size when nsb is a multiple of 8).  Every field of every
+ * super-block is then 16-byte aligned, which the GEMV lanes read with
+ * vector loads; the values and the arithmetic are those of Q6_K, so
+ * qx_gemv and qx_gemv_partials give the same bits on either layout.
+ *   from, to: QX_Q6_K -> QX_Q6_K_SOA, or QX_Q6_K_SOA -> QX_Q6_K (the exact
+ *             inverse: a round trip restores every byte).
+ *   src, dst: device, rows * qx_row_bytes(from / to, cols) bytes, 16-byte
+ *             aligned, not overlapping.
+ * QX_Q6_K_SOA is served by qx_gemv, qx_gemv_multi, qx_gemv_partials and
+ * prefill path 1 (and path 0, which then takes path 1); the other prefill
+ * paths and qx_gemv_chain return QX_ERR_FMT for it.
+ */
+qx_status qx_repack(qx_fmt from, qx_fmt to, const void* src, int64_t rows, int64_t cols, void* dst,
+                    qx_stream_t s);
 
 /* Synchronise stream s, then read and clear the device error word of the
  * current device: QX_OK, QX_ERR_DEVICE_TIMEOUT if a kernel's bounded wait ran

@@ -43,6 +43,12 @@ def test_row_bytes(lib):
     assert qx.qx_row_bytes(qx.QX_Q4_K, 896) == 0
     assert qx.qx_row_bytes(qx.QX_Q8_0, 0) == 0
     assert qx.qx_row_bytes(7, 256) == 0
+    # the repacked Q6_K layout: 208 bytes per super-block, then the f16 d values padded to 16 bytes
+    assert qx.qx_row_bytes(qx.QX_Q6_K_SOA, 4096) == 16 * 208 + 32 == qx.qx_row_bytes(qx.QX_Q6_K, 4096)
+    assert qx.qx_row_bytes(qx.QX_Q6_K_SOA, 14336) == 56 * 208 + 112
+    assert qx.qx_row_bytes(qx.QX_Q6_K_SOA, 2304) == 9 * 208 + 32
+    assert qx.qx_row_bytes(qx.QX_Q6_K_SOA, 256) == 208 + 16
+    assert qx.qx_row_bytes(qx.QX_Q6_K_SOA, 128) == 0
 
 
 def test_status_strings_and_version(lib):
@@ -95,6 +101,20 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.qx_gemm_prefill_ex(qx.QX_Q4_K, P(A16), 4, 256, ctypes.byref(act), P(A16), 5, s) == qx.QX_ERR_ARG
     # timeout probe limits
     assert lib.qx_debug_timeout_probe(10, s) == qx.QX_ERR_ARG
+    # repack: only Q6_K <-> QX_Q6_K_SOA, aligned, not overlapping
+    SOA, Q6 = qx.QX_Q6_K_SOA, qx.QX_Q6_K
+    assert lib.qx_repack(qx.QX_Q4_K, SOA, P(A16), 4, 256, P(2 * A16), s) == qx.QX_ERR_FMT
+    assert lib.qx_repack(Q6, Q6, P(A16), 4, 256, P(2 * A16), s) == qx.QX_ERR_FMT
+    assert lib.qx_repack(Q6, SOA, P(A16), 4, 384, P(2 * A16), s) == qx.QX_ERR_SHAPE
+    assert lib.qx_repack(Q6, SOA, P(A16 + 2), 4, 256, P(2 * A16), s) == qx.QX_ERR_ALIGN
+    assert lib.qx_repack(SOA, Q6, P(A16), 4, 256, None, s) == qx.QX_ERR_ARG
+    assert lib.qx_repack(Q6, SOA, P(A16), 4, 256, P(A16 + 256), s) == qx.QX_ERR_ARG  # overlap
+    # the repacked layout is read by the GEMV only: the chain and the GEMM prefill paths refuse it
+    act = qx._Act(A16, A16, A16, 4, 256)
+    for path in (2, 3, 4):
+        assert lib.qx_gemm_prefill_ex(SOA, P(A16), 4, 256, ctypes.byref(act), P(A16), path, s) == qx.QX_ERR_FMT
+    job = qx._Job(SOA, 1, (ctypes.c_void_p * 4)(A16), (ctypes.c_int64 * 4)(4), (ctypes.c_void_p * 4)(A16), 256, A16)
+    assert lib.qx_gemv_chain(1, ctypes.byref(job), P(A16), s) == qx.QX_ERR_FMT
 
 
 def test_python_binding_rejects_cpu_tensors(lib):
