@@ -298,6 +298,25 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(torch, value: float) -> float:
+    """The largest `value` over all ranks of the initialised process group (the
+    job's time is its slowest rank's); the value itself without one.  The
+    tensor lives where the backend needs it: CUDA for NCCL, host for gloo."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    device = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world_size: int, bytes_per_step: int, steps: int, max_ms: float) -> float:
+    """Whole-job weight GB/s: every rank streams bytes_per_step per step (weak
+    scaling), over the slowest rank's time."""
+    return world_size * bytes_per_step * steps / (max_ms * 1e-3) / 1e9
+
+
 def run_reference(args):
     """Time the CPU oracle itself on bounded samples of the workload (rank 0 only)."""
     ws, rank, _ = dist_env()
@@ -563,12 +582,7 @@ def main():
             graph.replay()
         e1.record(stream)
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1)
-        if ws > 1:
-            t = torch.tensor([ms], device="cuda")
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(torch, e0.elapsed_time(e1))
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -603,7 +617,7 @@ def main():
     assert int(wl.scratch.sum()) == 0
 
     hbm, _, peak_kind = measured_peaks()
-    per_s = lambda m: ws * wl.bytes_per_step * args.steps / (m * 1e-3) / 1e9  # noqa: E731
+    per_s = lambda m: job_throughput(ws, wl.bytes_per_step, args.steps, m)  # noqa: E731
     value_chain, value_pdl = per_s(ms), per_s(ms_pdl)
     chain_is_faster = ms <= ms_pdl
     ms_e2e = ms_e2e_chain if chain_is_faster else ms_e2e_pdl
