@@ -86,9 +86,15 @@ def test_llama8b_layer_full_size_sampled():
     qx.qx_gemv(F, Wd["o"], 4096, 4096, xd[1], y=y["o"], mode=FUSED_PDL, stream=stream)
     qx.qx_gemv_multi([F, F], [Wd["gate"], Wd["up"]], [14336, 14336], 4096, xd[2],
                      ys=[y["gate"], y["up"]], mode=FUSED_PDL, stream=stream)
-    qx.qx_gemv(synth.Q6_K, Wd["down"], 4096, 14336, xd[3], y=y["down"], mode=FUSED_PDL, stream=stream)
+    # the benchmark's down projection: repacked at load into QX_Q6_K_SOA; the
+    # GGUF-layout launch must give the same bits
+    down_soa = qx.qx_repack(synth.Q6_K, qx.QX_Q6_K_SOA, Wd["down"], 4096, 14336)
+    qx.qx_gemv(qx.QX_Q6_K_SOA, down_soa, 4096, 14336, xd[3], y=y["down"], mode=FUSED_PDL, stream=stream)
+    y_down_gguf = torch.empty(4096, dtype=torch.float32, device="cuda")
+    qx.qx_gemv(synth.Q6_K, Wd["down"], 4096, 14336, xd[3], y=y_down_gguf, mode=FUSED_PDL, stream=stream)
     stream.synchronize()
     assert qx.qx_device_check() == qx.QX_OK
+    assert np.array_equal(host(y["down"]).view(np.uint32), host(y_down_gguf).view(np.uint32))
     xin = {"q": 0, "k": 0, "v": 0, "o": 1, "gate": 2, "up": 2, "down": 3}
     for k in range(4):
         assert_codes_match(xs[k])
@@ -97,14 +103,24 @@ def test_llama8b_layer_full_size_sampled():
         check_w4a8_rows(f, Wh[n], c, xs[xin[n]], host(y[n]), sel, f"llama8b {n}")
 
 
+@pytest.mark.parametrize("layout", ["gguf", "soa"])
 @pytest.mark.parametrize("mode", ["w4a8", "f32"])
-def test_lm_head_q6k_full_size_sampled(mode):
-    """The Q6_K lm_head, 128256 x 4096 (431 MB): the launch the benchmark times."""
+def test_lm_head_q6k_full_size_sampled(mode, layout):
+    """The Q6_K lm_head, 128256 x 4096 (431 MB): the launches the benchmark
+    times, on the GGUF blocks and repacked at load (W4A8: the merged
+    producer/reducer variant, taken from 128 MB)."""
     _, fmt, rows, cols = synth.LLAMA8B_LM_HEAD_Q6K
     W = synth.weights(fmt, rows, cols, seed=20)
     x = synth.activation(1, cols, seed=21)[0]
     flag = FUSED_PDL if mode == "w4a8" else qx.QX_MODE_F32 | qx.QX_FLAG_PDL
-    y = host(qx.qx_gemv(fmt, dev(W), rows, cols, dev(x), mode=flag))
+    Wd = dev(W)
+    if layout == "soa":
+        y = host(qx.qx_gemv(qx.QX_Q6_K_SOA, qx.qx_repack(fmt, qx.QX_Q6_K_SOA, Wd, rows, cols), rows, cols, dev(x),
+                            mode=flag))
+        y_gguf = host(qx.qx_gemv(fmt, Wd, rows, cols, dev(x), mode=flag))
+        assert np.array_equal(y.view(np.uint32), y_gguf.view(np.uint32))
+    else:
+        y = host(qx.qx_gemv(fmt, Wd, rows, cols, dev(x), mode=flag))
     assert qx.qx_device_check() == qx.QX_OK
     sel = sample_rows(rows, 256, seed=22)
     if mode == "w4a8":
