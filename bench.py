@@ -636,7 +636,7 @@ def main():
     t_gu = gateup_traffic()
     roof_pdl = roofline(wl.dominant_pdl, wl.dominant_pdl_bytes, statistics.mean(dom_pdl_ms), t_gu,
                         GATEUP_PROFILE_NAME,
-                        "the largest launch of the Q4_K kernel, which takes 64% of the per-launch form's "
+                        "the largest launch of the Q4_K kernel, which takes 66% of the per-launch form's "
                         "device time (ncu launch list; gate/up is 48% of the step's weight bytes); timed with "
                         "CUDA events around each of its 32 launches in an instrumented copy of the step graph; "
                         "algorithmic bytes = the two Q4_K matrices (scales included)")
