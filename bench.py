@@ -484,6 +484,10 @@ def run_extra(args):
                     rec["path3_bf16_tflops"] = 3 * 2.0 * m * rows * cols / (ms * 1e-3) / 1e12
                     rec["path3_frac_of_bf16_peak"] = rec["path3_bf16_tflops"] / bf16
             sweep.append(rec)
+        # measured on this device, for context: the int8 tensor rate a prefill can use on sm_103a
+        # (legacy mma.sync; no int8 tcgen05) and the f16 mma.sync rate path 2 runs on
+        out["mma_sync_int8_tops_measured"] = qx.qx_debug_mma_rate(0, stream=stream) / 1e12
+        out["mma_sync_f16_tflops_measured"] = qx.qx_debug_mma_rate(1, stream=stream) / 1e12
         out.update({"sweep": sweep, "flops_per_row": 2 * rows * cols, "bf16_dense_peak_tflops": bf16,
                     "note": "path 1 = one W4A8 GEMV launch per row; path 2 = tensor cores (mma.sync f16 with "
                             "integer-valued operands); path 3 = tcgen05 bf16 GEMM over the split dequantised "

@@ -30,7 +30,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libqx.so")
 
 EXPORTS = ["qx_quantize_act_q8", "qx_gemv", "qx_gemv_multi", "qx_gemm_prefill", "qx_gemm_prefill_ex",
            "qx_gemm_prefill_ws", "qx_gemm_prefill_workspace_bytes", "qx_gemv_partials", "qx_gemv_chain", "qx_gemv_chain_scratch_bytes", "qx_row_bytes", "qx_repack",
-           "qx_device_check", "qx_debug_timeout_probe",
+           "qx_device_check", "qx_debug_timeout_probe", "qx_debug_mma_rate",
            "qx_status_string", "qx_last_error", "qx_version"]
 
 
@@ -80,6 +80,7 @@ def lib() -> ctypes.CDLL:
         L.qx_row_bytes.restype = ctypes.c_size_t
         L.qx_device_check.argtypes = [P]
         L.qx_repack.argtypes = [I, I, P, I64, I64, P, P]
+        L.qx_debug_mma_rate.argtypes = [I, ctypes.POINTER(ctypes.c_double), P]
         L.qx_debug_timeout_probe.argtypes = [ctypes.c_uint64, P]
         L.qx_status_string.argtypes = [I]
         L.qx_status_string.restype = ctypes.c_char_p
@@ -89,7 +90,7 @@ def lib() -> ctypes.CDLL:
         L.qx_version.restype = ctypes.c_char_p
         for n in ("qx_quantize_act_q8", "qx_gemv", "qx_gemv_multi", "qx_gemm_prefill", "qx_gemm_prefill_ex",
                   "qx_gemm_prefill_ws", "qx_gemv_partials", "qx_gemv_chain", "qx_device_check", "qx_debug_timeout_probe",
-                  "qx_repack"):
+                  "qx_repack", "qx_debug_mma_rate"):
             getattr(L, n).restype = I
         _lib = L
     return _lib
@@ -311,6 +312,13 @@ def qx_gemv_chain(jobs, scratch: torch.Tensor, stream=None, marshalled=None):
     arr = marshalled if marshalled is not None else make_chain(jobs)
     _check(lib().qx_gemv_chain(len(arr), arr, _ptr(scratch), _stream(stream)), "qx_gemv_chain")
     return jobs
+
+
+def qx_debug_mma_rate(kind: int, stream=None) -> float:
+    """Measured mma.sync rate (multiply-adds x 2 per second): kind 0 int8 m16n8k32, 1 f16 m16n8k16."""
+    v = ctypes.c_double(0.0)
+    _check(lib().qx_debug_mma_rate(kind, ctypes.byref(v), _stream(stream)), "qx_debug_mma_rate")
+    return v.value
 
 
 def qx_device_check(stream=None) -> int:

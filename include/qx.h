@@ -318,6 +318,15 @@ qx_status qx_device_check(qx_stream_t s);
  * QX_ERR_DEVICE_TIMEOUT. */
 qx_status qx_debug_timeout_probe(uint64_t limit_ns, qx_stream_t s);
 
+/* Measurement hook (no counterpart on the pages): the device's warp-level
+ * tensor-core rate, multiply-adds x 2 per second, of mma.sync int8
+ * m16n8k32 (kind 0) or f16 m16n8k16 with an f32 accumulator (kind 1), run
+ * from registers by every SM; sm_103a has no int8 tcgen05 MMA, so kind 0 is
+ * the int8 tensor rate a prefill can use.  It allocates and frees a small
+ * device buffer and synchronises stream s: not for use inside a graph
+ * capture.  QX_ERR_ARG for a null out pointer or another kind. */
+qx_status qx_debug_mma_rate(int kind, double* ops_per_s, qx_stream_t s);
+
 /* Static, NUL-terminated strings. */
 const char* qx_status_string(qx_status st);
 /* The CUDA call and error text behind the most recent QX_ERR_CUDA returned

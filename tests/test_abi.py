@@ -115,6 +115,10 @@ def test_host_validation_rejects_before_launch(lib):
         assert lib.qx_gemm_prefill_ex(SOA, P(A16), 4, 256, ctypes.byref(act), P(A16), path, s) == qx.QX_ERR_FMT
     job = qx._Job(SOA, 1, (ctypes.c_void_p * 4)(A16), (ctypes.c_int64 * 4)(4), (ctypes.c_void_p * 4)(A16), 256, A16)
     assert lib.qx_gemv_chain(1, ctypes.byref(job), P(A16), s) == qx.QX_ERR_FMT
+    # the mma.sync rate probe: two kinds, an out pointer
+    v = ctypes.c_double(0.0)
+    assert lib.qx_debug_mma_rate(2, ctypes.byref(v), s) == qx.QX_ERR_ARG
+    assert lib.qx_debug_mma_rate(0, None, s) == qx.QX_ERR_ARG
 
 
 def test_python_binding_rejects_cpu_tensors(lib):

@@ -342,6 +342,16 @@ def test_prefill_full_size_sampled(path):
     assert_close(Y[np.ix_(xr, wr)].reshape(-1), ref.reshape(-1), absdot.reshape(-1), f"prefill full size path {path}")
 
 
+# ------------------------------------------------------- mma rate probe ----
+
+def test_mma_rate_probe():
+    """The measured mma.sync rates are finite, positive and ordered (f16 above int8 on GB300)."""
+    int8 = qx.qx_debug_mma_rate(0)
+    f16 = qx.qx_debug_mma_rate(1)
+    assert 1e12 < int8 < 1e16 and 1e12 < f16 < 1e16
+    assert f16 > int8
+
+
 # ---------------------------------------------------- device error word ----
 
 def test_bounded_wait_reports_timeout_and_recovers():
