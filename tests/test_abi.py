@@ -125,3 +125,18 @@ def test_python_binding_rejects_cpu_tensors(lib):
     import torch
     with pytest.raises((ValueError, TypeError)):
         qx.qx_gemv(qx.QX_Q4_K, torch.zeros(144, dtype=torch.uint8), 1, 256, torch.zeros(256), mode=qx.QX_MODE_F32)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without libqx.so the binding raises; nothing falls back to another path."""
+    import subprocess
+    import sys
+    code = ("import block_quantized_gemv_q8_gb300 as qx\n"
+            f"qx.LIB_PATH = {str(tmp_path / 'missing' / 'libqx.so')!r}\n"
+            "try:\n"
+            "    qx.qx_row_bytes(qx.QX_Q4_K, 256)\n"
+            "except RuntimeError as e:\n"
+            "    print('raised:', e)\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert "raised:" in r.stdout and "libqx.so not found" in r.stdout
