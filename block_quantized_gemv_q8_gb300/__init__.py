@@ -118,6 +118,36 @@ def _ptr(t: torch.Tensor) -> ctypes.c_void_p:
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _nbytes(t: torch.Tensor) -> int:
+    return t.numel() * t.element_size()
+
+
+def _need(t: torch.Tensor, nbytes: int, what: str) -> torch.Tensor:
+    """A CUDA, contiguous tensor holding at least nbytes: the library writes and
+    reads through raw pointers, so a short buffer is refused here."""
+    _ptr(t)
+    if nbytes > 0 and _nbytes(t) < nbytes:
+        raise ValueError(f"{what}: {_nbytes(t)} bytes, need {nbytes}")
+    return t
+
+
+def _need_weights(W: torch.Tensor, fmt: int, rows: int, cols: int, what: str = "W") -> torch.Tensor:
+    rb = qx_row_bytes(fmt, cols)
+    return _need(W, rows * rb, what) if rb > 0 and rows > 0 else W  # invalid shapes: the library names them
+
+
+def _served_cols(fmt: int, cols: int) -> int:
+    """cols when the format serves that width, else 0: an invalid shape is left
+    to the library, which names it (QX_ERR_SHAPE / QX_ERR_FMT)."""
+    return cols if qx_row_bytes(fmt, cols) > 0 else 0
+
+
+def _need_act(a: "ActQ8", m: int, cols: int, what: str):
+    _need(a.q, m * cols, what + ".q")
+    _need(a.d, m * (cols // 32) * 4, what + ".d")
+    _need(a.sum, m * (cols // 32) * 4, what + ".sum")
+
+
 def _check(st: int, what: str):
     if st != QX_OK:
         raise QxError(st, what)
@@ -162,6 +192,8 @@ def qx_repack(from_fmt: int, to_fmt: int, W: torch.Tensor, rows: int, cols: int,
     nbytes = rows * qx_row_bytes(to_fmt, cols)
     if out is None:
         out = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
+    _need_weights(W, from_fmt, rows, cols)
+    _need(out, nbytes, "out")
     _check(lib().qx_repack(from_fmt, to_fmt, _ptr(W), rows, cols, _ptr(out), _stream(stream)), "qx_repack")
     return out
 
@@ -185,18 +217,20 @@ def qx_quantize_act_q8(x: torch.Tensor, out: ActQ8 | None = None, stream=None) -
     x2 = x.reshape(1, -1) if x.dim() == 1 else x
     m, cols = x2.shape
     out = out or ActQ8.empty(m, cols, x.device)
+    _need_act(out, m, cols, "out")
     a = out.c_struct()
     _check(lib().qx_quantize_act_q8(_ptr(x2), m, cols, ctypes.byref(a), _stream(stream)), "qx_quantize_act_q8")
     return out
 
 
-def _x_arg(x, mode):
+def _x_arg(x, mode, cols: int = 0):
     if (mode & 0xFF) in (QX_MODE_F32, QX_MODE_W4A8_FUSED):
         if not isinstance(x, torch.Tensor) or x.dtype != torch.float32:
             raise TypeError("f32 and fused-W4A8 modes take a float32 activation tensor")
-        return _ptr(x), None
+        return _ptr(_need(x, cols * 4, "x")), None
     if not isinstance(x, ActQ8):
         raise TypeError("W4A8 mode takes an ActQ8 (from qx_quantize_act_q8)")
+    _need_act(x, 1, cols, "x")
     a = x.c_struct()
     return ctypes.cast(ctypes.pointer(a), ctypes.c_void_p), a
 
@@ -208,7 +242,9 @@ def qx_gemv(fmt: int, W: torch.Tensor, rows: int, cols: int, x, y: torch.Tensor 
     mode: QX_MODE_F32 (x f32), QX_MODE_W4A8 (x an ActQ8) or QX_MODE_W4A8_FUSED
     (x f32, quantised inside the launch), optionally | QX_FLAG_PDL."""
     y = y if y is not None else torch.empty(rows, dtype=torch.float32, device=W.device)
-    xp, keep = _x_arg(x, mode)
+    _need_weights(W, fmt, rows, cols)
+    _need(y, rows * 4, "y")
+    xp, keep = _x_arg(x, mode, _served_cols(fmt, cols))
     _check(lib().qx_gemv(fmt, _ptr(W), rows, cols, xp, _ptr(y), mode, _stream(stream)), "qx_gemv")
     return y
 
@@ -217,11 +253,16 @@ def qx_gemv_multi(fmts, Ws, rows, cols: int, x, ys=None, mode: int = QX_MODE_W4A
     """Several GEMVs over one activation in one launch per format."""
     n = len(Ws)
     ys = ys if ys is not None else [torch.empty(r, dtype=torch.float32, device=Ws[0].device) for r in rows]
+    if not (len(fmts) == len(rows) == len(ys) == n):
+        raise ValueError("qx_gemv_multi: fmts, Ws, rows and ys differ in length")
+    for f, w, r, y in zip(fmts, Ws, rows, ys):
+        _need_weights(w, f, r, cols)
+        _need(y, r * 4, "y")
     F = (ctypes.c_int * n)(*fmts)
     Wp = (ctypes.c_void_p * n)(*[_ptr(w).value for w in Ws])
     R = (ctypes.c_int64 * n)(*rows)
     Yp = (ctypes.c_void_p * n)(*[_ptr(t).value for t in ys])
-    xp, keep = _x_arg(x, mode)
+    xp, keep = _x_arg(x, mode, min(_served_cols(f, cols) for f in fmts) if n else 0)
     _check(lib().qx_gemv_multi(n, F, Wp, R, cols, xp, Yp, mode, _stream(stream)), "qx_gemv_multi")
     return ys
 
@@ -231,6 +272,9 @@ def qx_gemv_partials(fmt: int, W: torch.Tensor, rows: int, cols: int, x: ActQ8, 
     """Exact int32 partial sums [rows, cols/32] (Q4_K, Q8_0) or [rows, cols/16] (Q6_K, QX_Q6_K_SOA)."""
     g = 16 if fmt in (QX_Q6_K, QX_Q6_K_SOA) else 32
     P = P if P is not None else torch.empty((rows, cols // g), dtype=torch.int32, device=W.device)
+    _need_weights(W, fmt, rows, cols)
+    _need(P, rows * (cols // g) * 4, "P")
+    _need_act(x, 1, _served_cols(fmt, cols), "x")
     a = x.c_struct()
     _check(lib().qx_gemv_partials(fmt, _ptr(W), rows, cols, ctypes.byref(a), _ptr(P), _stream(stream)),
            "qx_gemv_partials")
@@ -246,6 +290,9 @@ def qx_gemm_prefill(fmt: int, W: torch.Tensor, rows: int, cols: int, X: ActQ8, Y
 def qx_gemm_prefill_ex(fmt: int, W: torch.Tensor, rows: int, cols: int, X: ActQ8, Y: torch.Tensor | None = None,
                        path: int = 0, stream=None) -> torch.Tensor:
     Y = Y if Y is not None else torch.empty((X.m, rows), dtype=torch.float32, device=W.device)
+    _need_weights(W, fmt, rows, cols)
+    _need(Y, X.m * rows * 4, "Y")
+    _need_act(X, X.m, _served_cols(fmt, cols), "X")
     a = X.c_struct()
     _check(lib().qx_gemm_prefill_ex(fmt, _ptr(W), rows, cols, ctypes.byref(a), _ptr(Y), path, _stream(stream)),
            "qx_gemm_prefill_ex")
@@ -265,6 +312,10 @@ def qx_gemm_prefill_ws(fmt: int, W: torch.Tensor, rows: int, cols: int, X: ActQ8
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=W.device)
     nbytes = workspace.numel() * workspace.element_size()
+    _need_weights(W, fmt, rows, cols)
+    _need(Y, X.m * rows * 4, "Y")
+    _need_act(X, X.m, _served_cols(fmt, cols), "X")
+    _ptr(workspace)
     a = X.c_struct()
     _check(lib().qx_gemm_prefill_ws(fmt, _ptr(W), rows, cols, ctypes.byref(a), _ptr(Y), path, _ptr(workspace),
                                     nbytes, _stream(stream)), "qx_gemm_prefill_ws")
@@ -300,10 +351,12 @@ def make_chain(jobs) -> ctypes.Array:
         c = arr[j]
         c.fmt, c.n, c.cols = job.fmt, len(job.W), job.cols
         for k, (W, r, y) in enumerate(zip(job.W, job.rows, job.y)):
+            _need_weights(W, job.fmt, r, job.cols)
+            _need(y, r * 4, "y")
             c.W[k] = _ptr(W).value
             c.rows[k] = r
             c.y[k] = _ptr(y).value
-        c.x = _ptr(job.x).value
+        c.x = _ptr(_need(job.x, _served_cols(job.fmt, job.cols) * 4, "x")).value
     return arr
 
 

@@ -140,3 +140,12 @@ def test_missing_library_fails_loudly(tmp_path):
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     assert "raised:" in r.stdout and "libqx.so not found" in r.stdout
+
+
+
+def test_python_binding_refuses_host_tensors_before_sizes(lib):
+    """Every tensor goes through the same check (CUDA, contiguous, enough bytes);
+    a host tensor is refused first."""
+    import torch
+    with pytest.raises(ValueError):
+        qx._need(torch.zeros(4), 16, "t")

@@ -342,6 +342,23 @@ def test_prefill_full_size_sampled(path):
     assert_close(Y[np.ix_(xr, wr)].reshape(-1), ref.reshape(-1), absdot.reshape(-1), f"prefill full size path {path}")
 
 
+# ------------------------------------------------- binding size checks ----
+
+def test_binding_refuses_short_buffers():
+    """The binding checks every tensor's byte count before passing a raw pointer."""
+    W = torch.zeros(144 * 4, dtype=torch.uint8, device="cuda")
+    x = torch.zeros(256, device="cuda")
+    with pytest.raises(ValueError):
+        qx.qx_gemv(qx.QX_Q4_K, W, 5, 256, x, mode=qx.QX_MODE_F32)                  # W holds 4 rows
+    with pytest.raises(ValueError):
+        qx.qx_gemv(qx.QX_Q4_K, W, 4, 256, x, y=torch.zeros(3, device="cuda"), mode=qx.QX_MODE_F32)
+    with pytest.raises(ValueError):
+        qx.qx_gemv(qx.QX_Q4_K, W, 4, 256, x[:128], mode=qx.QX_MODE_W4A8_FUSED)      # x too short
+    with pytest.raises(ValueError):
+        qx.qx_repack(qx.QX_Q6_K, qx.QX_Q6_K_SOA, torch.zeros(210, dtype=torch.uint8, device="cuda"), 1, 256,
+                     out=torch.zeros(16, dtype=torch.uint8, device="cuda"))
+
+
 # ------------------------------------------------------- mma rate probe ----
 
 def test_mma_rate_probe():
