@@ -221,9 +221,13 @@ qx_status gemv_geometry(int fmt, int kmode, bool partials, bool fused, bool pdl,
     // following launches under PDL, costs the Llama-3.1-8B decode step more
     // than it saves on its 48 MB down projections: long launches only.
     const int64_t rb = row_bytes_of(fmt, cols);
-    const bool merged = gemv_has_merged(fmt, kmode, partials) && p.total_rows * rb >= kMergedMinBytes;
-    p.merged = merged ? 1 : 0;
+    bool merged = gemv_has_merged(fmt, kmode, partials) && p.total_rows * rb >= kMergedMinBytes;
     TeamGeom g;
+    // the merged variant's seven consumer warps cover rows of up to 28672
+    // columns; wider rows take the standard kernel
+    if (merged && team_geometry(fmt, kmode, partials, cols, gemv_consumer_warps(fmt, kmode, true), g) != QX_OK)
+        merged = false;
+    p.merged = merged ? 1 : 0;
     qx_status st = team_geometry(fmt, kmode, partials, cols, gemv_consumer_warps(fmt, kmode, merged), g);
     if (st != QX_OK) return st;
     const bool half_sm = (kmode == QX_MODE_W4A8 || fmt == QX_Q8_0);
@@ -505,7 +509,18 @@ qx_status prefill_dispatch(qx_fmt fmt, const void* W, int64_t rows, int64_t cols
         if (path != 0 && path != 1) return QX_ERR_FMT;  // the GEMM paths read the GGUF layouts
         path = 1;
     }
-    if (path == 0) path = X->m == 1 ? 1 : (X->m <= kPrefillBatchMaxRows ? 4 : 3);
+    if (path == 0) {
+        path = X->m == 1 ? 1 : (X->m <= kPrefillBatchMaxRows ? 4 : 3);
+        // rows wider than the small-batch lanes cover (eight-row lanes: 14336
+        // columns, four-row K-quant lanes: 28672) take one GEMV per row
+        if (path == 4) {
+            TeamGeom g;
+            const int mb = X->m > kBatchRows ? kBatchRowsWide : kBatchRows;
+            if (team_geometry(fmt, QX_MODE_W4A8, false, cols, kBatchConsumerWarps, g, mb) != QX_OK ||
+                team_geometry(fmt, QX_MODE_W4A8, false, cols, kBatchConsumerWarps, g, kBatchRows) != QX_OK)
+                path = 1;
+        }
+    }
     if (path == 4) {
         // eight rows of X per weight stream while more than four remain, then four
         for (int64_t m0 = 0; m0 < X->m;) {

@@ -132,7 +132,9 @@ qx_status qx_quantize_act_q8(const float* x, int64_t m, int64_t cols, qx_act_q8*
  *                      computes exactly what QX_MODE_W4A8 computes.
  * mode may carry QX_FLAG_PDL.
  * cols must be a positive multiple of the block width (256 for Q4_K/Q6_K,
- * 32 for Q8_0) and at most QX_MAX_COLS; rows >= 1.
+ * 32 for Q8_0) and at most QX_MAX_COLS; rows >= 1.  The lanes cover rows of
+ * up to 32768 columns for Q4_K / Q6_K in W4A8 mode, 24576 for Q4_K / Q6_K in
+ * f32 mode, and 8192 for Q8_0; wider rows return QX_ERR_SHAPE.
  */
 qx_status qx_gemv(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const void* x, float* y,
                   qx_mode mode, qx_stream_t s);
@@ -177,7 +179,9 @@ qx_status qx_gemm_prefill(qx_fmt fmt, const void* W, int64_t rows, int64_t cols,
  *       first use per device and keeps (growing it is refused with QX_ERR_ARG
  *       while the stream is being captured into a graph); calls that may run
  *       concurrently on different streams must use qx_gemm_prefill_ws.
- *   4 = small-batch GEMV, every format: the weights are streamed once per
+ *   4 = small-batch GEMV, every format (rows of up to 14336 columns, or
+ *       28672 for Q4_K / Q6_K when at most four rows of X remain; path 0
+ *       takes path 1 for wider rows): the weights are streamed once per
  *       group of four rows of X (decode of several tokens at once:
  *       speculative or batched decode), each lane holding its column slice
  *       of the four rows' codes and dotting every weight word with each;

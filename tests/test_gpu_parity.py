@@ -382,3 +382,48 @@ def test_bounded_wait_reports_timeout_and_recovers():
     y = qx.qx_gemv(fmt, dev(W), rows, cols, dev(x), mode=qx.QX_MODE_F32)
     ref, absdot = oracle.gemv_f32(fmt, W, rows, cols, x)
     assert_close(host(y), ref, absdot, "after probe")
+
+
+# ------------------------------------------------------------ width limits ----
+
+def test_wide_rows_take_a_variant_that_fits():
+    """A >= 128 MB Q6_K W4A8 launch normally takes the merged variant, whose
+    lanes cover 28672 columns: 32768-column rows take the standard kernel;
+    the automatic prefill path leaves the small-batch path for rows wider
+    than its lanes; the documented limits refuse wider rows by name."""
+    fmt, rows, cols = synth.Q6_K, 5120, 32768          # 137.6 MB of weights
+    W = synth.weights(fmt, rows, cols, seed=120)
+    x = synth.activation(1, cols, seed=121)
+    a, q, d, s = quantize_both(x)
+    Wd = dev(W)
+    y = qx.qx_gemv(fmt, Wd, rows, cols, dev(x[0]), mode=qx.QX_MODE_W4A8_FUSED | qx.QX_FLAG_PDL)
+    y2 = qx.qx_gemv(fmt, Wd, rows, cols, a, mode=qx.QX_MODE_W4A8)
+    assert np.array_equal(host(y).view(np.uint32), host(y2).view(np.uint32))
+    sel = np.unique(np.concatenate([np.random.default_rng(122).choice(rows, 64, replace=False), [0, rows - 1]]))
+    ref, absdot = oracle.gemv_w4a8(fmt, np.ascontiguousarray(W[sel]), len(sel), cols, q[0], d[0])
+    assert_close(host(y)[sel], ref, absdot, "wide merged-size Q6_K")
+    del Wd, W
+    # prefill: too wide for the small-batch lanes -> one GEMV per row of X
+    for m, c in ((4, 32768), (8, 16384)):
+        f, r = synth.Q4_K, 64
+        Wq = dev(synth.weights(f, r, c, seed=123 + m))
+        X = qx.qx_quantize_act_q8(dev(synth.activation(m, c, seed=124 + m)))
+        y_auto = host(qx.qx_gemm_prefill(f, Wq, r, c, X))
+        y_rows = host(qx.qx_gemm_prefill_ex(f, Wq, r, c, X, path=1))
+        assert np.array_equal(y_auto.view(np.uint32), y_rows.view(np.uint32))
+        with pytest.raises(qx.QxError) as ei:
+            qx.qx_gemm_prefill_ex(f, Wq, r, c, X, path=4)
+        assert ei.value.status == qx.QX_ERR_SHAPE
+    # documented limits: f32 Q4_K up to 24576 columns, Q8_0 up to 8192
+    for f, c_ok, c_bad, mode in ((synth.Q4_K, 24576, 24832, qx.QX_MODE_F32), (synth.Q8_0, 8192, 8224, qx.QX_MODE_F32),
+                                 (synth.Q8_0, 8192, 8224, qx.QX_MODE_W4A8_FUSED)):
+        for c, ok in ((c_ok, True), (c_bad, False)):
+            Wc = dev(synth.weights(f, 3, c, seed=125))
+            xc = dev(synth.activation(1, c, seed=126)[0])
+            if ok:
+                qx.qx_gemv(f, Wc, 3, c, xc, mode=mode)
+            else:
+                with pytest.raises(qx.QxError) as ei:
+                    qx.qx_gemv(f, Wc, 3, c, xc, mode=mode)
+                assert ei.value.status == qx.QX_ERR_SHAPE
+    assert qx.qx_device_check() == qx.QX_OK
