@@ -796,7 +796,8 @@ const char* qx_status_string(qx_status st) {
 const char* qx_last_error(void) { return g_last_error; }
 
 const char* qx_version(void) {
-    return "qx 0.1 sm_103a: actq8; gemv {q4_k,q6_k,q8_0} x {f32,w4a8} (bulk-copy stream); partials; multi";
+    return "qx 0.2 sm_103a: actq8; gemv {q4_k,q6_k,q6_k_soa,q8_0} x {f32,w4a8,w4a8 fused} (bulk-copy stream, "
+           "pdl); multi; chain; partials; prefill {gemv per row, mma.sync, tcgen05, small batch}; repack";
 }
 
 // ----------------------------------------------------------------------------
