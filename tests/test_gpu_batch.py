@@ -89,3 +89,28 @@ def test_batch_full_size_sampled(m):
     rng = np.random.default_rng(94)
     wr = np.sort(np.concatenate([rng.choice(rows, 300, replace=False), [0, rows - 1]]))
     check(fmt, W, rows, cols, X, f"full size m={m}", sample_rows=wr)
+
+
+def test_batch_and_repack_capture_in_a_graph():
+    """The small-batch path and the repack allocate nothing: captured in a CUDA
+    graph they replay to the eager bits."""
+    fmt, rows, cols, m = synth.Q4_K, 300, 1024, 6
+    W = dev(synth.weights(fmt, rows, cols, seed=130))
+    X = qx.qx_quantize_act_q8(dev(synth.activation(m, cols, seed=131)))
+    y_eager = host(qx.qx_gemm_prefill_ex(fmt, W, rows, cols, X, path=4))
+    W6 = dev(synth.weights(synth.Q6_K, rows, cols, seed=132))
+    x6 = dev(synth.activation(1, cols, seed=133)[0])
+    y6_eager = host(qx.qx_gemv(synth.Q6_K, W6, rows, cols, x6, mode=qx.QX_MODE_W4A8_FUSED))
+    Y = torch.full((m, rows), float("nan"), device="cuda")
+    R = torch.zeros(rows * qx.qx_row_bytes(qx.QX_Q6_K_SOA, cols), dtype=torch.uint8, device="cuda")
+    y6 = torch.full((rows,), float("nan"), device="cuda")
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        qx.qx_gemm_prefill_ex(fmt, W, rows, cols, X, Y=Y, path=4, stream=stream)
+        qx.qx_repack(synth.Q6_K, qx.QX_Q6_K_SOA, W6, rows, cols, out=R, stream=stream)
+        qx.qx_gemv(qx.QX_Q6_K_SOA, R, rows, cols, x6, y=y6, mode=qx.QX_MODE_W4A8_FUSED, stream=stream)
+    g.replay()
+    assert np.array_equal(host(Y).view(np.uint32), y_eager.view(np.uint32))
+    assert np.array_equal(host(y6).view(np.uint32), y6_eager.view(np.uint32))
+    assert qx.qx_device_check() == qx.QX_OK
