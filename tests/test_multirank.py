@@ -59,3 +59,22 @@ def test_reference_arm_under_torchrun_rank0_only():
     j = json.loads(lines[0])
     assert j["impl"] == "reference" and j["n_gpus"] == 2 and j["value"] > 0
     assert j["e2e"]["h2d_bytes_per_step"] == 0 and j["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_reference_arm_line_has_the_contract_keys():
+    """One process, CPU only: the reference arm prints one JSON line with the
+    keys the driver reads."""
+    env = dict(os.environ, QX_REF_STEP_S="0.2", OMP_NUM_THREADS="2")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3"], cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    j = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+              "vs_baseline", "dtype", "data", "config", "impl", "cpu_baseline", "e2e"):
+        assert k in j, k
+    assert j["metric"] == bench.METRIC and j["unit"] == "GB/s" and j["higher_is_better"] is True
+    assert j["steps"] == 1 and j["warmup"] == 3 and j["n_gpus"] == 1
+    assert j["cpu_baseline"]["cores"] >= 1 and j["cpu_baseline"]["value"] == j["value"]
+    assert j["e2e"]["value"] == j["value"] and j["e2e"]["unit"] == j["unit"]
