@@ -510,6 +510,11 @@ def run_extra(args):
         # (legacy mma.sync; no int8 tcgen05) and the f16 mma.sync rate path 2 runs on
         out["mma_sync_int8_tops_measured"] = qx.qx_debug_mma_rate(0, stream=stream) / 1e12
         out["mma_sync_f16_tflops_measured"] = qx.qx_debug_mma_rate(1, stream=stream) / 1e12
+        for rec in sweep:
+            for path in (2, 3, 4):
+                if f"path{path}_tflops" in rec:  # int8-equivalent multiply-adds x 2 per second
+                    rec[f"path{path}_frac_of_int8_mma_sync"] = (rec[f"path{path}_tflops"]
+                                                                / out["mma_sync_int8_tops_measured"])
         out.update({"sweep": sweep, "flops_per_row": 2 * rows * cols, "bf16_dense_peak_tflops": bf16,
                     "note": "path 1 = one W4A8 GEMV launch per row; path 2 = tensor cores (mma.sync f16 with "
                             "integer-valued operands); path 3 = tcgen05 bf16 GEMM over the split dequantised "
