@@ -38,6 +38,14 @@ MUTATIONS = [
     ("partials activation index", "(int64_t)qw * qx[col0 + i]", "(int64_t)qw * qx[i]"),
     ("w4a8 activation scale of the wrong block", "(double)dx[col0 / 32]", "(double)dx[col0 / 64]"),
     ("w4a8 q4_k sub-block index", "(int)((col0 % 256) / 32)", "(int)((col0 % 256) / 64)"),
+    ("q4_k d and dmin swapped", "double d = f16_at(blk), dmin = f16_at(blk + 2);",
+     "double d = f16_at(blk + 2), dmin = f16_at(blk);"),
+    ("q6_k d read from the front of the block", "double d = f16_at(blk + 208);", "double d = f16_at(blk);"),
+    ("w4a8 q4_k min scaled by d", "- f16_at(blk + 2) * m * dxg", "- f16_at(blk) * m * dxg"),
+    ("w4a8 q6_k scale of another group", "q6k_scale(blk, (int)(col0 % 256))", "q6k_scale(blk, (int)(col0 % 128))"),
+    ("f32 gemv drops the last column", "for (int64_t i = 0; i < cols; i++) {\n                acc += w[i] * x[i];",
+     "for (int64_t i = 0; i < cols - 1; i++) {\n                acc += w[i] * x[i];"),
+    ("prefill activation scales of the wrong row", "dx + i * (cols / 32)", "dx + i * (cols / 64)"),
 ]
 
 
