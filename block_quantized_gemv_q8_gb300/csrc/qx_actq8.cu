@@ -28,8 +28,23 @@ cudaError_t launch_actq8(const float* x, int64_t nblocks, int8_t* q, float* d, i
                          cudaStream_t s) {
     int64_t grid = (2 * nblocks + kActq8Threads - 1) / kActq8Threads;
     if (grid > int64_t(sm_count) * 8) grid = int64_t(sm_count) * 8;
-    actq8_kernel<<<static_cast<int>(grid), kActq8Threads, 0, s>>>(x, nblocks, q, d, sum);
-    return cudaGetLastError();
+    // Launched with programmatic stream serialisation: the CTAs may become
+    // resident while the previous kernel in the stream drains, and the wait at
+    // the top of the kernel keeps every read of x and write of q, d, sum after
+    // that kernel has completed, so the order is the plain stream order.  A
+    // following W4A8 GEMV launched with QX_FLAG_PDL then starts streaming its
+    // weights during this launch.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kActq8Threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, actq8_kernel, x, nblocks, q, d, sum);
 }
 
 }  // namespace qx

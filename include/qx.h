@@ -116,7 +116,10 @@ typedef struct {
  * Writes out->q, out->d, out->sum (device buffers sized for m x cols) and
  * sets out->m = m, out->cols = cols.  cols must be a positive multiple of 32
  * (QX_ERR_SHAPE), m >= 1.  Non-finite inputs are not checked; their outputs
- * are unspecified.
+ * are unspecified.  The launch uses programmatic dependent launch: it may
+ * start while the previous kernel in the stream drains, but reads x and
+ * writes the outputs only after that kernel has completed (plain stream
+ * order), so a following qx_gemv with QX_FLAG_PDL streams its weights early.
  */
 qx_status qx_quantize_act_q8(const float* x, int64_t m, int64_t cols, qx_act_q8* out, qx_stream_t s);
 

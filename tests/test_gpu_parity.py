@@ -184,6 +184,53 @@ def test_pdl_chain_matches_plain_launches():
     assert qx.qx_device_check() == qx.QX_OK
 
 
+def test_two_step_chain_reads_after_the_producer():
+    """GEMV -> quantise -> GEMV, each activation written by the kernel before.
+
+    The quantisation kernel may become resident while the GEMV before it
+    drains and the W4A8 GEMV after it runs under QX_FLAG_PDL; each must still
+    read what its predecessor wrote.  The output buffers start out filled with
+    a constant, so an early read would change the codes.  Checked eagerly and
+    replayed from a CUDA graph against the fused launches, bit for bit."""
+    fmt, rows, cols = synth.Q4_K, 4096, 4096
+    Ws = [dev(synth.weights(fmt, rows, cols, seed=80 + i)) for i in range(4)]
+    x0 = dev(synth.activation(1, cols, seed=85)[0])
+    PDL = qx.QX_FLAG_PDL
+    ys = [torch.full((rows,), 7.0, dtype=torch.float32, device="cuda") for _ in Ws]
+    acts = [qx.ActQ8.empty(1, cols) for _ in Ws]
+
+    def two_step():
+        x = x0
+        for W, y, a in zip(Ws, ys, acts):
+            qx.qx_quantize_act_q8(x, out=a)
+            qx.qx_gemv(fmt, W, rows, cols, a, y=y, mode=qx.QX_MODE_W4A8 | PDL)
+            x = y
+
+    x, ref = x0, []
+    for W in Ws:
+        x = qx.qx_gemv(fmt, W, rows, cols, x, mode=qx.QX_MODE_W4A8_FUSED | PDL)
+        ref.append(host(x).view(np.uint32))
+    two_step()
+    for y, r in zip(ys, ref):
+        assert np.array_equal(host(y).view(np.uint32), r)
+    for y in ys:
+        y.fill_(7.0)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            two_step()
+    for y in ys:
+        y.fill_(7.0)
+    torch.cuda.current_stream().wait_stream(stream)
+    g.replay()
+    torch.cuda.synchronize()
+    for y, r in zip(ys, ref):
+        assert np.array_equal(host(y).view(np.uint32), r)
+    assert qx.qx_device_check() == qx.QX_OK
+
+
 def test_gemv_zero_and_edge_values():
     """All-zero weights, all-zero activation, a zero-scale super-block."""
     rows, cols = 16, 1024
