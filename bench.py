@@ -196,16 +196,14 @@ class LlamaDecode:
                              for L in range(self.layers)])
         self.x_host = xs
         self.x_dev = torch.from_numpy(xs).cuda()
-        self.x_views, self.acts = [], []
+        self.x_views = []
         off = 0
         for L in range(self.layers):
-            views, acts = [], []
+            views = []
             for c in self.xcols:
                 views.append(self.x_dev[off:off + c])
-                acts.append(qx.ActQ8.empty(1, c))
                 off += c
             self.x_views.append(views)
-            self.acts.append(acts)
         # one output buffer so that the e2e path copies it back in one piece
         outs = [(L, n) for L in range(self.layers) for n in self.shapes]
         total = sum(self.shapes[n][1] for _, n in outs)
