@@ -282,9 +282,10 @@ class LlamaDecode:
             else:
                 qx.qx_gemv(qx.QX_Q6_K, W["down"], 4096, 14336, xv[3], y=y["down"], mode=mode, stream=stream)
 
-    def cpu_sample(self, oracle, budget_s: float = 10.0):
-        """Oracle on layer 0 (quantise + 7 W4A8 GEMVs), repeated for ~budget_s."""
-        threads = oracle.default_threads()
+    def cpu_sample(self, oracle, budget_s: float = 10.0, threads: int | None = None):
+        """Oracle on layer 0 (quantise + 7 W4A8 GEMVs), repeated for ~budget_s
+        (at least once), on `threads` host threads (default: every core)."""
+        threads = threads or oracle.default_threads()
         x = self.x_host
         acts = {}
         nbytes, reps = 0, 0
@@ -306,7 +307,8 @@ class LlamaDecode:
                 break
         return {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
                 "sample": f"layer 0 of the same workload (7 W4A8 GEMVs + 4 activation quantisations, "
-                          f"{nbytes // reps} weight bytes) x {reps} repetitions, {el:.1f} s, OpenMP over rows"}
+                          f"{nbytes // reps} weight bytes) x {reps} repetitions, {el:.1f} s, "
+                          + ("OpenMP over rows" if threads > 1 else "one thread")}
 
 
 # ------------------------------------------------------------------ main ----
@@ -712,6 +714,8 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
         cpu = wl.cpu_sample(oracle, budget_s=10.0)
+        one = wl.cpu_sample(oracle, budget_s=5.0, threads=1)
+        cpu["single_thread"] = {"value": one["value"], "unit": one["unit"], "cores": 1, "sample": one["sample"]}
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
