@@ -29,7 +29,7 @@ QX_CHAIN_MAX_ENTRIES = 4
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libqx.so")
 
 EXPORTS = ["qx_quantize_act_q8", "qx_gemv", "qx_gemv_multi", "qx_gemm_prefill", "qx_gemm_prefill_ex",
-           "qx_gemm_prefill_ws", "qx_gemm_prefill_workspace_bytes", "qx_gemv_partials", "qx_gemv_chain", "qx_gemv_chain_scratch_bytes", "qx_row_bytes", "qx_repack",
+           "qx_gemm_prefill_ws", "qx_gemm_prefill_workspace_bytes", "qx_gemv_partials", "qx_gemv_chain", "qx_gemv_chain_noalloc", "qx_gemv_chain_scratch_bytes", "qx_row_bytes", "qx_repack",
            "qx_device_check", "qx_debug_timeout_probe", "qx_debug_mma_rate",
            "qx_status_string", "qx_last_error", "qx_version"]
 
@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
         L.qx_gemm_prefill_workspace_bytes.restype = ctypes.c_size_t
         L.qx_gemv_partials.argtypes = [I, P, I64, I64, ctypes.POINTER(_Act), P, P]
         L.qx_gemv_chain.argtypes = [I, ctypes.POINTER(_Job), P, P]
+        L.qx_gemv_chain_noalloc.argtypes = [I, ctypes.POINTER(_Job), P]
         L.qx_gemv_chain_scratch_bytes.argtypes = [I]
         L.qx_gemv_chain_scratch_bytes.restype = ctypes.c_size_t
         L.qx_row_bytes.argtypes = [I, I64]
@@ -89,7 +90,8 @@ def lib() -> ctypes.CDLL:
         L.qx_version.argtypes = []
         L.qx_version.restype = ctypes.c_char_p
         for n in ("qx_quantize_act_q8", "qx_gemv", "qx_gemv_multi", "qx_gemm_prefill", "qx_gemm_prefill_ex",
-                  "qx_gemm_prefill_ws", "qx_gemv_partials", "qx_gemv_chain", "qx_device_check", "qx_debug_timeout_probe",
+                  "qx_gemm_prefill_ws", "qx_gemv_partials", "qx_gemv_chain", "qx_gemv_chain_noalloc",
+                  "qx_device_check", "qx_debug_timeout_probe",
                   "qx_repack", "qx_debug_mma_rate"):
             getattr(L, n).restype = I
         _lib = L
@@ -364,6 +366,14 @@ def qx_gemv_chain(jobs, scratch: torch.Tensor, stream=None, marshalled=None):
     """Run a chain of dependent GEMVs in one launch; returns the jobs (with y)."""
     arr = marshalled if marshalled is not None else make_chain(jobs)
     _check(lib().qx_gemv_chain(len(arr), arr, _ptr(scratch), _stream(stream)), "qx_gemv_chain")
+    return jobs
+
+
+def qx_gemv_chain_noalloc(jobs, stream=None, marshalled=None):
+    """qx_gemv_chain with the library's own arrival counters (no scratch; at
+    most QX_CHAIN_MAX_JOBS jobs; calls on one device must not overlap)."""
+    arr = marshalled if marshalled is not None else make_chain(jobs)
+    _check(lib().qx_gemv_chain_noalloc(len(arr), arr, _stream(stream)), "qx_gemv_chain_noalloc")
     return jobs
 
 

@@ -80,3 +80,28 @@ def test_noalloc_chain_rejects_too_many_jobs(lib):
     jobs = [qx.GemvJob(synth.Q4_K, [W], [4], 256, x) for _ in range(qx.QX_CHAIN_MAX_JOBS + 1)]
     arr = qx.make_chain(jobs)
     assert lib.qx_gemv_chain_noalloc(len(arr), arr, None) == qx.QX_ERR_ARG
+
+
+def test_noalloc_chain_through_the_binding(lib):
+    """The binding's qx_gemv_chain_noalloc gives the scratch chain's outputs bit for bit,
+    and refuses an over-long chain with a named status."""
+    specs = [(synth.Q4_K, [200, 56], 2048), (synth.Q8_0, [96], 896)]
+    jobs, again = [], []
+    for i, (fmt, rows, cols) in enumerate(specs):
+        Ws = [dev(synth.weights(fmt, r, cols, seed=970 + 10 * i + k)) for k, r in enumerate(rows)]
+        x = dev(synth.activation(1, cols, seed=990 + i)[0])
+        jobs.append(qx.GemvJob(fmt, Ws, rows, cols, x))
+        again.append(qx.GemvJob(fmt, Ws, rows, cols, x))
+    qx.qx_gemv_chain(jobs, qx.chain_scratch(len(jobs)))
+    qx.qx_gemv_chain_noalloc(again)
+    torch.cuda.synchronize()
+    for a, b in zip(jobs, again):
+        for ya, yb in zip(a.y, b.y):
+            assert torch.equal(ya.view(torch.int32), yb.view(torch.int32))
+    assert qx.qx_device_check() == qx.QX_OK
+    W = torch.zeros(144 * 4, dtype=torch.uint8, device="cuda")
+    x = torch.zeros(256, dtype=torch.float32, device="cuda")
+    too_many = [qx.GemvJob(synth.Q4_K, [W], [4], 256, x) for _ in range(qx.QX_CHAIN_MAX_JOBS + 1)]
+    with pytest.raises(qx.QxError) as e:
+        qx.qx_gemv_chain_noalloc(too_many)
+    assert e.value.status == qx.QX_ERR_ARG
