@@ -30,8 +30,11 @@
  *            w = d*sc*(q - 32).
  *       Q8_0 32 weights / 34 B: d f16, 32 int8 quants; w = d*q.
  *   - Every pointer named "device" is device memory owned by the caller.  The
- *     library allocates nothing and keeps no per-call state; it caches one
- *     device-property query per device.
+ *     library keeps no per-call state; it caches one device-property query
+ *     per device.  It allocates device memory in two places only: the
+ *     prefill workspace of qx_gemm_prefill / qx_gemm_prefill_ex (paths 0 and
+ *     3, grown on demand and kept per device; qx_gemm_prefill_ws takes the
+ *     caller's instead) and the short-lived buffer of qx_debug_mma_rate.
  *   - Calls are asynchronous on stream `s` (NULL = the legacy default stream)
  *     and run on the current device.  Argument, shape and alignment errors
  *     return before anything is launched or written; a failed launch returns
@@ -185,9 +188,10 @@ qx_status qx_gemm_prefill(qx_fmt fmt, const void* W, int64_t rows, int64_t cols,
  *   4 = small-batch GEMV, every format (rows of up to 14336 columns, or
  *       28672 for Q4_K / Q6_K when at most four rows of X remain; path 0
  *       takes path 1 for wider rows): the weights are streamed once per
- *       group of four rows of X (decode of several tokens at once:
- *       speculative or batched decode), each lane holding its column slice
- *       of the four rows' codes and dotting every weight word with each;
+ *       group of eight rows of X while five or more remain, else once per
+ *       group of up to four (decode of several tokens at once: speculative
+ *       or batched decode), each lane holding its column slice of the
+ *       group's codes and dotting every weight word with each row's;
  *       the same per-block integer dot products and scales as qx_gemv's
  *       W4A8 path, in a different f32 summation order (within the same
  *       tolerance, not bit-for-bit path 1).

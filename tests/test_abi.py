@@ -149,3 +149,22 @@ def test_python_binding_refuses_host_tensors_before_sizes(lib):
     import torch
     with pytest.raises(ValueError):
         qx._need(torch.zeros(4), 16, "t")
+
+
+def test_header_compiles_as_c_and_links_from_c(lib, tmp_path):
+    """include/qx.h is plain C: a C99 program built with -pedantic -Werror
+    links libqx.so, loads it and gets the declared results from the calls
+    that need no GPU."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    pkg = os.path.dirname(qx.LIB_PATH)
+    exe = tmp_path / "abi_consumer"
+    cmd = ["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+           os.path.join(ROOT, "tests", "abi_consumer.c"), "-o", str(exe), "-L", pkg, "-lqx",
+           f"-Wl,-rpath,{pkg}"]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.strip() == "ok"
