@@ -46,6 +46,17 @@ MUTATIONS = [
     ("f32 gemv drops the last column", "for (int64_t i = 0; i < cols; i++) {\n                acc += w[i] * x[i];",
      "for (int64_t i = 0; i < cols - 1; i++) {\n                acc += w[i] * x[i];"),
     ("prefill activation scales of the wrong row", "dx + i * (cols / 32)", "dx + i * (cols / 64)"),
+    ("act quant amax misses the last value", "for (int i = 0; i < 32; i++)\n            if (fabsf(xb[i]) > amax)",
+     "for (int i = 0; i < 31; i++)\n            if (fabsf(xb[i]) > amax)"),
+    ("q6_k low nibble for the upper quarters", "int low4 = t < 2 ? (lo & 15) : (lo >> 4);",
+     "int low4 = t < 2 ? (lo >> 4) : (lo & 15);"),
+    ("q6_k partial groups of 32", "if (fmt == ORC_Q6_K) return 16;", "if (fmt == ORC_Q6_K) return 32;"),
+    ("w4a8 q4_k min term over half the block", "for (int i = 0; i < 32; i++) S += qx[col0 + i];",
+     "for (int i = 0; i < 16; i++) S += qx[col0 + i];"),
+    ("w4a8 q8_0 scale read past d", "acc += f16_at(blk) * dxg * (double)P[g];",
+     "acc += f16_at(blk + 2) * dxg * (double)P[g];"),
+    ("tolerance scale without the absolute value", "aacc += fabs(w[i] * ((double)dx[i / 32] * qx[i]));",
+     "aacc += w[i] * ((double)dx[i / 32] * qx[i]);"),
 ]
 
 
