@@ -1,8 +1,12 @@
 /* A plain C99 consumer of include/qx.h: the header compiles as C, the library
  * links and loads from C, and the calls that need no GPU behave as declared
  * (row sizes, status strings, version, argument errors returned before any
- * device work).  Built and run by tests/test_abi.py; prints "ok" on success. */
+ * device work).  Built and run by tests/test_abi.py, also against a build of
+ * the library whose host code carries AddressSanitizer and
+ * UndefinedBehaviorSanitizer; prints "ok" on success. */
+#include <stdint.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "qx.h"
@@ -43,7 +47,68 @@ int main(void) {
     expect(qx_quantize_act_q8((const float*)a16, 1, 40, &act, NULL) == QX_ERR_SHAPE, "activation cols");
     expect(qx_quantize_act_q8(NULL, 1, 64, &act, NULL) == QX_ERR_ARG, "null activation");
     expect(qx_gemv_chain(0, NULL, NULL, NULL) == QX_ERR_ARG, "empty chain");
+    expect(qx_gemv_chain_noalloc(0, NULL, NULL) == QX_ERR_ARG, "empty chain without scratch");
 
+    /* byte counts that would overflow: refused as a shape, nothing computed */
+    expect(qx_gemv(QX_Q4_K, a16, INT64_MAX / 2, 256, a16, y, QX_MODE_F32, NULL) == QX_ERR_SHAPE, "huge rows");
+    expect(qx_gemv(QX_Q4_K, a16, 4, INT64_MAX - 255, a16, y, QX_MODE_F32, NULL) == QX_ERR_SHAPE, "huge cols");
+    expect(qx_quantize_act_q8((const float*)a16, INT64_MAX / 64, 64, &act, NULL) == QX_ERR_SHAPE,
+           "huge activation");
+
+    {
+        qx_fmt f9[9];
+        int i;
+        for (i = 0; i < 9; ++i) f9[i] = QX_Q4_K;
+        expect(qx_gemv_multi(0, f9, NULL, NULL, 256, a16, NULL, QX_MODE_F32, NULL) == QX_ERR_ARG, "multi of 0");
+        expect(qx_gemv_multi(9, f9, NULL, NULL, 256, a16, NULL, QX_MODE_F32, NULL) == QX_ERR_ARG, "multi of 9");
+    }
+    {
+        qx_act_q8 bad = act;
+        bad.d = NULL;
+        expect(qx_gemv_partials(QX_Q4_K, a16, 4, 256, &bad, (int32_t*)a16, NULL) == QX_ERR_ARG, "partials, no d");
+    }
+    {
+        qx_act_q8 x4 = act;
+        x4.m = 4;
+        x4.cols = 256;
+        expect(qx_gemm_prefill_ex(QX_Q4_K, a16, 4, 256, &x4, y, 5, NULL) == QX_ERR_ARG, "prefill path 5");
+        expect(qx_gemm_prefill_ex(QX_Q6_K_SOA, a16, 4, 256, &x4, y, 3, NULL) == QX_ERR_FMT, "prefill of SOA");
+    }
+    expect(qx_repack(QX_Q4_K, QX_Q6_K_SOA, a16, 4, 256, (void*)(2 * (uintptr_t)a16), NULL) == QX_ERR_FMT,
+           "repack from Q4_K");
+    expect(qx_repack(QX_Q6_K, QX_Q6_K_SOA, a16, 4, 256, (void*)((uintptr_t)a16 + 256), NULL) == QX_ERR_ARG,
+           "overlapping repack");
+    {
+        qx_gemv_job job;
+        memset(&job, 0, sizeof(job));
+        job.fmt = QX_Q6_K_SOA;
+        job.n = 1;
+        job.W[0] = a16;
+        job.rows[0] = 4;
+        job.y[0] = y;
+        job.cols = 256;
+        job.x = (const float*)a16;
+        expect(qx_gemv_chain(1, &job, a16, NULL) == QX_ERR_FMT, "chain of SOA");
+        job.fmt = QX_Q4_K;
+        job.n = QX_CHAIN_MAX_ENTRIES + 1;
+        expect(qx_gemv_chain(1, &job, a16, NULL) == QX_ERR_ARG, "chain job with too many entries");
+    }
+    {
+        double rate = 0.0;
+        expect(qx_debug_mma_rate(2, &rate, NULL) == QX_ERR_ARG, "mma rate kind");
+        expect(qx_debug_mma_rate(0, NULL, NULL) == QX_ERR_ARG, "mma rate output");
+    }
+    expect(qx_debug_timeout_probe(10, NULL) == QX_ERR_ARG, "timeout probe limit");
+
+#ifdef QX_PLANT_OOB
+    /* sanitizer builds only: one byte read past a heap block must be reported */
+    {
+        volatile char* p = (volatile char*)malloc(16);
+        volatile char c = p[16];
+        (void)c;
+        free((void*)p);
+    }
+#endif
     if (failures) return 1;
     printf("ok\n");
     return 0;

@@ -168,3 +168,41 @@ def test_header_compiles_as_c_and_links_from_c(lib, tmp_path):
     out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert out.returncode == 0, out.stderr
     assert out.stdout.strip() == "ok"
+
+
+def test_host_code_under_asan_and_ubsan(lib, tmp_path):
+    """The library's host code (argument checks, shape arithmetic, status
+    strings) compiled with -fsanitize=address,undefined, driven by the C
+    consumer: no report, and a planted heap overread in the consumer is
+    reported (the sanitizer is live in that process)."""
+    import shutil
+    import subprocess
+    from block_quantized_gemv_q8_gb300 import build as qb
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    asan = subprocess.run(["gcc", "-print-file-name=libasan.so"], capture_output=True, text=True).stdout.strip()
+    if not os.path.isabs(asan) or not os.path.exists(asan):
+        pytest.skip("no AddressSanitizer runtime")
+    san = ["-fsanitize=address", "-fsanitize=undefined", "-fno-sanitize-recover=undefined", "-fno-omit-frame-pointer"]
+    api_obj = tmp_path / "qx_api_san.o"
+    subprocess.run([qb.nvcc(), "-c", os.path.join(qb.CSRC, "qx_api.cu"), "-o", str(api_obj), "-O1", "-g",
+                    "-std=c++17", "-Xcompiler", ",".join(["-fPIC"] + san)] + qb.ARCH,
+                   check=True, capture_output=True, text=True)
+    objs = [os.path.join(qb.OUT_DIR, s.replace(".cu", ".o")) for s in qb.SOURCES if s != "qx_api.cu"]
+    so = tmp_path / "libqx.so"
+    subprocess.run([qb.nvcc(), "-shared", "-o", str(so), str(api_obj)] + objs + qb.ARCH +
+                   ["-cudart", "static", "-Xcompiler", ",".join(san)], check=True, capture_output=True, text=True)
+    env = dict(os.environ, ASAN_OPTIONS="detect_leaks=1", UBSAN_OPTIONS="print_stacktrace=1")
+    for plant, ok in ((False, True), (True, False)):
+        exe = tmp_path / ("consumer_planted" if plant else "consumer")
+        cmd = ["gcc", "-std=c99", "-g", "-I", os.path.join(ROOT, "include"), os.path.join(ROOT, "tests", "abi_consumer.c"),
+               "-o", str(exe), "-L", str(tmp_path), "-lqx", f"-Wl,-rpath,{tmp_path}"] + san
+        if plant:
+            cmd.append("-DQX_PLANT_OOB")
+        subprocess.run(cmd, check=True, capture_output=True, text=True)
+        r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120, env=env)
+        if ok:
+            assert r.returncode == 0 and r.stdout.strip() == "ok", r.stderr[-3000:]
+            assert "runtime error" not in r.stderr and "AddressSanitizer" not in r.stderr, r.stderr[-3000:]
+        else:
+            assert r.returncode != 0 and "AddressSanitizer" in r.stderr, (r.stdout, r.stderr[-2000:])
