@@ -206,3 +206,22 @@ def test_host_code_under_asan_and_ubsan(lib, tmp_path):
             assert "runtime error" not in r.stderr and "AddressSanitizer" not in r.stderr, r.stderr[-3000:]
         else:
             assert r.returncode != 0 and "AddressSanitizer" in r.stderr, (r.stdout, r.stderr[-2000:])
+
+
+def test_size_queries_need_no_gpu(lib):
+    """Workspace and scratch sizes follow the header's formulas; invalid shapes give 0."""
+    rows, cols, m = 14336, 4096, 512
+    q4 = qx.qx_gemm_prefill_workspace_bytes(qx.QX_Q4_K, rows, cols, m)
+    q6 = qx.qx_gemm_prefill_workspace_bytes(qx.QX_Q6_K, rows, cols, m)
+    q8 = qx.qx_gemm_prefill_workspace_bytes(qx.QX_Q8_0, rows, cols, m)
+    assert 4 * cols * m <= q4 < 4 * cols * m + (1 << 20)                    # activation hi / lo only
+    for v in (q6, q8):
+        assert 4 * cols * (m + rows) <= v < 4 * cols * (m + rows) + (1 << 20)  # and the weights' hi / lo
+    assert qx.qx_gemm_prefill_workspace_bytes(qx.QX_Q4_K, rows, cols + 1, m) == 0
+    assert qx.qx_gemm_prefill_workspace_bytes(qx.QX_Q4_K, rows, cols, 0) == 0
+    assert qx.qx_gemm_prefill_workspace_bytes(qx.QX_Q4_K, 0, cols, m) == 0
+    assert qx.qx_gemm_prefill_workspace_bytes(7, rows, cols, m) == 0
+    assert qx.qx_gemv_chain_scratch_bytes(1) == 8
+    assert qx.qx_gemv_chain_scratch_bytes(qx.QX_CHAIN_MAX_JOBS) == 4 * (qx.QX_CHAIN_MAX_JOBS + 1)
+    assert qx.qx_gemv_chain_scratch_bytes(0) == 0
+    assert qx.qx_gemv_chain_scratch_bytes(qx.QX_CHAIN_MAX_JOBS + 1) == 0
