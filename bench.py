@@ -519,7 +519,8 @@ def run_extra(args):
                     "note": "path 1 = one W4A8 GEMV launch per row; path 2 = tensor cores (mma.sync f16 with "
                             "integer-valued operands); path 3 = tcgen05 bf16 GEMM over the split dequantised "
                             "operands (3 passes of K), timed with its dequantise passes; path 4 = small-batch "
-                            "GEMV, one weight stream per 4 rows of X; tflops count the int8-equivalent "
+                            "GEMV, one weight stream per 8 rows of X while five or more remain, else per up to 4; "
+                            "tflops count the int8-equivalent "
                             "multiply-adds x2"})
     print(json.dumps(out), flush=True)
     return 0
