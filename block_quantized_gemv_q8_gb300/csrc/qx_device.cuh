@@ -176,6 +176,13 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
 // the sum's bit pattern is rne(t) as a two's-complement byte (the pattern of
 // 1.5 * 2^23 has a zero low byte).  |x| <= amax for every x of the block, so
 // the largest |t| is fl(amax * fl(1 / d)): one range check per block.
+//
+// The clamp binds only when d is an f32 subnormal: then d = fl(amax / 127)
+// may carry a relative error far above 2^-24 (d = 2^-149 for amax = 178 *
+// 2^-149 gives x / d = 178).  The fast path is taken only when
+// fl(amax * fl(1 / d)) < 127.5, so all of its codes lie in [-127, 127]
+// already; every other block (all blocks with 1 / d overflowing among them)
+// takes the exact quotient and clamps it.
 constexpr float kMagicRne = 12582912.0f;            // 1.5 * 2^23
 constexpr float kTieMargin = 0.49993896484375f;     // 0.5 - 2^-14
 
@@ -216,7 +223,7 @@ __device__ __forceinline__ void quantize_block_values(const float (&v)[N], int8_
     uint32_t bits[N];  // low byte: the code
     if (db != 0.0f) {
         const float rcp = __frcp_rn(db);
-        bool safe = amax * rcp <= 128.0f;
+        bool safe = amax * rcp < 127.5f;
         const uint64_t rcp2 = f32x2_pack(rcp, rcp);
         const uint64_t magic2 = f32x2_pack(kMagicRne, kMagicRne), unmagic2 = f32x2_pack(-kMagicRne, -kMagicRne);
 #pragma unroll
@@ -229,16 +236,15 @@ __device__ __forceinline__ void quantize_block_values(const float (&v)[N], int8_
             bits[i] = __float_as_uint(mm.x);
             bits[i + 1] = __float_as_uint(mm.y);
         }
-        if (!safe) {  // rare: some quotient lies too close to a rounding boundary
+        if (!safe) {  // rare: a quotient near a rounding boundary, or a subnormal d
 #pragma unroll
-            for (int i = 0; i < N; ++i) bits[i] = __float_as_uint(rintf(__fdiv_rn(v[i], db)) + kMagicRne);
+            for (int i = 0; i < N; ++i)
+                bits[i] = __float_as_uint(fminf(fmaxf(rintf(__fdiv_rn(v[i], db)), -127.0f), 127.0f) + kMagicRne);
         }
     } else {
 #pragma unroll
         for (int i = 0; i < N; ++i) bits[i] = 0u;
     }
-    // |x / d| <= 127 (1 + 2^-23) for every x of the block, so every code is
-    // already within [-127, 127]: the clamp of the definition never binds.
     uint32_t packed[N / 4];
     int s = 0;
 #pragma unroll

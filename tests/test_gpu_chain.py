@@ -90,6 +90,26 @@ def test_chain_against_oracle():
     assert np.all(err <= 1e-4 * absdot)
 
 
+def test_chain_quantises_subnormal_scale_blocks_like_the_oracle():
+    """A chain job over an activation whose block scales are f32 subnormals (the
+    codes clamp to +-127): same int8 codes as the oracle, so the same y as the
+    two-step path with the oracle-checked standalone quantiser."""
+    from tests.test_gpu_parity import subnormal_scale_activation
+    fmt, rows = synth.Q4_K, 96
+    x = subnormal_scale_activation(128, seed=9)
+    cols = x.shape[1]
+    W = dev(synth.weights(fmt, rows, cols, seed=510))
+    a = qx.qx_quantize_act_q8(dev(x))
+    q, d, s = oracle.quantize_act_q8(x)
+    torch.cuda.synchronize()
+    assert np.array_equal(a.q.cpu().numpy(), q) and np.array_equal(a.sum.cpu().numpy(), s)
+    y_two_step = qx.qx_gemv(fmt, W, rows, cols, a, mode=qx.QX_MODE_W4A8)
+    job = qx.GemvJob(fmt, [W], [rows], cols, dev(x[0]))
+    qx.qx_gemv_chain([job], qx.chain_scratch(1))
+    assert np.array_equal(bits(job.y[0]), bits(y_two_step))
+    assert qx.qx_device_check() == qx.QX_OK
+
+
 def test_chain_argument_errors():
     W = torch.zeros(144 * 4, dtype=torch.uint8, device="cuda")
     x = torch.zeros(256, dtype=torch.float32, device="cuda")

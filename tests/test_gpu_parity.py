@@ -70,7 +70,40 @@ def test_actq8_special_values():
     x[0, 97:103] = np.array([2.5, 3.5, -2.5, 0.5, 1.5, -126.5]) / 8
     x[0, 128:160] = -3.0                  # constant block
     x[0, 160:192] = np.float32(1e-30) * np.arange(32)
-    quantize_both(x)
+    # subnormal scales: amax = 178 and 383 times 2^-149 give d = 1 and 3 times
+    # 2^-149, so x / d reaches 178 and 127.7; the codes clamp to +-127
+    sub = lambda k: np.array([k], np.uint32).view(np.float32)[0]
+    x[0, 192:196] = [sub(178), -sub(178), sub(50), -sub(3)]
+    x[0, 224:228] = [sub(383), sub(192), sub(190), -sub(383)]
+    a, q, d, s = quantize_both(x)
+    assert list(q[0, 192:196]) == [127, -127, 50, -3] and list(q[0, 224:228]) == [127, 64, 63, -127]
+
+
+def subnormal_scale_activation(nblocks: int, seed: int) -> np.ndarray:
+    """Blocks whose scale d = amax / 127 is an f32 subnormal, amax swept from the
+    smallest subnormal up to 127 * 2^-126 (so d passes through every subnormal
+    precision); there x / d can exceed 127 and the clamp decides the code."""
+    rng = np.random.default_rng(seed)
+    top = int(np.array([np.float32(127.0 * 2.0 ** -126)], np.float32).view(np.uint32)[0])
+    first = np.arange(1, nblocks // 2 + 1)
+    rest = np.exp(rng.uniform(np.log(nblocks // 2 + 1), np.log(top), nblocks - first.size)).astype(np.int64)
+    amax = np.concatenate([first, rest]).astype(np.uint32).view(np.float32)
+    x = (rng.uniform(-1, 1, (nblocks, 32)) * amax[:, None]).astype(np.float32)
+    col = rng.integers(0, 32, nblocks)
+    sign = np.where(rng.integers(0, 2, nblocks) == 1, 1, -1).astype(np.float32)
+    x[np.arange(nblocks), col] = sign * amax
+    return x.reshape(1, -1)
+
+
+def test_actq8_subnormal_scales_clamp():
+    x = subnormal_scale_activation(4096, seed=8)
+    a, q, d, s = quantize_both(x)
+    assert np.abs(q.astype(np.int32)).max() == 127
+    # the sweep reaches blocks where the clamp binds (and, at its low end, blocks
+    # whose scale underflows to 0)
+    xb, dd = x.reshape(-1, 32).astype(np.float64), d.reshape(-1).astype(np.float64)
+    live = dd > 0
+    assert np.any(np.abs(xb[live] / dd[live, None]) >= 127.5) and np.any(~live)
 
 
 def near_tie_activation(nblocks: int, seed: int) -> np.ndarray:
@@ -96,10 +129,13 @@ def test_actq8_near_ties_bit_exact():
 
 # 4096 columns: two lanes per block; 2048: four; 896: eight (narrow activations)
 @pytest.mark.parametrize("nblocks", [128, 64, 28])
-def test_fused_quantisation_near_ties(nblocks):
-    """In-kernel quantisation of near-tie activations matches the standalone kernel."""
+@pytest.mark.parametrize("kind", ["near_ties", "subnormal_scales"])
+def test_fused_quantisation_hard_blocks(nblocks, kind):
+    """In-kernel quantisation of near-tie and subnormal-scale activations matches
+    the standalone kernel (itself bit-exact against the oracle)."""
     fmt, rows = synth.Q8_0, 64
-    x = near_tie_activation(nblocks, seed=6 + nblocks)
+    gen = near_tie_activation if kind == "near_ties" else subnormal_scale_activation
+    x = gen(nblocks, seed=6 + nblocks)
     cols = x.shape[1]
     W = dev(synth.weights(fmt, rows, cols, seed=7))
     a, q, d, s = quantize_both(x)

@@ -32,6 +32,9 @@ MUTATIONS = [
     ("act quant scale 1/128", "amax / 127.0f", "amax / 128.0f"),
     ("act quant multiplies by the reciprocal", "nearbyintf(xb[i] / db)", "nearbyintf(xb[i] * (1.0f / db))"),
     ("act quant block sum of magnitudes", "s += v;", "s += v < 0 ? -v : v;"),
+    ("act quant clamp dropped", "v = r > 127.0f ? 127 : (r < -127.0f ? -127 : (int)r);", "v = (int)r;"),
+    ("act quant clamp at 128", "v = r > 127.0f ? 127 : (r < -127.0f ? -127 : (int)r);",
+     "v = r > 128.0f ? 128 : (r < -128.0f ? -128 : (int)r);"),
     ("gemv reversed activation index", "acc += w[i] * x[i];", "acc += w[i] * x[cols - 1 - i];"),
     ("w4a8 min term sign", "- f16_at(blk + 2) * m * dxg * (double)S", "+ f16_at(blk + 2) * m * dxg * (double)S"),
     ("w4a8 q6_k partial without -32", "qw = q6k_quant(blk, e0 + i) - 32;", "qw = q6k_quant(blk, e0 + i);"),

@@ -238,6 +238,28 @@ def test_quant_tiny_scale_underflows_to_zero():
     assert d[0, 0] == 0 and np.all(q == 0) and s[0, 0] == 0
 
 
+def test_quant_clamps_codes_of_subnormal_scales():
+    """Where d = fl(amax / 127) is an f32 subnormal it can be far below amax / 127,
+    so x / d exceeds 127 and the clamp to [-127, 127] decides the code.
+
+    Values worked by hand in units of u = 2^-149 (the smallest subnormal):
+      block 0: amax = 178u -> amax / 127 = 1.40u rounds to d = 1u;
+               x = 178u, -178u, 50u, -3u -> 178, -178 clamp to 127, -127; 50, -3 stay.
+      block 1: amax = 383u -> 3.016u rounds to d = 3u;
+               x = 383u -> 127.67 -> 128 clamps to 127; 192u -> 64; 190u -> 63.33 -> 63;
+               -383u -> -128 clamps to -127.
+    """
+    u = lambda k: np.array([k], np.uint32).view(np.float32)[0] if k >= 0 else -u(-k)
+    x = np.zeros((1, 64), np.float32)
+    x[0, 0:4] = [u(178), u(-178), u(50), u(-3)]
+    x[0, 32:36] = [u(383), u(192), u(190), u(-383)]
+    q, d, s = oracle.quantize_act_q8(x)
+    assert list(d[0].view(np.uint32)) == [1, 3]
+    assert list(q[0, 0:4]) == [127, -127, 50, -3] and np.all(q[0, 4:32] == 0)
+    assert list(q[0, 32:36]) == [127, 64, 63, -127] and np.all(q[0, 36:] == 0)
+    assert list(s[0]) == [47, 127]
+
+
 def test_quant_rejects_non_finite():
     x = np.zeros((1, 32), np.float32)
     x[0, 3] = np.inf
