@@ -30,9 +30,10 @@ def nvcc() -> str:
 
 
 def _deps() -> list[str]:
-    inc = os.path.join(os.path.dirname(HERE), "include", "qx.h")
+    inc_dir = os.path.join(os.path.dirname(HERE), "include")
+    inc = [os.path.join(inc_dir, f) for f in os.listdir(inc_dir) if f.endswith(".h")]
     hdrs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
-    return hdrs + [inc]
+    return hdrs + inc
 
 
 def _stale(target: str, sources: list[str]) -> bool:

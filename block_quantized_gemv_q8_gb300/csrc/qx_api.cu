@@ -12,6 +12,7 @@
 #include <tuple>
 
 #include "../../include/qx.h"
+#include "../../include/qx_debug.h"
 #include "qx_internal.h"
 
 namespace qx {
@@ -574,6 +575,41 @@ qx_status prefill_dispatch(qx_fmt fmt, const void* W, int64_t rows, int64_t cols
     return QX_OK;
 }
 
+// Validate a chain's jobs and copy them into the launch descriptor (shared by
+// qx_gemv_chain and qx_gemv_chain_noalloc); every check runs before any
+// device work.  p.n_jobs is set; the geometry is left to chain_geometry.
+qx_status marshal_chain(int n_jobs, const qx_gemv_job* jobs, ChainParams& p) {
+    if (n_jobs < 1 || n_jobs > QX_CHAIN_MAX_JOBS || !jobs) return QX_ERR_ARG;
+    std::memset(&p, 0, sizeof(p));
+    p.n_jobs = n_jobs;
+    qx_status st;
+    for (int j = 0; j < n_jobs; ++j) {
+        const qx_gemv_job& in = jobs[j];
+        if (in.n < 1 || in.n > QX_CHAIN_MAX_ENTRIES) return QX_ERR_ARG;
+        if (!in.x) return QX_ERR_ARG;
+        if (!aligned16(in.x)) return QX_ERR_ALIGN;
+        if (in.fmt == QX_Q6_K_SOA) return QX_ERR_FMT;  // the chain kernel reads the GGUF layouts
+        ChainJob& jb = p.job[j];
+        jb.fmt = in.fmt;
+        jb.n_entries = in.n;
+        jb.cols = in.cols;
+        jb.x = in.x;
+        int64_t total = 0;
+        for (int k = 0; k < in.n; ++k) {
+            if ((st = check_shape(in.fmt, in.rows[k], in.cols)) != QX_OK) return st;
+            if (!in.W[k] || !in.y[k]) return QX_ERR_ARG;
+            if (!aligned16(in.W[k]) || !aligned4(in.y[k])) return QX_ERR_ALIGN;
+            jb.e[k].W = static_cast<const uint8_t*>(in.W[k]);
+            jb.e[k].y = in.y[k];
+            jb.e[k].rows = in.rows[k];
+            jb.e[k].row0 = total;
+            total += in.rows[k];
+        }
+        jb.total_rows = total;
+    }
+    return QX_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -714,33 +750,8 @@ qx_status qx_gemv_chain(int n_jobs, const qx_gemv_job* jobs, void* scratch, qx_s
     if (n_jobs < 1 || n_jobs > QX_CHAIN_MAX_JOBS || !jobs || !scratch) return QX_ERR_ARG;
     if (!aligned4(scratch)) return QX_ERR_ALIGN;
     static thread_local ChainParams p;  // large (tens of KB): not on the stack
-    std::memset(&p, 0, sizeof(p));
-    p.n_jobs = n_jobs;
-    qx_status st;
-    for (int j = 0; j < n_jobs; ++j) {
-        const qx_gemv_job& in = jobs[j];
-        if (in.n < 1 || in.n > QX_CHAIN_MAX_ENTRIES) return QX_ERR_ARG;
-        if (!in.x) return QX_ERR_ARG;
-        if (!aligned16(in.x)) return QX_ERR_ALIGN;
-        if (in.fmt == QX_Q6_K_SOA) return QX_ERR_FMT;  // the chain kernel reads the GGUF layouts
-        ChainJob& jb = p.job[j];
-        jb.fmt = in.fmt;
-        jb.n_entries = in.n;
-        jb.cols = in.cols;
-        jb.x = in.x;
-        int64_t total = 0;
-        for (int k = 0; k < in.n; ++k) {
-            if ((st = check_shape(in.fmt, in.rows[k], in.cols)) != QX_OK) return st;
-            if (!in.W[k] || !in.y[k]) return QX_ERR_ARG;
-            if (!aligned16(in.W[k]) || !aligned4(in.y[k])) return QX_ERR_ALIGN;
-            jb.e[k].W = static_cast<const uint8_t*>(in.W[k]);
-            jb.e[k].y = in.y[k];
-            jb.e[k].rows = in.rows[k];
-            jb.e[k].row0 = total;
-            total += in.rows[k];
-        }
-        jb.total_rows = total;
-    }
+    qx_status st = marshal_chain(n_jobs, jobs, p);
+    if (st != QX_OK) return st;
     DeviceInfo* dev = nullptr;
     if ((st = device_info(&dev)) != QX_OK) return st;
     size_t smem = 0;
@@ -841,35 +852,10 @@ qx_status noalloc_counters(unsigned** out) {
 }  // namespace
 
 qx_status qx_gemv_chain_noalloc(int n_jobs, const qx_gemv_job* jobs, qx_stream_t s) {
-    if (n_jobs < 1 || n_jobs > kNoallocMaxJobs || !jobs) return QX_ERR_ARG;
+    if (n_jobs > kNoallocMaxJobs) return QX_ERR_ARG;  // the array's capacity
     static thread_local ChainParams p;  // large (tens of KB): not on the stack
-    std::memset(&p, 0, sizeof(p));
-    p.n_jobs = n_jobs;
-    qx_status st;
-    for (int j = 0; j < n_jobs; ++j) {
-        const qx_gemv_job& in = jobs[j];
-        if (in.n < 1 || in.n > QX_CHAIN_MAX_ENTRIES) return QX_ERR_ARG;
-        if (!in.x) return QX_ERR_ARG;
-        if (!aligned16(in.x)) return QX_ERR_ALIGN;
-        if (in.fmt == QX_Q6_K_SOA) return QX_ERR_FMT;  // the chain kernel reads the GGUF layouts
-        ChainJob& jb = p.job[j];
-        jb.fmt = in.fmt;
-        jb.n_entries = in.n;
-        jb.cols = in.cols;
-        jb.x = in.x;
-        int64_t total = 0;
-        for (int k = 0; k < in.n; ++k) {
-            if ((st = check_shape(in.fmt, in.rows[k], in.cols)) != QX_OK) return st;
-            if (!in.W[k] || !in.y[k]) return QX_ERR_ARG;
-            if (!aligned16(in.W[k]) || !aligned4(in.y[k])) return QX_ERR_ALIGN;
-            jb.e[k].W = static_cast<const uint8_t*>(in.W[k]);
-            jb.e[k].y = in.y[k];
-            jb.e[k].rows = in.rows[k];
-            jb.e[k].row0 = total;
-            total += in.rows[k];
-        }
-        jb.total_rows = total;
-    }
+    qx_status st = marshal_chain(n_jobs, jobs, p);
+    if (st != QX_OK) return st;
     DeviceInfo* dev = nullptr;
     if ((st = device_info(&dev)) != QX_OK) return st;
     size_t smem = 0;
@@ -884,6 +870,23 @@ qx_status qx_gemv_chain_noalloc(int n_jobs, const qx_gemv_job* jobs, qx_stream_t
     p.counters = counters;
     e = launch_chain(p, smem, cs);
     return e == cudaSuccess ? QX_OK : cuda_fail(e, "chain launch");
+}
+
+qx_status qx_debug_noalloc_fill(uint32_t value, qx_stream_t s) {
+    DeviceInfo* dev = nullptr;
+    qx_status st = device_info(&dev);
+    if (st != QX_OK) return st;
+    unsigned* counters = nullptr;
+    if ((st = noalloc_counters(&counters)) != QX_OK) return st;
+    const unsigned n = kNoallocMaxJobs + 1;
+    // a copy from host memory, then a synchronisation: a test hook, not a hot path
+    static thread_local unsigned host[kNoallocMaxJobs + 1];
+    for (unsigned i = 0; i < n; ++i) host[i] = value;
+    const cudaError_t e = cudaMemcpyAsync(counters, host, sizeof(host), cudaMemcpyHostToDevice,
+                                          reinterpret_cast<cudaStream_t>(s));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+    const cudaError_t e2 = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(s));
+    return e2 == cudaSuccess ? QX_OK : cuda_fail(e2, "cudaStreamSynchronize");
 }
 
 }  // extern "C"

@@ -10,6 +10,7 @@
 #include <cstdint>
 
 #include "../../include/qx.h"
+#include "../../include/qx_debug.h"
 
 namespace qx {
 

@@ -30,11 +30,15 @@
  *            w = d*sc*(q - 32).
  *       Q8_0 32 weights / 34 B: d f16, 32 int8 quants; w = d*q.
  *   - Every pointer named "device" is device memory owned by the caller.  The
- *     library keeps no per-call state; it caches one device-property query
- *     per device.  It allocates device memory in two places only: the
- *     prefill workspace of qx_gemm_prefill / qx_gemm_prefill_ex (paths 0 and
- *     3, grown on demand and kept per device; qx_gemm_prefill_ws takes the
- *     caller's instead) and the short-lived buffer of qx_debug_mma_rate.
+ *     library keeps no per-call state.  Per device it holds: one cached
+ *     device-property query, the device error word (below), and the
+ *     QX_CHAIN_MAX_JOBS + 1 arrival counters of qx_gemv_chain_noalloc (file-
+ *     scope device arrays, present on every GPU that loads the library).  It
+ *     allocates device memory in two places only: the prefill workspace of
+ *     qx_gemm_prefill / qx_gemm_prefill_ex (paths 0 and 3, grown on demand and
+ *     kept per device; qx_gemm_prefill_ws takes the caller's instead) and the
+ *     short-lived buffer of the measurement hook qx_debug_mma_rate
+ *     (qx_debug.h).
  *   - Calls are asynchronous on stream `s` (NULL = the legacy default stream)
  *     and run on the current device.  Argument, shape and alignment errors
  *     return before anything is launched or written; a failed launch returns
@@ -147,7 +151,13 @@ qx_status qx_gemv(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const v
 
 /*
  * n independent GEMVs over one activation in a single launch, e.g. the Q, K
- * and V projections, or gate and up: y[k] = W[k] . x for k in [0, n).
+ * and V projections, or gate and up: y[k] = W[k] . x for k in [0, n).  The
+ * activation is read (and in QX_MODE_W4A8_FUSED quantised) once for all n
+ * matrices: the pages quantise it to int8 once per matmul (llamay docs,
+ * "Backends and hardware", section "CPU"), and matrices that share one input
+ * are one matmul over their stacked rows, whose rows are independent
+ * (llambda.lisp README, "Features & Architecture": the GEMV's outer loop runs
+ * in parallel with isolated writes).
  * fmt, W, rows and y are host arrays of n entries; W[k] and y[k] are device
  * pointers.  All entries share cols, x and mode; 1 <= n <= QX_MAX_MULTI.
  * Entries of different formats are run as one launch per format.
@@ -322,21 +332,6 @@ qx_status qx_repack(qx_fmt from, qx_fmt to, const void* src, int64_t rows, int64
  * current device: QX_OK, QX_ERR_DEVICE_TIMEOUT if a kernel's bounded wait ran
  * out since the last check, or QX_ERR_CUDA if the synchronisation failed. */
 qx_status qx_device_check(qx_stream_t s);
-
-/* Test hook: launch one CTA that waits on a barrier nothing will complete,
- * with a wait limit of `limit_ns` nanoseconds (1 ms .. 10 s), so that the
- * bounded-wait path runs without any fault.  qx_device_check() then returns
- * QX_ERR_DEVICE_TIMEOUT. */
-qx_status qx_debug_timeout_probe(uint64_t limit_ns, qx_stream_t s);
-
-/* Measurement hook (no counterpart on the pages): the device's warp-level
- * tensor-core rate, multiply-adds x 2 per second, of mma.sync int8
- * m16n8k32 (kind 0) or f16 m16n8k16 with an f32 accumulator (kind 1), run
- * from registers by every SM; sm_103a has no int8 tcgen05 MMA, so kind 0 is
- * the int8 tensor rate a prefill can use.  It allocates and frees a small
- * device buffer and synchronises stream s: not for use inside a graph
- * capture.  QX_ERR_ARG for a null out pointer or another kind. */
-qx_status qx_debug_mma_rate(int kind, double* ops_per_s, qx_stream_t s);
 
 /* Static, NUL-terminated strings. */
 const char* qx_status_string(qx_status st);

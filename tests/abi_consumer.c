@@ -1,4 +1,4 @@
-/* A plain C99 consumer of include/qx.h: the header compiles as C, the library
+/* A plain C99 consumer of include/qx.h and include/qx_debug.h: the header compiles as C, the library
  * links and loads from C, and the calls that need no GPU behave as declared
  * (row sizes, status strings, version, argument errors returned before any
  * device work).  Built and run by tests/test_abi.py, also against a build of
@@ -10,6 +10,7 @@
 #include <string.h>
 
 #include "qx.h"
+#include "qx_debug.h"
 
 static int failures = 0;
 

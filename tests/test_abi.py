@@ -1,4 +1,4 @@
-"""The C-ABI library loads, exports every entry point declared in include/qx.h,
+"""The C-ABI library loads, exports every entry point declared in include/*.h,
 and rejects bad arguments on the host before any launch (no GPU needed)."""
 import ctypes
 import os
@@ -17,10 +17,22 @@ def lib():
     return qx.lib()
 
 
-def declared_functions():
-    text = open(os.path.join(ROOT, "include", "qx.h")).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(qx_[a-z0-9_]+)\s*\(", text)))
+def declared_functions(header=None):
+    """qx_* functions declared in one header, or in every header of include/."""
+    inc = os.path.join(ROOT, "include")
+    names = [header] if header else sorted(f for f in os.listdir(inc) if f.endswith(".h"))
+    found = set()
+    for h in names:
+        text = re.sub(r"/\*.*?\*/", "", open(os.path.join(inc, h)).read(), flags=re.S)
+        found |= set(re.findall(r"\b(qx_[a-z0-9_]+)\s*\(", text))
+    return sorted(found)
+
+
+def test_product_header_declares_no_debug_hooks():
+    """Test and measurement hooks live in qx_debug.h, apart from the product calls."""
+    product, debug = declared_functions("qx.h"), declared_functions("qx_debug.h")
+    assert not [n for n in product if n.startswith("qx_debug")]
+    assert debug and all(n.startswith("qx_debug") for n in debug)
 
 
 def test_header_declares_the_entry_points():
@@ -32,7 +44,7 @@ def test_header_declares_the_entry_points():
 
 def test_every_declared_symbol_is_exported(lib):
     for n in declared_functions():
-        assert hasattr(lib, n), f"{n} declared in qx.h but not exported by libqx.so"
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported by libqx.so"
     assert set(qx.EXPORTS) <= set(declared_functions())
 
 

@@ -74,6 +74,32 @@ def test_noalloc_chain_matches_chain_with_scratch(lib):
                 assert np.all(err <= TOL * absdot[j][k]), f"call {call} job {j} entry {k}: max err {err.max()}"
 
 
+@pytest.mark.parametrize("left_over", [1, 152, 0x7FFFFFFF])
+def test_noalloc_chain_starts_from_stale_counters(lib, left_over):
+    """The library's counter array keeps whatever the last call left (a chain
+    stopped by a wait that ran out leaves counts behind).  Fill it with such
+    values, then run the entry point: it clears the counters itself, so the
+    outputs match qx_gemv_chain with fresh caller scratch, bit for bit."""
+    specs = [(synth.Q4_K, [256, 64], 2048), (synth.Q8_0, [96], 896), (synth.Q6_K, [40], 4096)]
+    jobs, again = [], []
+    for i, (fmt, rows, cols) in enumerate(specs):
+        Ws = [dev(synth.weights(fmt, r, cols, seed=1200 + 10 * i + k)) for k, r in enumerate(rows)]
+        x = dev(synth.activation(1, cols, seed=1250 + i)[0])
+        jobs.append(qx.GemvJob(fmt, Ws, rows, cols, x))
+        again.append(qx.GemvJob(fmt, Ws, rows, cols, x))
+    qx.qx_gemv_chain(jobs, qx.chain_scratch(len(jobs)))
+    qx.qx_debug_noalloc_fill(left_over)
+    for job in again:
+        job.y = [torch.full((r,), float("nan"), dtype=torch.float32, device="cuda") for r in job.rows]
+    stream = torch.cuda.current_stream()
+    arr = qx.make_chain(again)
+    assert lib.qx_gemv_chain_noalloc(len(arr), arr, ctypes.c_void_p(stream.cuda_stream)) == qx.QX_OK
+    assert qx.qx_device_check(stream) == qx.QX_OK
+    for a, b in zip(jobs, again):
+        for ya, yb in zip(a.y, b.y):
+            assert torch.equal(ya.view(torch.int32), yb.view(torch.int32))
+
+
 def test_noalloc_chain_rejects_too_many_jobs(lib):
     W = torch.zeros(144 * 4, dtype=torch.uint8, device="cuda")
     x = torch.zeros(256, dtype=torch.float32, device="cuda")
