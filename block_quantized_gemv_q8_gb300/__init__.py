@@ -31,7 +31,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libqx.so")
 EXPORTS = ["qx_quantize_act_q8", "qx_gemv", "qx_gemv_multi", "qx_gemm_prefill", "qx_gemm_prefill_ex",
            "qx_gemm_prefill_ws", "qx_gemm_prefill_workspace_bytes", "qx_gemv_partials", "qx_gemv_chain", "qx_gemv_chain_noalloc", "qx_gemv_chain_scratch_bytes", "qx_row_bytes", "qx_repack",
            "qx_device_check", "qx_debug_timeout_probe", "qx_debug_mma_rate", "qx_debug_noalloc_fill",
-           "qx_status_string", "qx_last_error", "qx_version"]
+           "qx_debug_trace_read", "qx_status_string", "qx_last_error", "qx_version"]
 
 
 class QxError(RuntimeError):
@@ -84,6 +84,7 @@ def lib() -> ctypes.CDLL:
         L.qx_debug_mma_rate.argtypes = [I, ctypes.POINTER(ctypes.c_double), P]
         L.qx_debug_timeout_probe.argtypes = [ctypes.c_uint64, P]
         L.qx_debug_noalloc_fill.argtypes = [ctypes.c_uint32, P]
+        L.qx_debug_trace_read.argtypes = [P, ctypes.c_size_t]
         L.qx_status_string.argtypes = [I]
         L.qx_status_string.restype = ctypes.c_char_p
         L.qx_last_error.argtypes = []
@@ -93,7 +94,8 @@ def lib() -> ctypes.CDLL:
         for n in ("qx_quantize_act_q8", "qx_gemv", "qx_gemv_multi", "qx_gemm_prefill", "qx_gemm_prefill_ex",
                   "qx_gemm_prefill_ws", "qx_gemv_partials", "qx_gemv_chain", "qx_gemv_chain_noalloc",
                   "qx_device_check", "qx_debug_timeout_probe",
-                  "qx_repack", "qx_debug_mma_rate", "qx_debug_noalloc_fill"):
+                  "qx_repack", "qx_debug_mma_rate", "qx_debug_noalloc_fill",
+                  "qx_debug_trace_read"):
             getattr(L, n).restype = I
         _lib = L
     return _lib

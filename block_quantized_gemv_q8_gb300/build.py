@@ -20,6 +20,9 @@ LIB = os.path.join(HERE, "libqx.so")
 SOURCES = ["qx_api.cu", "qx_actq8.cu", "qx_gemv.cu", "qx_chain.cu", "qx_prefill.cu", "qx_tc.cu", "qx_repack.cu", "qx_mma_rate.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"] + ARCH
+# Extra defines for measurement sweeps of the launch geometry (e.g.
+# QX_NVCC_DEFINES="QX_STAGE_KB=24 QX_INFLIGHT_KB=48"); empty in normal builds.
+NVCC_FLAGS += ["-D" + d for d in os.environ.get("QX_NVCC_DEFINES", "").split()]
 
 
 def nvcc() -> str:

@@ -24,7 +24,33 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;  // 2 s bound on every pipeline wait
-constexpr size_t kStageTargetBytes = 48 * 1024;
+// Build-time knobs for measurement sweeps (defaults are the shipped values).
+// In-flight cap: with every SM streaming, the latency of every other load an
+// SM makes (activation, parameters, the next kernel's first accesses) grows
+// with the bytes queued in the memory system -- 0.2 us at 32 KB per SM, 0.3
+// us at 64 KB, 0.85 us at 192 KB (GB300, L2-resident pointer chase beside a
+// bulk-copy stream), while the stream itself needs only about 64 KB per SM to
+// run at full rate.  A streaming GEMV CTA (two per SM) therefore keeps one
+// stage in flight (Llama-3.1-8B decode step 1.167 -> 1.135 ms, same box;
+// smaller stages were slower: the per-stage hand-offs cost more).
+#ifndef QX_STAGE_KB
+#define QX_STAGE_KB 48
+#endif
+#ifndef QX_INFLIGHT_KB
+#define QX_INFLIGHT_KB 48
+#endif
+#ifndef QX_PREWAIT_KB
+#define QX_PREWAIT_KB 0
+#endif
+constexpr size_t kStageTargetBytes = size_t(QX_STAGE_KB) * 1024;
+// Most bytes a streaming CTA keeps in flight (0: no cap beyond the ring).
+constexpr size_t kInflightBytes = size_t(QX_INFLIGHT_KB) * 1024;
+#ifndef QX_CHAIN_INFLIGHT_KB
+#define QX_CHAIN_INFLIGHT_KB 0
+#endif
+constexpr size_t kChainInflightBytes = size_t(QX_CHAIN_INFLIGHT_KB) * 1024;
+// Bytes a large launch fetches before its dependency resolves (0: one stage).
+constexpr size_t kPrewaitBytes = size_t(QX_PREWAIT_KB) * 1024;
 // Shared memory of a CTA that leaves room for a second one on the SM.
 constexpr size_t kHalfSmBytes = 110 * 1024;
 // Automatic prefill path (measured on GB300, X [m, 4096] x Q4_K [14336,
@@ -33,8 +59,11 @@ constexpr size_t kHalfSmBytes = 110 * 1024;
 // against 18.7, 33.0, 61.9, 121.4 us row by row and about 60 us on
 // tcgen05); the tcgen05 GEMM above (m = 64: 61.8 us against 197 us).
 constexpr int64_t kPrefillBatchMaxRows = 16;
-// Shared memory of a chain CTA (one per SM).
+// Shared memory of a chain CTA (one per SM): the ring, partial sums and
+// activation within kChainSmBytes, and all of it with the job descriptors
+// within kChainMaxSmem.
 constexpr size_t kChainSmBytes = 200 * 1024;
+constexpr size_t kChainMaxSmem = 227 * 1024;
 constexpr int kMaxStageRows = 256;
 // Launch bytes per SM up to which a PDL launch runs one CTA per SM.
 constexpr int64_t kOneCtaPerSmBytes = 192 * 1024;
@@ -273,6 +302,12 @@ qx_status gemv_geometry(int fmt, int kmode, bool partials, bool fused, bool pdl,
     // step: 1.217 ms against 1.230 ms with one stage everywhere, 1.241 ms
     // with the whole ring everywhere).
     p.prewait = small ? stages : 1;
+    if (!small && kPrewaitBytes > 0)
+        p.prewait = std::max(1, std::min(stages, static_cast<int>(kPrewaitBytes / slot)));
+    // the cap is per CTA at two CTAs per SM; a CTA alone on its SM keeps twice as much in flight
+    const size_t inflight_cta = kInflightBytes * (want == 1 || per_sm < 2 ? 2 : 1);
+    p.inflight = kInflightBytes > 0 ? std::max(1, static_cast<int>(inflight_cta / slot)) : 0;
+    if (p.inflight >= stages) p.inflight = 0;
     const int64_t max_cta = int64_t(dev.sm_count) * (per_sm < want ? per_sm : want);
     const int64_t groups = (p.total_rows + g.quantum - 1) / g.quantum;
     p.cols = cols;
@@ -315,9 +350,12 @@ qx_status chain_geometry(const DeviceInfo& dev, ChainParams& p, size_t& smem) {
     }
     const size_t slot = (max_stage + kSlotPad + 127) / 128 * 128;
     const size_t act = (size_t(max_cols) + size_t(max_cols / 32) * 8 + 15) / 16 * 16;
+    const size_t jobs_bytes = size_t(p.n_jobs) * (sizeof(ChainJob) + 2 * sizeof(int64_t));
     const auto bytes_for = [&](int st) { return size_t(st) * (slot + 24 + red_slot * 4) + 16 + act; };
+    // the ring takes what the job descriptors leave of the budget
+    const size_t ring_budget = std::min(kChainSmBytes, size_t(kChainMaxSmem) - jobs_bytes - 64);
     int stages = 2;
-    while (stages < 8 && bytes_for(stages + 1) <= kChainSmBytes) ++stages;
+    while (stages < 8 && bytes_for(stages + 1) <= ring_budget) ++stages;
     p.stages = stages;
     p.slot_bytes = static_cast<int>(slot);
     p.red_slot_floats = static_cast<int>(red_slot);
@@ -325,13 +363,17 @@ qx_status chain_geometry(const DeviceInfo& dev, ChainParams& p, size_t& smem) {
     p.bar_off = static_cast<int>(size_t(stages) * slot);
     p.red_off = static_cast<int>((size_t(p.bar_off) + 24 * size_t(stages) + 15) / 16 * 16);
     p.act_off = static_cast<int>((size_t(p.red_off) + size_t(stages) * red_slot * 4 + 15) / 16 * 16);
-    smem = size_t(p.act_off) + act;
+    p.jobs_off = static_cast<int>((size_t(p.act_off) + act + 15) / 16 * 16);
+    p.ranges_off = static_cast<int>(size_t(p.jobs_off) + size_t(p.n_jobs) * sizeof(ChainJob));
+    smem = size_t(p.jobs_off) + jobs_bytes;
     if (smem > 227 * 1024) return QX_ERR_SHAPE;
     int per_sm = 0;
     const cudaError_t e = chain_max_ctas_per_sm(smem, &per_sm);
     if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
     if (per_sm < 1) return cuda_fail(cudaErrorInvalidConfiguration, "no CTA fits on an SM");
     p.n_cta = dev.sm_count;  // one CTA per SM (the kernel is built for one)
+    p.inflight = kChainInflightBytes > 0 ? std::max(1, static_cast<int>(kChainInflightBytes / slot)) : 0;
+    if (p.inflight >= stages) p.inflight = 0;
     p.err = dev.err_word;
     p.wait_ns = kDefaultWaitNs;
     return QX_OK;
@@ -887,6 +929,12 @@ qx_status qx_debug_noalloc_fill(uint32_t value, qx_stream_t s) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
     const cudaError_t e2 = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(s));
     return e2 == cudaSuccess ? QX_OK : cuda_fail(e2, "cudaStreamSynchronize");
+}
+
+qx_status qx_debug_trace_read(void* host, size_t bytes) {
+    if (!host) return QX_ERR_ARG;
+    const cudaError_t e = chain_trace_read(host, bytes);
+    return e == cudaSuccess ? QX_OK : cuda_fail(e, "trace read (library built without QX_TRACE?)");
 }
 
 }  // extern "C"

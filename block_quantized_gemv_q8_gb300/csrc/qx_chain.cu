@@ -30,6 +30,17 @@ namespace {
 using namespace lanes;
 constexpr int NW = kChainConsumerWarps;
 
+#ifdef QX_TRACE
+// Measurement builds only: %globaltimer stamps per (CTA, job, event).
+constexpr int kTraceCtas = 160, kTraceEvents = 12;
+__device__ unsigned long long g_trace[kTraceCtas * QX_CHAIN_MAX_JOBS * kTraceEvents];
+__device__ __forceinline__ void stamp(int j, int ev) {
+    if (blockIdx.x < kTraceCtas) g_trace[(blockIdx.x * QX_CHAIN_MAX_JOBS + j) * kTraceEvents + ev] = global_timer_ns();
+}
+#else
+__device__ __forceinline__ void stamp(int, int) {}
+#endif
+
 // First row of CTA i in a job: an even split rounded down within its entry
 // to a multiple of the alignment quantum (as in the single-launch kernel).
 __device__ __forceinline__ int64_t job_row_begin(const ChainJob& j, int n_cta, int i) {
@@ -98,19 +109,26 @@ struct Ring {
 // producer walks the same sequence).  Returns false if a wait ran out.
 template <int FMT>
 __device__ __forceinline__ bool run_job(const ChainParams& p, const ChainJob& jb, int jidx, int& k, const Ring& rg,
-                                        const int8_t* q, const float* d, const int32_t* s, int warp, int lane) {
+                                        const int8_t* q, const float* d, const int32_t* s, const Team& tm,
+                                        const int64_t* range, int lane) {
     using LaneT = Lane<FMT, QX_MODE_W4A8>;
     static_assert(LaneT::kRows == gemv_rows_per_call(FMT, QX_MODE_W4A8), "row count must match the host geometry");
-    const Team tm = make_team(warp, lane, jb.team_lanes, jb.team_warps, jb.nteams, jb.L);
+    if (threadIdx.x == 0) stamp(jidx, 8);
     LaneT X;
     if (tm.active) X.load(q, d, s, tm.slice, FMT != QX_Q8_0);  // slices permuted in shared memory
+    if (threadIdx.x == 0) stamp(jidx, 9);
     const uint32_t rb = static_cast<uint32_t>(jb.row_bytes);
-    JobWalker wk{job_row_begin(jb, p.n_cta, blockIdx.x), job_row_begin(jb, p.n_cta, blockIdx.x + 1), 0};
+    JobWalker wk{range[0], range[1], 0};
+    if (threadIdx.x == 0) stamp(jidx, 10);
     int e, nrows;
     int64_t lrow;
+    bool first = true;
     while (wk.next(jb, e, lrow, nrows)) {
         const int slot = k % rg.S;
+        if (first && threadIdx.x == 0) stamp(jidx, 11);
         if (!mbar_wait_bounded(&rg.full[slot], (k / rg.S) & 1, p.wait_ns, p.err, kErrTimeoutFull)) return false;
+        if (first && threadIdx.x == 0) stamp(jidx, 4);
+        first = false;
         const uint8_t* sbuf = rg.smem + size_t(slot) * rg.slot_bytes;
         consume_stage<FMT, QX_MODE_W4A8, false>(X, tm, sbuf, nrows, rb, rg.red + size_t(slot) * rg.red_slot_floats,
                                                 jb.RS, nullptr, 0);
@@ -121,7 +139,6 @@ __device__ __forceinline__ bool run_job(const ChainParams& p, const ChainJob& jb
         }
         ++k;
     }
-    (void)jidx;
     return true;
 }
 
@@ -151,6 +168,26 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
         abort_flag = 0;
         fence_barrier_init();
     }
+    // The job descriptors, copied once from the launch parameters into shared
+    // memory: read from the parameter space, every job's first use would miss
+    // the constant cache on each boundary's critical path (a few dependent
+    // round trips to L2 while the weight stream loads it).
+    ChainJob* jobs = reinterpret_cast<ChainJob*>(smem + p.jobs_off);
+    {
+        const uint4* src = reinterpret_cast<const uint4*>(&p.job[0]);
+        uint4* dst = reinterpret_cast<uint4*>(jobs);
+        const int words = p.n_jobs * int(sizeof(ChainJob) / 16);
+        for (int i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
+    }
+    // This CTA's row range of every job, [ranges[2j], ranges[2j + 1]), also
+    // once at kernel start: the 64-bit divisions behind it would otherwise
+    // sit on every job boundary of every role.
+    int64_t* ranges = reinterpret_cast<int64_t*>(smem + p.ranges_off);
+    for (int j = threadIdx.x; j < p.n_jobs; j += blockDim.x) {
+        const ChainJob& jb = p.job[j];
+        ranges[2 * j] = job_row_begin(jb, p.n_cta, blockIdx.x);
+        ranges[2 * j + 1] = job_row_begin(jb, p.n_cta, blockIdx.x + 1);
+    }
     __syncthreads();
 
     if (warp == NW) {
@@ -161,10 +198,11 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
         unsigned tail_slots = 0;
         bool ok = true;
         for (int j = 0; j < p.n_jobs && ok; ++j) {
-            const ChainJob& jb = p.job[j];
-            JobWalker wk{job_row_begin(jb, p.n_cta, blockIdx.x), job_row_begin(jb, p.n_cta, blockIdx.x + 1), 0};
+            const ChainJob& jb = jobs[j];
+            JobWalker wk{ranges[2 * j], ranges[2 * j + 1], 0};
             int e, nrows;
             int64_t lrow;
+            bool first = true;
             while (wk.next(jb, e, lrow, nrows)) {
                 const int slot = k % rg.S;
                 if (k >= rg.S &&
@@ -172,6 +210,18 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
                     ok = false;
                     break;
                 }
+                // at most p.inflight stages issued and not landed (0: the ring's
+                // depth); stage k - p.inflight's slot is not reused before stage
+                // k, so the parity is that stage's
+                if (p.inflight > 0 && p.inflight < rg.S && k >= p.inflight) {
+                    const int q = k - p.inflight;
+                    if (!mbar_wait_bounded(&rg.full[q % rg.S], (q / rg.S) & 1, p.wait_ns, p.err, kErrTimeoutFull)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (first) stamp(j, 0);
+                first = false;
                 const uint8_t* src = jb.e[e].W + lrow * jb.row_bytes;
                 const uint32_t bytes = static_cast<uint32_t>(int64_t(nrows) * jb.row_bytes);
                 const uint32_t abytes = bytes & ~15u;
@@ -187,6 +237,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
                 if (abytes) bulk_g2s_evict_first(dst, src, abytes, &rg.full[slot], policy);
                 issued = ++k;
             }
+            stamp(j, 1);
         }
         for (int kk = issued > rg.S ? issued - rg.S : 0; kk < issued; ++kk)
             mbar_wait_bounded(&rg.full[kk % rg.S], (kk / rg.S) & 1, p.wait_ns, p.err, kErrTimeoutDrain);
@@ -198,8 +249,8 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
         int k = 0;
         bool ok = true;
         for (int j = 0; j < p.n_jobs && ok; ++j) {
-            const ChainJob& jb = p.job[j];
-            JobWalker wk{job_row_begin(jb, p.n_cta, blockIdx.x), job_row_begin(jb, p.n_cta, blockIdx.x + 1), 0};
+            const ChainJob& jb = jobs[j];
+            JobWalker wk{ranges[2 * j], ranges[2 * j + 1], 0};
             int e, nrows;
             int64_t lrow;
             while (wk.next(jb, e, lrow, nrows)) {
@@ -214,10 +265,16 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
                 ++k;
             }
             if (!ok) break;
-            // every y of job j from this CTA is written: count the CTA
-            __threadfence();
+            if (lane == 0) stamp(j, 6);
+            // every y of job j from this CTA is written: count the CTA.  The
+            // warp barrier orders every lane's y stores before lane 0's
+            // release, which makes them visible at GPU scope before the count
+            // (release is cumulative).
             __syncwarp();
-            if (lane == 0) arrive_release_gpu(&p.counters[j]);
+            if (lane == 0) {
+                arrive_release_gpu(&p.counters[j]);
+                stamp(j, 7);
+            }
         }
         if (ok && lane == 0) {
             // the last CTA to finish the chain resets the counters for the next
@@ -237,26 +294,37 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
     float* sd = reinterpret_cast<float*>(sq + p.max_cols);
     int32_t* ss = reinterpret_cast<int32_t*>(sd + p.max_cols / 32);
     int k = 0;
+    // the team layout of the previous job, rebuilt only when a job's differs
+    Team tm = make_team(warp, lane, jobs[0].team_lanes, jobs[0].team_warps, jobs[0].nteams, jobs[0].L);
     for (int j = 0; j < p.n_jobs; ++j) {
-        const ChainJob& jb = p.job[j];
+        const ChainJob& jb = jobs[j];
         if (j > 0) {
             // job j may read job j - 1's output: wait for every CTA to finish it
             if (threadIdx.x == 0 && !wait_count(&p.counters[j - 1], unsigned(p.n_cta), p.wait_ns, p.err))
                 abort_flag = 1;
+            if (threadIdx.x == 0) stamp(j, 2);
             consumer_barrier<NW>();
             if (abort_flag) break;
+        } else if (threadIdx.x == 0) {
+            stamp(j, 2);
         }
         const int nblk = static_cast<int>(jb.cols / 32);
         quantize_all<2>(jb.x, nblk, threadIdx.x, NW * 32, sq, sd, ss, jb.fmt != QX_Q8_0);
         consumer_barrier<NW>();
+        if (threadIdx.x == 0) stamp(j, 3);
+        if (jb.team_lanes != tm.team_lanes || jb.team_warps != tm.team_warps || jb.nteams != tm.nteams ||
+            jb.L != tm.L)
+            tm = make_team(warp, lane, jb.team_lanes, jb.team_warps, jb.nteams, jb.L);
+        const int64_t* rj = ranges + 2 * j;
         bool jok;
         switch (jb.fmt) {
-            case QX_Q4_K: jok = run_job<QX_Q4_K>(p, jb, j, k, rg, sq, sd, ss, warp, lane); break;
-            case QX_Q6_K: jok = run_job<QX_Q6_K>(p, jb, j, k, rg, sq, sd, ss, warp, lane); break;
-            default: jok = run_job<QX_Q8_0>(p, jb, j, k, rg, sq, sd, ss, warp, lane); break;
+            case QX_Q4_K: jok = run_job<QX_Q4_K>(p, jb, j, k, rg, sq, sd, ss, tm, rj, lane); break;
+            case QX_Q6_K: jok = run_job<QX_Q6_K>(p, jb, j, k, rg, sq, sd, ss, tm, rj, lane); break;
+            default: jok = run_job<QX_Q8_0>(p, jb, j, k, rg, sq, sd, ss, tm, rj, lane); break;
         }
         if (!jok) abort_flag = 1;
         consumer_barrier<NW>();  // every consumer has loaded its slice: the activation area may be rewritten
+        if (threadIdx.x == 0) stamp(j, 5);
         if (abort_flag) break;
     }
 }
@@ -285,6 +353,17 @@ cudaError_t chain_max_ctas_per_sm(size_t smem, int* out) {
     cudaError_t err = configure_chain_once();
     if (err != cudaSuccess) return err;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, gemv_chain_kernel, kChainThreads, smem);
+}
+
+cudaError_t chain_trace_read(void* host, size_t bytes) {
+#ifdef QX_TRACE
+    if (bytes > sizeof(g_trace)) bytes = sizeof(g_trace);
+    return cudaMemcpyFromSymbol(host, g_trace, bytes);
+#else
+    (void)host;
+    (void)bytes;
+    return cudaErrorNotSupported;
+#endif
 }
 
 cudaError_t launch_chain(const ChainParams& p, size_t smem, cudaStream_t s) {

@@ -196,6 +196,16 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
             for (int k = issued > S ? issued - S : 0; k < issued; ++k)
                 mbar_wait_bounded(&full[k % S], (k / S) & 1, p.wait_ns, p.err, kErrTimeoutDrain);
         };
+        // With a cap of p.inflight < S stages in flight, stage k is issued only
+        // once stage k - p.inflight has landed.  Its slot is not reused before
+        // stage k - p.inflight + S > k, so the phase parity below is that
+        // stage's.  Fewer bytes queued in the memory system keep the latency
+        // of every other load (activation, parameters) low.
+        const auto landed_before = [&](int k) -> bool {
+            if (p.inflight <= 0 || p.inflight >= S || k < p.inflight) return true;
+            const int j = k - p.inflight;
+            return mbar_wait_bounded(&full[j % S], (j / S) & 1, p.wait_ns, p.err, kErrTimeoutFull);
+        };
         if constexpr (!kMerged) {
             const bool helps = FUSED && helpers;
             if (!helps) {
@@ -209,6 +219,7 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
                     if (k >= S &&
                         !mbar_wait_bounded(&empty[slot], ((k / S) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty))
                         break;
+                    if (!landed_before(k)) break;
                     const uint8_t* src = p.e[e].W + lrow * p.row_bytes;
                     const uint32_t bytes = static_cast<uint32_t>(int64_t(nrows) * p.row_bytes);
                     const uint32_t abytes = bytes & ~15u;
@@ -249,10 +260,13 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
             };
             // the first S stages (no slot to wait for), then the quantisation
             // share, then every later stage once its slot is released
+            // (no more stages than may be in flight before the quantisation:
+            // this warp takes part in it)
             int k = 0;
             bool more = true;
+            const int first = (p.inflight > 0 && p.inflight < S) ? p.inflight : S;
             if (lane == 0) {
-                for (; k < S && (more = pw.next(p, e, lrow, nrows)); ++k) {
+                for (; k < first && (more = pw.next(p, e, lrow, nrows)); ++k) {
                     if (k == p.prewait) pdl_wait_prior_grid();
                     issue_stage(k);
                 }
@@ -263,7 +277,10 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
             if (more) {
                 for (; pw.next(p, e, lrow, nrows); ++k) {
                     if (k == p.prewait) pdl_wait_prior_grid();
-                    if (!mbar_wait_bounded(&empty[k % S], ((k / S) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty)) break;
+                    if (k >= S &&
+                        !mbar_wait_bounded(&empty[k % S], ((k / S) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty))
+                        break;
+                    if (!landed_before(k)) break;
                     issue_stage(k);
                 }
             }

@@ -64,6 +64,7 @@ struct GemvParams {
     int RS;           // floats per row of the per-lane partial-sum area
     int n_cta;
     int prewait;       // stages the producer issues before waiting on the preceding kernel
+    int inflight;      // most stages in flight (issued, not landed) per CTA; 0: up to `stages`
     int merged;        // 1: the merged producer/reducer variant (gemv_has_merged)
     const float* x;    // f32 mode activation [cols]
     const int8_t* xq;  // W4A8 activation quants [cols]
@@ -103,14 +104,21 @@ __host__ __device__ constexpr int gemv_cols_per_lane(int fmt, int mode) {
 }
 
 // A chain of dependent W4A8 GEMVs in one launch (qx_gemv_chain).
-struct ChainJob {
-    GemvEntry e[QX_CHAIN_MAX_ENTRIES];  // P unused
+struct ChainEntry {
+    const uint8_t* W;  // device, rows * row_bytes
+    float* y;          // device, [rows]
+    int64_t rows;
+    int64_t row0;      // first row of this entry in the job's concatenated row space
+};
+struct alignas(16) ChainJob {
+    ChainEntry e[QX_CHAIN_MAX_ENTRIES];
     const float* x;                      // f32 activation [cols], quantised in-kernel
     int64_t cols;
     int64_t row_bytes;
     int64_t total_rows;
     int fmt, n_entries, team_lanes, team_warps, nteams, quantum, G, L, RS;
 };
+static_assert(sizeof(ChainJob) % 16 == 0, "job descriptors are copied to shared memory in 16-byte words");
 
 struct ChainParams {
     int n_jobs;
@@ -118,11 +126,14 @@ struct ChainParams {
     int stages;
     int slot_bytes;
     int bar_off, red_off, act_off;
+    int jobs_off;        // shared-memory copy of job[0 .. n_jobs), made once at kernel start
+    int ranges_off;      // shared memory: this CTA's row range of every job (2 x int64 per job)
     int red_slot_floats; // floats of the partial-sum area per slot (most G * RS of any job)
     int64_t max_cols;    // widest activation (size of the quantised-activation area)
     unsigned* counters;  // caller scratch: [n_jobs + 1] arrival counters, zero on entry and exit
     unsigned* err;
     uint64_t wait_ns;
+    int inflight;        // most stages in flight (issued, not landed); 0: up to `stages`
     ChainJob job[QX_CHAIN_MAX_JOBS];
 };
 
@@ -153,6 +164,8 @@ cudaError_t launch_chain(const ChainParams& p, size_t smem, cudaStream_t s);
 cudaError_t launch_prefill_q4k(const uint8_t* W, int64_t N, int64_t K, const int8_t* xq, const float* xd,
                                const int32_t* xs, int64_t M, float* Y, cudaStream_t s);
 cudaError_t chain_max_ctas_per_sm(size_t smem, int* out);
+// Measurement builds (QX_TRACE): copy the chain kernel's timestamps to host.
+cudaError_t chain_trace_read(void* host, size_t bytes);
 // tcgen05 prefill (qx_tc.cu): dequantise-and-split passes into `ws`
 // (prefill_tc_workspace_bytes), then the split-bf16 GEMM into Y [M, N].
 size_t prefill_tc_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t M);

@@ -645,7 +645,7 @@ struct Team {
     int slice;      // this lane's column slice within the team
     bool in_team;   // the warp belongs to a team (a few warps may be spare)
     bool active;    // the slice holds columns
-    int team_lanes, team_warps, nteams;
+    int team_lanes, team_warps, nteams, L;
 };
 
 __device__ __forceinline__ Team make_team(int warp, int lane, int team_lanes, int team_warps, int nteams, int L) {
@@ -665,6 +665,7 @@ __device__ __forceinline__ Team make_team(int warp, int lane, int team_lanes, in
     t.team_lanes = team_lanes;
     t.team_warps = team_warps;
     t.nteams = nteams;
+    t.L = L;
     return t;
 }
 

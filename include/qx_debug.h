@@ -33,6 +33,11 @@ qx_status qx_debug_mma_rate(int kind, double* ops_per_s, qx_stream_t s);
  * earlier call left there. */
 qx_status qx_debug_noalloc_fill(uint32_t value, qx_stream_t s);
 
+/* Measurement builds only (compiled with QX_TRACE): copy up to `bytes` of
+ * the chain kernel's per-(CTA, job, event) timestamps to host memory.  Other
+ * builds return QX_ERR_CUDA. */
+qx_status qx_debug_trace_read(void* host, size_t bytes);
+
 #ifdef __cplusplus
 }
 #endif
