@@ -396,17 +396,20 @@ def graph_time_ms(torch, fn, reps: int, stream):
     return e0.elapsed_time(e1) / reps
 
 
-def run_extra(args):
-    """The other configurations, measured for the record (not the headline)."""
-    import torch
-    import block_quantized_gemv_q8_gb300 as qx
-    qx.build_library()
-    torch.cuda.set_device(0)
-    stream = torch.cuda.Stream()
-    hbm, bf16, peak_kind = measured_peaks()
-    out = {"workload": args.workload, "peak_hbm_gbs": hbm, "peak_kind": peak_kind}
+def gemv_roofline(nbytes: int, us: float, hbm: float, peak_kind: str, kernel: str) -> dict:
+    achieved = nbytes / (us * 1e-6) / 1e9
+    return {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "peak_kind": peak_kind, "bytes_per_launch": nbytes, "mean_launch_us": us}
+
+
+def measure_config(name: str, qx, torch, stream, hbm: float, bf16: float, peak_kind: str,
+                   prefill_m: int = 0, prefill_path: int = 3) -> dict:
+    """One of the other workloads (Q4_K 1024 x 1024, the Q6_K lm_head, the
+    Qwen2-0.5B step, the prefill sweep), timed with CUDA events on `stream`
+    around CUDA-graph replays; one dict with its own roofline figures."""
+    out = {"workload": name}
     FUSED, F32, PDL = qx.QX_MODE_W4A8_FUSED, qx.QX_MODE_F32, qx.QX_FLAG_PDL
-    if args.workload == "q4k_1024":
+    if name == "q4k_1024":
         fmt, rows, cols = synth.Q4_K, 1024, 1024
         nbytes = rows * synth.row_bytes(fmt, cols)
         copies = 512  # 302 MB rotating pool, larger than L2
@@ -414,18 +417,24 @@ def run_extra(args):
         pool = pool.repeat(copies // 8, 1).reshape(copies, rows, -1)
         x = torch.from_numpy(synth.activation(1, cols, seed=9)[0]).cuda()
         y = torch.empty(rows, dtype=torch.float32, device="cuda")
-        for name, mode in (("w4a8", FUSED | PDL), ("f32", F32 | PDL)):
+        out["config"] = ("Q4_K GEMV 1024 x 1024, batch 1; a rotating pool of 512 weight copies (302 MB, larger "
+                         "than L2) streamed by back-to-back PDL launches in a CUDA graph; single serial launches "
+                         "on one L2-resident copy reported beside")
+        for mname, mode in (("w4a8", FUSED | PDL), ("f32", F32 | PDL)):
             def rot():
                 for c in range(copies):
                     qx.qx_gemv(fmt, pool[c], rows, cols, x, y=y, mode=mode, stream=stream)
-            ms = graph_time_ms(torch, rot, 5, stream) / copies
+            us = graph_time_ms(torch, rot, 5, stream) / copies * 1e3
             def hot():
                 for _ in range(64):
                     qx.qx_gemv(fmt, pool[0], rows, cols, x, y=y, mode=mode & 0xFF, stream=stream)
-            ms_hot = graph_time_ms(torch, hot, 5, stream) / 64
-            out[name] = {"GB_per_s_rotating_pool": nbytes / (ms * 1e-3) / 1e9, "us_per_gemv_rotating": ms * 1e3,
-                         "us_per_gemv_l2_hot_serial": ms_hot * 1e3}
-    elif args.workload == "lmhead_q6k":
+            us_hot = graph_time_ms(torch, hot, 5, stream) / 64 * 1e3
+            out[mname] = {"GB_per_s_rotating_pool": nbytes / (us * 1e-6) / 1e9, "us_per_gemv_rotating": us,
+                          "us_per_gemv_l2_hot_serial": us_hot,
+                          "roofline": gemv_roofline(nbytes, us, hbm, peak_kind,
+                                                    f"gemv_kernel<Q4_K, {mname}> (rotating pool)")}
+        del pool
+    elif name == "lmhead_q6k":
         fmt, rows, cols = synth.LLAMA8B_LM_HEAD_Q6K[1:]
         nbytes = rows * synth.row_bytes(fmt, cols)
         W = torch.from_numpy(synth.weights(fmt, rows, cols, seed=20)).cuda()
@@ -433,13 +442,17 @@ def run_extra(args):
         y = torch.empty(rows, dtype=torch.float32, device="cuda")
         # the GGUF layout, and the same weights repacked at load time into QX_Q6_K_SOA (same bytes per row)
         Ws = qx.qx_repack(qx.QX_Q6_K, qx.QX_Q6_K_SOA, W, rows, cols)
-        for name, f, Wm, mode in (("w4a8", fmt, W, FUSED | PDL), ("f32", fmt, W, F32 | PDL),
-                                  ("w4a8_soa", qx.QX_Q6_K_SOA, Ws, FUSED | PDL), ("f32_soa", qx.QX_Q6_K_SOA, Ws, F32 | PDL)):
-            ms = graph_time_ms(torch, lambda: qx.qx_gemv(f, Wm, rows, cols, x, y=y, mode=mode, stream=stream),
-                               50, stream)
-            out[name] = {"GB_per_s": nbytes / (ms * 1e-3) / 1e9, "us": ms * 1e3, "frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm}
+        out["config"] = "Q6_K lm_head 128256 x 4096 (430.9 MB, larger than L2), batch 1, f32 and W4A8 modes"
+        for mname, f, Wm, mode in (("w4a8", fmt, W, FUSED | PDL), ("f32", fmt, W, F32 | PDL),
+                                   ("w4a8_soa", qx.QX_Q6_K_SOA, Ws, FUSED | PDL),
+                                   ("f32_soa", qx.QX_Q6_K_SOA, Ws, F32 | PDL)):
+            us = graph_time_ms(torch, lambda: qx.qx_gemv(f, Wm, rows, cols, x, y=y, mode=mode, stream=stream),
+                               50, stream) * 1e3
+            out[mname] = {"GB_per_s": nbytes / (us * 1e-6) / 1e9, "us": us, "frac_of_hbm": nbytes / (us * 1e-6) / 1e9 / hbm,
+                          "roofline": gemv_roofline(nbytes, us, hbm, peak_kind, f"gemv_kernel lm_head {mname}")}
         out["weight_bytes"] = nbytes
-    elif args.workload == "qwen05b":
+        del W, Ws
+    elif name == "qwen05b":
         shapes = {n: (f, r, c) for n, f, r, c in synth.QWEN05B_LAYER}
         L = synth.QWEN05B_LAYERS
         Ws = [{n: torch.from_numpy(synth.weights(f, r, c, seed=synth.seed_for(3, l, j))).cuda()
@@ -465,7 +478,7 @@ def run_extra(args):
                                  ys=[ys["gate"], ys["up"]], mode=mode, stream=stream)
                 qx.qx_gemv(Q4, W["down"], 896, 4864, xd, y=ys["down"], mode=mode, stream=stream)
             qx.qx_gemv(Q8, Wlm, lr, lc, xs[0][:896], y=ylm, mode=mode, stream=stream)
-        ms = graph_time_ms(torch, step, 50, stream)
+        us = graph_time_ms(torch, step, 50, stream) * 1e3
         jobs = []
         for l in range(L):
             W = Ws[l]
@@ -476,13 +489,19 @@ def run_extra(args):
                      qx.GemvJob(Q4, [W["down"]], [896], 4864, xd, [ys["down"]])]
         jobs.append(qx.GemvJob(Q8, [Wlm], [lr], lc, xs[0][:896], [ylm]))
         arr, scratch = qx.make_chain(jobs), qx.chain_scratch(len(jobs))
-        ms_chain = graph_time_ms(torch, lambda: qx.qx_gemv_chain(jobs, scratch, stream=stream, marshalled=arr),
-                                 50, stream)
-        out.update({"weight_bytes_per_token": nbytes, "us_per_token_pdl_launches": ms * 1e3,
-                    "us_per_token_chain": ms_chain * 1e3, "GB_per_s_pdl": nbytes / (ms * 1e-3) / 1e9,
-                    "GB_per_s_chain": nbytes / (ms_chain * 1e-3) / 1e9,
-                    "launches_per_token_pdl": 4 * L + 1, "hbm_bound_us": nbytes / (hbm * 1e9) * 1e6})
-    elif args.workload == "prefill":
+        us_chain = graph_time_ms(torch, lambda: qx.qx_gemv_chain(jobs, scratch, stream=stream, marshalled=arr),
+                                 50, stream) * 1e3
+        best = min(us, us_chain)
+        out.update({"config": "Qwen2-0.5B decode step, 24 layers + Q8_0 lm_head 896 -> 151936, W4A8, batch 1 "
+                              "(Q4_K gate/up stored with 896 columns padded to 1024)",
+                    "weight_bytes_per_token": nbytes, "us_per_token_pdl_launches": us,
+                    "us_per_token_chain": us_chain, "us_per_token": best,
+                    "GB_per_s_pdl": nbytes / (us * 1e-6) / 1e9, "GB_per_s_chain": nbytes / (us_chain * 1e-6) / 1e9,
+                    "launches_per_token_pdl": 4 * L + 1, "hbm_bound_us": nbytes / (hbm * 1e9) * 1e6,
+                    "roofline": gemv_roofline(nbytes, best, hbm, peak_kind,
+                                              "the whole step (" + ("PDL launches" if us <= us_chain else "chain") + ")")})
+        del Ws, Wlm
+    elif name == "prefill":
         fmt, rows, cols = synth.PREFILL[1:]
         W = torch.from_numpy(synth.weights(fmt, rows, cols, seed=70)).cuda()
         X = torch.from_numpy(synth.activation(synth.PREFILL_M, cols, seed=71)).cuda()
@@ -490,11 +509,11 @@ def run_extra(args):
         torch.cuda.synchronize()
         nbytes = rows * synth.row_bytes(fmt, cols)
         sweep = []
-        for m in ([args.prefill_m] if args.prefill_m else synth.PREFILL_SWEEP_M):
+        for m in ([prefill_m] if prefill_m else synth.PREFILL_SWEEP_M):
             a = qx.ActQ8(act.q[:m], act.d[:m], act.sum[:m])
             Y = torch.empty((m, rows), dtype=torch.float32, device="cuda")
             rec = {"m": m}
-            for path in ((args.prefill_path,) if args.prefill_m else (1, 2, 3, 4)):
+            for path in ((prefill_path,) if prefill_m else (1, 2, 3, 4)):
                 if path in (1, 4) and m > 64:
                     continue
                 ms = graph_time_ms(torch, lambda: qx.qx_gemm_prefill_ex(fmt, W, rows, cols, a, Y=Y, path=path,
@@ -502,9 +521,11 @@ def run_extra(args):
                 rec[f"path{path}_us"] = ms * 1e3
                 rec[f"path{path}_tflops"] = 2.0 * m * rows * cols / (ms * 1e-3) / 1e12
                 rec[f"path{path}_weight_GB_per_s"] = nbytes / (ms * 1e-3) / 1e9
-                if path == 3:  # three bf16 passes over K on tcgen05, whole call incl. the dequantise passes
+                if path == 3:  # three bf16 passes over K on tcgen05
                     rec["path3_bf16_tflops"] = 3 * 2.0 * m * rows * cols / (ms * 1e-3) / 1e12
                     rec["path3_frac_of_bf16_peak"] = rec["path3_bf16_tflops"] / bf16
+            paths = {k[:-3]: v for k, v in rec.items() if k.endswith("_us")}
+            rec["fastest"] = min(paths, key=paths.get)
             sweep.append(rec)
         # measured on this device, for context: the int8 tensor rate a prefill can use on sm_103a
         # (legacy mma.sync; no int8 tcgen05) and the f16 mma.sync rate path 2 runs on
@@ -515,13 +536,40 @@ def run_extra(args):
                 if f"path{path}_tflops" in rec:  # int8-equivalent multiply-adds x 2 per second
                     rec[f"path{path}_frac_of_int8_mma_sync"] = (rec[f"path{path}_tflops"]
                                                                 / out["mma_sync_int8_tops_measured"])
-        out.update({"sweep": sweep, "flops_per_row": 2 * rows * cols, "bf16_dense_peak_tflops": bf16,
+        tensor_from = [r["m"] for r in sweep if r["fastest"] in ("path2", "path3")]
+        out["crossover_m"] = min(tensor_from) if tensor_from else None
+        top = max(sweep, key=lambda r: r["m"])
+        if "path3_us" in top:
+            fl = 3 * 2.0 * top["m"] * rows * cols
+            out["roofline"] = {"bound": "tensor", "kernel": f"tcgen05 prefill (path 3) at M = {top['m']}",
+                               "achieved": fl / (top["path3_us"] * 1e-6) / 1e12, "peak": bf16, "unit": "TFLOP/s",
+                               "frac": fl / (top["path3_us"] * 1e-6) / 1e12 / bf16, "peak_kind": peak_kind,
+                               "flops_per_launch": fl, "mean_launch_us": top["path3_us"],
+                               "note": "bf16 FLOP of the three split products (Xh Wh + Xh Wl + Xl Wh)"}
+        out.update({"config": "prefill X[M, 4096] x Q4_K [14336, 4096], M in {1, 8, 64, 512}",
+                    "sweep": sweep, "flops_per_row": 2 * rows * cols, "bf16_dense_peak_tflops": bf16,
                     "note": "path 1 = one W4A8 GEMV launch per row; path 2 = tensor cores (mma.sync f16 with "
                             "integer-valued operands); path 3 = tcgen05 bf16 GEMM over the split dequantised "
-                            "operands (3 passes of K), timed with its dequantise passes; path 4 = small-batch "
-                            "GEMV, one weight stream per 8 rows of X while five or more remain, else per up to 4; "
-                            "tflops count the int8-equivalent "
-                            "multiply-adds x2"})
+                            "operands (3 passes of K); path 4 = small-batch GEMV, one weight stream per 8 rows "
+                            "of X while five or more remain, else per up to 4; tflops count the int8-equivalent "
+                            "multiply-adds x2; crossover_m = the smallest swept M whose fastest path is a "
+                            "tensor-core one"})
+        del W, X
+    torch.cuda.synchronize()
+    return out
+
+
+def run_extra(args):
+    """One of the other configurations, as its own JSON line."""
+    import torch
+    import block_quantized_gemv_q8_gb300 as qx
+    qx.build_library()
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream()
+    hbm, bf16, peak_kind = measured_peaks()
+    with ClockSampler(0) as clk:
+        out = measure_config(args.workload, qx, torch, stream, hbm, bf16, peak_kind, args.prefill_m, args.prefill_path)
+    out.update({"peak_hbm_gbs": hbm, "peak_kind": peak_kind, "clocks": clk.summary()})
     print(json.dumps(out), flush=True)
     return 0
 
@@ -539,6 +587,8 @@ def main():
     ap.add_argument("--workload", default="llama8b", choices=["llama8b", "q4k_1024", "lmhead_q6k", "qwen05b",
                                                                "prefill"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="default workload: skip the sub-records of the other configurations")
     ap.add_argument("--layers", type=int, default=synth.LLAMA8B_LAYERS)
     ap.add_argument("--down-layout", default="soa", choices=["soa", "gguf"],
                     help="Llama step: the Q6_K down projection repacked at load time (QX_Q6_K_SOA) or as stored")
@@ -687,7 +737,7 @@ def main():
         raise RuntimeError(f"device error after the timed region: {qx.qx_status_string(st)}")
     assert int(wl.scratch.sum()) == 0
 
-    hbm, _, peak_kind = measured_peaks()
+    hbm, bf16, peak_kind = measured_peaks()
     per_s = lambda m: job_throughput(ws, wl.bytes_per_step, args.steps, m)  # noqa: E731
     value_chain, value_pdl = per_s(ms), per_s(ms_pdl)
     chain_is_faster = ms <= ms_pdl
@@ -711,6 +761,15 @@ def main():
                         "device time (ncu launch list; gate/up is 48% of the step's weight bytes); timed with "
                         "CUDA events around each of its 32 launches in an instrumented copy of the step graph; "
                         "algorithmic bytes = the two Q4_K matrices (scales included)")
+    configs = None
+    if rank == 0 and not args.no_configs:
+        # the other configurations, each with its own roofline and clock record
+        configs = {}
+        for name in ("q4k_1024", "lmhead_q6k", "qwen05b", "prefill"):
+            with ClockSampler(local) as cclk:
+                rec = measure_config(name, qx, torch, stream, hbm, bf16, peak_kind)
+            rec["clocks"] = cclk.summary()
+            configs[name] = rec
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         import oracle
@@ -750,6 +809,7 @@ def main():
             "gpu_launches": args.steps * (1 if chain_is_faster else wl.launches_per_step),
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
