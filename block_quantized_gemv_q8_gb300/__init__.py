@@ -29,7 +29,7 @@ QX_CHAIN_MAX_ENTRIES = 4
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libqx.so")
 
 EXPORTS = ["qx_quantize_act_q8", "qx_gemv", "qx_gemv_multi", "qx_gemm_prefill", "qx_gemm_prefill_ex",
-           "qx_gemm_prefill_ws", "qx_gemm_prefill_workspace_bytes", "qx_gemv_partials", "qx_gemv_chain", "qx_gemv_chain_noalloc", "qx_gemv_chain_scratch_bytes", "qx_row_bytes", "qx_repack",
+           "qx_gemv_partials", "qx_gemv_chain", "qx_gemv_chain_noalloc", "qx_gemv_chain_scratch_bytes", "qx_row_bytes", "qx_repack",
            "qx_device_check", "qx_debug_timeout_probe", "qx_debug_mma_rate", "qx_debug_noalloc_fill",
            "qx_debug_trace_read", "qx_status_string", "qx_last_error", "qx_version"]
 
@@ -69,9 +69,6 @@ def lib() -> ctypes.CDLL:
         L.qx_gemv_multi.argtypes = [I, P, P, P, I64, P, P, I, P]
         L.qx_gemm_prefill.argtypes = [I, P, I64, I64, ctypes.POINTER(_Act), P, P]
         L.qx_gemm_prefill_ex.argtypes = [I, P, I64, I64, ctypes.POINTER(_Act), P, I, P]
-        L.qx_gemm_prefill_ws.argtypes = [I, P, I64, I64, ctypes.POINTER(_Act), P, I, P, ctypes.c_size_t, P]
-        L.qx_gemm_prefill_workspace_bytes.argtypes = [I, I64, I64, I64]
-        L.qx_gemm_prefill_workspace_bytes.restype = ctypes.c_size_t
         L.qx_gemv_partials.argtypes = [I, P, I64, I64, ctypes.POINTER(_Act), P, P]
         L.qx_gemv_chain.argtypes = [I, ctypes.POINTER(_Job), P, P]
         L.qx_gemv_chain_noalloc.argtypes = [I, ctypes.POINTER(_Job), P]
@@ -92,7 +89,7 @@ def lib() -> ctypes.CDLL:
         L.qx_version.argtypes = []
         L.qx_version.restype = ctypes.c_char_p
         for n in ("qx_quantize_act_q8", "qx_gemv", "qx_gemv_multi", "qx_gemm_prefill", "qx_gemm_prefill_ex",
-                  "qx_gemm_prefill_ws", "qx_gemv_partials", "qx_gemv_chain", "qx_gemv_chain_noalloc",
+                  "qx_gemv_partials", "qx_gemv_chain", "qx_gemv_chain_noalloc",
                   "qx_device_check", "qx_debug_timeout_probe",
                   "qx_repack", "qx_debug_mma_rate", "qx_debug_noalloc_fill",
                   "qx_debug_trace_read"):
@@ -301,29 +298,6 @@ def qx_gemm_prefill_ex(fmt: int, W: torch.Tensor, rows: int, cols: int, X: ActQ8
     a = X.c_struct()
     _check(lib().qx_gemm_prefill_ex(fmt, _ptr(W), rows, cols, ctypes.byref(a), _ptr(Y), path, _stream(stream)),
            "qx_gemm_prefill_ex")
-    return Y
-
-
-def qx_gemm_prefill_workspace_bytes(fmt: int, rows: int, cols: int, m: int) -> int:
-    """Device bytes of workspace the tcgen05 prefill path needs (0 for a bad shape)."""
-    return int(lib().qx_gemm_prefill_workspace_bytes(fmt, rows, cols, m))
-
-
-def qx_gemm_prefill_ws(fmt: int, W: torch.Tensor, rows: int, cols: int, X: ActQ8, Y: torch.Tensor | None = None,
-                       path: int = 0, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """qx_gemm_prefill_ex with caller-owned workspace (allocated here if not given)."""
-    Y = Y if Y is not None else torch.empty((X.m, rows), dtype=torch.float32, device=W.device)
-    need = qx_gemm_prefill_workspace_bytes(fmt, rows, cols, X.m)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=W.device)
-    nbytes = workspace.numel() * workspace.element_size()
-    _need_weights(W, fmt, rows, cols)
-    _need(Y, X.m * rows * 4, "Y")
-    _need_act(X, X.m, _served_cols(fmt, cols), "X")
-    _ptr(workspace)
-    a = X.c_struct()
-    _check(lib().qx_gemm_prefill_ws(fmt, _ptr(W), rows, cols, ctypes.byref(a), _ptr(Y), path, _ptr(workspace),
-                                    nbytes, _stream(stream)), "qx_gemm_prefill_ws")
     return Y
 
 

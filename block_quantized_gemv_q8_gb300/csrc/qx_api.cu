@@ -500,48 +500,8 @@ using namespace qx;
 
 namespace {
 
-// The library's own prefill workspace, one per device, grown on demand (never
-// while the stream is being captured into a graph).
-struct PrefillWorkspace {
-    void* ptr = nullptr;
-    size_t bytes = 0;
-};
-PrefillWorkspace g_prefill_ws[kMaxDevices];
-
-qx_status prefill_workspace(size_t need, cudaStream_t s, void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice, "device index");
-    std::lock_guard<std::mutex> lock(g_mu);
-    PrefillWorkspace& w = g_prefill_ws[dev];
-    if (w.bytes < need) {
-        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-        if ((e = cudaStreamIsCapturing(s, &cs)) != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
-        if (cs != cudaStreamCaptureStatusNone) {
-            snprintf(g_last_error, sizeof(g_last_error),
-                     "prefill workspace of %zu bytes must be allocated before graph capture "
-                     "(run once uncaptured, or pass a workspace to qx_gemm_prefill_ws)",
-                     need);
-            return QX_ERR_ARG;
-        }
-        if (w.ptr) {
-            if ((e = cudaFree(w.ptr)) != cudaSuccess) return cuda_fail(e, "cudaFree");
-            w.ptr = nullptr;
-            w.bytes = 0;
-        }
-        if ((e = cudaMalloc(&w.ptr, need)) != cudaSuccess) {
-            w.ptr = nullptr;
-            return cuda_fail(e, "cudaMalloc (prefill workspace)");
-        }
-        w.bytes = need;
-    }
-    *out = w.ptr;
-    return QX_OK;
-}
-
 qx_status prefill_dispatch(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, float* Y,
-                           int path, void* ws, size_t ws_bytes, bool own_ws, qx_stream_t s) {
+                           int path, qx_stream_t s) {
     qx_status st = check_shape(fmt, rows, cols);
     if (st != QX_OK) return st;
     if (!W || !Y) return QX_ERR_ARG;
@@ -552,8 +512,11 @@ qx_status prefill_dispatch(qx_fmt fmt, const void* W, int64_t rows, int64_t cols
         if (path != 0 && path != 1) return QX_ERR_FMT;  // the GEMM paths read the GGUF layouts
         path = 1;
     }
+    const int64_t rb = row_bytes_of(fmt, cols);
     if (path == 0) {
         path = X->m == 1 ? 1 : (X->m <= kPrefillBatchMaxRows ? 4 : 3);
+        // shapes beyond the tensor-core kernel's 32-bit copy coordinates take one GEMV per row
+        if (path == 3 && !prefill_tc_serves(fmt, rows, cols, X->m, rb)) path = 1;
         // rows wider than the small-batch lanes cover (eight-row lanes: 14336
         // columns, four-row K-quant lanes: 28672) take one GEMV per row
         if (path == 4) {
@@ -581,19 +544,11 @@ qx_status prefill_dispatch(qx_fmt fmt, const void* W, int64_t rows, int64_t cols
         return QX_OK;
     }
     if (path == 3) {
-        if (X->m > INT32_MAX || rows > INT32_MAX) return QX_ERR_SHAPE;
+        if (!prefill_tc_serves(fmt, rows, cols, X->m, rb)) return QX_ERR_SHAPE;
         DeviceInfo* dev = nullptr;
         if ((st = device_info(&dev)) != QX_OK) return st;
-        const size_t need = prefill_tc_workspace_bytes(fmt, rows, cols, X->m);
-        const cudaStream_t cs = reinterpret_cast<cudaStream_t>(s);
-        if (own_ws) {
-            if ((st = prefill_workspace(need, cs, &ws)) != QX_OK) return st;
-        } else {
-            if (!ws || ws_bytes < need) return QX_ERR_ARG;
-            if (!aligned16(ws)) return QX_ERR_ALIGN;
-        }
-        const cudaError_t e = launch_prefill_tc(fmt, static_cast<const uint8_t*>(W), rows, cols, int64_t(cols / block_weights(fmt)) * block_bytes(fmt),
-                                                X->q, X->d, X->m, Y, ws, dev->err_word, cs);
+        const cudaError_t e = launch_prefill_tc(fmt, static_cast<const uint8_t*>(W), rows, cols, rb, X->q, X->d, X->m,
+                                                Y, dev->err_word, reinterpret_cast<cudaStream_t>(s));
         return e == cudaSuccess ? QX_OK : cuda_fail(e, "tcgen05 prefill launch");
     }
     const bool tensor = path == 2;
@@ -765,22 +720,12 @@ qx_status qx_gemv_partials(qx_fmt fmt, const void* W, int64_t rows, int64_t cols
 
 qx_status qx_gemm_prefill_ex(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, float* Y,
                              int path, qx_stream_t s) {
-    return prefill_dispatch(fmt, W, rows, cols, X, Y, path, nullptr, 0, true, s);
+    return prefill_dispatch(fmt, W, rows, cols, X, Y, path, s);
 }
 
 qx_status qx_gemm_prefill(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, float* Y,
                           qx_stream_t s) {
-    return prefill_dispatch(fmt, W, rows, cols, X, Y, 0, nullptr, 0, true, s);
-}
-
-size_t qx_gemm_prefill_workspace_bytes(qx_fmt fmt, int64_t rows, int64_t cols, int64_t m) {
-    if (check_shape(fmt, rows, cols) != QX_OK || m < 1) return 0;
-    return prefill_tc_workspace_bytes(fmt, rows, cols, m);
-}
-
-qx_status qx_gemm_prefill_ws(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, float* Y,
-                             int path, void* workspace, size_t workspace_bytes, qx_stream_t s) {
-    return prefill_dispatch(fmt, W, rows, cols, X, Y, path, workspace, workspace_bytes, false, s);
+    return prefill_dispatch(fmt, W, rows, cols, X, Y, 0, s);
 }
 
 size_t qx_gemv_chain_scratch_bytes(int n_jobs) {

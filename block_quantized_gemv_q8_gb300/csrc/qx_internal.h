@@ -166,10 +166,11 @@ cudaError_t launch_prefill_q4k(const uint8_t* W, int64_t N, int64_t K, const int
 cudaError_t chain_max_ctas_per_sm(size_t smem, int* out);
 // Measurement builds (QX_TRACE): copy the chain kernel's timestamps to host.
 cudaError_t chain_trace_read(void* host, size_t bytes);
-// tcgen05 prefill (qx_tc.cu): dequantise-and-split passes into `ws`
-// (prefill_tc_workspace_bytes), then the split-bf16 GEMM into Y [M, N].
-size_t prefill_tc_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t M);
+// tcgen05 prefill (qx_tc.cu): both operands converted in shared memory, no
+// workspace.  prefill_tc_serves: whether the kernel's 32-bit copy coordinates
+// cover the shape.
+bool prefill_tc_serves(int fmt, int64_t N, int64_t K, int64_t M, int64_t row_bytes);
 cudaError_t launch_prefill_tc(int fmt, const uint8_t* W, int64_t N, int64_t K, int64_t row_bytes, const int8_t* xq,
-                              const float* xd, int64_t M, float* Y, void* ws, unsigned* err, cudaStream_t s);
+                              const float* xd, int64_t M, float* Y, unsigned* err, cudaStream_t s);
 
 }  // namespace qx

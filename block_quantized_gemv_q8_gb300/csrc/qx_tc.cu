@@ -5,29 +5,37 @@
 // "CPU" and "CUDA") is Y[m, n] = sum_k xhat[m, k] * what[n, k] with
 // xhat = dx * q_x (the dequantised int8 activation) and what the dequantised
 // weight (Q4_K: d*sc*q - dmin*m, Q6_K: d*sc*(q - 32), Q8_0: d*q).  sm_103a has
-// no integer tensor-core MMA, and the per-sub-block scales differ along K, so
-// the integer partial sums cannot be scaled inside the MMA accumulation.
-// Instead each operand is written once as two bf16 terms whose sum carries 16
-// significant bits (hi = bf16(v), lo = bf16(v - hi)), and
+// no integer tensor-core MMA, and the per-block scales differ along K, so the
+// integer partial sums cannot be scaled inside the MMA accumulation.  Instead
+// each operand is written as two bf16 terms whose sum carries 16 significant
+// bits (hi = bf16(v), lo = bf16(v - hi)), and
 //     Y = Xh Wh^T + Xh Wl^T + Xl Wh^T
-// is one bf16 GEMM over three passes of K, accumulated in f32 in tensor
-// memory.  The dropped Xl Wl^T term and the split truncation bound the error
-// of every product by about 2^-15 of |xhat * what|, well inside the tolerance
-// of 1e-4 * sum |w * x| per output.
+// is accumulated in f32 in tensor memory.  The dropped Xl Wl^T term and the
+// split rounding bound the error of every product by about 2^-15 of
+// |xhat * what|, well inside the tolerance of 1e-4 * sum |w * x| per output.
 //
-// Kernels:
-//   * Q4_K: the activation is split by a small pass; the weight terms are
-//     formed inside the GEMM (tc_q4k_fused_kernel): TMA brings the raw
-//     super-blocks of 128 weight rows into shared memory, 16 converter warps
-//     dequantise each 64-wide K slice and write Wh / Wl directly in the
-//     128-byte-swizzled K-major layout the tensor cores read, and one thread
-//     issues the three split products per slice (M = 128, N = 128, K = 16).
-//   * Q6_K, Q8_0: a dequantise-and-split pass per operand (memory-bound),
-//     then tc_gemm_kernel: 128 x 256 tiles over three passes of K.
-// In both, warp 0 issues the TMA loads, warp 1 owns the tensor memory and
-// issues tcgen05.mma from one thread, and four warps drain the accumulator
-// with tcgen05.ld.  Every wait is bounded and reports through the device
-// error word.
+// One kernel per format, and no pass outside it.  A CTA computes a 256 x 128
+// tile of Y (256 rows of X, 128 weight rows) as two 128 x 128 accumulators in
+// tensor memory that share every converted weight slice.  Per 32-wide K
+// slice, TMA brings the int8 activation codes of the 256 rows into shared
+// memory, and per K group the raw blocks of the 128 weight rows; sixteen
+// converter warps dequantise both, split them into hi and lo bf16 and write
+// them straight into the 64-byte-swizzled K-major tiles the tensor cores read;
+// one thread issues the split products (M = 128, N = 128, K = 16 each).  The
+// library needs no workspace, so the call allocates nothing and may be
+// captured in a CUDA graph on first use.
+//
+// Weight rows (llamay docs, "Backends and hardware", section "CUDA": the
+// prefill kernel should stage the next weight tile behind the current
+// multiply): rows that are a 16-byte multiple (Q4_K always; Q6_K and Q8_0 at
+// 2048 and 256 columns and their multiples) come as one 2-D box per group and
+// tile.  Otherwise each row's group is fetched by a 1-D box that starts at the
+// 16-byte boundary at or below it (the group plus up to 14 bytes before it),
+// and the converter indexes from the remainder.  Boxes that run past the end
+// of a row or of the matrix are zero-filled by the copy engine, never read
+// out of bounds.
+//
+// Every wait is bounded and reports through the device error word.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -42,142 +50,98 @@ namespace qx {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int kTcThreads = 192;
-constexpr size_t kTcSmem = size_t(STAGES) * STAGE_BYTES + 1024 + 256;
+constexpr int TBM = 256, TBN = 128, TBK = 32;  // CTA tile; K slice
+constexpr int OP_STAGES = 2, XR_STAGES = 4;
+constexpr int T_TILE = 128 * TBK * 2;       // one 128-row x 32 bf16 tile: 8 KB
+// one K slice of operands: Xh (two 128-row halves), Xl (two halves), Wh, Wl
+constexpr int OP_XH = 0, OP_XL = 2 * T_TILE, OP_WH = 4 * T_TILE, OP_WL = 5 * T_TILE, OP_BYTES = 6 * T_TILE;
+constexpr int XR_BYTES = TBM * TBK;         // int8 codes of 256 rows x 32 columns
+constexpr int kConvWarps = 16;              // converter warps; the first eight drain the accumulators
+constexpr int kTcThreads = 32 * (2 + kConvWarps);
+constexpr int kRowStride1d = 256;           // shared-memory row stride of the per-row boxes (128-byte aligned)
+constexpr uint32_t kIdesc =  // kind::f16: f32 accumulator, bf16 A and B, both K-major, M = 128, N = 128
+    (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(TBN >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+
+// Raw weight groups per format: K columns per group, its bytes in a row, the
+// box fetched per row (bytes, a 16-byte multiple covering the group from the
+// 16-byte boundary at or below it), and the number of shared-memory slots.
+template <int FMT>
+struct RawGeom;
+template <>
+struct RawGeom<QX_Q4_K> {
+    static constexpr int kGroupK = 256, kGroupBytes = 144, kBox = 144, kSlots = 3;
+};
+template <>
+struct RawGeom<QX_Q6_K> {
+    static constexpr int kGroupK = 256, kGroupBytes = 210, kBox = 224, kSlots = 2;
+};
+template <>
+struct RawGeom<QX_Q8_0> {
+    static constexpr int kGroupK = 128, kGroupBytes = 136, kBox = 160, kSlots = 2;
+};
+// Bytes of one raw slot (128 rows): dense rows of the 2-D box, or the per-row
+// boxes at kRowStride1d.
+template <int FMT>
+__host__ __device__ constexpr int raw_slot_bytes() {
+    return (FMT == QX_Q4_K ? RawGeom<FMT>::kBox : kRowStride1d) * TBN;
+}
+
+template <int FMT>
+constexpr size_t tc_smem_bytes() {
+    return size_t(OP_STAGES) * OP_BYTES + size_t(XR_STAGES) * XR_BYTES +
+           size_t(RawGeom<FMT>::kSlots) * raw_slot_bytes<FMT>() + 1024 + 256;
+}
+static_assert(tc_smem_bytes<QX_Q6_K>() <= 227 * 1024 && tc_smem_bytes<QX_Q8_0>() <= 227 * 1024 &&
+                  tc_smem_bytes<QX_Q4_K>() <= 227 * 1024,
+              "a CTA's shared memory");
 
 struct TcParams {
-    CUtensorMap a_map[2];  // Xh, Xl: [M, K] bf16
-    CUtensorMap b_map[2];  // Wh, Wl: [N, K] bf16
+    CUtensorMap x_map;  // q_x as bytes [M rows, K], boxes 32 x 256
+    CUtensorMap w_map;  // [N rows, row_bytes] bytes, boxes kBox x 128 (w2d); else all N * row_bytes bytes, 1-D boxes
+    const float* xd;    // [M, K / 32] activation scales
     int M, N, K;
-    float* Y;  // [M, N] f32
+    int w2d;            // 1: weight rows are a 16-byte multiple, one 2-D box per group
+    int64_t row_bytes;
+    float* Y;           // [M, N] f32
     unsigned* err;
     unsigned long long wait_ns;
 };
 
 // ---------------------------------------------------------------------------
-// dequantise and split
+// tcgen05 and TMA helpers
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ void split_store(const float (&w)[32], uint16_t* hi, uint16_t* lo) {
-    uint32_t h[16], l[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const __nv_bfloat16 h0 = __float2bfloat16_rn(w[2 * i]), h1 = __float2bfloat16_rn(w[2 * i + 1]);
-        const __nv_bfloat16 l0 = __float2bfloat16_rn(w[2 * i] - __bfloat162float(h0));
-        const __nv_bfloat16 l1 = __float2bfloat16_rn(w[2 * i + 1] - __bfloat162float(h1));
-        h[i] = uint32_t(__bfloat16_as_ushort(h0)) | (uint32_t(__bfloat16_as_ushort(h1)) << 16);
-        l[i] = uint32_t(__bfloat16_as_ushort(l0)) | (uint32_t(__bfloat16_as_ushort(l1)) << 16);
-    }
-    uint4* hp = reinterpret_cast<uint4*>(hi);
-    uint4* lp = reinterpret_cast<uint4*>(lo);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        hp[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
-        lp[i] = make_uint4(l[4 * i], l[4 * i + 1], l[4 * i + 2], l[4 * i + 3]);
-    }
-}
-
-__device__ __forceinline__ float f16_at(const uint8_t* p) {
-    return __half2float(__ushort_as_half(uint16_t(p[0] | (uint16_t(p[1]) << 8))));
-}
-
-// One thread per (row, group of 32 weights).  Q4_K (GGUF layout): d, dmin,
-// 12 bytes of 6-bit scales and mins, 128 bytes of nibbles; group j of a super-
-// block is sub-block j.  Q6_K: group = quarter t of half h; Q8_0: group = block.
-template <int FMT>
-__global__ void __launch_bounds__(256) dequant_w_kernel(const uint8_t* __restrict__ W, int64_t N, int64_t K,
-                                                        int64_t row_bytes, uint16_t* __restrict__ Wh,
-                                                        uint16_t* __restrict__ Wl) {
-    const int64_t groups = K / 32;
-    const int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (t >= N * groups) return;
-    const int64_t n = t / groups, g = t % groups;
-    const uint8_t* row = W + n * row_bytes;
-    float w[32];
-    if constexpr (FMT == QX_Q4_K) {
-        const uint8_t* b = row + (g / 8) * 144;
-        const int j = int(g % 8);
-        const float d = f16_at(b), dmin = f16_at(b + 2);
-        const uint8_t* s = b + 4;
-        int sc, m;
-        if (j < 4) {
-            sc = s[j] & 63;
-            m = s[j + 4] & 63;
-        } else {
-            sc = (s[j + 4] & 15) | ((s[j - 4] >> 6) << 4);
-            m = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
-        }
-        const float a = d * float(sc), c = dmin * float(m);  // exact products
-        const uint8_t* qs = b + 16 + 32 * (j / 2);
-        const int sh = 4 * (j & 1);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = fmaf(a, float((qs[i] >> sh) & 15), -c);
-    } else if constexpr (FMT == QX_Q6_K) {
-        const uint8_t* b = row + (g / 8) * 210;
-        const int q8 = int(g % 8), h = q8 / 4, tq = q8 % 4;
-        const float d = f16_at(b + 208);
-        const uint8_t* ql = b + 64 * h + 32 * (tq & 1);
-        const uint8_t* qh = b + 128 + 32 * h;
-        const int8_t* sc = reinterpret_cast<const int8_t*>(b + 192 + 8 * h);
-        const int nsh = (tq >= 2) ? 4 : 0;
-        const float s0 = d * float(sc[2 * tq]), s1 = d * float(sc[2 * tq + 1]);  // l < 16, l >= 16
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int q = ((ql[i] >> nsh) & 15) | (((qh[i] >> (2 * tq)) & 3) << 4);
-            w[i] = (i < 16 ? s0 : s1) * float(q - 32);
-        }
-    } else {
-        const uint8_t* b = row + g * 34;
-        const float d = f16_at(b);
-        const int8_t* q = reinterpret_cast<const int8_t*>(b + 2);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = d * float(q[i]);
-    }
-    split_store(w, Wh + n * K + 32 * g, Wl + n * K + 32 * g);
-}
-
-// xhat = dx * q_x per block of 32, split into two bf16 terms.
-__global__ void __launch_bounds__(256) dequant_x_kernel(const int8_t* __restrict__ q, const float* __restrict__ d,
-                                                        int64_t M, int64_t K, uint16_t* __restrict__ Xh,
-                                                        uint16_t* __restrict__ Xl) {
-    const int64_t groups = K / 32;
-    const int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (t >= M * groups) return;
-    const float dx = d[t];
-    const int8_t* qp = q + 32 * t;
-    float w[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) w[i] = dx * float(qp[i]);
-    split_store(w, Xh + 32 * t, Xl + 32 * t);
-}
-
-// ---------------------------------------------------------------------------
-// tcgen05 GEMM
-// ---------------------------------------------------------------------------
-
-// Shared-memory matrix descriptor of a K-major tile with the 128-byte swizzle
-// written by TMA: rows of 128 bytes, 8-row atoms 1024 bytes apart.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+// Shared-memory matrix descriptor of a K-major tile with the 64-byte swizzle:
+// rows of 64 bytes (32 bf16), 8-row atoms 512 bytes apart; within an atom the
+// 16-byte chunk j of row r sits at chunk j ^ ((r / 2) % 4).
+__device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr) {
     uint64_t d = 0;
     d |= uint64_t((saddr & 0x3FFFF) >> 4);  // start address
     d |= uint64_t(1) << 16;                  // leading byte offset (unused for swizzled K-major)
-    d |= uint64_t(1024 >> 4) << 32;          // stride byte offset: one 8-row atom
+    d |= uint64_t(512 >> 4) << 32;           // stride byte offset: one 8-row atom
     d |= uint64_t(1) << 46;                  // descriptor version
-    d |= uint64_t(2) << 61;                  // 128-byte swizzle
+    d |= uint64_t(4) << 61;                  // 64-byte swizzle
     return d;
 }
-// Instruction descriptor, kind::f16: f32 accumulator, bf16 A and B, both
-// K-major, M = 128, N = 256.
-constexpr uint32_t kIdesc =
-    (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+// Byte offset of 16-byte chunk j of row r in such a tile.
+__device__ __forceinline__ uint32_t sw64_off(int r, int j) {
+    return uint32_t(r) * 64u + uint32_t((j ^ ((r >> 1) & 3)) << 4);
+}
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
             smem_addr(dst)),
         "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+// x: a byte offset that is a multiple of 16 (the copy engine's rule for the
+// innermost coordinate); bytes past the end of the tensor arrive as zeros.
+__device__ __forceinline__ void tma_load_1d(void* dst, const CUtensorMap* map, int x, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.1d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2}], [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(map), "r"(x), "r"(smem_addr(bar))
         : "memory");
 }
 // Every lane of the warp waits on the barrier itself (so each observes the
@@ -211,224 +175,222 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// blockIdx.x: M tile (fastest, so the CTAs that share a weight tile run
-// together and read it from DRAM once), blockIdx.y: N tile.
-__global__ void __launch_bounds__(kTcThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_addr(smem_raw);
-    uint8_t* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);  // 1024-byte aligned stages
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-    uint64_t* empty = full + STAGES;
-    uint64_t* acc_full = empty + STAGES;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+// ---------------------------------------------------------------------------
+// operand conversion: 16 consecutive K values of one row into hi / lo bf16
+// (two 16-byte chunks each)
+// ---------------------------------------------------------------------------
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
-    const int kt_per_pass = (p.K + BK - 1) / BK, n_iters = 3 * kt_per_pass;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        mbar_init(acc_full, 1);
-        fence_barrier_init();
-    }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
-                     "r"(BN)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-
-    if (warp == 0 && lane == 0) {
-        // ---- TMA producer: pass 0 = (Xh, Wh), 1 = (Xh, Wl), 2 = (Xl, Wh)
-        int issued = 0;
-        for (int it = 0; it < n_iters; ++it) {
-            const int s = it % STAGES;
-            if (it >= STAGES &&
-                !mbar_wait_bounded(&empty[s], ((it / STAGES) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty))
-                break;
-            const int pass = it / kt_per_pass, kt = it % kt_per_pass;
-            uint8_t* a_s = smem + s * STAGE_BYTES;
-            mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-            tma_load_2d(a_s, &p.a_map[pass == 2 ? 1 : 0], kt * BK, m0, &full[s]);
-            tma_load_2d(a_s + A_BYTES, &p.b_map[pass == 1 ? 1 : 0], kt * BK, n0, &full[s]);
-            issued = it + 1;
-        }
-        // keep the CTA alive until every copy it issued has landed
-        for (int it = issued > STAGES ? issued - STAGES : 0; it < issued; ++it)
-            mbar_wait_bounded(&full[it % STAGES], (it / STAGES) & 1, p.wait_ns, p.err, kErrTimeoutDrain);
-    } else if (warp == 1 && lane == 0) {
-        // ---- MMA issuer
-        for (int it = 0; it < n_iters; ++it) {
-            const int s = it % STAGES;
-            if (!mbar_wait_bounded(&full[s], (it / STAGES) & 1, p.wait_ns, p.err, kErrTimeoutMma)) break;
-            tc_fence_after();
-            const uint32_t a_s = smem_addr(smem + s * STAGE_BYTES);
-            const uint64_t ad = sw128_desc(a_s), bd = sw128_desc(a_s + A_BYTES);
+// Split 2N f32 values, pairs in packed f32x2 form, into hi = bf16(v) and
+// lo = bf16(v - hi), both rounded to nearest (v - hi is exact in f32): hi + lo
+// is within 2^-17 |v| of v.  (The subtraction is a scalar round-to-nearest
+// intrinsic: ptxas may fold packed two-wide cancellation patterns such as
+// g - (g - v) at -O3.)
+template <int N>
+__device__ __forceinline__ void split_pairs(const uint64_t (&v)[N], uint32_t (&h)[N], uint32_t (&l)[N]) {
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k)  // K = 16 per MMA: 32 bytes further along the swizzled row
-                tc_mma(tmem, ad + uint64_t(2 * k), bd + uint64_t(2 * k), kIdesc, (it | k) != 0 ? 1u : 0u);
-            tc_commit(&empty[s]);
-        }
-        tc_commit(acc_full);  // also after a failed wait: arrives once the issued MMAs are done
-    } else if (warp >= 2) {
-        // ---- epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31
-        if (warp_wait(acc_full, 0, p.wait_ns, p.err, kErrTimeoutMma)) {
-            tc_fence_after();
-            const int q = warp & 3;
-            const int row = m0 + 32 * q + lane;
-            const bool row_ok = row < p.M;
-            const bool vec = (n0 + BN <= p.N) && (p.N % 4 == 0);
-            float* yrow = p.Y + size_t(row_ok ? row : 0) * p.N + n0;
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t v[32];
-                tc_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(32 * c), v);
-                if (!row_ok) continue;
-                if (vec) {
-                    float4* dst = reinterpret_cast<float4*>(yrow + 32 * c);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                             __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (n0 + 32 * c + i < p.N) yrow[32 * c + i] = __uint_as_float(v[i]);
-                }
-            }
-        }
+    for (int i = 0; i < N; ++i) {
+        const float2 f = f32x2_unpack(v[i]);
+        const __nv_bfloat162 hb = __floats2bfloat162_rn(f.x, f.y);
+        h[i] = *reinterpret_cast<const uint32_t*>(&hb);
+        const float h0 = __uint_as_float(h[i] << 16), h1 = __uint_as_float(h[i] & 0xFFFF0000u);
+        const __nv_bfloat162 lb = __floats2bfloat162_rn(__fsub_rn(f.x, h0), __fsub_rn(f.y, h1));
+        l[i] = *reinterpret_cast<const uint32_t*>(&lb);
     }
-    tc_fence_before();
-    __syncthreads();
-    __syncwarp();
-    if (warp == 1)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BN) : "memory");
+}
+__device__ __forceinline__ void split16(const uint64_t (&v)[8], uint4 (&hi)[2], uint4 (&lo)[2]) {
+    uint32_t h[8], l[8];
+    split_pairs<8>(v, h, l);
+    hi[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    hi[1] = make_uint4(h[4], h[5], h[6], h[7]);
+    lo[0] = make_uint4(l[0], l[1], l[2], l[3]);
+    lo[1] = make_uint4(l[4], l[5], l[6], l[7]);
+}
+__device__ __forceinline__ void split8(const uint64_t (&v)[4], uint4& hi, uint4& lo) {
+    uint32_t h[4], l[4];
+    split_pairs<4>(v, h, l);
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// ---------------------------------------------------------------------------
-// fused Q4_K GEMM: the weight operand is dequantised and split inside the
-// kernel, from the raw super-blocks, straight into the swizzled tiles
-// ---------------------------------------------------------------------------
+// Byte k of w as the float 2^23 + byte (one byte-permute into the exponent
+// pattern 0x4B); the caller subtracts 2^23 (plus any offset) exactly.
+__device__ __forceinline__ float byte_biased(uint32_t w, int k) {
+    return __int_as_float(__byte_perm(w, 0x4B000000u, 0x7540u + uint32_t(k)));
+}
 
-constexpr int FBM = 128, FBN = 128, FBK = 64;
-constexpr int X_STAGES = 3, W_STAGES = 2, RAW_SLOTS = 3;
-constexpr int F_TILE = FBM * FBK * 2;                 // one 128 x 64 bf16 tile: 16 KB
-constexpr int F_PAIR = 2 * F_TILE;                    // hi and lo tiles of one operand
-constexpr int F_RAW_BYTES = FBN * 144;                // 128 rows of one Q4_K super-block
-constexpr int kConvWarps = 16;                        // converter warps; the first four drain the accumulator
-constexpr int kFusedThreads = 32 * (2 + kConvWarps);
-constexpr size_t kFusedSmem =
-    size_t(X_STAGES + W_STAGES) * F_PAIR + size_t(RAW_SLOTS) * F_RAW_BYTES + 1024 + 256;
-static_assert(F_RAW_BYTES % 1024 == 0, "raw slots keep the 1024-byte alignment");
-constexpr uint32_t kIdescF =
-    (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(FBN >> 3) << 17) | (uint32_t(FBM >> 4) << 24);
+// N little-endian words at the 2-byte-aligned shared-memory address p: N + 1
+// aligned words, funnel-shifted (reads up to 4 bytes past the N words).
+template <int N>
+__device__ __forceinline__ void words_a2(const uint8_t* p, uint32_t (&out)[N]) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
+    const uint32_t sh = static_cast<uint32_t>(a & 3u) * 8u;
+    uint32_t prev = w[0];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const uint32_t next = w[i + 1];
+        out[i] = __funnelshift_r(prev, next, sh);
+        prev = next;
+    }
+}
 
-struct FusedParams {
-    CUtensorMap x_map[2];  // Xh, Xl: [M, K] bf16, boxes 64 x 128, 128-byte swizzle
-    CUtensorMap w_map;     // Q4_K rows as bytes [N, row_bytes], boxes 144 x 128
-    int M, N, K;
-    float* Y;
-    unsigned* err;
-    unsigned long long wait_ns;
-};
+__device__ __forceinline__ float f16_at_a2(const uint8_t* p) {
+    return __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(p)));
+}
 
-// One row's quarter of a 64-wide K slice (chunk c of the super-block): 16
-// weights of sub-block 2c + half, the column groups 4 half + g0 and
-// 4 half + g0 + 1 (g0 = 0 or 2), dequantised and split into hi and lo bf16.
-// The sub-block's weights are the low nibbles (half 0) or high nibbles
-// (half 1) of the chunk's 32 quant bytes.
-__device__ __forceinline__ void q4k_convert_quarter(const uint8_t* rawrow, int c, int half, int g0, uint4 (&hi)[2],
-                                                    uint4 (&lo)[2]) {
-    const uint4 hdr = *reinterpret_cast<const uint4*>(rawrow);
-    const uint4 qv = *reinterpret_cast<const uint4*>(rawrow + 16 + 32 * c + 8 * g0);
+// Bytes k, k + 1 of w as the packed floats (2^23 + byte_k, 2^23 + byte_k+1).
+__device__ __forceinline__ uint64_t byte_pair_biased(uint32_t w, int k) {
+    return f32x2_pack(byte_biased(w, k), byte_biased(w, k + 1));
+}
+
+// The activation: xhat = dx * q for the 16 codes at `codes` (16-byte aligned);
+// q - 0 comes out exactly (bytes offset by 128 into 2^23 + 128 + q, minus the
+// same), then one rounding in the multiply.
+__device__ __forceinline__ void convert_x16(const uint8_t* codes, float dx, uint4 (&hi)[2], uint4 (&lo)[2]) {
+    const uint4 c = *reinterpret_cast<const uint4*>(codes);
+    const uint32_t w[4] = {c.x ^ 0x80808080u, c.y ^ 0x80808080u, c.z ^ 0x80808080u, c.w ^ 0x80808080u};
+    const uint64_t bias = f32x2_pack(8388736.0f, 8388736.0f), dx2 = f32x2_pack(dx, dx);  // 2^23 + 128
+    uint64_t v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = f32x2_mul(f32x2_sub(byte_pair_biased(w[i >> 1], 2 * (i & 1)), bias), dx2);
+    split16(v, hi, lo);
+}
+
+// The weights: elements 8 qq .. 8 qq + 7 of K slice c (32 wide) of the group
+// whose bytes start at `blk` (2-byte aligned), as one 16-byte chunk of hi and
+// one of lo.
+template <int FMT>
+__device__ __forceinline__ void convert_w8(const uint8_t* blk, int c, int qq, uint4& hi, uint4& lo);
+
+// Q4_K (super-block: d, dmin, 12 bytes of 6-bit scales / mins, 128 bytes of
+// nibbles).  Slice c is sub-block c: the low (c even) or high (c odd) nibbles
+// of quant chunk c / 2.  w = d * sc * q - dmin * m.
+template <>
+__device__ __forceinline__ void convert_w8<QX_Q4_K>(const uint8_t* blk, int c, int qq, uint4& hi, uint4& lo) {
+    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
+    const uint2 qv = *reinterpret_cast<const uint2*>(blk + 16 + 32 * (c >> 1) + 8 * qq);
     const float d = __half2float(__ushort_as_half(uint16_t(hdr.x & 0xFFFFu)));
     const float dmin = __half2float(__ushort_as_half(uint16_t(hdr.x >> 16)));
-    const int sub = 2 * c + half;
     int sc, m;
-    if (sub < 4) {
-        sc = (hdr.y >> (8 * sub)) & 63;
-        m = (hdr.z >> (8 * sub)) & 63;
+    if (c < 4) {
+        sc = (hdr.y >> (8 * c)) & 63;
+        m = (hdr.z >> (8 * c)) & 63;
     } else {
-        const int u = sub - 4;
+        const int u = c - 4;
         sc = ((hdr.w >> (8 * u)) & 15) | (((hdr.y >> (8 * u + 6)) & 3) << 4);
         m = ((hdr.w >> (8 * u + 4)) & 15) | (((hdr.z >> (8 * u + 6)) & 3) << 4);
     }
     const float a = d * float(sc), cm = dmin * float(m);  // exact products
-    const uint32_t sh = 4u * uint32_t(half);
-    // the nibbles of this half, one per byte
-    const uint32_t nb[4] = {(qv.x >> sh) & 0x0F0F0F0Fu, (qv.y >> sh) & 0x0F0F0F0Fu, (qv.z >> sh) & 0x0F0F0F0Fu,
-                            (qv.w >> sh) & 0x0F0F0F0Fu};
+    const uint32_t sh = 4u * uint32_t(c & 1);
+    const uint32_t nb[2] = {(qv.x >> sh) & 0x0F0F0F0Fu, (qv.y >> sh) & 0x0F0F0F0Fu};
+    const uint64_t bias = f32x2_pack(8388608.0f, 8388608.0f), a2 = f32x2_pack(a, a), ncm = f32x2_pack(-cm, -cm);
+    uint64_t v[4];
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
-        uint32_t h[4], l[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t word = nb[2 * g + (i >> 1)];
-            const int b0 = 2 * (i & 1);
-            const float w0 = fmaf(a, float((word >> (8 * b0)) & 0xFFu), -cm);
-            const float w1 = fmaf(a, float((word >> (8 * b0 + 8)) & 0xFFu), -cm);
-            const __nv_bfloat162 hb = __floats2bfloat162_rn(w0, w1);
-            const float2 hf = __bfloat1622float2(hb);
-            const __nv_bfloat162 lb = __floats2bfloat162_rn(w0 - hf.x, w1 - hf.y);
-            h[i] = *reinterpret_cast<const uint32_t*>(&hb);
-            l[i] = *reinterpret_cast<const uint32_t*>(&lb);
-        }
-        hi[g] = make_uint4(h[0], h[1], h[2], h[3]);
-        lo[g] = make_uint4(l[0], l[1], l[2], l[3]);
-    }
+    for (int i = 0; i < 4; ++i)  // d * sc * q - dmin * m with one rounding (a fused multiply-add)
+        v[i] = f32x2_fma(a2, f32x2_sub(byte_pair_biased(nb[i >> 1], 2 * (i & 1)), bias), ncm);
+    split8(v, hi, lo);
 }
 
-// blockIdx.x: M tile (fastest), blockIdx.y: N tile.  Warp 0: TMA producer
-// (activation tiles per K step, raw super-blocks two ahead); warp 1: tensor
-// memory and the MMA issuer (three split products per K slice); warps 2-17:
-// convert raw super-blocks into the Wh / Wl tiles; warps 2-5 then drain the
-// accumulator (warp w reads tensor-memory lanes 32 (w % 4) .. + 31).
-__global__ void __launch_bounds__(kFusedThreads, 1) tc_q4k_fused_kernel(const __grid_constant__ FusedParams p) {
+// Q6_K (ql[128], qh[64], scales[16] int8, d f16; element e = 128 h + 32 t + l
+// has its low four bits in ql[64 h + 32 (t & 1) + l] -- the low nibble for
+// t < 2 -- and its high two bits at bits 2t of qh[32 h + l]).  Slice c is
+// h = c / 4, t = c % 4; the thread's l = 8 qq .. 8 qq + 7 share scale
+// 2c + qq / 2.  w = d * sc * (q - 32).
+template <>
+__device__ __forceinline__ void convert_w8<QX_Q6_K>(const uint8_t* blk, int c, int qq, uint4& hi, uint4& lo) {
+    const int h = c >> 2, t = c & 3, l0 = 8 * qq;
+    uint32_t ql[2], qh[2];
+    words_a2<2>(blk + 64 * h + 32 * (t & 1) + l0, ql);
+    words_a2<2>(blk + 128 + 32 * h + l0, qh);
+    const float a = f16_at_a2(blk + 208) * float(reinterpret_cast<const int8_t*>(blk)[192 + 2 * c + (qq >> 1)]);
+    const uint32_t nsh = (t >= 2) ? 4u : 0u, hsh = 2u * uint32_t(t);
+    const uint64_t bias = f32x2_pack(8388640.0f, 8388640.0f), a2 = f32x2_pack(a, a);  // 2^23 + 32
+    uint64_t v[4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const uint32_t q = ((ql[j] >> nsh) & 0x0F0F0F0Fu) | (((qh[j] >> hsh) & 0x03030303u) << 4);
+        v[2 * j] = f32x2_mul(a2, f32x2_sub(byte_pair_biased(q, 0), bias));
+        v[2 * j + 1] = f32x2_mul(a2, f32x2_sub(byte_pair_biased(q, 2), bias));
+    }
+    split8(v, hi, lo);
+}
+
+// Q8_0 (blocks of d f16 and 32 int8), four blocks per group: slice c is
+// block c.  w = d * q.
+template <>
+__device__ __forceinline__ void convert_w8<QX_Q8_0>(const uint8_t* blk, int c, int qq, uint4& hi, uint4& lo) {
+    const uint8_t* b = blk + 34 * c;
+    uint32_t qw[2];
+    words_a2<2>(b + 2 + 8 * qq, qw);
+    const float d = f16_at_a2(b);
+    const uint64_t bias = f32x2_pack(8388736.0f, 8388736.0f), d2 = f32x2_pack(d, d);  // 2^23 + 128
+    uint64_t v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        v[i] = f32x2_mul(d2, f32x2_sub(byte_pair_biased(qw[i >> 1] ^ 0x80808080u, 2 * (i & 1)), bias));
+    split8(v, hi, lo);
+}
+
+// ---------------------------------------------------------------------------
+// the GEMM
+// ---------------------------------------------------------------------------
+
+// blockIdx.x: M tile (fastest, so the CTAs that share a weight tile run
+// together and read it from DRAM once), blockIdx.y: N tile.
+//   warp 0: TMA producer (the whole warp: per-row boxes take four rows a lane);
+//   warp 1: tensor memory (two 128-column accumulators) and the MMA issuer;
+//   warps 2-17: converters -- per K slice, thread ct converts X row ct / 2
+//           (16 codes, half ct % 2) and weight row ct / 4 (8 values, quarter
+//           ct % 4); warps 2-9 then drain the accumulators (warp w: rows
+//           128 ((w - 2) / 4) + 32 (w % 4) .. + 31 of the tile).
+template <int FMT>
+__global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_constant__ TcParams p) {
+    using G = RawGeom<FMT>;
+    constexpr int SPG = G::kGroupK / TBK;        // K slices per raw group
+    constexpr int RAW_BYTES = raw_slot_bytes<FMT>();
+    constexpr int RAW_TX = G::kBox * TBN;        // bytes the copies of one group bring
+    constexpr int RS = G::kSlots;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t rawaddr = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + ((1024 - (rawaddr & 1023)) & 1023);
-    uint8_t* xst = smem;                                     // [X_STAGES][Xh, Xl]
-    uint8_t* wst = xst + X_STAGES * F_PAIR;                  // [W_STAGES][Wh, Wl]
-    uint8_t* raw = wst + W_STAGES * F_PAIR;                  // [RAW_SLOTS][128 rows x 144 bytes]
-    uint64_t* full_x = reinterpret_cast<uint64_t*>(raw + RAW_SLOTS * F_RAW_BYTES);
-    uint64_t* empty_x = full_x + X_STAGES;
-    uint64_t* full_w = empty_x + X_STAGES;
-    uint64_t* empty_w = full_w + W_STAGES;
-    uint64_t* full_raw = empty_w + W_STAGES;
-    uint64_t* empty_raw = full_raw + RAW_SLOTS;
-    uint64_t* acc_full = empty_raw + RAW_SLOTS;
+    uint8_t* ops = smem;                               // [OP_STAGES][Xh0, Xh1, Xl0, Xl1, Wh, Wl]
+    uint8_t* xr = ops + OP_STAGES * OP_BYTES;          // [XR_STAGES][256 rows x 32 codes]
+    uint8_t* wr = xr + XR_STAGES * XR_BYTES;           // [RS][128 rows of raw blocks]
+    uint64_t* full_op = reinterpret_cast<uint64_t*>(wr + RS * RAW_BYTES);
+    uint64_t* empty_op = full_op + OP_STAGES;
+    uint64_t* full_xr = empty_op + OP_STAGES;
+    uint64_t* empty_xr = full_xr + XR_STAGES;
+    uint64_t* full_wr = empty_xr + XR_STAGES;
+    uint64_t* empty_wr = full_wr + RS;
+    uint64_t* acc_full = empty_wr + RS;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * FBM, n0 = blockIdx.y * FBN;
-    const int n_k = p.K / FBK, n_sb = p.K / 256;
+    const int m0 = blockIdx.x * TBM, n0 = blockIdx.y * TBN;
+    const int halves = (m0 + 128 < p.M) ? 2 : 1;  // 128-row halves of the tile with rows of X
+    const int n_k = p.K / TBK, n_groups = (p.K + G::kGroupK - 1) / G::kGroupK;
+    const bool w2d = FMT == QX_Q4_K || p.w2d != 0;
+    const int wstride = w2d ? G::kBox : kRowStride1d;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < X_STAGES; ++s) {
-            mbar_init(&full_x[s], 1);
-            mbar_init(&empty_x[s], 1);
+        for (int s = 0; s < OP_STAGES; ++s) {
+            mbar_init(&full_op[s], kConvWarps);
+            mbar_init(&empty_op[s], 1);
         }
-        for (int s = 0; s < W_STAGES; ++s) {
-            mbar_init(&full_w[s], kConvWarps);
-            mbar_init(&empty_w[s], 1);
+        for (int s = 0; s < XR_STAGES; ++s) {
+            mbar_init(&full_xr[s], 1);
+            mbar_init(&empty_xr[s], kConvWarps);
         }
-        for (int r = 0; r < RAW_SLOTS; ++r) {
-            mbar_init(&full_raw[r], 1);
-            mbar_init(&empty_raw[r], kConvWarps);
+        for (int r = 0; r < RS; ++r) {
+            mbar_init(&full_wr[r], 1);
+            mbar_init(&empty_wr[r], kConvWarps);
         }
         mbar_init(acc_full, 1);
         fence_barrier_init();
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
-                     "r"(FBN)
+                     "r"(2 * TBN)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -437,101 +399,143 @@ __global__ void __launch_bounds__(kFusedThreads, 1) tc_q4k_fused_kernel(const __
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0 && lane == 0) {
-        // ---- producer: activation tiles per K slice, raw super-blocks two ahead
-        int x_issued = 0, raw_issued = 0;
-        auto issue_raw = [&](int sb) {
-            const int r = sb % RAW_SLOTS;
-            if (sb >= RAW_SLOTS &&
-                !mbar_wait_bounded(&empty_raw[r], ((sb / RAW_SLOTS) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty))
+    if (warp == 0) {
+        // ---- producer: raw weight groups up to RS - 1 ahead, an activation tile per slice
+        int wr_issued = 0, xr_issued = 0;
+        bool ok = true;
+        const auto issue_group = [&](int g) -> bool {
+            const int r = g % RS;
+            if (g >= RS && !warp_wait(&empty_wr[r], ((g / RS) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty))
                 return false;
-            mbar_arrive_expect_tx(&full_raw[r], F_RAW_BYTES);
-            tma_load_2d(raw + r * F_RAW_BYTES, &p.w_map, sb * 144, n0, &full_raw[r]);
-            raw_issued = sb + 1;
+            uint8_t* dst = wr + r * RAW_BYTES;
+            if (lane == 0) mbar_arrive_expect_tx(&full_wr[r], RAW_TX);
+            __syncwarp();
+            if (w2d) {
+                // the same offset in every row: one box, from the 16-byte boundary at or below the group
+                if (lane == 0)
+                    tma_load_2d(dst, &p.w_map, (g * G::kGroupBytes) & ~15, n0, &full_wr[r]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < TBN / 32; ++i) {
+                    const int row = lane + 32 * i;
+                    const int64_t a = int64_t(n0 + row) * p.row_bytes + int64_t(g) * G::kGroupBytes;
+                    tma_load_1d(dst + row * kRowStride1d, &p.w_map, static_cast<int>(a & ~int64_t(15)), &full_wr[r]);
+                }
+            }
+            wr_issued = g + 1;
             return true;
         };
-        bool ok = issue_raw(0);
-        if (ok && n_sb > 1) ok = issue_raw(1);
+        for (int g = 0; g < RS - 1 && g < n_groups && ok; ++g) ok = issue_group(g);
         for (int t = 0; t < n_k && ok; ++t) {
-            const int s = t % X_STAGES;
-            if (t >= X_STAGES &&
-                !mbar_wait_bounded(&empty_x[s], ((t / X_STAGES) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty))
+            const int ga = t / SPG + RS - 1;  // the group RS - 1 ahead of this slice's
+            if (t % SPG == 0 && ga < n_groups && !issue_group(ga)) break;
+            const int s = t % XR_STAGES;
+            if (t >= XR_STAGES && !warp_wait(&empty_xr[s], ((t / XR_STAGES) - 1) & 1, p.wait_ns, p.err,
+                                             kErrTimeoutEmpty))
                 break;
-            uint8_t* st = xst + s * F_PAIR;
-            mbar_arrive_expect_tx(&full_x[s], F_PAIR);
-            tma_load_2d(st, &p.x_map[0], t * FBK, m0, &full_x[s]);
-            tma_load_2d(st + F_TILE, &p.x_map[1], t * FBK, m0, &full_x[s]);
-            x_issued = t + 1;
-            if ((t & 3) == 0 && t / 4 + 2 < n_sb) ok = issue_raw(t / 4 + 2);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full_xr[s], XR_BYTES);
+                tma_load_2d(xr + s * XR_BYTES, &p.x_map, t * TBK, m0, &full_xr[s]);
+            }
+            xr_issued = t + 1;
         }
         // keep the CTA alive until every copy it issued has landed
-        for (int t = x_issued > X_STAGES ? x_issued - X_STAGES : 0; t < x_issued; ++t)
-            mbar_wait_bounded(&full_x[t % X_STAGES], (t / X_STAGES) & 1, p.wait_ns, p.err, kErrTimeoutDrain);
-        for (int sb = raw_issued > RAW_SLOTS ? raw_issued - RAW_SLOTS : 0; sb < raw_issued; ++sb)
-            mbar_wait_bounded(&full_raw[sb % RAW_SLOTS], (sb / RAW_SLOTS) & 1, p.wait_ns, p.err, kErrTimeoutDrain);
-    } else if (warp == 1 && lane == 0) {
-        // ---- MMA issuer: Xh Wh + Xh Wl + Xl Wh per K slice of 64
-        for (int t = 0; t < n_k; ++t) {
-            const int sx = t % X_STAGES, sw = t % W_STAGES;
-            if (!mbar_wait_bounded(&full_x[sx], (t / X_STAGES) & 1, p.wait_ns, p.err, kErrTimeoutMma)) break;
-            if (!mbar_wait_bounded(&full_w[sw], (t / W_STAGES) & 1, p.wait_ns, p.err, kErrTimeoutMma)) break;
-            tc_fence_after();
-            const uint32_t xa = smem_addr(xst + sx * F_PAIR), wa = smem_addr(wst + sw * F_PAIR);
-            const uint64_t xh = sw128_desc(xa), xl = sw128_desc(xa + F_TILE);
-            const uint64_t wh = sw128_desc(wa), wl = sw128_desc(wa + F_TILE);
-#pragma unroll
-            for (int k = 0; k < FBK / 16; ++k) {
-                const uint64_t o = uint64_t(2 * k);
-                tc_mma(tmem, xh + o, wh + o, kIdescF, (t | k) != 0 ? 1u : 0u);
-                tc_mma(tmem, xh + o, wl + o, kIdescF, 1u);
-                tc_mma(tmem, xl + o, wh + o, kIdescF, 1u);
-            }
-            tc_commit(&empty_x[sx]);  // both arrive once these MMAs have read their operands
-            tc_commit(&empty_w[sw]);
+        if (lane == 0) {
+            for (int t = xr_issued > XR_STAGES ? xr_issued - XR_STAGES : 0; t < xr_issued; ++t)
+                mbar_wait_bounded(&full_xr[t % XR_STAGES], (t / XR_STAGES) & 1, p.wait_ns, p.err, kErrTimeoutDrain);
+            for (int g = wr_issued > RS ? wr_issued - RS : 0; g < wr_issued; ++g)
+                mbar_wait_bounded(&full_wr[g % RS], (g / RS) & 1, p.wait_ns, p.err, kErrTimeoutDrain);
         }
-        tc_commit(acc_full);  // also after a failed wait: arrives once the issued MMAs are done
-    } else if (warp >= 2) {
-        // ---- converters: thread ct takes row ct / 4, sub-block half (ct / 2) % 2,
-        //      column groups 2 (ct % 2) and 2 (ct % 2) + 1 of that half
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---- MMA issuer: per half, Xh Wh + Xh Wl + Xl Wh per K slice of 32
+            for (int t = 0; t < n_k; ++t) {
+                const int s = t % OP_STAGES;
+                if (!mbar_wait_bounded(&full_op[s], (t / OP_STAGES) & 1, p.wait_ns, p.err, kErrTimeoutMma)) break;
+                tc_fence_after();
+                const uint32_t base = smem_addr(ops + s * OP_BYTES);
+                const uint64_t wh = sw64_desc(base + OP_WH), wl = sw64_desc(base + OP_WL);
+                for (int a = 0; a < halves; ++a) {
+                    const uint64_t xh = sw64_desc(base + OP_XH + a * T_TILE), xl = sw64_desc(base + OP_XL + a * T_TILE);
+                    const uint32_t acc = tmem + uint32_t(a * TBN);
+#pragma unroll
+                    for (int k = 0; k < TBK / 16; ++k) {  // K = 16 per MMA: 32 bytes further along the swizzled row
+                        const uint64_t o = uint64_t(2 * k);
+                        tc_mma(acc, xh + o, wh + o, kIdesc, (t | k) != 0 ? 1u : 0u);
+                        tc_mma(acc, xh + o, wl + o, kIdesc, 1u);
+                        tc_mma(acc, xl + o, wh + o, kIdesc, 1u);
+                    }
+                }
+                tc_commit(&empty_op[s]);  // arrives once these MMAs have read the stage
+            }
+            tc_commit(acc_full);  // also after a failed wait: arrives once the issued MMAs are done
+        }
+    } else {
+        // ---- converters
         const int ct = threadIdx.x - 64;
-        const int row = ct >> 2, half = (ct >> 1) & 1, g0 = 2 * (ct & 1);
+        const int xrow = ct >> 1, xh = ct & 1;  // X: row of the tile, half of the slice
+        const int wrow = ct >> 2, wq = ct & 3;  // W: row of the tile, quarter of the slice
+        const int xm = m0 + xrow;
+        const int nblk_x = p.K / 32;
+        const float* xd_row = p.xd + int64_t(xm < p.M ? xm : 0) * nblk_x;
+        const auto load_dx = [&](int t) -> float { return xm < p.M ? xd_row[t] : 0.0f; };  // block t of the row
+        // scales two slices ahead, in flight while the slices before them convert
+        float dx0 = load_dx(0), dx1 = n_k > 1 ? load_dx(1) : 0.0f;
+        const uint32_t xa = uint32_t(OP_XH + (xrow >> 7) * T_TILE), xla = uint32_t(OP_XL + (xrow >> 7) * T_TILE);
+        const int xr7 = xrow & 127;
         bool ok = true;
         for (int t = 0; t < n_k && ok; ++t) {
-            const int sb = t >> 2, c = t & 3, r = sb % RAW_SLOTS, s = t % W_STAGES;
-            if ((c == 0 && !warp_wait(&full_raw[r], (sb / RAW_SLOTS) & 1, p.wait_ns, p.err, kErrTimeoutFull)) ||
-                (t >= W_STAGES &&
-                 !warp_wait(&empty_w[s], ((t / W_STAGES) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty))) {
+            const int g = t / SPG, c = t % SPG, r = g % RS, s = t % OP_STAGES, xs = t % XR_STAGES;
+            const float dx = dx0;
+            dx0 = dx1;
+            if (t + 2 < n_k) dx1 = load_dx(t + 2);
+            if ((c == 0 && !warp_wait(&full_wr[r], (g / RS) & 1, p.wait_ns, p.err, kErrTimeoutFull)) ||
+                !warp_wait(&full_xr[xs], (t / XR_STAGES) & 1, p.wait_ns, p.err, kErrTimeoutFull) ||
+                (t >= OP_STAGES &&
+                 !warp_wait(&empty_op[s], ((t / OP_STAGES) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty))) {
                 ok = false;
                 break;
             }
-            uint8_t* whs = wst + s * F_PAIR + row * 128;
-            uint4 hi[2], lo[2];
-            q4k_convert_quarter(raw + r * F_RAW_BYTES + row * 144, c, half, g0, hi, lo);
-#pragma unroll
-            for (int g = 0; g < 2; ++g) {  // 128-byte swizzle: column group j of row r at (j ^ (r % 8)) * 16
-                const uint32_t off = uint32_t(((4 * half + g0 + g) ^ (row & 7)) * 16);
-                *reinterpret_cast<uint4*>(whs + off) = hi[g];
-                *reinterpret_cast<uint4*>(whs + F_TILE + off) = lo[g];
+            uint4 xhi[2], xlo[2], whi, wlo;
+            convert_x16(xr + xs * XR_BYTES + xrow * TBK + 16 * xh, dx, xhi, xlo);
+            {
+                const int64_t a = int64_t(n0 + wrow) * p.row_bytes + int64_t(g) * G::kGroupBytes;
+                const uint8_t* blk = wr + r * RAW_BYTES + wrow * wstride + (a & 15);  // the group in its box
+                convert_w8<FMT>(blk, c, wq, whi, wlo);
             }
+            uint8_t* st = ops + s * OP_BYTES;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const uint32_t off = sw64_off(xr7, 2 * xh + i);
+                *reinterpret_cast<uint4*>(st + xa + off) = xhi[i];
+                *reinterpret_cast<uint4*>(st + xla + off) = xlo[i];
+            }
+            const uint32_t woff = sw64_off(wrow, wq);
+            *reinterpret_cast<uint4*>(st + OP_WH + woff) = whi;
+            *reinterpret_cast<uint4*>(st + OP_WL + woff) = wlo;
             fence_proxy_async_smem();  // generic-proxy stores, read by the tensor cores
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&full_w[s]);
-                if (c == 3) mbar_arrive(&empty_raw[r]);
+                mbar_arrive(&full_op[s]);
+                mbar_arrive(&empty_xr[xs]);
+                if (c == SPG - 1 || t == n_k - 1) mbar_arrive(&empty_wr[r]);
             }
         }
-        // ---- epilogue: warps 2-5; warp w reads tensor-memory lanes 32 (w % 4) .. + 31
-        if (warp < 6 && warp_wait(acc_full, 0, p.wait_ns, p.err, kErrTimeoutMma) && ok) {
+        // ---- epilogue: warps 2-9; warp w drains rows 32 (w % 4) .. + 31 of accumulator (w - 2) / 4
+        const int half = (warp - 2) >> 2;
+        if (warp < 10 && warp_wait(acc_full, 0, p.wait_ns, p.err, kErrTimeoutMma) && ok && half < halves) {
             tc_fence_after();
             const int q = warp & 3;
-            const int yr = m0 + 32 * q + lane;
+            const int yr = m0 + 128 * half + 32 * q + lane;
             const bool row_ok = yr < p.M;
-            const bool vec = (n0 + FBN <= p.N) && (p.N % 4 == 0);
+            // vector stores only where every row of the tile starts 16-byte aligned (Y is only
+            // required to be 4-byte aligned)
+            const bool vec = (n0 + TBN <= p.N) && (p.N % 4 == 0) && (reinterpret_cast<uintptr_t>(p.Y) & 15) == 0;
             float* yrow = p.Y + size_t(row_ok ? yr : 0) * p.N + n0;
 #pragma unroll 1
-            for (int cc = 0; cc < FBN / 32; ++cc) {
+            for (int cc = 0; cc < TBN / 32; ++cc) {
                 uint32_t v[32];
-                tc_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(32 * cc), v);
+                tc_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(half * TBN + 32 * cc), v);
                 if (!row_ok) continue;
                 if (vec) {
                     float4* dst = reinterpret_cast<float4*>(yrow + 32 * cc);
@@ -551,7 +555,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) tc_q4k_fused_kernel(const __
     __syncthreads();
     __syncwarp();
     if (warp == 1)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(FBN) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * TBN) : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -572,128 +576,86 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// [rows, K] bf16 row-major, boxes of 64 K x box_rows rows, 128-byte swizzle.
-bool encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t K, int box_rows) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
-    cuuint64_t strides[1] = {cuuint64_t(K) * 2};
-    cuuint32_t box[2] = {cuuint32_t(BK), cuuint32_t(box_rows)};
-    cuuint32_t es[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// Q4_K rows as a byte matrix [rows, row_bytes], boxes of one super-block
-// (144 bytes) x 128 rows, no swizzle.
-bool encode_raw_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t row_bytes) {
+// A byte matrix [rows, row_bytes] (row_bytes a 16-byte multiple), boxes of
+// box_x bytes x box_rows rows, no swizzle.
+bool encode_bytes_2d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t row_bytes, int box_x, int box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {cuuint64_t(row_bytes), cuuint64_t(rows)};
     cuuint64_t strides[1] = {cuuint64_t(row_bytes)};
-    cuuint32_t box[2] = {144u, cuuint32_t(FBN)};
+    cuuint32_t box[2] = {cuuint32_t(box_x), cuuint32_t(box_rows)};
     cuuint32_t es[2] = {1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+// `bytes` bytes as a one-dimensional tensor, boxes of box_x bytes.
+bool encode_bytes_1d(CUtensorMap* m, const void* ptr, int64_t bytes, int box_x) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[1] = {cuuint64_t(bytes)};
+    cuuint64_t strides[1] = {0};  // no outer dimension, but the encoder wants the array
+    cuuint32_t box[1] = {cuuint32_t(box_x)};
+    cuuint32_t es[1] = {1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, const_cast<void*>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
-cudaError_t configure_smem(const void* kernel, size_t bytes, bool* done) {
+template <int FMT>
+cudaError_t launch_fmt(TcParams& p, const uint8_t* W, int64_t N, const int8_t* xq, int64_t M, int64_t K,
+                       cudaStream_t s) {
+    using G = RawGeom<FMT>;
+    if (!encode_bytes_2d(&p.x_map, xq, M, K, TBK, TBM)) return cudaErrorInvalidValue;
+    p.w2d = (FMT == QX_Q4_K || p.row_bytes % 16 == 0) ? 1 : 0;
+    const bool wok = p.w2d ? encode_bytes_2d(&p.w_map, W, N, p.row_bytes, G::kBox, TBN)
+                           : encode_bytes_1d(&p.w_map, W, N * p.row_bytes, G::kBox);
+    if (!wok) return cudaErrorInvalidValue;
+    static bool configured[64] = {false};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
-    if (e == cudaSuccess) done[dev] = true;
-    return e;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(tc_prefill_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(tc_smem_bytes<FMT>()));
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    const dim3 grid(unsigned((M + TBM - 1) / TBM), unsigned((N + TBN - 1) / TBN));
+    tc_prefill_kernel<FMT><<<grid, kTcThreads, tc_smem_bytes<FMT>(), s>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t prefill_tc_workspace_bytes(int fmt, int64_t N, int64_t K, int64_t M) {
-    const size_t x = 2 * round256(size_t(M) * K * 2);
-    return fmt == QX_Q4_K ? x : x + 2 * round256(size_t(N) * K * 2);  // Q4_K: weights split in-kernel
+bool prefill_tc_serves(int fmt, int64_t N, int64_t K, int64_t M, int64_t row_bytes) {
+    if (fmt != QX_Q4_K && fmt != QX_Q6_K && fmt != QX_Q8_0) return false;
+    // copy coordinates are 32-bit: the last box of the last tile must start below 2^31
+    const int64_t limit = (int64_t(1) << 31) - 4096;
+    const int64_t tiles_n = (N + TBN - 1) / TBN;
+    return M <= INT32_MAX && N <= INT32_MAX && K <= INT32_MAX && tiles_n * TBN * row_bytes < limit;
 }
 
 cudaError_t launch_prefill_tc(int fmt, const uint8_t* W, int64_t N, int64_t K, int64_t row_bytes, const int8_t* xq,
-                              const float* xd, int64_t M, float* Y, void* ws, unsigned* err, cudaStream_t s) {
-    uint8_t* base = static_cast<uint8_t*>(ws);
-    if (fmt == QX_Q4_K) {
-        // activation split, then the fused kernel (weights split in shared memory)
-        uint16_t* Xh = reinterpret_cast<uint16_t*>(base);
-        uint16_t* Xl = reinterpret_cast<uint16_t*>(base + round256(size_t(M) * K * 2));
-        const int64_t xthreads = M * (K / 32);
-        dequant_x_kernel<<<unsigned((xthreads + 255) / 256), 256, 0, s>>>(xq, xd, M, K, Xh, Xl);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        FusedParams p;
-        memset(&p, 0, sizeof(p));
-        if (!encode_map(&p.x_map[0], Xh, M, K, FBM) || !encode_map(&p.x_map[1], Xl, M, K, FBM) ||
-            !encode_raw_map(&p.w_map, W, N, row_bytes))
-            return cudaErrorInvalidValue;
-        p.M = int(M);
-        p.N = int(N);
-        p.K = int(K);
-        p.Y = Y;
-        p.err = err;
-        p.wait_ns = 2000000000ull;
-        static bool configured[64] = {false};
-        if ((e = configure_smem(reinterpret_cast<const void*>(tc_q4k_fused_kernel), kFusedSmem, configured)) !=
-            cudaSuccess)
-            return e;
-        const dim3 grid(unsigned((M + FBM - 1) / FBM), unsigned((N + FBN - 1) / FBN));
-        tc_q4k_fused_kernel<<<grid, kFusedThreads, kFusedSmem, s>>>(p);
-        return cudaGetLastError();
-    }
-    uint16_t* Wh = reinterpret_cast<uint16_t*>(base);
-    uint16_t* Wl = reinterpret_cast<uint16_t*>(base + round256(size_t(N) * K * 2));
-    uint16_t* Xh = reinterpret_cast<uint16_t*>(base + 2 * round256(size_t(N) * K * 2));
-    uint16_t* Xl = reinterpret_cast<uint16_t*>(base + 2 * round256(size_t(N) * K * 2) + round256(size_t(M) * K * 2));
-
-    const int64_t wthreads = N * (K / 32), xthreads = M * (K / 32);
-    switch (fmt) {
-        case QX_Q4_K:
-            dequant_w_kernel<QX_Q4_K><<<unsigned((wthreads + 255) / 256), 256, 0, s>>>(W, N, K, row_bytes, Wh, Wl);
-            break;
-        case QX_Q6_K:
-            dequant_w_kernel<QX_Q6_K><<<unsigned((wthreads + 255) / 256), 256, 0, s>>>(W, N, K, row_bytes, Wh, Wl);
-            break;
-        default:
-            dequant_w_kernel<QX_Q8_0><<<unsigned((wthreads + 255) / 256), 256, 0, s>>>(W, N, K, row_bytes, Wh, Wl);
-            break;
-    }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    dequant_x_kernel<<<unsigned((xthreads + 255) / 256), 256, 0, s>>>(xq, xd, M, K, Xh, Xl);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-
+                              const float* xd, int64_t M, float* Y, unsigned* err, cudaStream_t s) {
     TcParams p;
     memset(&p, 0, sizeof(p));
-    if (!encode_map(&p.a_map[0], Xh, M, K, BM) || !encode_map(&p.a_map[1], Xl, M, K, BM) ||
-        !encode_map(&p.b_map[0], Wh, N, K, BN) || !encode_map(&p.b_map[1], Wl, N, K, BN))
-        return cudaErrorInvalidValue;
+    p.xd = xd;
     p.M = int(M);
     p.N = int(N);
     p.K = int(K);
+    p.row_bytes = row_bytes;
     p.Y = Y;
     p.err = err;
     p.wait_ns = 2000000000ull;
-    static bool configured[64] = {false};
-    int dev = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kTcSmem));
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
+    switch (fmt) {
+        case QX_Q4_K: return launch_fmt<QX_Q4_K>(p, W, N, xq, M, K, s);
+        case QX_Q6_K: return launch_fmt<QX_Q6_K>(p, W, N, xq, M, K, s);
+        case QX_Q8_0: return launch_fmt<QX_Q8_0>(p, W, N, xq, M, K, s);
+        default: return cudaErrorInvalidValue;
     }
-    const dim3 grid(unsigned((M + BM - 1) / BM), unsigned((N + BN - 1) / BN));
-    tc_gemm_kernel<<<grid, kTcThreads, kTcSmem, s>>>(p);
-    return cudaGetLastError();
 }
 
 }  // namespace qx

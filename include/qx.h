@@ -33,12 +33,10 @@
  *     library keeps no per-call state.  Per device it holds: one cached
  *     device-property query, the device error word (below), and the
  *     QX_CHAIN_MAX_JOBS + 1 arrival counters of qx_gemv_chain_noalloc (file-
- *     scope device arrays, present on every GPU that loads the library).  It
- *     allocates device memory in two places only: the prefill workspace of
- *     qx_gemm_prefill / qx_gemm_prefill_ex (paths 0 and 3, grown on demand and
- *     kept per device; qx_gemm_prefill_ws takes the caller's instead) and the
- *     short-lived buffer of the measurement hook qx_debug_mma_rate
- *     (qx_debug.h).
+ *     scope device arrays, present on every GPU that loads the library).  No
+ *     entry point of this header allocates device memory; the one allocation
+ *     in the library is the short-lived buffer of the measurement hook
+ *     qx_debug_mma_rate (qx_debug.h).
  *   - Calls are asynchronous on stream `s` (NULL = the legacy default stream)
  *     and run on the current device.  Argument, shape and alignment errors
  *     return before anything is launched or written; a failed launch returns
@@ -185,16 +183,15 @@ qx_status qx_gemm_prefill(qx_fmt fmt, const void* W, int64_t rows, int64_t cols,
  *   3 = tcgen05 tensor-core GEMM, every format: the W4A8 product is the dot
  *       product of the dequantised activation dx*q_x with the dequantised
  *       weight (llamay docs, "Backends and hardware", sections "CPU" and
- *       "CUDA"); both are written once as two bf16 terms (hi + lo, 16
- *       significant bits) and Y = Xh Wh^T + Xh Wl^T + Xl Wh^T is accumulated
- *       in f32 in tensor memory.  Each product's error is about 2^-15 of its
- *       magnitude.  For Q4_K the weight terms are formed inside the GEMM
- *       from the raw super-blocks; the other formats are dequantised into
- *       the workspace first.  Paths 0 and 3 use a workspace of
- *       qx_gemm_prefill_workspace_bytes bytes that the library allocates on
- *       first use per device and keeps (growing it is refused with QX_ERR_ARG
- *       while the stream is being captured into a graph); calls that may run
- *       concurrently on different streams must use qx_gemm_prefill_ws.
+ *       "CUDA"); both are formed inside the kernel, in shared memory, from
+ *       the int8 codes and the raw weight blocks, each as two bf16 terms (hi
+ *       + lo, 16 significant bits), and Y = Xh Wh^T + Xh Wl^T + Xl Wh^T is
+ *       accumulated in f32 in tensor memory.  Each product's error is about
+ *       2^-15 of its magnitude.  No workspace: the call allocates nothing, may
+ *       be captured in a CUDA graph on its first use and may run concurrently
+ *       on several streams.  Shapes whose weights span 2 GiB or more (the
+ *       copy engine's 32-bit coordinates) return QX_ERR_SHAPE; path 0 takes
+ *       path 1 for them.
  *   4 = small-batch GEMV, every format (rows of up to 14336 columns, or
  *       28672 for Q4_K / Q6_K when at most four rows of X remain; path 0
  *       takes path 1 for wider rows): the weights are streamed once per
@@ -210,23 +207,6 @@ qx_status qx_gemm_prefill(qx_fmt fmt, const void* W, int64_t rows, int64_t cols,
  */
 qx_status qx_gemm_prefill_ex(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X,
                              float* Y, int path, qx_stream_t s);
-
-/*
- * Device bytes of the workspace that path 3 needs for this shape (two bf16
- * copies of the activation, 4 * cols * m bytes, plus for Q6_K and Q8_0 two
- * bf16 copies of the weights, 4 * cols * rows bytes; rounded up), or 0 for
- * an invalid shape.
- */
-size_t qx_gemm_prefill_workspace_bytes(qx_fmt fmt, int64_t rows, int64_t cols, int64_t m);
-
-/*
- * qx_gemm_prefill_ex with caller-owned device workspace (16-byte aligned, at
- * least qx_gemm_prefill_workspace_bytes bytes; used by paths 0 and 3, ignored
- * by paths 1 and 2).  QX_ERR_ARG if it is missing or too small.  The
- * workspace is overwritten; it must not be in use by another call.
- */
-qx_status qx_gemm_prefill_ws(qx_fmt fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, float* Y,
-                             int path, void* workspace, size_t workspace_bytes, qx_stream_t s);
 
 /*
  * The exact integer partial sums of the W4A8 product, written instead of y:

@@ -221,18 +221,9 @@ def test_host_code_under_asan_and_ubsan(lib, tmp_path):
 
 
 def test_size_queries_need_no_gpu(lib):
-    """Workspace and scratch sizes follow the header's formulas; invalid shapes give 0."""
-    rows, cols, m = 14336, 4096, 512
-    q4 = qx.qx_gemm_prefill_workspace_bytes(qx.QX_Q4_K, rows, cols, m)
-    q6 = qx.qx_gemm_prefill_workspace_bytes(qx.QX_Q6_K, rows, cols, m)
-    q8 = qx.qx_gemm_prefill_workspace_bytes(qx.QX_Q8_0, rows, cols, m)
-    assert 4 * cols * m <= q4 < 4 * cols * m + (1 << 20)                    # activation hi / lo only
-    for v in (q6, q8):
-        assert 4 * cols * (m + rows) <= v < 4 * cols * (m + rows) + (1 << 20)  # and the weights' hi / lo
-    assert qx.qx_gemm_prefill_workspace_bytes(qx.QX_Q4_K, rows, cols + 1, m) == 0
-    assert qx.qx_gemm_prefill_workspace_bytes(qx.QX_Q4_K, rows, cols, 0) == 0
-    assert qx.qx_gemm_prefill_workspace_bytes(qx.QX_Q4_K, 0, cols, m) == 0
-    assert qx.qx_gemm_prefill_workspace_bytes(7, rows, cols, m) == 0
+    """Chain scratch sizes follow the header's formula; invalid counts give 0.
+    The prefill needs no workspace: the header declares no size query for one."""
+    assert not [n for n in declared_functions() if "workspace" in n]
     assert qx.qx_gemv_chain_scratch_bytes(1) == 8
     assert qx.qx_gemv_chain_scratch_bytes(qx.QX_CHAIN_MAX_JOBS) == 4 * (qx.QX_CHAIN_MAX_JOBS + 1)
     assert qx.qx_gemv_chain_scratch_bytes(0) == 0

@@ -373,40 +373,43 @@ def test_prefill_auto_and_refusals():
     assert ei.value.status == qx.QX_ERR_ARG
 
 
-@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")  # the refused capture below launches nothing
-def test_prefill_caller_workspace_and_graph_capture():
-    fmt, rows, cols, m = synth.Q6_K, 200, 2048, 48
-    W = dev(synth.weights(fmt, rows, cols, seed=66))
-    a, q, d, s = quantize_both(synth.activation(m, cols, seed=67))
-    need = qx.qx_gemm_prefill_workspace_bytes(fmt, rows, cols, m)
-    assert need >= 4 * cols * (rows + m)
-    assert 4 * cols * m <= qx.qx_gemm_prefill_workspace_bytes(synth.Q4_K, rows, cols, m) < need
-    assert qx.qx_gemm_prefill_workspace_bytes(fmt, rows, cols + 1, m) == 0
-    y_lib = host(qx.qx_gemm_prefill_ex(fmt, W, rows, cols, a, path=3))
-    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
-    y_ws = host(qx.qx_gemm_prefill_ws(fmt, W, rows, cols, a, path=3, workspace=ws))
-    assert np.array_equal(y_lib.view(np.uint32), y_ws.view(np.uint32))
-    with pytest.raises(qx.QxError) as ei:
-        qx.qx_gemm_prefill_ws(fmt, W, rows, cols, a, path=3, workspace=ws[: need - 256])
-    assert ei.value.status == qx.QX_ERR_ARG
-    # caller workspace: the whole prefill is capturable and replays to the same bits
-    Y = torch.full((m, rows), float("nan"), device="cuda")
+def test_prefill_tcgen05_capturable_on_first_use_and_on_two_streams():
+    """The tcgen05 path allocates nothing: its very first call on a fresh shape
+    can be captured in a CUDA graph, and two streams can run it at once (no
+    shared workspace), each giving the eager result bit for bit."""
+    cases = []
+    for i, (fmt, rows, cols, m) in enumerate([(synth.Q6_K, 200, 2048, 48), (synth.Q8_0, 136, 864, 40),
+                                             (synth.Q4_K, 256, 1024, 33)]):
+        W = dev(synth.weights(fmt, rows, cols, seed=66 + i))
+        a, q, d, s = quantize_both(synth.activation(m, cols, seed=67 + i))
+        cases.append((fmt, W, rows, cols, m, a, q, d))
     stream = torch.cuda.Stream()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        qx.qx_gemm_prefill_ws(fmt, W, rows, cols, a, Y=Y, path=3, workspace=ws, stream=stream)
-    g.replay()
-    assert np.array_equal(host(Y).view(np.uint32), y_lib.view(np.uint32))
-    # the library workspace cannot grow inside a capture: refused before any launch
-    big_rows = 1 << 17
-    Wbig = torch.zeros(big_rows * qx.qx_row_bytes(fmt, cols), dtype=torch.uint8, device="cuda")
-    Ybig = torch.empty((m, big_rows), device="cuda")
-    g2 = torch.cuda.CUDAGraph()
-    with pytest.raises(qx.QxError) as ei:
-        with torch.cuda.graph(g2, stream=stream):
-            qx.qx_gemm_prefill_ex(fmt, Wbig, big_rows, cols, a, Y=Ybig, path=3, stream=stream)
-    assert ei.value.status == qx.QX_ERR_ARG
+    for fmt, W, rows, cols, m, a, q, d in cases:
+        Y = torch.full((m, rows), float("nan"), device="cuda")
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):  # the first call of this shape and format
+            qx.qx_gemm_prefill_ex(fmt, W, rows, cols, a, Y=Y, path=3, stream=stream)
+        g.replay()
+        y_graph = host(Y).copy()
+        y_eager = host(qx.qx_gemm_prefill_ex(fmt, W, rows, cols, a, path=3))
+        assert np.array_equal(y_graph.view(np.uint32), y_eager.view(np.uint32)), synth.NAMES[fmt]
+        ref, absdot = oracle.gemm_w4a8(fmt, host(W), rows, cols, q, d)
+        assert_close(y_eager.reshape(-1), ref.reshape(-1), absdot.reshape(-1), f"captured {synth.NAMES[fmt]}")
+    # two streams, interleaved launches of two different problems, many times over
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    (f1, W1, r1, c1, m1, a1, _, _), (f2, W2, r2, c2, m2, a2, _, _) = cases[0], cases[1]
+    want1 = host(qx.qx_gemm_prefill_ex(f1, W1, r1, c1, a1, path=3))
+    want2 = host(qx.qx_gemm_prefill_ex(f2, W2, r2, c2, a2, path=3))
+    Y1 = [torch.empty((m1, r1), device="cuda") for _ in range(8)]
+    Y2 = [torch.empty((m2, r2), device="cuda") for _ in range(8)]
     torch.cuda.synchronize()
+    for k in range(8):
+        qx.qx_gemm_prefill_ex(f1, W1, r1, c1, a1, Y=Y1[k], path=3, stream=s1)
+        qx.qx_gemm_prefill_ex(f2, W2, r2, c2, a2, Y=Y2[k], path=3, stream=s2)
+    torch.cuda.synchronize()
+    for k in range(8):
+        assert np.array_equal(host(Y1[k]).view(np.uint32), want1.view(np.uint32))
+        assert np.array_equal(host(Y2[k]).view(np.uint32), want2.view(np.uint32))
     assert qx.qx_device_check() == qx.QX_OK
 
 
