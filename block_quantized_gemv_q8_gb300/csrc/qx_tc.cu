@@ -16,12 +16,16 @@
 //
 // One kernel per format, and no pass outside it.  A CTA computes a 256 x 128
 // tile of Y (256 rows of X, 128 weight rows) as two 128 x 128 accumulators in
-// tensor memory that share every converted weight slice.  Per 32-wide K
-// slice, TMA brings the int8 activation codes of the 256 rows into shared
-// memory, and per K group the raw blocks of the 128 weight rows; sixteen
-// converter warps dequantise both, split them into hi and lo bf16 and write
-// them straight into the 64-byte-swizzled K-major tiles the tensor cores read;
-// one thread issues the split products (M = 128, N = 128, K = 16 each).  The
+// tensor memory that share every converted weight slice.  Per K group TMA
+// brings the raw blocks of the 128 weight rows into shared memory; sixteen
+// converter warps dequantise them and the int8 activation codes of the 256
+// rows, 32 columns (one activation block) per K slice, split both into hi and
+// lo bf16 and write them straight into the 64-byte-swizzled K-major tiles the
+// tensor cores read; one thread issues the split products (M = 128, N = 128,
+// K = 16 each).  The activation codes and scales go from global memory (L2:
+// every CTA of an M tile reads them) straight into the converters' registers,
+// several slices ahead; three operand stages let the conversion run up to two
+// slices ahead of the tensor cores.  The
 // library needs no workspace, so the call allocates nothing and may be
 // captured in a CUDA graph on first use.
 //
@@ -51,11 +55,11 @@ namespace qx {
 namespace {
 
 constexpr int TBM = 256, TBN = 128, TBK = 32;  // CTA tile; K slice
-constexpr int OP_STAGES = 2, XR_STAGES = 4;
+constexpr int OP_STAGES = 3;               // operand stages: conversion runs up to two slices ahead of the MMAs
 constexpr int T_TILE = 128 * TBK * 2;       // one 128-row x 32 bf16 tile: 8 KB
 // one K slice of operands: Xh (two 128-row halves), Xl (two halves), Wh, Wl
 constexpr int OP_XH = 0, OP_XL = 2 * T_TILE, OP_WH = 4 * T_TILE, OP_WL = 5 * T_TILE, OP_BYTES = 6 * T_TILE;
-constexpr int XR_BYTES = TBM * TBK;         // int8 codes of 256 rows x 32 columns
+constexpr int kXAhead = 4;                  // slices of activation codes and scales in flight per thread
 constexpr int kConvWarps = 16;              // converter warps; the first eight drain the accumulators
 constexpr int kTcThreads = 32 * (2 + kConvWarps);
 constexpr int kRowStride1d = 256;           // shared-memory row stride of the per-row boxes (128-byte aligned)
@@ -88,16 +92,15 @@ __host__ __device__ constexpr int raw_slot_bytes() {
 
 template <int FMT>
 constexpr size_t tc_smem_bytes() {
-    return size_t(OP_STAGES) * OP_BYTES + size_t(XR_STAGES) * XR_BYTES +
-           size_t(RawGeom<FMT>::kSlots) * raw_slot_bytes<FMT>() + 1024 + 256;
+    return size_t(OP_STAGES) * OP_BYTES + size_t(RawGeom<FMT>::kSlots) * raw_slot_bytes<FMT>() + 1024 + 256;
 }
 static_assert(tc_smem_bytes<QX_Q6_K>() <= 227 * 1024 && tc_smem_bytes<QX_Q8_0>() <= 227 * 1024 &&
                   tc_smem_bytes<QX_Q4_K>() <= 227 * 1024,
               "a CTA's shared memory");
 
 struct TcParams {
-    CUtensorMap x_map;  // q_x as bytes [M rows, K], boxes 32 x 256
     CUtensorMap w_map;  // [N rows, row_bytes] bytes, boxes kBox x 128 (w2d); else all N * row_bytes bytes, 1-D boxes
+    const int8_t* xq;   // [M, K] activation codes, 16-byte aligned (K a multiple of 32)
     const float* xd;    // [M, K / 32] activation scales
     int M, N, K;
     int w2d;            // 1: weight rows are a 16-byte multiple, one 2-D box per group
@@ -243,11 +246,10 @@ __device__ __forceinline__ uint64_t byte_pair_biased(uint32_t w, int k) {
     return f32x2_pack(byte_biased(w, k), byte_biased(w, k + 1));
 }
 
-// The activation: xhat = dx * q for the 16 codes at `codes` (16-byte aligned);
-// q - 0 comes out exactly (bytes offset by 128 into 2^23 + 128 + q, minus the
+// The activation: xhat = dx * q for the 16 codes in c (little-endian bytes);
+// q comes out exactly (bytes offset by 128 into 2^23 + 128 + q, minus the
 // same), then one rounding in the multiply.
-__device__ __forceinline__ void convert_x16(const uint8_t* codes, float dx, uint4 (&hi)[2], uint4 (&lo)[2]) {
-    const uint4 c = *reinterpret_cast<const uint4*>(codes);
+__device__ __forceinline__ void convert_x16(const uint4 c, float dx, uint4 (&hi)[2], uint4 (&lo)[2]) {
     const uint32_t w[4] = {c.x ^ 0x80808080u, c.y ^ 0x80808080u, c.z ^ 0x80808080u, c.w ^ 0x80808080u};
     const uint64_t bias = f32x2_pack(8388736.0f, 8388736.0f), dx2 = f32x2_pack(dx, dx);  // 2^23 + 128
     uint64_t v[8];
@@ -340,7 +342,8 @@ __device__ __forceinline__ void convert_w8<QX_Q8_0>(const uint8_t* blk, int c, i
 //   warp 0: TMA producer (the whole warp: per-row boxes take four rows a lane);
 //   warp 1: tensor memory (two 128-column accumulators) and the MMA issuer;
 //   warps 2-17: converters -- per K slice, thread ct converts X row ct / 2
-//           (16 codes, half ct % 2) and weight row ct / 4 (8 values, quarter
+//           (16 codes, half ct % 2; zeros past M, nothing stored for an
+//           unused half) and weight row ct / 4 (8 values, quarter
 //           ct % 4); warps 2-9 then drain the accumulators (warp w: rows
 //           128 ((w - 2) / 4) + 32 (w % 4) .. + 31 of the tile).
 template <int FMT>
@@ -354,13 +357,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
     const uint32_t rawaddr = smem_addr(smem_raw);
     uint8_t* smem = smem_raw + ((1024 - (rawaddr & 1023)) & 1023);
     uint8_t* ops = smem;                               // [OP_STAGES][Xh0, Xh1, Xl0, Xl1, Wh, Wl]
-    uint8_t* xr = ops + OP_STAGES * OP_BYTES;          // [XR_STAGES][256 rows x 32 codes]
-    uint8_t* wr = xr + XR_STAGES * XR_BYTES;           // [RS][128 rows of raw blocks]
+    uint8_t* wr = ops + OP_STAGES * OP_BYTES;          // [RS][128 rows of raw blocks]
     uint64_t* full_op = reinterpret_cast<uint64_t*>(wr + RS * RAW_BYTES);
     uint64_t* empty_op = full_op + OP_STAGES;
-    uint64_t* full_xr = empty_op + OP_STAGES;
-    uint64_t* empty_xr = full_xr + XR_STAGES;
-    uint64_t* full_wr = empty_xr + XR_STAGES;
+    uint64_t* full_wr = empty_op + OP_STAGES;
     uint64_t* empty_wr = full_wr + RS;
     uint64_t* acc_full = empty_wr + RS;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
@@ -376,10 +376,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
         for (int s = 0; s < OP_STAGES; ++s) {
             mbar_init(&full_op[s], kConvWarps);
             mbar_init(&empty_op[s], 1);
-        }
-        for (int s = 0; s < XR_STAGES; ++s) {
-            mbar_init(&full_xr[s], 1);
-            mbar_init(&empty_xr[s], kConvWarps);
         }
         for (int r = 0; r < RS; ++r) {
             mbar_init(&full_wr[r], 1);
@@ -400,13 +396,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ---- producer: raw weight groups up to RS - 1 ahead, an activation tile per slice
-        int wr_issued = 0, xr_issued = 0;
-        bool ok = true;
-        const auto issue_group = [&](int g) -> bool {
+        // ---- producer: raw weight groups, up to RS ahead of the group being converted
+        int wr_issued = 0;
+        for (int g = 0; g < n_groups; ++g) {
             const int r = g % RS;
-            if (g >= RS && !warp_wait(&empty_wr[r], ((g / RS) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty))
-                return false;
+            if (g >= RS && !warp_wait(&empty_wr[r], ((g / RS) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty)) break;
             uint8_t* dst = wr + r * RAW_BYTES;
             if (lane == 0) mbar_arrive_expect_tx(&full_wr[r], RAW_TX);
             __syncwarp();
@@ -423,29 +417,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
                 }
             }
             wr_issued = g + 1;
-            return true;
-        };
-        for (int g = 0; g < RS - 1 && g < n_groups && ok; ++g) ok = issue_group(g);
-        for (int t = 0; t < n_k && ok; ++t) {
-            const int ga = t / SPG + RS - 1;  // the group RS - 1 ahead of this slice's
-            if (t % SPG == 0 && ga < n_groups && !issue_group(ga)) break;
-            const int s = t % XR_STAGES;
-            if (t >= XR_STAGES && !warp_wait(&empty_xr[s], ((t / XR_STAGES) - 1) & 1, p.wait_ns, p.err,
-                                             kErrTimeoutEmpty))
-                break;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&full_xr[s], XR_BYTES);
-                tma_load_2d(xr + s * XR_BYTES, &p.x_map, t * TBK, m0, &full_xr[s]);
-            }
-            xr_issued = t + 1;
         }
         // keep the CTA alive until every copy it issued has landed
-        if (lane == 0) {
-            for (int t = xr_issued > XR_STAGES ? xr_issued - XR_STAGES : 0; t < xr_issued; ++t)
-                mbar_wait_bounded(&full_xr[t % XR_STAGES], (t / XR_STAGES) & 1, p.wait_ns, p.err, kErrTimeoutDrain);
+        if (lane == 0)
             for (int g = wr_issued > RS ? wr_issued - RS : 0; g < wr_issued; ++g)
                 mbar_wait_bounded(&full_wr[g % RS], (g / RS) & 1, p.wait_ns, p.err, kErrTimeoutDrain);
-        }
     } else if (warp == 1) {
         if (lane == 0) {
             // ---- MMA issuer: per half, Xh Wh + Xh Wl + Xl Wh per K slice of 32
@@ -476,39 +452,54 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
         const int xrow = ct >> 1, xh = ct & 1;  // X: row of the tile, half of the slice
         const int wrow = ct >> 2, wq = ct & 3;  // W: row of the tile, quarter of the slice
         const int xm = m0 + xrow;
-        const int nblk_x = p.K / 32;
-        const float* xd_row = p.xd + int64_t(xm < p.M ? xm : 0) * nblk_x;
-        const auto load_dx = [&](int t) -> float { return xm < p.M ? xd_row[t] : 0.0f; };  // block t of the row
-        // scales two slices ahead, in flight while the slices before them convert
-        float dx0 = load_dx(0), dx1 = n_k > 1 ? load_dx(1) : 0.0f;
+        const bool xlive = xm < p.M;             // rows of X past M are zeros
+        const bool xstore = (xrow >> 7) < halves;  // (warp-uniform) rows of an unused half are never read
+        // The thread's 16 codes of slice t are word 2 t + xh of its row (K is a multiple of 32 and the
+        // codes are 16-byte aligned); codes and scales of kXAhead slices are in flight at a time.
+        const uint4* xq_row = reinterpret_cast<const uint4*>(p.xq + int64_t(xlive ? xm : 0) * p.K) + xh;
+        const float* xd_row = p.xd + int64_t(xlive ? xm : 0) * (p.K / 32);
+        uint4 qa[kXAhead];
+        float da[kXAhead];
+#pragma unroll
+        for (int i = 0; i < kXAhead; ++i) {
+            const bool live = xlive && i < n_k;
+            qa[i] = live ? __ldg(xq_row + 2 * i) : make_uint4(0u, 0u, 0u, 0u);
+            da[i] = live ? __ldg(xd_row + i) : 0.0f;
+        }
         const uint32_t xa = uint32_t(OP_XH + (xrow >> 7) * T_TILE), xla = uint32_t(OP_XL + (xrow >> 7) * T_TILE);
         const int xr7 = xrow & 127;
         bool ok = true;
-        for (int t = 0; t < n_k && ok; ++t) {
-            const int g = t / SPG, c = t % SPG, r = g % RS, s = t % OP_STAGES, xs = t % XR_STAGES;
-            const float dx = dx0;
-            dx0 = dx1;
-            if (t + 2 < n_k) dx1 = load_dx(t + 2);
+        // slice t, its codes and scale in slot j = t % kXAhead (the loop is unrolled by kXAhead so
+        // that j is static), which then takes slice t + kXAhead
+        const auto convert_slice = [&](int t, uint4& qx, float& dx) -> bool {
+            const int g = t / SPG, c = t % SPG, r = g % RS, s = t % OP_STAGES;
             if ((c == 0 && !warp_wait(&full_wr[r], (g / RS) & 1, p.wait_ns, p.err, kErrTimeoutFull)) ||
-                !warp_wait(&full_xr[xs], (t / XR_STAGES) & 1, p.wait_ns, p.err, kErrTimeoutFull) ||
                 (t >= OP_STAGES &&
-                 !warp_wait(&empty_op[s], ((t / OP_STAGES) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty))) {
-                ok = false;
-                break;
-            }
+                 !warp_wait(&empty_op[s], ((t / OP_STAGES) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty)))
+                return false;
             uint4 xhi[2], xlo[2], whi, wlo;
-            convert_x16(xr + xs * XR_BYTES + xrow * TBK + 16 * xh, dx, xhi, xlo);
+            if (xlive) {
+                convert_x16(qx, dx, xhi, xlo);
+            } else {
+                xhi[0] = xhi[1] = xlo[0] = xlo[1] = make_uint4(0u, 0u, 0u, 0u);
+            }
+            if (xlive && t + kXAhead < n_k) {
+                qx = __ldg(xq_row + 2 * (t + kXAhead));
+                dx = __ldg(xd_row + t + kXAhead);
+            }
             {
                 const int64_t a = int64_t(n0 + wrow) * p.row_bytes + int64_t(g) * G::kGroupBytes;
                 const uint8_t* blk = wr + r * RAW_BYTES + wrow * wstride + (a & 15);  // the group in its box
                 convert_w8<FMT>(blk, c, wq, whi, wlo);
             }
             uint8_t* st = ops + s * OP_BYTES;
+            if (xstore) {
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const uint32_t off = sw64_off(xr7, 2 * xh + i);
-                *reinterpret_cast<uint4*>(st + xa + off) = xhi[i];
-                *reinterpret_cast<uint4*>(st + xla + off) = xlo[i];
+                for (int i = 0; i < 2; ++i) {
+                    const uint32_t off = sw64_off(xr7, 2 * xh + i);
+                    *reinterpret_cast<uint4*>(st + xa + off) = xhi[i];
+                    *reinterpret_cast<uint4*>(st + xla + off) = xlo[i];
+                }
             }
             const uint32_t woff = sw64_off(wrow, wq);
             *reinterpret_cast<uint4*>(st + OP_WH + woff) = whi;
@@ -517,8 +508,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&full_op[s]);
-                mbar_arrive(&empty_xr[xs]);
                 if (c == SPG - 1 || t == n_k - 1) mbar_arrive(&empty_wr[r]);
+            }
+            return true;
+        };
+        for (int t0 = 0; t0 < n_k && ok; t0 += kXAhead) {
+#pragma unroll
+            for (int j = 0; j < kXAhead; ++j) {
+                if (ok && t0 + j < n_k) ok = convert_slice(t0 + j, qa[j], da[j]);
             }
         }
         // ---- epilogue: warps 2-9; warp w drains rows 32 (w % 4) .. + 31 of accumulator (w - 2) / 4
@@ -607,7 +604,8 @@ template <int FMT>
 cudaError_t launch_fmt(TcParams& p, const uint8_t* W, int64_t N, const int8_t* xq, int64_t M, int64_t K,
                        cudaStream_t s) {
     using G = RawGeom<FMT>;
-    if (!encode_bytes_2d(&p.x_map, xq, M, K, TBK, TBM)) return cudaErrorInvalidValue;
+    if ((reinterpret_cast<uintptr_t>(xq) & 15) != 0 || K % TBK != 0) return cudaErrorInvalidValue;
+    p.xq = xq;
     p.w2d = (FMT == QX_Q4_K || p.row_bytes % 16 == 0) ? 1 : 0;
     const bool wok = p.w2d ? encode_bytes_2d(&p.w_map, W, N, p.row_bytes, G::kBox, TBN)
                            : encode_bytes_1d(&p.w_map, W, N * p.row_bytes, G::kBox);
