@@ -548,7 +548,7 @@ qx_status prefill_dispatch(qx_fmt fmt, const void* W, int64_t rows, int64_t cols
         DeviceInfo* dev = nullptr;
         if ((st = device_info(&dev)) != QX_OK) return st;
         const cudaError_t e = launch_prefill_tc(fmt, static_cast<const uint8_t*>(W), rows, cols, rb, X->q, X->d, X->m,
-                                                Y, dev->err_word, reinterpret_cast<cudaStream_t>(s));
+                                                Y, dev->err_word, dev->sm_count, reinterpret_cast<cudaStream_t>(s));
         return e == cudaSuccess ? QX_OK : cuda_fail(e, "tcgen05 prefill launch");
     }
     const bool tensor = path == 2;

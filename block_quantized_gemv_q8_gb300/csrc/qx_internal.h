@@ -171,6 +171,6 @@ cudaError_t chain_trace_read(void* host, size_t bytes);
 // cover the shape.
 bool prefill_tc_serves(int fmt, int64_t N, int64_t K, int64_t M, int64_t row_bytes);
 cudaError_t launch_prefill_tc(int fmt, const uint8_t* W, int64_t N, int64_t K, int64_t row_bytes, const int8_t* xq,
-                              const float* xd, int64_t M, float* Y, unsigned* err, cudaStream_t s);
+                              const float* xd, int64_t M, float* Y, unsigned* err, int sm_count, cudaStream_t s);
 
 }  // namespace qx

@@ -104,6 +104,10 @@ struct TcParams {
     const float* xd;    // [M, K / 32] activation scales
     int M, N, K;
     int w2d;            // 1: weight rows are a 16-byte multiple, one 2-D box per group
+    int tiles_m;        // M tiles; tile i is M tile i % tiles_m of N tile i / tiles_m
+    int tile_base;      // the launch's first tile
+    int split;          // 1: two CTAs (a cluster) per tile, one per half of the K groups
+    int g_split;        // K groups of the first half
     int64_t row_bytes;
     float* Y;           // [M, N] f32
     unsigned* err;
@@ -166,6 +170,27 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
                  : "memory");
 }
+// Thread-block clusters: this CTA's rank, the address of one of this CTA's
+// shared-memory locations in the cluster's CTA `rank`, a 16-byte store there,
+// and a barrier over every thread of the cluster.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t peer_addr(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_peer_v4(uint32_t raddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(raddr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -337,8 +362,13 @@ __device__ __forceinline__ void convert_w8<QX_Q8_0>(const uint8_t* blk, int c, i
 // the GEMM
 // ---------------------------------------------------------------------------
 
-// blockIdx.x: M tile (fastest, so the CTAs that share a weight tile run
-// together and read it from DRAM once), blockIdx.y: N tile.
+// Tiles are numbered M tile fastest, so the CTAs that share a weight tile run
+// together and read it from DRAM once.  A launch takes tiles tile_base ..:
+// one CTA per tile, or (split) a cluster of two CTAs per tile, one per half of
+// the K groups, whose second CTA hands its f32 partial sums to the first
+// through distributed shared memory (Y = first half + second half, in that
+// order).  The host splits the tiles of a last, at most half-full wave, so
+// that it takes half as long.
 //   warp 0: TMA producer (the whole warp: per-row boxes take four rows a lane);
 //   warp 1: tensor memory (two 128-column accumulators) and the MMA issuer;
 //   warps 2-17: converters -- per K slice, thread ct converts X row ct / 2
@@ -366,11 +396,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * TBM, n0 = blockIdx.y * TBN;
+    const int tile = p.tile_base + (p.split ? int(blockIdx.x >> 1) : int(blockIdx.x));
+    const int m0 = (tile % p.tiles_m) * TBM, n0 = (tile / p.tiles_m) * TBN;
     const int halves = (m0 + 128 < p.M) ? 2 : 1;  // 128-row halves of the tile with rows of X
     const int n_k = p.K / TBK, n_groups = (p.K + G::kGroupK - 1) / G::kGroupK;
+    // this CTA's K groups [g0, g1) and slices [t0, t1); ring positions count from g0 and t0
+    const uint32_t rank = p.split ? cluster_rank() : 0u;
+    const int g0 = rank == 0 ? 0 : p.g_split, g1 = (p.split && rank == 0) ? p.g_split : n_groups;
+    const int t0 = g0 * SPG, t1 = g1 * SPG < n_k ? g1 * SPG : n_k;
     const bool w2d = FMT == QX_Q4_K || p.w2d != 0;
     const int wstride = w2d ? G::kBox : kRowStride1d;
+    if (!p.split) pdl_launch_dependents();  // a split launch of the last tiles may start beside this one
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < OP_STAGES; ++s) {
@@ -394,13 +430,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    bool ok = true;  // converter warps: every wait of the main loop succeeded
 
     if (warp == 0) {
         // ---- producer: raw weight groups, up to RS ahead of the group being converted
-        int wr_issued = 0;
-        for (int g = 0; g < n_groups; ++g) {
-            const int r = g % RS;
-            if (g >= RS && !warp_wait(&empty_wr[r], ((g / RS) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty)) break;
+        int wr_issued = 0;  // ring positions issued
+        for (int g = g0; g < g1; ++g) {
+            const int lg = g - g0, r = lg % RS;
+            if (lg >= RS && !warp_wait(&empty_wr[r], ((lg / RS) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty)) break;
             uint8_t* dst = wr + r * RAW_BYTES;
             if (lane == 0) mbar_arrive_expect_tx(&full_wr[r], RAW_TX);
             __syncwarp();
@@ -416,7 +453,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
                     tma_load_1d(dst + row * kRowStride1d, &p.w_map, static_cast<int>(a & ~int64_t(15)), &full_wr[r]);
                 }
             }
-            wr_issued = g + 1;
+            wr_issued = lg + 1;
         }
         // keep the CTA alive until every copy it issued has landed
         if (lane == 0)
@@ -425,9 +462,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
     } else if (warp == 1) {
         if (lane == 0) {
             // ---- MMA issuer: per half, Xh Wh + Xh Wl + Xl Wh per K slice of 32
-            for (int t = 0; t < n_k; ++t) {
-                const int s = t % OP_STAGES;
-                if (!mbar_wait_bounded(&full_op[s], (t / OP_STAGES) & 1, p.wait_ns, p.err, kErrTimeoutMma)) break;
+            for (int lt = 0; lt < t1 - t0; ++lt) {
+                const int s = lt % OP_STAGES;
+                if (!mbar_wait_bounded(&full_op[s], (lt / OP_STAGES) & 1, p.wait_ns, p.err, kErrTimeoutMma)) break;
                 tc_fence_after();
                 const uint32_t base = smem_addr(ops + s * OP_BYTES);
                 const uint64_t wh = sw64_desc(base + OP_WH), wl = sw64_desc(base + OP_WL);
@@ -437,7 +474,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
 #pragma unroll
                     for (int k = 0; k < TBK / 16; ++k) {  // K = 16 per MMA: 32 bytes further along the swizzled row
                         const uint64_t o = uint64_t(2 * k);
-                        tc_mma(acc, xh + o, wh + o, kIdesc, (t | k) != 0 ? 1u : 0u);
+                        tc_mma(acc, xh + o, wh + o, kIdesc, (lt | k) != 0 ? 1u : 0u);
                         tc_mma(acc, xh + o, wl + o, kIdesc, 1u);
                         tc_mma(acc, xl + o, wh + o, kIdesc, 1u);
                     }
@@ -462,20 +499,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
         float da[kXAhead];
 #pragma unroll
         for (int i = 0; i < kXAhead; ++i) {
-            const bool live = xlive && i < n_k;
-            qa[i] = live ? __ldg(xq_row + 2 * i) : make_uint4(0u, 0u, 0u, 0u);
-            da[i] = live ? __ldg(xd_row + i) : 0.0f;
+            const bool live = xlive && t0 + i < t1;
+            qa[i] = live ? __ldg(xq_row + 2 * (t0 + i)) : make_uint4(0u, 0u, 0u, 0u);
+            da[i] = live ? __ldg(xd_row + t0 + i) : 0.0f;
         }
         const uint32_t xa = uint32_t(OP_XH + (xrow >> 7) * T_TILE), xla = uint32_t(OP_XL + (xrow >> 7) * T_TILE);
         const int xr7 = xrow & 127;
-        bool ok = true;
-        // slice t, its codes and scale in slot j = t % kXAhead (the loop is unrolled by kXAhead so
-        // that j is static), which then takes slice t + kXAhead
+        // slice t (ring position lt = t - t0), its codes and scale in slot j = lt % kXAhead (the loop
+        // is unrolled by kXAhead so that j is static), which then takes slice t + kXAhead
         const auto convert_slice = [&](int t, uint4& qx, float& dx) -> bool {
-            const int g = t / SPG, c = t % SPG, r = g % RS, s = t % OP_STAGES;
-            if ((c == 0 && !warp_wait(&full_wr[r], (g / RS) & 1, p.wait_ns, p.err, kErrTimeoutFull)) ||
-                (t >= OP_STAGES &&
-                 !warp_wait(&empty_op[s], ((t / OP_STAGES) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty)))
+            const int lt = t - t0, g = t / SPG, c = t % SPG, lg = g - g0, r = lg % RS, s = lt % OP_STAGES;
+            if ((c == 0 && !warp_wait(&full_wr[r], (lg / RS) & 1, p.wait_ns, p.err, kErrTimeoutFull)) ||
+                (lt >= OP_STAGES &&
+                 !warp_wait(&empty_op[s], ((lt / OP_STAGES) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty)))
                 return false;
             uint4 xhi[2], xlo[2], whi, wlo;
             if (xlive) {
@@ -483,7 +519,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
             } else {
                 xhi[0] = xhi[1] = xlo[0] = xlo[1] = make_uint4(0u, 0u, 0u, 0u);
             }
-            if (xlive && t + kXAhead < n_k) {
+            if (xlive && t + kXAhead < t1) {
                 qx = __ldg(xq_row + 2 * (t + kXAhead));
                 dx = __ldg(xd_row + t + kXAhead);
             }
@@ -508,46 +544,84 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&full_op[s]);
-                if (c == SPG - 1 || t == n_k - 1) mbar_arrive(&empty_wr[r]);
+                if (c == SPG - 1 || t == t1 - 1) mbar_arrive(&empty_wr[r]);
             }
             return true;
         };
-        for (int t0 = 0; t0 < n_k && ok; t0 += kXAhead) {
+        for (int tb = t0; tb < t1 && ok; tb += kXAhead) {
 #pragma unroll
             for (int j = 0; j < kXAhead; ++j) {
-                if (ok && t0 + j < n_k) ok = convert_slice(t0 + j, qa[j], da[j]);
+                if (ok && tb + j < t1) ok = convert_slice(tb + j, qa[j], da[j]);
             }
         }
-        // ---- epilogue: warps 2-9; warp w drains rows 32 (w % 4) .. + 31 of accumulator (w - 2) / 4
-        const int half = (warp - 2) >> 2;
-        if (warp < 10 && warp_wait(acc_full, 0, p.wait_ns, p.err, kErrTimeoutMma) && ok && half < halves) {
-            tc_fence_after();
-            const int q = warp & 3;
-            const int yr = m0 + 128 * half + 32 * q + lane;
-            const bool row_ok = yr < p.M;
-            // vector stores only where every row of the tile starts 16-byte aligned (Y is only
-            // required to be 4-byte aligned)
-            const bool vec = (n0 + TBN <= p.N) && (p.N % 4 == 0) && (reinterpret_cast<uintptr_t>(p.Y) & 15) == 0;
-            float* yrow = p.Y + size_t(row_ok ? yr : 0) * p.N + n0;
+    }
+    // ---- epilogue: warps 2-9; warp w drains rows 32 (w % 4) .. + 31 of accumulator (w - 2) / 4
+    const int half = (warp - 2) >> 2, q = warp & 3;
+    const bool drains = warp >= 2 && warp < 10 && half < halves;
+    const bool acc_ok = warp >= 2 && warp < 10 && warp_wait(acc_full, 0, p.wait_ns, p.err, kErrTimeoutMma) && ok;
+    if (acc_ok) tc_fence_after();
+    // Split tiles: the partial sums of the second CTA go into the first CTA's operand stages (free
+    // once its MMAs are done), row r of accumulator h at byte 65536 h + 512 r, 16-byte chunk j at
+    // position j ^ (r % 32) (so that the 32 rows a warp touches fall on different banks).
+    const uint32_t xbuf = smem_addr(ops);
+    const int row = 32 * q + lane;  // of the warp's accumulator
+    const auto xchunk = [&](int j) -> uint32_t {
+        return uint32_t(half * 65536 + row * 512 + ((j ^ lane) << 4));
+    };
+    if (p.split) {
+        cluster_sync_all();  // both CTAs' MMAs are done: the first's stages are free
+        if (rank == 1 && drains && acc_ok) {
+            const uint32_t dst0 = peer_addr(xbuf, 0u);
 #pragma unroll 1
             for (int cc = 0; cc < TBN / 32; ++cc) {
                 uint32_t v[32];
                 tc_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(half * TBN + 32 * cc), v);
-                if (!row_ok) continue;
-                if (vec) {
-                    float4* dst = reinterpret_cast<float4*>(yrow + 32 * cc);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                             __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-                } else {
+                for (int i = 0; i < 8; ++i)
+                    st_peer_v4(dst0 + xchunk(8 * cc + i), v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            }
+        }
+        cluster_sync_all();  // the partial sums have landed
+    }
+    if (rank == 0 && drains && acc_ok) {
+        const int yr = m0 + 128 * half + row;
+        const bool row_ok = yr < p.M;
+        // vector stores only where every row of the tile starts 16-byte aligned (Y is only
+        // required to be 4-byte aligned)
+        const bool vec = (n0 + TBN <= p.N) && (p.N % 4 == 0) && (reinterpret_cast<uintptr_t>(p.Y) & 15) == 0;
+        float* yrow = p.Y + size_t(row_ok ? yr : 0) * p.N + n0;
+#pragma unroll 1
+        for (int cc = 0; cc < TBN / 32; ++cc) {
+            uint32_t v[32];
+            tc_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(half * TBN + 32 * cc), v);
+            if (p.split) {
+                const auto add = [](uint32_t& a, float b) { a = __float_as_uint(__uint_as_float(a) + b); };
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (n0 + 32 * cc + i < p.N) yrow[32 * cc + i] = __uint_as_float(v[i]);
+                for (int i = 0; i < 8; ++i) {
+                    const float4 o = *reinterpret_cast<const float4*>(ops + xchunk(8 * cc + i));
+                    add(v[4 * i], o.x);
+                    add(v[4 * i + 1], o.y);
+                    add(v[4 * i + 2], o.z);
+                    add(v[4 * i + 3], o.w);
                 }
+            }
+            if (!row_ok) continue;
+            if (vec) {
+                float4* dst = reinterpret_cast<float4*>(yrow + 32 * cc);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                         __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (n0 + 32 * cc + i < p.N) yrow[32 * cc + i] = __uint_as_float(v[i]);
             }
         }
     }
+    // A split launch runs beside the launch of the other tiles (programmatic
+    // dependent launch); it completes only after that one has.
+    if (p.split) pdl_wait_prior_grid();
     tc_fence_before();
     __syncthreads();
     __syncwarp();
@@ -602,7 +676,7 @@ bool encode_bytes_1d(CUtensorMap* m, const void* ptr, int64_t bytes, int box_x) 
 
 template <int FMT>
 cudaError_t launch_fmt(TcParams& p, const uint8_t* W, int64_t N, const int8_t* xq, int64_t M, int64_t K,
-                       cudaStream_t s) {
+                       int sm_count, cudaStream_t s) {
     using G = RawGeom<FMT>;
     if ((reinterpret_cast<uintptr_t>(xq) & 15) != 0 || K % TBK != 0) return cudaErrorInvalidValue;
     p.xq = xq;
@@ -610,20 +684,56 @@ cudaError_t launch_fmt(TcParams& p, const uint8_t* W, int64_t N, const int8_t* x
     const bool wok = p.w2d ? encode_bytes_2d(&p.w_map, W, N, p.row_bytes, G::kBox, TBN)
                            : encode_bytes_1d(&p.w_map, W, N * p.row_bytes, G::kBox);
     if (!wok) return cudaErrorInvalidValue;
-    static bool configured[64] = {false};
+    static int per_sm[64] = {0};  // resident CTAs per SM, per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
+    if (per_sm[dev] == 0) {
         e = cudaFuncSetAttribute(tc_prefill_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(tc_smem_bytes<FMT>()));
         if (e != cudaSuccess) return e;
-        configured[dev] = true;
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tc_prefill_kernel<FMT>, kTcThreads, tc_smem_bytes<FMT>());
+        if (e != cudaSuccess) return e;
+        per_sm[dev] = n > 0 ? n : 1;
     }
-    const dim3 grid(unsigned((M + TBM - 1) / TBM), unsigned((N + TBN - 1) / TBN));
-    tc_prefill_kernel<FMT><<<grid, kTcThreads, tc_smem_bytes<FMT>(), s>>>(p);
-    return cudaGetLastError();
+    // Waves of tiles: when the last wave is at most half full (and there is
+    // more than one), its tiles are split in two along K and run as clusters
+    // of two CTAs beside the others' last wave, so that it takes half as long.
+    const int64_t tiles_m = (M + TBM - 1) / TBM, tiles_n = (N + TBN - 1) / TBN, tiles = tiles_m * tiles_n;
+    const int64_t slots = int64_t(sm_count > 0 ? sm_count : 1) * per_sm[dev];
+    const int n_groups = int((K + G::kGroupK - 1) / G::kGroupK);
+    int64_t tail = 0;
+    if (tiles > slots && n_groups >= 2 && 2 * (tiles % slots) <= slots) tail = tiles % slots;
+    p.tiles_m = int(tiles_m);
+    p.g_split = n_groups / 2;
+    if (tiles - tail > 0) {
+        p.tile_base = 0;
+        p.split = 0;
+        tc_prefill_kernel<FMT><<<unsigned(tiles - tail), kTcThreads, tc_smem_bytes<FMT>(), s>>>(p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (tail > 0) {
+        p.tile_base = int(tiles - tail);
+        p.split = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(unsigned(2 * tail));
+        cfg.blockDim = dim3(kTcThreads);
+        cfg.dynamicSmemBytes = tc_smem_bytes<FMT>();
+        cfg.stream = s;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        if ((e = cudaLaunchKernelEx(&cfg, tc_prefill_kernel<FMT>, p)) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -633,11 +743,13 @@ bool prefill_tc_serves(int fmt, int64_t N, int64_t K, int64_t M, int64_t row_byt
     // copy coordinates are 32-bit: the last box of the last tile must start below 2^31
     const int64_t limit = (int64_t(1) << 31) - 4096;
     const int64_t tiles_n = (N + TBN - 1) / TBN;
-    return M <= INT32_MAX && N <= INT32_MAX && K <= INT32_MAX && tiles_n * TBN * row_bytes < limit;
+    const int64_t tiles = tiles_n * ((M + TBM - 1) / TBM);
+    return M <= INT32_MAX && N <= INT32_MAX && K <= INT32_MAX && 2 * tiles <= INT32_MAX &&
+           tiles_n * TBN * row_bytes < limit;
 }
 
 cudaError_t launch_prefill_tc(int fmt, const uint8_t* W, int64_t N, int64_t K, int64_t row_bytes, const int8_t* xq,
-                              const float* xd, int64_t M, float* Y, unsigned* err, cudaStream_t s) {
+                              const float* xd, int64_t M, float* Y, unsigned* err, int sm_count, cudaStream_t s) {
     TcParams p;
     memset(&p, 0, sizeof(p));
     p.xd = xd;
@@ -649,9 +761,9 @@ cudaError_t launch_prefill_tc(int fmt, const uint8_t* W, int64_t N, int64_t K, i
     p.err = err;
     p.wait_ns = 2000000000ull;
     switch (fmt) {
-        case QX_Q4_K: return launch_fmt<QX_Q4_K>(p, W, N, xq, M, K, s);
-        case QX_Q6_K: return launch_fmt<QX_Q6_K>(p, W, N, xq, M, K, s);
-        case QX_Q8_0: return launch_fmt<QX_Q8_0>(p, W, N, xq, M, K, s);
+        case QX_Q4_K: return launch_fmt<QX_Q4_K>(p, W, N, xq, M, K, sm_count, s);
+        case QX_Q6_K: return launch_fmt<QX_Q6_K>(p, W, N, xq, M, K, sm_count, s);
+        case QX_Q8_0: return launch_fmt<QX_Q8_0>(p, W, N, xq, M, K, sm_count, s);
         default: return cudaErrorInvalidValue;
     }
 }

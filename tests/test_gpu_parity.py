@@ -413,6 +413,38 @@ def test_prefill_tcgen05_capturable_on_first_use_and_on_two_streams():
     assert qx.qx_device_check() == qx.QX_OK
 
 
+@pytest.mark.parametrize("fmt,cols", [(synth.Q6_K, 512), (synth.Q8_0, 384), (synth.Q4_K, 768)])
+def test_prefill_tcgen05_split_last_wave(fmt, cols):
+    """More tiles than SMs, the last wave under half full: its tiles run as
+    two CTAs each, one per half of the K groups (Q8_0 with three groups: one
+    and two), the second handing its partial sums to the first.  Ragged M
+    (the second M tile has one 128-row half) and ragged N (the last tile has
+    57 rows).  Every row of the split tiles and sampled rows of the others
+    against the oracle; a CUDA graph of the call gives the eager bits."""
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    m = 300                                   # two M tiles of 256
+    tiles_n = (sm + 28 + 1) // 2              # sm + 28 (or 29) tiles: a last wave of 28 or 29
+    rows = (tiles_n - 1) * 128 + 57
+    W = synth.weights(fmt, rows, cols, seed=80 + cols)
+    X = synth.activation(m, cols, seed=81 + cols)
+    a, q, d, s = quantize_both(X)
+    Wd = dev(W)
+    Y = host(qx.qx_gemm_prefill_ex(fmt, Wd, rows, cols, a, path=3))
+    first_split = (sm // 2) * 128             # tiles sm .. (M tile fastest): N tiles sm / 2 ..
+    rng = np.random.default_rng(82)
+    wr = np.sort(np.concatenate([np.arange(first_split, rows), rng.choice(first_split, 100, replace=False)]))
+    ref, absdot = oracle.gemm_w4a8(fmt, np.ascontiguousarray(W[wr]), len(wr), cols, q, d)
+    assert_close(Y[:, wr].reshape(-1), ref.reshape(-1), absdot.reshape(-1), f"split {synth.NAMES[fmt]}")
+    stream = torch.cuda.Stream()
+    Yg = torch.full((m, rows), float("nan"), device="cuda")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        qx.qx_gemm_prefill_ex(fmt, Wd, rows, cols, a, Y=Yg, path=3, stream=stream)
+    g.replay()
+    assert np.array_equal(host(Yg).view(np.uint32), Y.view(np.uint32))
+    assert qx.qx_device_check() == qx.QX_OK
+
+
 @pytest.mark.parametrize("path", [2, 3])
 def test_prefill_full_size_sampled(path):
     """X [512, 4096] against Q4_K [14336, 4096]: sampled rows of X and of W against the oracle."""
