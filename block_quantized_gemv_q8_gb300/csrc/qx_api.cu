@@ -421,6 +421,62 @@ qx_status run_gemv(int fmt, int n, const void* const* W, const int64_t* rows, in
 // One small-batch launch (gemv_batch_kernel): rows m0 .. m0 + mvalid - 1 of
 // X (mvalid <= mb, mb = kBatchRows or kBatchRowsWide) against W [rows,
 // cols], into Y [X->m, rows].
+// Whether the integer-tensor small-batch kernel serves the shape (Q4_K rows of
+// at most 16 super-blocks).
+bool batch_mma_serves(int fmt, int64_t cols) {
+    return fmt == QX_Q4_K && cols % 256 == 0 && cols / 256 >= 1 && cols / 256 <= kMmaBatchMaxSuperBlocks;
+}
+
+// Up to eight rows of X (from row m0) against Q4_K rows on the integer tensor
+// path (gemv_batch_mma_q4k_kernel).  Stage: 16 P rows (P = 16 / super-blocks
+// per row) at a padded stride of row_bytes + 16; per stage the consumers'
+// partials [P][nsb][16 x 8] floats; one table of the activation scales.
+qx_status run_gemv_batch_mma(const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, int64_t m0, int mvalid,
+                             float* Y, cudaStream_t s) {
+    DeviceInfo* dev = nullptr;
+    qx_status st = device_info(&dev);
+    if (st != QX_OK) return st;
+    GemvParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.n_entries = 1;
+    p.e[0].W = static_cast<const uint8_t*>(W);
+    p.e[0].y = Y + m0 * rows;
+    p.e[0].rows = rows;
+    p.e[0].row0 = 0;
+    p.total_rows = rows;
+    p.xq = X->q + m0 * cols;
+    p.xd = X->d + m0 * (cols / 32);
+    p.xs = X->sum + m0 * (cols / 32);
+    p.mb = kMmaBatchRows;
+    p.m_valid = mvalid;
+    p.y_stride = rows;
+    const int nsb = static_cast<int>(cols / 256), P = 16 / nsb;
+    const int64_t rb = row_bytes_of(QX_Q4_K, cols);
+    const size_t slot = (size_t(16 * P) * size_t(rb + 16) + 127) / 128 * 128;
+    const size_t red_stage = size_t(P) * nsb * 128 * 4;
+    const size_t act = size_t(cols / 32) * 64;  // per 32-block: four float4
+    const size_t budget = 200 * 1024;
+    int stages = 2;
+    while (stages < 8 && size_t(stages + 1) * (slot + red_stage + 24) + act + 32 <= budget) ++stages;
+    p.red_off = static_cast<int>(size_t(stages) * slot);
+    p.act_off = static_cast<int>(size_t(p.red_off) + size_t(stages) * red_stage);
+    p.bar_off = static_cast<int>(size_t(p.act_off) + act);
+    const size_t smem = size_t(p.bar_off) + 24 * size_t(stages);
+    if (smem > 227 * 1024) return QX_ERR_SHAPE;
+    p.cols = cols;
+    p.row_bytes = rb;
+    p.quantum = 16;
+    p.G = 16 * P;
+    p.stages = stages;
+    p.slot_bytes = static_cast<int>(slot);
+    const int64_t groups = (rows + 15) / 16;
+    p.n_cta = static_cast<int>(groups < dev->sm_count ? groups : dev->sm_count);
+    p.err = dev->err_word;
+    p.wait_ns = kDefaultWaitNs;
+    const cudaError_t e = launch_gemv_batch_mma(p, smem, s);
+    return e == cudaSuccess ? QX_OK : cuda_fail(e, "batched gemv (tensor) launch");
+}
+
 qx_status run_gemv_batch(int fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, int64_t m0,
                          int mvalid, int mb, float* Y, cudaStream_t s) {
     DeviceInfo* dev = nullptr;
@@ -528,17 +584,20 @@ qx_status prefill_dispatch(qx_fmt fmt, const void* W, int64_t rows, int64_t cols
         }
     }
     if (path == 4) {
-        // eight rows of X per weight stream while more than four remain, then four
+        // Q4_K rows of up to 4096 columns: eight rows of X per weight stream on
+        // the integer tensor path.  Otherwise the lanes: eight rows of X per
+        // stream while more than four remain, then four.
+        const bool mma = batch_mma_serves(fmt, cols);
         for (int64_t m0 = 0; m0 < X->m;) {
             const int64_t left = X->m - m0;
-            const int mb = left > kBatchRows ? kBatchRowsWide : kBatchRows;
+            const int mb = mma ? kMmaBatchRows : (left > kBatchRows ? kBatchRowsWide : kBatchRows);
             const int mv = static_cast<int>(left < mb ? left : mb);
             if (!aligned16(X->q + m0 * cols) || !aligned16(X->d + m0 * (cols / 32)) ||
                 !aligned16(X->sum + m0 * (cols / 32)))
                 return QX_ERR_ALIGN;
-            if ((st = run_gemv_batch(fmt, W, rows, cols, X, m0, mv, mb, Y, reinterpret_cast<cudaStream_t>(s))) !=
-                QX_OK)
-                return st;
+            st = mma ? run_gemv_batch_mma(W, rows, cols, X, m0, mv, Y, reinterpret_cast<cudaStream_t>(s))
+                     : run_gemv_batch(fmt, W, rows, cols, X, m0, mv, mb, Y, reinterpret_cast<cudaStream_t>(s));
+            if (st != QX_OK) return st;
             m0 += mv;
         }
         return QX_OK;

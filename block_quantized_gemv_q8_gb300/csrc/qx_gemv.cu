@@ -481,6 +481,235 @@ __global__ void __launch_bounds__(kBatchThreads, 1) gemv_batch_kernel(const __gr
     }
 }
 
+// ----------------------------------------------------------------------------
+// Small-batch Q4_K GEMV on the integer tensor path (mma.sync m16n8k32, u8
+// weight quants x s8 activation codes, s32 partials): Y[m, r] for up to eight
+// rows of a quantised activation X.  The eight rows of X are the MMA's N = 8
+// columns, sixteen weight rows its M rows and one 32-column sub-block its K,
+// so one MMA yields the integer partial P of 16 x 8 (weight row, row of X)
+// pairs for one sub-block, and the scales apply in registers:
+//     y[m, r] += d sc_j dx[m, j] P - dmin m_j dx[m, j] S[m, j]
+// (the W4A8 sum of the batch-1 lanes, term by term).  The low nibbles of a
+// weight word are one mask; the high nibbles enter as 16 q (a mask, no
+// shift) and their scale carries the 1/16.  (The f16 form -- 1024 + q as an
+// f16, two m16n8k16 MMAs per sub-block -- keeps the tensor pipe idler but
+// needs more integer work per weight and measured slower.)
+//
+// Same weight stream as gemv_batch_kernel (a CTA's contiguous rows, a ring
+// of stages, a producer warp, a reducer warp), but each stage is 16 P rows
+// copied one row at a time to a padded stride (rows row_bytes + 16 apart,
+// so that the eight row groups of a fragment load fall on different banks).
+// Consumer warp w owns super-block w % nsb of row group w / nsb of every
+// stage (nsb = cols / 256 <= 16, P = 16 / nsb groups a stage), so its slice
+// of X (the MMA's B fragments) stays in registers for the whole launch.
+// Each warp writes its 16 x 8 partial of a stage to shared memory; the
+// reducer adds the nsb partials of each group and writes Y for the valid
+// rows of X.
+// ----------------------------------------------------------------------------
+constexpr int kMmaBatchWarps = 16;
+
+// Every lane waits on the barrier itself; the outcome is made warp-uniform.
+__device__ __forceinline__ bool warp_wait_all(uint64_t* bar, uint32_t parity, uint64_t ns, unsigned* err,
+                                              unsigned code) {
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, ns, err, code));
+}
+
+__device__ __forceinline__ void mma_u8s8_k32(int (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %10, %10, %10};"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "r"(0));
+}
+
+// The 6-bit scales and mins of a Q4_K super-block header (d, dmin, 12 bytes)
+// as bytes: sc of sub-blocks 0-3 and 4-7, m of 0-3 and 4-7.
+struct Q4kSubScales {
+    uint32_t sc[2], m[2];
+    float d, nd, d16, nd16, dmin, ndmin;  // d, -2^23 d, d / 16, -2^23 d / 16, dmin, -2^23 dmin
+    __device__ __forceinline__ explicit Q4kSubScales(const uint4 h) {
+        sc[0] = h.y & 0x3F3F3F3Fu;
+        m[0] = h.z & 0x3F3F3F3Fu;
+        sc[1] = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
+        m[1] = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
+        d = f16_bits_to_f32(h.x & 0xFFFFu);
+        dmin = f16_bits_to_f32(h.x >> 16);
+        d16 = d * 0.0625f;
+        nd = d * -8388608.0f;
+        nd16 = d16 * -8388608.0f;
+        ndmin = dmin * -8388608.0f;
+    }
+    // a_j = d sc_j (/ 16 for odd j: the high nibbles enter as 16 q) and
+    // b_j = dmin m_j, exact (an f16 times a 6-bit integer): byte -> 2^23 +
+    // byte, then one FMA.
+    __device__ __forceinline__ void ab(int j, float& a, float& b) const {
+        const float fs = __int_as_float(__byte_perm(sc[j >> 2], 0x4B000000u, 0x7650u + uint32_t(j & 3)));
+        const float fm = __int_as_float(__byte_perm(m[j >> 2], 0x4B000000u, 0x7650u + uint32_t(j & 3)));
+        a = (j & 1) ? fmaf(d16, fs, nd16) : fmaf(d, fs, nd);
+        b = fmaf(dmin, fm, ndmin);
+    }
+};
+
+__global__ void __launch_bounds__(kMmaBatchThreads, 1) gemv_batch_mma_q4k_kernel(const __grid_constant__ GemvParams p) {
+    constexpr int NW = kMmaBatchWarps;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int S = p.stages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
+    uint64_t* empty = full + S;
+    uint64_t* part = empty + S;
+    const int nsb = static_cast<int>(p.cols / 256), P = NW / nsb;  // groups of 16 rows per stage
+    float* red = reinterpret_cast<float*>(smem + p.red_off);          // [S][P][nsb][16 rows x 8]
+    const int red_stage = P * nsb * 128;
+    const int rstride = static_cast<int>(p.row_bytes) + 16;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t r0 = cta_row_begin(p, blockIdx.x), r1 = cta_row_begin(p, blockIdx.x + 1);
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < S; ++k) {
+            mbar_init(&full[k], 1);
+            mbar_init(&empty[k], NW + 1);
+            mbar_init(&part[k], NW);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    if (warp == NW) {
+        // ---------------- producer: one bulk copy per row, lanes in parallel -
+        const uint64_t policy = policy_evict_first();
+        const uint32_t rb = static_cast<uint32_t>(p.row_bytes);
+        StageWalker pw{r0, r1, 0};
+        int e, nrows, issued = 0;
+        int64_t lrow;
+        for (int k = 0; pw.next(p, e, lrow, nrows); ++k) {
+            const int slot = k % S;
+            if (k >= S && !warp_wait_all(&empty[slot], ((k / S) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty)) break;
+            if (lane == 0) mbar_arrive_expect_tx(&full[slot], uint32_t(nrows) * rb);
+            __syncwarp();
+            uint8_t* dst = smem + size_t(slot) * p.slot_bytes;
+            const uint8_t* src = p.e[e].W + lrow * p.row_bytes;
+            for (int r = lane; r < nrows; r += 32)
+                bulk_g2s_evict_first(dst + r * rstride, src + int64_t(r) * rb, rb, &full[slot], policy);
+            issued = k + 1;
+        }
+        if (lane == 0)
+            for (int k = issued > S ? issued - S : 0; k < issued; ++k)
+                mbar_wait_bounded(&full[k % S], (k / S) & 1, p.wait_ns, p.err, kErrTimeoutDrain);
+        return;
+    }
+    if (warp == NW + 1) {
+        // ---------------- reducer: the nsb partials of each (row, row of X) --
+        pdl_wait_prior_grid();  // y may be read by the previous kernel
+        StageWalker wk{r0, r1, 0};
+        int e, nrows;
+        int64_t lrow;
+        const int n = lane & 7;
+        for (int k = 0; wk.next(p, e, lrow, nrows); ++k) {
+            const int slot = k % S;
+            if (!mbar_wait_bounded(&part[slot], (k / S) & 1, p.wait_ns, p.err, kErrTimeoutFull)) break;
+            const float* rs = red + size_t(slot) * red_stage;
+            for (int gi = 0; gi < P && 16 * gi < nrows; ++gi) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const int rr = (lane >> 3) + 4 * kk, row = 16 * gi + rr;
+                    float acc = 0.0f;
+                    for (int sb = 0; sb < nsb; ++sb) acc += rs[(gi * nsb + sb) * 128 + rr * 8 + n];
+                    if (n < p.m_valid && row < nrows) p.e[e].y[int64_t(n) * p.y_stride + lrow + row] = acc;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------------------------------------
+    pdl_wait_prior_grid();  // X may come from the previous kernel
+    const int sb = warp % nsb, gsub = warp / nsb;
+    const bool active = gsub < P;
+    const int gid = lane >> 2, t = lane & 3;
+    const int nblk = static_cast<int>(p.cols / 32);
+    // Scales of X: for sub-block q of the row and rows 2 t', 2 t' + 1 of X,
+    // (dx, dx, dx S, dx S) at act[q][t'] (zeros for rows past m_valid); the
+    // consumer warps fill it once.
+    float4* act = reinterpret_cast<float4*>(smem + p.act_off);
+    for (int i = threadIdx.x; i < nblk * 4; i += NW * 32) {
+        const int q = i >> 2, tt = i & 3;
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int n = 2 * tt + u;
+            const int64_t bi = int64_t(n) * nblk + q;
+            const float dx = n < p.m_valid ? __ldg(p.xd + bi) : 0.0f;
+            v[u] = dx;
+            v[2 + u] = n < p.m_valid ? dx * float(__ldg(p.xs + bi)) : 0.0f;
+        }
+        act[i] = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    // B fragments: X row gid, sub-block j, codes 4 t .. 4 t + 3 and 16 + 4 t .. 19 + 4 t
+    uint32_t bx[8][2];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const bool live = active && gid < p.m_valid;
+            const int8_t* xr = p.xq + int64_t(gid) * p.cols + 256 * sb + 32 * j + 16 * u + 4 * t;
+            bx[j][u] = live ? __ldg(reinterpret_cast<const uint32_t*>(xr)) : 0u;
+        }
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");  // the consumer warps: the table is filled
+    const float4* my_act = act + (8 * sb) * 4 + t;  // sub-block j: my_act[4 j]
+    StageWalker wk{r0, r1, 0};
+    int e, nrows;
+    int64_t lrow;
+    for (int k = 0; wk.next(p, e, lrow, nrows); ++k) {
+        const int slot = k % S;
+        if (!mbar_wait_bounded(&full[slot], (k / S) & 1, p.wait_ns, p.err, kErrTimeoutFull)) break;
+        if (active && 16 * gsub < nrows) {
+            const uint8_t* ra = smem + size_t(slot) * p.slot_bytes + (16 * gsub + gid) * rstride + 144 * sb;
+            const uint8_t* rbp = ra + 8 * rstride;
+            const Q4kSubScales sa(*reinterpret_cast<const uint4*>(ra)), sbs(*reinterpret_cast<const uint4*>(rbp));
+            uint64_t ya2 = f32x2_pack(0.0f, 0.0f), yb2 = ya2;  // rows gid, gid + 8; rows 2 t, 2 t + 1 of X
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t w[2][2];  // [half][row gid, gid + 8]: bytes 4 t .. 4 t + 3 of the half
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int o = 16 + 32 * c + 16 * u + 4 * t;
+                    w[u][0] = *reinterpret_cast<const uint32_t*>(ra + o);
+                    w[u][1] = *reinterpret_cast<const uint32_t*>(rbp + o);
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {  // sub-block 2 c (low nibbles), 2 c + 1 (high nibbles, as 16 q)
+                    const int j = 2 * c + h;
+                    // the partials P (16 P for high nibbles): rows gid, gid + 8 x rows 2 t, 2 t + 1 of X
+                    const uint32_t mask = h ? 0xF0F0F0F0u : 0x0F0F0F0Fu;
+                    const uint32_t a[4] = {w[0][0] & mask, w[0][1] & mask, w[1][0] & mask, w[1][1] & mask};
+                    int d[4];
+                    mma_u8s8_k32(d, a, bx[j][0], bx[j][1]);
+                    float aa, ba, ab, bb;
+                    sa.ab(j, aa, ba);
+                    sbs.ab(j, ab, bb);
+                    const float4 xv = my_act[4 * j];  // dx, dx, dx S, dx S of rows 2 t, 2 t + 1 of X
+                    const uint64_t dx2 = f32x2_pack(xv.x, xv.y), ds2 = f32x2_pack(xv.z, xv.w);
+                    ya2 = f32x2_fma(f32x2_pack(aa, aa), f32x2_mul(f32x2_pack(float(d[0]), float(d[1])), dx2), ya2);
+                    ya2 = f32x2_fma(f32x2_pack(-ba, -ba), ds2, ya2);
+                    yb2 = f32x2_fma(f32x2_pack(ab, ab), f32x2_mul(f32x2_pack(float(d[2]), float(d[3])), dx2), yb2);
+                    yb2 = f32x2_fma(f32x2_pack(-bb, -bb), ds2, yb2);
+                }
+            }
+            const float2 ya = f32x2_unpack(ya2), yb = f32x2_unpack(yb2);
+            float* rs = red + size_t(slot) * red_stage + (gsub * nsb + sb) * 128;
+            *reinterpret_cast<float2*>(rs + gid * 8 + 2 * t) = ya;
+            *reinterpret_cast<float2*>(rs + (gid + 8) * 8 + 2 * t) = yb;
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&part[slot]);
+            mbar_arrive(&empty[slot]);
+        }
+    }
+}
+
 // Largest shared memory (static + dynamic) a CTA may use on sm_103a.
 constexpr int kMaxDynamicSmem = 227 * 1024;
 
@@ -549,6 +778,24 @@ cudaError_t launch_batch_one(const GemvParams& p, size_t smem, cudaStream_t s) {
 }
 
 }  // namespace
+
+cudaError_t launch_gemv_batch_mma(const GemvParams& p, size_t smem, cudaStream_t s) {
+    static bool done[64] = {false};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!done[dev]) {
+        cudaFuncAttributes fa;
+        if ((err = cudaFuncGetAttributes(&fa, gemv_batch_mma_q4k_kernel)) != cudaSuccess) return err;
+        err = cudaFuncSetAttribute(gemv_batch_mma_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   kMaxDynamicSmem - static_cast<int>(fa.sharedSizeBytes));
+        if (err != cudaSuccess) return err;
+        done[dev] = true;
+    }
+    gemv_batch_mma_q4k_kernel<<<p.n_cta, kMmaBatchThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_gemv_batch(int fmt, const GemvParams& p, size_t smem, cudaStream_t s) {
     const bool wide = p.mb == kBatchRowsWide;

@@ -55,11 +55,15 @@ def check(fmt, W, rows, cols, X, what, sample_rows=None):
     return Y
 
 
-# ragged batches (1..9 rows of X: whole and partial groups of four), ragged
-# row counts (not multiples of the CTA split or of the stage), narrow and wide rows
+# ragged batches (1..16 rows of X: whole and partial groups of four or eight),
+# ragged row counts (not multiples of the CTA split, of the stage or of the
+# 16-row groups of the tensor path), narrow and wide rows (Q4_K up to 4096
+# columns takes the integer tensor path: 1, 2, 3, 4, 9 and 16 super-blocks a
+# row, so 16, 8, 5, 4, 1 and 1 row groups a stage, some consumer warps idle)
 @pytest.mark.parametrize("fmt,m,rows,cols", [
     (synth.Q4_K, 1, 70, 1024), (synth.Q4_K, 2, 300, 4096), (synth.Q4_K, 3, 129, 256),
     (synth.Q4_K, 4, 1000, 4096), (synth.Q4_K, 5, 77, 14336), (synth.Q4_K, 8, 513, 1024),
+    (synth.Q4_K, 9, 200, 768), (synth.Q4_K, 16, 45, 2304), (synth.Q4_K, 7, 1, 4096), (synth.Q4_K, 3, 1111, 512),
     (synth.Q6_K, 2, 300, 1024), (synth.Q6_K, 4, 129, 14336), (synth.Q6_K, 7, 33, 256),
     (synth.Q8_0, 2, 151, 896), (synth.Q8_0, 4, 300, 32), (synth.Q8_0, 6, 513, 864), (synth.Q8_0, 9, 128, 4096),
 ])
@@ -78,6 +82,22 @@ def test_batch_zero_rows_of_x_and_tail_bytes():
     X[1] = 0.0
     Y = check(fmt, W, rows, cols, X, "zero row / tail bytes")
     assert np.all(Y[1] == 0.0)
+
+
+def test_batch_tensor_path_zero_weights_give_exact_zeros():
+    """Q4_K rows whose quants and dmin are zero (d and the 6-bit scales left
+    as they are) are zero weights: the integer tensor path must give exact
+    zeros there (integer partials of zero, a min term of zero), and the
+    oracle's values elsewhere."""
+    fmt, rows, cols, m = synth.Q4_K, 200, 4096, 8
+    W = synth.weights(fmt, rows, cols, seed=95)
+    blocks = W.reshape(rows, cols // 256, 144)
+    zero_rows = np.array([0, 17, 63, 64, 150, 199])
+    blocks[zero_rows, :, 2:4] = 0      # dmin
+    blocks[zero_rows, :, 16:] = 0      # quants
+    X = synth.activation(m, cols, seed=96)
+    Y = check(fmt, W, rows, cols, X, "zero weight rows")
+    assert np.all(Y[:, zero_rows] == 0.0)
 
 
 @pytest.mark.parametrize("m", [4, 8])
