@@ -628,6 +628,18 @@ __global__ void __launch_bounds__(kMmaBatchThreads, 1) gemv_batch_mma_q4k_kernel
     const bool active = gsub < P;
     const int gid = lane >> 2, t = lane & 3;
     const int nblk = static_cast<int>(p.cols / 32);
+    // B fragments: X row gid, sub-block j, codes 4 t .. 4 t + 3 and 16 + 4 t .. 19 + 4 t
+    // (in flight while the table below is filled)
+    uint32_t bx[8][2];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const bool live = active && gid < p.m_valid;
+            const int8_t* xr = p.xq + int64_t(gid) * p.cols + 256 * sb + 32 * j + 16 * u + 4 * t;
+            bx[j][u] = live ? __ldg(reinterpret_cast<const uint32_t*>(xr)) : 0u;
+        }
+    }
     // Scales of X: for sub-block q of the row and rows 2 t', 2 t' + 1 of X,
     // (dx, dx, dx S, dx S) at act[q][t'] (zeros for rows past m_valid); the
     // consumer warps fill it once.
@@ -644,17 +656,6 @@ __global__ void __launch_bounds__(kMmaBatchThreads, 1) gemv_batch_mma_q4k_kernel
             v[2 + u] = n < p.m_valid ? dx * float(__ldg(p.xs + bi)) : 0.0f;
         }
         act[i] = make_float4(v[0], v[1], v[2], v[3]);
-    }
-    // B fragments: X row gid, sub-block j, codes 4 t .. 4 t + 3 and 16 + 4 t .. 19 + 4 t
-    uint32_t bx[8][2];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const bool live = active && gid < p.m_valid;
-            const int8_t* xr = p.xq + int64_t(gid) * p.cols + 256 * sb + 32 * j + 16 * u + 4 * t;
-            bx[j][u] = live ? __ldg(reinterpret_cast<const uint32_t*>(xr)) : 0u;
-        }
     }
     asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");  // the consumer warps: the table is filled
     const float4* my_act = act + (8 * sb) * 4 + t;  // sub-block j: my_act[4 j]
