@@ -187,21 +187,29 @@ qx_status qx_gemm_prefill(qx_fmt fmt, const void* W, int64_t rows, int64_t cols,
  *       the int8 codes and the raw weight blocks, each as two bf16 terms (hi
  *       + lo, 16 significant bits), and Y = Xh Wh^T + Xh Wl^T + Xl Wh^T is
  *       accumulated in f32 in tensor memory.  Each product's error is about
- *       2^-15 of its magnitude.  No workspace: the call allocates nothing, may
+ *       2^-15 of its magnitude.  When the tiles (256 rows of X x 128 weight
+ *       rows) leave a last wave over the SMs at most half full, that wave's
+ *       tiles are split in two along K (a second launch, started beside the
+ *       first by programmatic dependent launch; Y = the first half's sum plus
+ *       the second's), so results depend on the shape and the GPU's SM count
+ *       but not on the run.  No workspace: the call allocates nothing, may
  *       be captured in a CUDA graph on its first use and may run concurrently
  *       on several streams.  Shapes whose weights span 2 GiB or more (the
- *       copy engine's 32-bit coordinates) return QX_ERR_SHAPE; path 0 takes
- *       path 1 for them.
- *   4 = small-batch GEMV, every format (rows of up to 14336 columns, or
- *       28672 for Q4_K / Q6_K when at most four rows of X remain; path 0
- *       takes path 1 for wider rows): the weights are streamed once per
- *       group of eight rows of X while five or more remain, else once per
- *       group of up to four (decode of several tokens at once: speculative
- *       or batched decode), each lane holding its column slice of the
- *       group's codes and dotting every weight word with each row's;
- *       the same per-block integer dot products and scales as qx_gemv's
- *       W4A8 path, in a different f32 summation order (within the same
- *       tolerance, not bit-for-bit path 1).
+ *       copy engine's 32-bit coordinates) or need more than 65535 weight
+ *       tiles return QX_ERR_SHAPE; path 0 takes path 1 for them.
+ *   4 = small-batch GEMV (decode of several tokens at once: speculative or
+ *       batched decode), every format, the weights streamed once per group
+ *       of rows of X.  Q4_K rows of up to 4096 columns: groups of up to
+ *       eight rows on the integer tensor path (mma.sync m16n8k32, the rows
+ *       of X as its eight columns: exact integer partials per 32-column
+ *       sub-block, scaled in registers).  Other shapes (rows of up to 14336
+ *       columns, or 28672 for Q4_K / Q6_K when at most four rows of X
+ *       remain; path 0 takes path 1 for wider rows): groups of eight rows
+ *       while five or more remain, else of up to four, each lane holding its
+ *       column slice of the group's codes and dotting every weight word with
+ *       each row's.  Both: the same per-block integer dot products and
+ *       scales as qx_gemv's W4A8 path, in a different f32 summation order
+ *       (within the same tolerance, not bit-for-bit path 1).
  * A path that cannot serve the call returns QX_ERR_FMT rather than falling
  * back.
  */
