@@ -550,9 +550,9 @@ def measure_config(name: str, qx, torch, stream, hbm: float, bf16: float, peak_k
                     "sweep": sweep, "flops_per_row": 2 * rows * cols, "bf16_dense_peak_tflops": bf16,
                     "note": "path 1 = one W4A8 GEMV launch per row; path 2 = tensor cores (mma.sync f16 with "
                             "integer-valued operands); path 3 = tcgen05 bf16 GEMM over the split dequantised "
-                            "operands (3 passes of K); path 4 = small-batch GEMV (Q4_K up to 4096 columns: int8 "
-                            "mma.sync, one weight stream per 8 rows of X; other shapes: dp4a lanes, per 8 rows "
-                            "while five or more remain, else per up to 4); tflops count the int8-equivalent "
+                            "operands (3 passes of K); path 4 = small-batch GEMV, one weight stream per 8 rows of "
+                            "X while five or more remain (int8 mma.sync for rows of up to 4096 columns, else "
+                            "dp4a lanes), else per up to 4 (dp4a lanes); tflops count the int8-equivalent "
                             "multiply-adds x2; crossover_m = the smallest swept M whose fastest path is a "
                             "tensor-core one"})
         del W, X

@@ -421,18 +421,23 @@ qx_status run_gemv(int fmt, int n, const void* const* W, const int64_t* rows, in
 // One small-batch launch (gemv_batch_kernel): rows m0 .. m0 + mvalid - 1 of
 // X (mvalid <= mb, mb = kBatchRows or kBatchRowsWide) against W [rows,
 // cols], into Y [X->m, rows].
-// Whether the integer-tensor small-batch kernel serves the shape (Q4_K rows of
-// at most 16 super-blocks).
+// Whether the integer-tensor small-batch kernel serves the shape: rows of
+// 256 to 4096 columns in whole 256-column units (a Q4_K or Q6_K super-block,
+// eight Q8_0 blocks), each row a 16-byte multiple (copied row by row; Q6_K
+// rows of 2048 or 4096 columns).
 bool batch_mma_serves(int fmt, int64_t cols) {
-    return fmt == QX_Q4_K && cols % 256 == 0 && cols / 256 >= 1 && cols / 256 <= kMmaBatchMaxSuperBlocks;
+    if (fmt != QX_Q4_K && fmt != QX_Q6_K && fmt != QX_Q8_0) return false;
+    if (cols % 256 != 0 || cols / 256 < 1 || cols / 256 > kMmaBatchMaxSuperBlocks) return false;
+    return row_bytes_of(fmt, cols) % 16 == 0;
 }
 
-// Up to eight rows of X (from row m0) against Q4_K rows on the integer tensor
-// path (gemv_batch_mma_q4k_kernel).  Stage: 16 P rows (P = 16 / super-blocks
-// per row) at a padded stride of row_bytes + 16; per stage the consumers'
-// partials [P][nsb][16 x 8] floats; one table of the activation scales.
-qx_status run_gemv_batch_mma(const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, int64_t m0, int mvalid,
-                             float* Y, cudaStream_t s) {
+// Up to eight rows of X (from row m0) on the integer tensor path
+// (gemv_batch_mma_kernel).  Stage: 16 P rows (P = 16 / units per row) at a
+// padded stride of row_bytes + 16; per stage the consumers' partials
+// [P][units][16 x 8] floats; one table of the activation scales (one float4
+// per 32-column block and pair of rows of X; Q6_K: per 16-column group).
+qx_status run_gemv_batch_mma(int fmt, const void* W, int64_t rows, int64_t cols, const qx_act_q8* X, int64_t m0,
+                             int mvalid, float* Y, cudaStream_t s) {
     DeviceInfo* dev = nullptr;
     qx_status st = device_info(&dev);
     if (st != QX_OK) return st;
@@ -451,10 +456,10 @@ qx_status run_gemv_batch_mma(const void* W, int64_t rows, int64_t cols, const qx
     p.m_valid = mvalid;
     p.y_stride = rows;
     const int nsb = static_cast<int>(cols / 256), P = 16 / nsb;
-    const int64_t rb = row_bytes_of(QX_Q4_K, cols);
+    const int64_t rb = row_bytes_of(fmt, cols);
     const size_t slot = (size_t(16 * P) * size_t(rb + 16) + 127) / 128 * 128;
     const size_t red_stage = size_t(P) * nsb * 128 * 4;
-    const size_t act = size_t(cols / 32) * 64;  // per 32-block: four float4
+    const size_t act = size_t(cols / 32) * 64 * (fmt == QX_Q6_K ? 2 : 1);  // four float4 per block (group)
     const size_t budget = 200 * 1024;
     int stages = 2;
     while (stages < 8 && size_t(stages + 1) * (slot + red_stage + 24) + act + 32 <= budget) ++stages;
@@ -473,7 +478,7 @@ qx_status run_gemv_batch_mma(const void* W, int64_t rows, int64_t cols, const qx
     p.n_cta = static_cast<int>(groups < dev->sm_count ? groups : dev->sm_count);
     p.err = dev->err_word;
     p.wait_ns = kDefaultWaitNs;
-    const cudaError_t e = launch_gemv_batch_mma(p, smem, s);
+    const cudaError_t e = launch_gemv_batch_mma(fmt, p, smem, s);
     return e == cudaSuccess ? QX_OK : cuda_fail(e, "batched gemv (tensor) launch");
 }
 
@@ -584,18 +589,22 @@ qx_status prefill_dispatch(qx_fmt fmt, const void* W, int64_t rows, int64_t cols
         }
     }
     if (path == 4) {
-        // Q4_K rows of up to 4096 columns: eight rows of X per weight stream on
-        // the integer tensor path.  Otherwise the lanes: eight rows of X per
-        // stream while more than four remain, then four.
-        const bool mma = batch_mma_serves(fmt, cols);
+        // While more than four rows of X remain, eight of them per weight
+        // stream: on the integer tensor path for rows of up to 4096 columns in
+        // whole 256-column units, else on the eight-row lanes.  Then up to four
+        // on the four-row lanes (faster than the tensor path at four rows or
+        // fewer: 14.4 against 16.4 us for Q4_K, 20.5 against 22.8-24.1 for
+        // Q6_K, equal for Q8_0, on 14336 x 4096).
+        const bool mma_shape = batch_mma_serves(fmt, cols);
         for (int64_t m0 = 0; m0 < X->m;) {
             const int64_t left = X->m - m0;
+            const bool mma = mma_shape && left > kBatchRows;
             const int mb = mma ? kMmaBatchRows : (left > kBatchRows ? kBatchRowsWide : kBatchRows);
             const int mv = static_cast<int>(left < mb ? left : mb);
             if (!aligned16(X->q + m0 * cols) || !aligned16(X->d + m0 * (cols / 32)) ||
                 !aligned16(X->sum + m0 * (cols / 32)))
                 return QX_ERR_ALIGN;
-            st = mma ? run_gemv_batch_mma(W, rows, cols, X, m0, mv, Y, reinterpret_cast<cudaStream_t>(s))
+            st = mma ? run_gemv_batch_mma(fmt, W, rows, cols, X, m0, mv, Y, reinterpret_cast<cudaStream_t>(s))
                      : run_gemv_batch(fmt, W, rows, cols, X, m0, mv, mb, Y, reinterpret_cast<cudaStream_t>(s));
             if (st != QX_OK) return st;
             m0 += mv;

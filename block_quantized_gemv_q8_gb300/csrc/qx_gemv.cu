@@ -514,6 +514,19 @@ __device__ __forceinline__ bool warp_wait_all(uint64_t* bar, uint32_t parity, ui
     return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, ns, err, code));
 }
 
+__device__ __forceinline__ void mma_s8s8_k32(int (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %10, %10, %10};"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "r"(0));
+}
+// m16n8k16: A rows gid, gid + 8 (one register each), B one register.
+__device__ __forceinline__ void mma_u8s8_k16(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+    asm("mma.sync.aligned.m16n8k16.row.col.s32.u8.s8.s32 {%0, %1, %2, %3}, {%4, %5}, {%6}, {%7, %7, %7, %7};"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(a0), "r"(a1), "r"(b0), "r"(0));
+}
+
 __device__ __forceinline__ void mma_u8s8_k32(int (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm("mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%10, %10, %10, %10};"
@@ -549,7 +562,156 @@ struct Q4kSubScales {
     }
 };
 
-__global__ void __launch_bounds__(kMmaBatchThreads, 1) gemv_batch_mma_q4k_kernel(const __grid_constant__ GemvParams p) {
+// One 256-column unit of a row (a Q4_K or Q6_K super-block, eight Q8_0
+// blocks) against the warp's slice of X: rows gid and gid + 8 of the unit's
+// 16-row group (ra, rb: their unit bases in shared memory), rows 2 t and
+// 2 t + 1 of X; adds y[row][row of X] into ya2 (row gid) and yb2 (row gid + 8).
+// bx: the unit's B fragments; act: its scale-table entries (see the kernel).
+template <int FMT>
+struct BatchMmaUnit;
+
+// Q4_K: eight sub-blocks of 32, one m16n8k32 each (u8 quants: low nibbles as
+// q, high nibbles as 16 q); table entry per sub-block (dx, dx, dx S, dx S).
+template <>
+struct BatchMmaUnit<QX_Q4_K> {
+    static constexpr int kBytes = 144, kB = 16, kActPerUnit = 8;
+    __device__ __forceinline__ static void load_b(const int8_t* xr, int t, bool live, uint32_t (&bx)[kB]) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                bx[2 * j + u] = live ? __ldg(reinterpret_cast<const uint32_t*>(xr + 32 * j + 16 * u + 4 * t)) : 0u;
+    }
+    __device__ __forceinline__ static void run(const uint8_t* ra, const uint8_t* rb, int t, const uint32_t (&bx)[kB],
+                                               const float4* act, uint64_t& ya2, uint64_t& yb2) {
+        const Q4kSubScales sa(*reinterpret_cast<const uint4*>(ra)), sbs(*reinterpret_cast<const uint4*>(rb));
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t w[2][2];  // [half][row gid, gid + 8]: bytes 4 t .. 4 t + 3 of the half
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int o = 16 + 32 * c + 16 * u + 4 * t;
+                w[u][0] = *reinterpret_cast<const uint32_t*>(ra + o);
+                w[u][1] = *reinterpret_cast<const uint32_t*>(rb + o);
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // sub-block 2 c (low nibbles), 2 c + 1 (high nibbles, as 16 q)
+                const int j = 2 * c + h;
+                // the partials P (16 P for high nibbles): rows gid, gid + 8 x rows 2 t, 2 t + 1 of X
+                const uint32_t mask = h ? 0xF0F0F0F0u : 0x0F0F0F0Fu;
+                const uint32_t a[4] = {w[0][0] & mask, w[0][1] & mask, w[1][0] & mask, w[1][1] & mask};
+                int d[4];
+                mma_u8s8_k32(d, a, bx[2 * j], bx[2 * j + 1]);
+                float aa, ba, ab, bb;
+                sa.ab(j, aa, ba);
+                sbs.ab(j, ab, bb);
+                const float4 xv = act[4 * j];  // dx, dx, dx S, dx S of rows 2 t, 2 t + 1 of X
+                const uint64_t dx2 = f32x2_pack(xv.x, xv.y), ds2 = f32x2_pack(xv.z, xv.w);
+                ya2 = f32x2_fma(f32x2_pack(aa, aa), f32x2_mul(f32x2_pack(float(d[0]), float(d[1])), dx2), ya2);
+                ya2 = f32x2_fma(f32x2_pack(-ba, -ba), ds2, ya2);
+                yb2 = f32x2_fma(f32x2_pack(ab, ab), f32x2_mul(f32x2_pack(float(d[2]), float(d[3])), dx2), yb2);
+                yb2 = f32x2_fma(f32x2_pack(-bb, -bb), ds2, yb2);
+            }
+        }
+    }
+};
+
+// Q8_0: eight blocks of 34 bytes (d, 32 int8), one m16n8k32 each (s8 weights
+// as stored, read at 2-byte-aligned offsets); table entry per block (dx, dx, -, -).
+template <>
+struct BatchMmaUnit<QX_Q8_0> {
+    static constexpr int kBytes = 272, kB = 16, kActPerUnit = 8;
+    __device__ __forceinline__ static void load_b(const int8_t* xr, int t, bool live, uint32_t (&bx)[kB]) {
+        BatchMmaUnit<QX_Q4_K>::load_b(xr, t, live, bx);
+    }
+    __device__ __forceinline__ static void run(const uint8_t* ra, const uint8_t* rb, int t, const uint32_t (&bx)[kB],
+                                               const float4* act, uint64_t& ya2, uint64_t& yb2) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint8_t* ba = ra + 34 * j;
+            const uint8_t* bb = rb + 34 * j;
+            const uint32_t a[4] = {lds_u32_a2(ba + 2 + 4 * t), lds_u32_a2(bb + 2 + 4 * t), lds_u32_a2(ba + 18 + 4 * t),
+                                   lds_u32_a2(bb + 18 + 4 * t)};
+            int d[4];
+            mma_s8s8_k32(d, a, bx[2 * j], bx[2 * j + 1]);
+            const float da = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(ba));
+            const float db = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(bb));
+            const float4 xv = act[4 * j];
+            const uint64_t dx2 = f32x2_pack(xv.x, xv.y);
+            ya2 = f32x2_fma(f32x2_pack(da, da), f32x2_mul(f32x2_pack(float(d[0]), float(d[1])), dx2), ya2);
+            yb2 = f32x2_fma(f32x2_pack(db, db), f32x2_mul(f32x2_pack(float(d[2]), float(d[3])), dx2), yb2);
+        }
+    }
+};
+
+// Q6_K (ql[128], qh[64], scales[16] int8, d): sixteen groups of 16 with their
+// own scales, one m16n8k16 each (u8 q = 0..63; P = D - 32 S16, exact).  The
+// two groups of one 32-column block share dx, so their partials are combined
+// in integers first: sc_a (D_a - 32 S_a) + sc_b (D_b - 32 S_b) (|.| < 2^25).
+// Table entry per group (dx, dx, S16, S16) with S16 the group's sum of codes
+// (as integers in float bits).
+template <>
+struct BatchMmaUnit<QX_Q6_K> {
+    static constexpr int kBytes = 210, kB = 16, kActPerUnit = 16;
+    __device__ __forceinline__ static void load_b(const int8_t* xr, int t, bool live, uint32_t (&bx)[kB]) {
+#pragma unroll
+        for (int g = 0; g < 16; ++g)
+            bx[g] = live ? __ldg(reinterpret_cast<const uint32_t*>(xr + 16 * g + 4 * t)) : 0u;
+    }
+    __device__ __forceinline__ static void run(const uint8_t* ra, const uint8_t* rb, int t, const uint32_t (&bx)[kB],
+                                               const float4* act, uint64_t& ya2, uint64_t& yb2) {
+        const float da = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(ra + 208));
+        const float db = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(rb + 208));
+        const int8_t* sca = reinterpret_cast<const int8_t*>(ra + 192);
+        const int8_t* scb = reinterpret_cast<const int8_t*>(rb + 192);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            // words of elements 128 h + 32 tq + 16 u + 4 t .. + 3: ql for quarters 0 / 2 and 1 / 3, qh
+            uint32_t ql[2][2][2], qh[2][2];  // [u][quarter parity][row], [u][row]
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int o = 16 * u + 4 * t;
+#pragma unroll
+                for (int qp = 0; qp < 2; ++qp) {
+                    ql[u][qp][0] = lds_u32_a2(ra + 64 * h + 32 * qp + o);
+                    ql[u][qp][1] = lds_u32_a2(rb + 64 * h + 32 * qp + o);
+                }
+                qh[u][0] = lds_u32_a2(ra + 128 + 32 * h + o);
+                qh[u][1] = lds_u32_a2(rb + 128 + 32 * h + o);
+            }
+#pragma unroll
+            for (int tq = 0; tq < 4; ++tq) {  // the 32-column block 4 h + tq: groups 8 h + 2 tq + u
+                int p[4] = {0, 0, 0, 0};  // sum over its two groups of sc (D - 32 S16)
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int g = 8 * h + 2 * tq + u;
+                    uint32_t a[2];
+#pragma unroll
+                    for (int r = 0; r < 2; ++r)
+                        a[r] = ((ql[u][tq & 1][r] >> (4 * (tq >> 1))) & 0x0F0F0F0Fu) |
+                               (((qh[u][r] >> (2 * tq)) & 0x03030303u) << 4);
+                    int d[4];
+                    mma_u8s8_k16(d, a[0], a[1], bx[g]);
+                    const float4 xv = act[4 * g];
+                    const int s0 = __float_as_int(xv.z), s1 = __float_as_int(xv.w);
+                    const int ka = sca[g], kb = scb[g];
+                    p[0] += ka * (d[0] - 32 * s0);
+                    p[1] += ka * (d[1] - 32 * s1);
+                    p[2] += kb * (d[2] - 32 * s0);
+                    p[3] += kb * (d[3] - 32 * s1);
+                }
+                const float4 xv = act[4 * (8 * h + 2 * tq)];
+                const uint64_t dx2 = f32x2_pack(xv.x, xv.y);
+                ya2 = f32x2_fma(f32x2_pack(da, da), f32x2_mul(f32x2_pack(float(p[0]), float(p[1])), dx2), ya2);
+                yb2 = f32x2_fma(f32x2_pack(db, db), f32x2_mul(f32x2_pack(float(p[2]), float(p[3])), dx2), yb2);
+            }
+        }
+    }
+};
+
+template <int FMT>
+__global__ void __launch_bounds__(kMmaBatchThreads, 1) gemv_batch_mma_kernel(const __grid_constant__ GemvParams p) {
+    using U = BatchMmaUnit<FMT>;
     constexpr int NW = kMmaBatchWarps;
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = p.stages;
@@ -628,37 +790,45 @@ __global__ void __launch_bounds__(kMmaBatchThreads, 1) gemv_batch_mma_q4k_kernel
     const bool active = gsub < P;
     const int gid = lane >> 2, t = lane & 3;
     const int nblk = static_cast<int>(p.cols / 32);
-    // B fragments: X row gid, sub-block j, codes 4 t .. 4 t + 3 and 16 + 4 t .. 19 + 4 t
-    // (in flight while the table below is filled)
-    uint32_t bx[8][2];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const bool live = active && gid < p.m_valid;
-            const int8_t* xr = p.xq + int64_t(gid) * p.cols + 256 * sb + 32 * j + 16 * u + 4 * t;
-            bx[j][u] = live ? __ldg(reinterpret_cast<const uint32_t*>(xr)) : 0u;
-        }
-    }
-    // Scales of X: for sub-block q of the row and rows 2 t', 2 t' + 1 of X,
-    // (dx, dx, dx S, dx S) at act[q][t'] (zeros for rows past m_valid); the
-    // consumer warps fill it once.
+    // B fragments: X row gid, the warp's unit (in flight while the table below is filled)
+    uint32_t bx[U::kB];
+    U::load_b(p.xq + int64_t(gid) * p.cols + 256 * sb, t, active && gid < p.m_valid, bx);
+    // Scales of X, per 32-column block (Q6_K: per 16-column group) q and
+    // rows 2 t', 2 t' + 1 of X: act[q][t'] = (dx, dx, dx S, dx S) (Q6_K: the
+    // group's code sums S16 as integers in the last two), zeros for rows past
+    // m_valid; the consumer warps fill it once.
     float4* act = reinterpret_cast<float4*>(smem + p.act_off);
-    for (int i = threadIdx.x; i < nblk * 4; i += NW * 32) {
+    const int nact = nblk * (U::kActPerUnit / 8);
+    for (int i = threadIdx.x; i < nact * 4; i += NW * 32) {
         const int q = i >> 2, tt = i & 3;
         float v[4];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const int n = 2 * tt + u;
-            const int64_t bi = int64_t(n) * nblk + q;
-            const float dx = n < p.m_valid ? __ldg(p.xd + bi) : 0.0f;
-            v[u] = dx;
-            v[2 + u] = n < p.m_valid ? dx * float(__ldg(p.xs + bi)) : 0.0f;
+            const bool ln = n < p.m_valid;
+            if constexpr (FMT == QX_Q6_K) {
+                const int64_t bi = int64_t(n) * nblk + (q >> 1);
+                v[u] = ln ? __ldg(p.xd + bi) : 0.0f;
+                int s16 = 0;
+                if (ln) {
+                    const uint4 c = __ldg(reinterpret_cast<const uint4*>(p.xq + int64_t(n) * p.cols + 16 * q));
+                    s16 = __dp4a(int(c.x), 0x01010101, s16);
+                    s16 = __dp4a(int(c.y), 0x01010101, s16);
+                    s16 = __dp4a(int(c.z), 0x01010101, s16);
+                    s16 = __dp4a(int(c.w), 0x01010101, s16);
+                }
+                v[2 + u] = __int_as_float(s16);
+            } else {
+                const int64_t bi = int64_t(n) * nblk + q;
+                const float dx = ln ? __ldg(p.xd + bi) : 0.0f;
+                v[u] = dx;
+                v[2 + u] = (FMT == QX_Q4_K && ln) ? dx * float(__ldg(p.xs + bi)) : 0.0f;
+            }
         }
         act[i] = make_float4(v[0], v[1], v[2], v[3]);
     }
     asm volatile("bar.sync 1, %0;" ::"r"(NW * 32) : "memory");  // the consumer warps: the table is filled
-    const float4* my_act = act + (8 * sb) * 4 + t;  // sub-block j: my_act[4 j]
+    const float4* my_act = act + (U::kActPerUnit * sb) * 4 + t;  // entry q of the unit: my_act[4 q]
     StageWalker wk{r0, r1, 0};
     int e, nrows;
     int64_t lrow;
@@ -666,38 +836,9 @@ __global__ void __launch_bounds__(kMmaBatchThreads, 1) gemv_batch_mma_q4k_kernel
         const int slot = k % S;
         if (!mbar_wait_bounded(&full[slot], (k / S) & 1, p.wait_ns, p.err, kErrTimeoutFull)) break;
         if (active && 16 * gsub < nrows) {
-            const uint8_t* ra = smem + size_t(slot) * p.slot_bytes + (16 * gsub + gid) * rstride + 144 * sb;
-            const uint8_t* rbp = ra + 8 * rstride;
-            const Q4kSubScales sa(*reinterpret_cast<const uint4*>(ra)), sbs(*reinterpret_cast<const uint4*>(rbp));
+            const uint8_t* ra = smem + size_t(slot) * p.slot_bytes + (16 * gsub + gid) * rstride + U::kBytes * sb;
             uint64_t ya2 = f32x2_pack(0.0f, 0.0f), yb2 = ya2;  // rows gid, gid + 8; rows 2 t, 2 t + 1 of X
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t w[2][2];  // [half][row gid, gid + 8]: bytes 4 t .. 4 t + 3 of the half
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int o = 16 + 32 * c + 16 * u + 4 * t;
-                    w[u][0] = *reinterpret_cast<const uint32_t*>(ra + o);
-                    w[u][1] = *reinterpret_cast<const uint32_t*>(rbp + o);
-                }
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {  // sub-block 2 c (low nibbles), 2 c + 1 (high nibbles, as 16 q)
-                    const int j = 2 * c + h;
-                    // the partials P (16 P for high nibbles): rows gid, gid + 8 x rows 2 t, 2 t + 1 of X
-                    const uint32_t mask = h ? 0xF0F0F0F0u : 0x0F0F0F0Fu;
-                    const uint32_t a[4] = {w[0][0] & mask, w[0][1] & mask, w[1][0] & mask, w[1][1] & mask};
-                    int d[4];
-                    mma_u8s8_k32(d, a, bx[j][0], bx[j][1]);
-                    float aa, ba, ab, bb;
-                    sa.ab(j, aa, ba);
-                    sbs.ab(j, ab, bb);
-                    const float4 xv = my_act[4 * j];  // dx, dx, dx S, dx S of rows 2 t, 2 t + 1 of X
-                    const uint64_t dx2 = f32x2_pack(xv.x, xv.y), ds2 = f32x2_pack(xv.z, xv.w);
-                    ya2 = f32x2_fma(f32x2_pack(aa, aa), f32x2_mul(f32x2_pack(float(d[0]), float(d[1])), dx2), ya2);
-                    ya2 = f32x2_fma(f32x2_pack(-ba, -ba), ds2, ya2);
-                    yb2 = f32x2_fma(f32x2_pack(ab, ab), f32x2_mul(f32x2_pack(float(d[2]), float(d[3])), dx2), yb2);
-                    yb2 = f32x2_fma(f32x2_pack(-bb, -bb), ds2, yb2);
-                }
-            }
+            U::run(ra, ra + 8 * rstride, t, bx, my_act, ya2, yb2);
             const float2 ya = f32x2_unpack(ya2), yb = f32x2_unpack(yb2);
             float* rs = red + size_t(slot) * red_stage + (gsub * nsb + sb) * 128;
             *reinterpret_cast<float2*>(rs + gid * 8 + 2 * t) = ya;
@@ -778,9 +919,8 @@ cudaError_t launch_batch_one(const GemvParams& p, size_t smem, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-}  // namespace
-
-cudaError_t launch_gemv_batch_mma(const GemvParams& p, size_t smem, cudaStream_t s) {
+template <int FMT>
+cudaError_t launch_batch_mma_one(const GemvParams& p, size_t smem, cudaStream_t s) {
     static bool done[64] = {false};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -788,14 +928,25 @@ cudaError_t launch_gemv_batch_mma(const GemvParams& p, size_t smem, cudaStream_t
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!done[dev]) {
         cudaFuncAttributes fa;
-        if ((err = cudaFuncGetAttributes(&fa, gemv_batch_mma_q4k_kernel)) != cudaSuccess) return err;
-        err = cudaFuncSetAttribute(gemv_batch_mma_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if ((err = cudaFuncGetAttributes(&fa, gemv_batch_mma_kernel<FMT>)) != cudaSuccess) return err;
+        err = cudaFuncSetAttribute(gemv_batch_mma_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    kMaxDynamicSmem - static_cast<int>(fa.sharedSizeBytes));
         if (err != cudaSuccess) return err;
         done[dev] = true;
     }
-    gemv_batch_mma_q4k_kernel<<<p.n_cta, kMmaBatchThreads, smem, s>>>(p);
+    gemv_batch_mma_kernel<FMT><<<p.n_cta, kMmaBatchThreads, smem, s>>>(p);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_batch_mma(int fmt, const GemvParams& p, size_t smem, cudaStream_t s) {
+    switch (fmt) {
+        case QX_Q4_K: return launch_batch_mma_one<QX_Q4_K>(p, smem, s);
+        case QX_Q6_K: return launch_batch_mma_one<QX_Q6_K>(p, smem, s);
+        case QX_Q8_0: return launch_batch_mma_one<QX_Q8_0>(p, smem, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_gemv_batch(int fmt, const GemvParams& p, size_t smem, cudaStream_t s) {

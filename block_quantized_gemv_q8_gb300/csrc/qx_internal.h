@@ -97,8 +97,8 @@ constexpr int kBatchThreads = 32 * (kBatchConsumerWarps + 2);
 __host__ __device__ constexpr int batch_cols_per_lane(int fmt, int mb) {
     return (fmt == QX_Q8_0 || mb > kBatchRows) ? 32 : 64;
 }
-// Small-batch Q4_K on the integer tensor path (gemv_batch_mma_q4k_kernel):
-// up to eight rows of X per launch, rows of at most 16 super-blocks (4096
+// Small-batch GEMV on the integer tensor path (gemv_batch_mma_kernel): up to
+// eight rows of X per launch, rows of at most 16 units of 256 columns (4096
 // columns); 16 consumer warps, a producer and a reducer.
 constexpr int kMmaBatchRows = 8;
 constexpr int kMmaBatchMaxSuperBlocks = 16;
@@ -162,7 +162,7 @@ cudaError_t launch_gemv(int fmt, int mode, bool partials, const GemvParams& p, s
                         bool pdl);
 cudaError_t gemv_max_ctas_per_sm(int fmt, int mode, bool partials, bool merged, bool fused, size_t smem, int* out);
 cudaError_t launch_gemv_batch(int fmt, const GemvParams& p, size_t smem, cudaStream_t s);
-cudaError_t launch_gemv_batch_mma(const GemvParams& p, size_t smem, cudaStream_t s);
+cudaError_t launch_gemv_batch_mma(int fmt, const GemvParams& p, size_t smem, cudaStream_t s);
 // Q6_K <-> QX_Q6_K_SOA (qx_repack.cu); row bytes of each side.
 cudaError_t launch_repack_q6k(bool to_soa, const uint8_t* src, int64_t rows, int64_t nsb, int64_t src_row_bytes,
                               uint8_t* dst, int64_t dst_row_bytes, cudaStream_t s);

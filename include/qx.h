@@ -199,15 +199,17 @@ qx_status qx_gemm_prefill(qx_fmt fmt, const void* W, int64_t rows, int64_t cols,
  *       tiles return QX_ERR_SHAPE; path 0 takes path 1 for them.
  *   4 = small-batch GEMV (decode of several tokens at once: speculative or
  *       batched decode), every format, the weights streamed once per group
- *       of rows of X.  Q4_K rows of up to 4096 columns: groups of up to
- *       eight rows on the integer tensor path (mma.sync m16n8k32, the rows
- *       of X as its eight columns: exact integer partials per 32-column
- *       sub-block, scaled in registers).  Other shapes (rows of up to 14336
- *       columns, or 28672 for Q4_K / Q6_K when at most four rows of X
- *       remain; path 0 takes path 1 for wider rows): groups of eight rows
- *       while five or more remain, else of up to four, each lane holding its
- *       column slice of the group's codes and dotting every weight word with
- *       each row's.  Both: the same per-block integer dot products and
+ *       of rows of X: groups of eight while five or more rows remain, then
+ *       one of up to four.  Groups of five to eight rows against rows of up
+ *       to 4096 columns in whole 256-column units whose bytes are a 16-byte
+ *       multiple (Q4_K, Q8_0; Q6_K at 2048 and 4096 columns) run on the
+ *       integer tensor path (mma.sync, the rows of X as the MMA's eight
+ *       columns: exact integer partials per 32-column block, or per 16 for
+ *       Q6_K, scaled in registers); the others on dp4a lanes, each holding
+ *       its column slice of the group's codes and dotting every weight word
+ *       with each row's (rows of up to 14336 columns, or 28672 for Q4_K /
+ *       Q6_K when at most four rows of X remain; path 0 takes path 1 for
+ *       wider rows).  Both: the same per-block integer dot products and
  *       scales as qx_gemv's W4A8 path, in a different f32 summation order
  *       (within the same tolerance, not bit-for-bit path 1).
  * A path that cannot serve the call returns QX_ERR_FMT rather than falling

@@ -57,15 +57,20 @@ def check(fmt, W, rows, cols, X, what, sample_rows=None):
 
 # ragged batches (1..16 rows of X: whole and partial groups of four or eight),
 # ragged row counts (not multiples of the CTA split, of the stage or of the
-# 16-row groups of the tensor path), narrow and wide rows (Q4_K up to 4096
-# columns takes the integer tensor path: 1, 2, 3, 4, 9 and 16 super-blocks a
-# row, so 16, 8, 5, 4, 1 and 1 row groups a stage, some consumer warps idle)
+# 16-row groups of the tensor path), narrow and wide rows.  Groups of five to
+# eight rows of X against rows of up to 4096 columns in whole 256-column units
+# whose bytes are a 16-byte multiple take the integer tensor path: Q4_K with
+# 2, 3, 4, 9 and 16 units a row (8, 5, 4, 1 and 1 row groups a stage, some
+# consumer warps idle), Q6_K at 2048 and 4096 columns, Q8_0 at 256 to 4096;
+# the others, and groups of up to four rows, the dp4a lanes.
 @pytest.mark.parametrize("fmt,m,rows,cols", [
-    (synth.Q4_K, 1, 70, 1024), (synth.Q4_K, 2, 300, 4096), (synth.Q4_K, 3, 129, 256),
+    (synth.Q4_K, 1, 70, 1024), (synth.Q4_K, 2, 300, 4096), (synth.Q4_K, 6, 129, 256),
     (synth.Q4_K, 4, 1000, 4096), (synth.Q4_K, 5, 77, 14336), (synth.Q4_K, 8, 513, 1024),
-    (synth.Q4_K, 9, 200, 768), (synth.Q4_K, 16, 45, 2304), (synth.Q4_K, 7, 1, 4096), (synth.Q4_K, 3, 1111, 512),
+    (synth.Q4_K, 9, 200, 768), (synth.Q4_K, 16, 45, 2304), (synth.Q4_K, 7, 1, 4096), (synth.Q4_K, 5, 1111, 512),
     (synth.Q6_K, 2, 300, 1024), (synth.Q6_K, 4, 129, 14336), (synth.Q6_K, 7, 33, 256),
+    (synth.Q6_K, 6, 300, 2048), (synth.Q6_K, 8, 129, 4096), (synth.Q6_K, 16, 45, 2048),
     (synth.Q8_0, 2, 151, 896), (synth.Q8_0, 4, 300, 32), (synth.Q8_0, 6, 513, 864), (synth.Q8_0, 9, 128, 4096),
+    (synth.Q8_0, 5, 77, 256), (synth.Q8_0, 8, 1000, 2048), (synth.Q8_0, 6, 3, 512),
 ])
 def test_batch_matches_oracle(fmt, m, rows, cols):
     W = synth.weights(fmt, rows, cols, seed=80 + m + rows)
@@ -98,6 +103,18 @@ def test_batch_tensor_path_zero_weights_give_exact_zeros():
     X = synth.activation(m, cols, seed=96)
     Y = check(fmt, W, rows, cols, X, "zero weight rows")
     assert np.all(Y[:, zero_rows] == 0.0)
+
+
+@pytest.mark.parametrize("fmt", [synth.Q6_K, synth.Q8_0])
+def test_batch_tensor_path_full_width(fmt):
+    """Q6_K and Q8_0 rows of 4096 columns on the integer tensor path, eight
+    rows of X, 2000 weight rows (several stages a CTA), sampled rows."""
+    rows, cols, m = 2000, 4096, 8
+    W = synth.weights(fmt, rows, cols, seed=97)
+    X = synth.activation(m, cols, seed=98)
+    rng = np.random.default_rng(99)
+    wr = np.sort(np.concatenate([rng.choice(rows, 200, replace=False), [0, rows - 1]]))
+    check(fmt, W, rows, cols, X, f"tensor path {synth.NAMES[fmt]}", sample_rows=wr)
 
 
 @pytest.mark.parametrize("m", [4, 8])
