@@ -546,7 +546,7 @@ def measure_config(name: str, qx, torch, stream, hbm: float, bf16: float, peak_k
                                "frac": fl / (top["path3_us"] * 1e-6) / 1e12 / bf16, "peak_kind": peak_kind,
                                "flops_per_launch": fl, "mean_launch_us": top["path3_us"],
                                "note": "bf16 FLOP of the three split products (Xh Wh + Xh Wl + Xl Wh)"}
-        out.update({"config": "prefill X[M, 4096] x Q4_K [14336, 4096], M in {1, 8, 64, 512}",
+        out.update({"config": "prefill X[M, 4096] x Q4_K [14336, 4096], M in " + str(list(synth.PREFILL_SWEEP_M)),
                     "sweep": sweep, "flops_per_row": 2 * rows * cols, "bf16_dense_peak_tflops": bf16,
                     "note": "path 1 = one W4A8 GEMV launch per row; path 2 = tensor cores (mma.sync f16 with "
                             "integer-valued operands); path 3 = tcgen05 bf16 GEMM over the split dequantised "

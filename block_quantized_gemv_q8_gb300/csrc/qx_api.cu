@@ -53,11 +53,16 @@ constexpr size_t kChainInflightBytes = size_t(QX_CHAIN_INFLIGHT_KB) * 1024;
 constexpr size_t kPrewaitBytes = size_t(QX_PREWAIT_KB) * 1024;
 // Shared memory of a CTA that leaves room for a second one on the SM.
 constexpr size_t kHalfSmBytes = 110 * 1024;
-// Automatic prefill path (measured on GB300, X [m, 4096] x Q4_K [14336,
-// 4096]): one GEMV for a single row of X (10.9 us); the small-batch GEMV up
-// to kPrefillBatchMaxRows rows (m = 2, 4, 8, 16: 14.8, 14.8, 27.1, 51.6 us,
-// against 18.7, 33.0, 61.9, 121.4 us row by row and about 60 us on
-// tcgen05); the tcgen05 GEMM above (m = 64: 61.8 us against 197 us).
+// Automatic prefill path (measured on GB300, X [m, 4096] against Q4_K,
+// Q6_K and Q8_0 weights of 4096, 14336 and 28672 rows): one GEMV for a single
+// row of X (10.6 us on 14336 Q4_K rows); the small-batch GEMV up to
+// prefill_batch_max_rows() rows; the tcgen05 GEMM above, which takes about
+// 80 us for any M up to 256 (one tile row, every tile's K pipeline the same
+// length) and 193 us at M = 512.  The small batch on the integer tensor path
+// costs about 14.4 us per group of eight rows of X for 14336 x 4096 Q4_K
+// (Q6_K 22-24, Q8_0 16-17): it beats tcgen05 up to 40 rows for Q4_K (71.9
+// against 82.2 us), 32 for Q8_0 (67.9 against 80.1) and 24 for Q6_K (67.8
+// against 89.6); on the lanes up to 16 (m = 16: 41 against 80 us).
 constexpr int64_t kPrefillBatchMaxRows = 16;
 // Shared memory of a chain CTA (one per SM): the ring, partial sums and
 // activation within kChainSmBytes, and all of it with the job descriptors
@@ -431,6 +436,12 @@ bool batch_mma_serves(int fmt, int64_t cols) {
     return row_bytes_of(fmt, cols) % 16 == 0;
 }
 
+// The most rows of X the automatic prefill path gives the small-batch GEMV.
+int64_t prefill_batch_max_rows(int fmt, int64_t cols) {
+    if (!batch_mma_serves(fmt, cols)) return kPrefillBatchMaxRows;
+    return fmt == QX_Q4_K ? 40 : (fmt == QX_Q8_0 ? 32 : 24);
+}
+
 // Up to eight rows of X (from row m0) on the integer tensor path
 // (gemv_batch_mma_kernel).  Stage: 16 P rows (P = 16 / units per row) at a
 // padded stride of row_bytes + 16; per stage the consumers' partials
@@ -575,7 +586,7 @@ qx_status prefill_dispatch(qx_fmt fmt, const void* W, int64_t rows, int64_t cols
     }
     const int64_t rb = row_bytes_of(fmt, cols);
     if (path == 0) {
-        path = X->m == 1 ? 1 : (X->m <= kPrefillBatchMaxRows ? 4 : 3);
+        path = X->m == 1 ? 1 : (X->m <= prefill_batch_max_rows(fmt, cols) ? 4 : 3);
         // shapes beyond the tensor-core kernel's 32-bit copy coordinates take one GEMV per row
         if (path == 3 && !prefill_tc_serves(fmt, rows, cols, X->m, rb)) path = 1;
         // rows wider than the small-batch lanes cover (eight-row lanes: 14336

@@ -143,7 +143,7 @@ QWEN05B_LM_HEAD = ("lm_head", Q8_0, 151936, 896)
 LLAMA8B_LM_HEAD_Q6K = ("lm_head", Q6_K, 128256, 4096)
 PREFILL = ("prefill", Q4_K, 14336, 4096)  # X[512, 4096]
 PREFILL_M = 512
-PREFILL_SWEEP_M = (1, 2, 4, 8, 16, 64, 512)
+PREFILL_SWEEP_M = (1, 2, 4, 8, 16, 32, 64, 512)
 
 
 def seed_for(workload: int, layer: int, proj: int) -> int:

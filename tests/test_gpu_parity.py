@@ -357,9 +357,12 @@ def test_prefill_tcgen05_formats(fmt, m, rows, cols):
 def test_prefill_auto_and_refusals():
     fmt, rows, cols = synth.Q4_K, 96, 1024
     W = dev(synth.weights(fmt, rows, cols, seed=60))
-    # automatic path: a GEMV for one row, the small-batch GEMV for 2..16 rows, tcgen05 above
+    # automatic path: a GEMV for one row, the small-batch GEMV for 2..40 rows (Q4_K rows the integer
+    # tensor path serves; Q8_0 32, Q6_K 24; 16 on the lanes: Q6_K at 1024 columns), tcgen05 above
     W6 = dev(synth.weights(synth.Q6_K, rows, cols, seed=62))
-    for Wm, f, m, forced in ((W, fmt, 1, 1), (W, fmt, 2, 4), (W, fmt, 16, 4), (W, fmt, 17, 3), (W, fmt, 200, 3),
+    W8 = dev(synth.weights(synth.Q8_0, rows, cols, seed=63))
+    for Wm, f, m, forced in ((W, fmt, 1, 1), (W, fmt, 2, 4), (W, fmt, 16, 4), (W, fmt, 40, 4), (W, fmt, 41, 3),
+                             (W, fmt, 200, 3), (W8, synth.Q8_0, 32, 4), (W8, synth.Q8_0, 33, 3),
                              (W6, synth.Q6_K, 15, 4), (W6, synth.Q6_K, 17, 3)):
         a, q, d, s = quantize_both(synth.activation(m, cols, seed=61 + m))
         y_auto = host(qx.qx_gemm_prefill(f, Wm, rows, cols, a))
