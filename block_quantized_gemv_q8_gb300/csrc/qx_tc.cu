@@ -368,7 +368,8 @@ __device__ __forceinline__ void convert_w8<QX_Q8_0>(const uint8_t* blk, int c, i
 // the K groups, whose second CTA hands its f32 partial sums to the first
 // through distributed shared memory (Y = first half + second half, in that
 // order).  The host splits the tiles of a last, at most half-full wave, so
-// that it takes half as long.
+// that it takes half as long, and every tile when all of them fill at most
+// half a wave.
 //   warp 0: TMA producer (the whole warp: per-row boxes take four rows a lane);
 //   warp 1: tensor memory (two 128-column accumulators) and the MMA issuer;
 //   warps 2-17: converters -- per K slice, thread ct converts X row ct / 2
@@ -619,8 +620,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
             }
         }
     }
-    // A split launch runs beside the launch of the other tiles (programmatic
-    // dependent launch); it completes only after that one has.
+    // A split launch beside the launch of the other tiles (programmatic
+    // dependent launch) completes only after that one has; launched alone,
+    // this wait returns at once.
     if (p.split) pdl_wait_prior_grid();
     tc_fence_before();
     __syncthreads();
@@ -701,11 +703,16 @@ cudaError_t launch_fmt(TcParams& p, const uint8_t* W, int64_t N, const int8_t* x
     // Waves of tiles: when the last wave is at most half full (and there is
     // more than one), its tiles are split in two along K and run as clusters
     // of two CTAs beside the others' last wave, so that it takes half as long.
+    // When all the tiles fill at most half a wave, every tile is split (one
+    // launch of clusters, after the preceding work like any launch).
     const int64_t tiles_m = (M + TBM - 1) / TBM, tiles_n = (N + TBN - 1) / TBN, tiles = tiles_m * tiles_n;
     const int64_t slots = int64_t(sm_count > 0 ? sm_count : 1) * per_sm[dev];
     const int n_groups = int((K + G::kGroupK - 1) / G::kGroupK);
     int64_t tail = 0;
-    if (tiles > slots && n_groups >= 2 && 2 * (tiles % slots) <= slots) tail = tiles % slots;
+    if (n_groups >= 2) {
+        if (tiles > slots && 2 * (tiles % slots) <= slots) tail = tiles % slots;
+        else if (2 * tiles <= slots) tail = tiles;
+    }
     p.tiles_m = int(tiles_m);
     p.g_split = n_groups / 2;
     if (tiles - tail > 0) {
@@ -727,10 +734,12 @@ cudaError_t launch_fmt(TcParams& p, const uint8_t* W, int64_t N, const int8_t* x
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        // beside the first launch (which lets it start at its own start, so
+        // after the preceding work); alone, an ordinary stream-ordered launch
         attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 2;
+        cfg.numAttrs = tiles > tail ? 2 : 1;
         if ((e = cudaLaunchKernelEx(&cfg, tc_prefill_kernel<FMT>, p)) != cudaSuccess) return e;
     }
     return cudaSuccess;
