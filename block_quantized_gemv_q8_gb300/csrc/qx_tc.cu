@@ -506,13 +506,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
         }
         const uint32_t xa = uint32_t(OP_XH + (xrow >> 7) * T_TILE), xla = uint32_t(OP_XL + (xrow >> 7) * T_TILE);
         const int xr7 = xrow & 127;
+        // Ring positions, advanced slice by slice (no divisions): operand stage s and the parity of
+        // its release phase to wait for, K slice c of group g, raw slot r and its fill parity.
+        int s = 0, lap = 0, c = 0, g = g0, r = 0, wph = 0;
+        const int64_t wrow_byte0 = int64_t(n0 + wrow) * p.row_bytes;  // this thread's weight row in the matrix
+        const uint8_t* blk = nullptr;  // the thread's row of the current raw group in its slot
         // slice t (ring position lt = t - t0), its codes and scale in slot j = lt % kXAhead (the loop
         // is unrolled by kXAhead so that j is static), which then takes slice t + kXAhead
         const auto convert_slice = [&](int t, uint4& qx, float& dx) -> bool {
-            const int lt = t - t0, g = t / SPG, c = t % SPG, lg = g - g0, r = lg % RS, s = lt % OP_STAGES;
-            if ((c == 0 && !warp_wait(&full_wr[r], (lg / RS) & 1, p.wait_ns, p.err, kErrTimeoutFull)) ||
-                (lt >= OP_STAGES &&
-                 !warp_wait(&empty_op[s], ((lt / OP_STAGES) - 1) & 1, p.wait_ns, p.err, kErrTimeoutEmpty)))
+            if (c == 0) {
+                if (!warp_wait(&full_wr[r], wph, p.wait_ns, p.err, kErrTimeoutFull)) return false;
+                const int64_t a = wrow_byte0 + int64_t(g) * G::kGroupBytes;
+                blk = wr + r * RAW_BYTES + wrow * wstride + (a & 15);  // the group in its box
+            }
+            if (t - t0 >= OP_STAGES && !warp_wait(&empty_op[s], lap ^ 1, p.wait_ns, p.err, kErrTimeoutEmpty))
                 return false;
             uint4 xhi[2], xlo[2], whi, wlo;
             if (xlive) {
@@ -524,11 +531,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
                 qx = __ldg(xq_row + 2 * (t + kXAhead));
                 dx = __ldg(xd_row + t + kXAhead);
             }
-            {
-                const int64_t a = int64_t(n0 + wrow) * p.row_bytes + int64_t(g) * G::kGroupBytes;
-                const uint8_t* blk = wr + r * RAW_BYTES + wrow * wstride + (a & 15);  // the group in its box
-                convert_w8<FMT>(blk, c, wq, whi, wlo);
-            }
+            convert_w8<FMT>(blk, c, wq, whi, wlo);
             uint8_t* st = ops + s * OP_BYTES;
             if (xstore) {
 #pragma unroll
@@ -543,9 +546,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
             *reinterpret_cast<uint4*>(st + OP_WL + woff) = wlo;
             fence_proxy_async_smem();  // generic-proxy stores, read by the tensor cores
             __syncwarp();
+            const bool group_done = c == SPG - 1 || t == t1 - 1;
             if (lane == 0) {
                 mbar_arrive(&full_op[s]);
-                if (c == SPG - 1 || t == t1 - 1) mbar_arrive(&empty_wr[r]);
+                if (group_done) mbar_arrive(&empty_wr[r]);
+            }
+            if (++s == OP_STAGES) {
+                s = 0;
+                lap ^= 1;
+            }
+            if (group_done) {
+                c = 0;
+                ++g;
+                if (++r == RS) {
+                    r = 0;
+                    wph ^= 1;
+                }
+            } else {
+                ++c;
             }
             return true;
         };
