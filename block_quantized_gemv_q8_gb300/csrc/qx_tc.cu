@@ -106,8 +106,7 @@ struct TcParams {
     int w2d;            // 1: weight rows are a 16-byte multiple, one 2-D box per group
     int tiles_m;        // M tiles; tile i is M tile i % tiles_m of N tile i / tiles_m
     int tile_base;      // the launch's first tile
-    int split;          // 1: two CTAs (a cluster) per tile, one per half of the K groups
-    int g_split;        // K groups of the first half
+    int split;          // 0, or the CTAs per tile (a cluster of 2 or 4), each taking its share of the K groups
     int64_t row_bytes;
     float* Y;           // [M, N] f32
     unsigned* err;
@@ -186,6 +185,14 @@ __device__ __forceinline__ uint32_t peer_addr(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void st_peer_v4(uint32_t raddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(raddr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
+}
+__device__ __forceinline__ uint4 ld_peer_v4(uint32_t raddr) {
+    uint4 v;
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(raddr)
+                 : "memory");
+    return v;
 }
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -364,12 +371,13 @@ __device__ __forceinline__ void convert_w8<QX_Q8_0>(const uint8_t* blk, int c, i
 
 // Tiles are numbered M tile fastest, so the CTAs that share a weight tile run
 // together and read it from DRAM once.  A launch takes tiles tile_base ..:
-// one CTA per tile, or (split) a cluster of two CTAs per tile, one per half of
-// the K groups, whose second CTA hands its f32 partial sums to the first
-// through distributed shared memory (Y = first half + second half, in that
-// order).  The host splits the tiles of a last, at most half-full wave, so
-// that it takes half as long, and every tile when all of them fill at most
-// half a wave.
+// one CTA per tile, or (split) a cluster of two or four CTAs per tile, each
+// taking an equal share of the K groups, whose f32 partial sums meet in the
+// first CTA through distributed shared memory: Y = a0 + a1 for two, and
+// (a0 + a1) + (a2 + a3) for four, in that order.  The host splits the tiles
+// of a last, at most half-full wave in two, so that it takes half as long;
+// every tile in two when all of them fill at most half a wave, and in four
+// when they fill at most a quarter (and K has four groups or more).
 //   warp 0: TMA producer (the whole warp: per-row boxes take four rows a lane);
 //   warp 1: tensor memory (two 128-column accumulators) and the MMA issuer;
 //   warps 2-17: converters -- per K slice, thread ct converts X row ct / 2
@@ -397,13 +405,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tile = p.tile_base + (p.split ? int(blockIdx.x >> 1) : int(blockIdx.x));
+    const int tile = p.tile_base + (p.split ? int(blockIdx.x / unsigned(p.split)) : int(blockIdx.x));
     const int m0 = (tile % p.tiles_m) * TBM, n0 = (tile / p.tiles_m) * TBN;
     const int halves = (m0 + 128 < p.M) ? 2 : 1;  // 128-row halves of the tile with rows of X
     const int n_k = p.K / TBK, n_groups = (p.K + G::kGroupK - 1) / G::kGroupK;
     // this CTA's K groups [g0, g1) and slices [t0, t1); ring positions count from g0 and t0
     const uint32_t rank = p.split ? cluster_rank() : 0u;
-    const int g0 = rank == 0 ? 0 : p.g_split, g1 = (p.split && rank == 0) ? p.g_split : n_groups;
+    const int ks = p.split ? p.split : 1;  // CTAs sharing the tile's K groups
+    const int g0 = int(int64_t(n_groups) * int(rank) / ks), g1 = int(int64_t(n_groups) * (int(rank) + 1) / ks);
     const int t0 = g0 * SPG, t1 = g1 * SPG < n_k ? g1 * SPG : n_k;
     const bool w2d = FMT == QX_Q4_K || p.w2d != 0;
     const int wstride = w2d ? G::kBox : kRowStride1d;
@@ -587,20 +596,47 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
     const auto xchunk = [&](int j) -> uint32_t {
         return uint32_t(half * 65536 + row * 512 + ((j ^ lane) << 4));
     };
+    // Two CTAs: the second hands its sums to the first, which adds them to its own.  Four: the odd
+    // ranks hand theirs to the rank below; rank 2 adds them to its own and hands the result to
+    // rank 1's (idle) buffer, while rank 0 adds rank 1's into its own buffer; rank 0 stores
+    // (a0 + a1) + (a2 + a3).
     if (p.split) {
-        cluster_sync_all();  // both CTAs' MMAs are done: the first's stages are free
-        if (rank == 1 && drains && acc_ok) {
-            const uint32_t dst0 = peer_addr(xbuf, 0u);
+        cluster_sync_all();  // every CTA's MMAs are done: their stages are free
+        if ((rank & 1u) && drains && acc_ok) {
+            const uint32_t dst = peer_addr(xbuf, rank - 1u);
 #pragma unroll 1
             for (int cc = 0; cc < TBN / 32; ++cc) {
                 uint32_t v[32];
                 tc_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(half * TBN + 32 * cc), v);
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    st_peer_v4(dst0 + xchunk(8 * cc + i), v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                    st_peer_v4(dst + xchunk(8 * cc + i), v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
             }
         }
-        cluster_sync_all();  // the partial sums have landed
+        cluster_sync_all();  // the odd ranks' sums have landed
+        if (p.split == 4) {
+            if ((rank == 0u || rank == 2u) && drains && acc_ok) {
+#pragma unroll 1
+                for (int cc = 0; cc < TBN / 32; ++cc) {
+                    uint32_t v[32];
+                    tc_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(half * TBN + 32 * cc), v);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float4 o = *reinterpret_cast<const float4*>(ops + xchunk(8 * cc + i));
+                        o.x = __uint_as_float(v[4 * i]) + o.x;
+                        o.y = __uint_as_float(v[4 * i + 1]) + o.y;
+                        o.z = __uint_as_float(v[4 * i + 2]) + o.z;
+                        o.w = __uint_as_float(v[4 * i + 3]) + o.w;
+                        if (rank == 2u)
+                            st_peer_v4(peer_addr(xbuf, 1u) + xchunk(8 * cc + i), __float_as_uint(o.x),
+                                       __float_as_uint(o.y), __float_as_uint(o.z), __float_as_uint(o.w));
+                        else
+                            *reinterpret_cast<float4*>(ops + xchunk(8 * cc + i)) = o;
+                    }
+                }
+            }
+            cluster_sync_all();  // rank 0 holds a0 + a1, rank 1 holds a2 + a3
+        }
     }
     if (rank == 0 && drains && acc_ok) {
         const int yr = m0 + 128 * half + row;
@@ -609,19 +645,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
         // required to be 4-byte aligned)
         const bool vec = (n0 + TBN <= p.N) && (p.N % 4 == 0) && (reinterpret_cast<uintptr_t>(p.Y) & 15) == 0;
         float* yrow = p.Y + size_t(row_ok ? yr : 0) * p.N + n0;
+        const uint32_t src1 = p.split == 4 ? peer_addr(xbuf, 1u) : 0u;
 #pragma unroll 1
         for (int cc = 0; cc < TBN / 32; ++cc) {
             uint32_t v[32];
-            tc_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(half * TBN + 32 * cc), v);
-            if (p.split) {
-                const auto add = [](uint32_t& a, float b) { a = __float_as_uint(__uint_as_float(a) + b); };
+            if (p.split == 4) {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const float4 o = *reinterpret_cast<const float4*>(ops + xchunk(8 * cc + i));
-                    add(v[4 * i], o.x);
-                    add(v[4 * i + 1], o.y);
-                    add(v[4 * i + 2], o.z);
-                    add(v[4 * i + 3], o.w);
+                    const uint4 r = ld_peer_v4(src1 + xchunk(8 * cc + i));
+                    v[4 * i] = __float_as_uint(o.x + __uint_as_float(r.x));
+                    v[4 * i + 1] = __float_as_uint(o.y + __uint_as_float(r.y));
+                    v[4 * i + 2] = __float_as_uint(o.z + __uint_as_float(r.z));
+                    v[4 * i + 3] = __float_as_uint(o.w + __uint_as_float(r.w));
+                }
+            } else {
+                tc_ld32(tmem + (uint32_t(32 * q) << 16) + uint32_t(half * TBN + 32 * cc), v);
+                if (p.split) {
+                    const auto add = [](uint32_t& a, float b) { a = __float_as_uint(__uint_as_float(a) + b); };
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 o = *reinterpret_cast<const float4*>(ops + xchunk(8 * cc + i));
+                        add(v[4 * i], o.x);
+                        add(v[4 * i + 1], o.y);
+                        add(v[4 * i + 2], o.z);
+                        add(v[4 * i + 3], o.w);
+                    }
                 }
             }
             if (!row_ok) continue;
@@ -638,6 +687,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_prefill_kernel(const __grid_
             }
         }
     }
+    if (p.split == 4) cluster_sync_all();  // rank 1's buffer stays until rank 0 has read it
     // A split launch beside the launch of the other tiles (programmatic
     // dependent launch) completes only after that one has; launched alone,
     // this wait returns at once.
@@ -722,17 +772,24 @@ cudaError_t launch_fmt(TcParams& p, const uint8_t* W, int64_t N, const int8_t* x
     // more than one), its tiles are split in two along K and run as clusters
     // of two CTAs beside the others' last wave, so that it takes half as long.
     // When all the tiles fill at most half a wave, every tile is split (one
-    // launch of clusters, after the preceding work like any launch).
+    // launch of clusters, after the preceding work like any launch), in four
+    // when they fill at most a quarter of one and there are four K groups.
     const int64_t tiles_m = (M + TBM - 1) / TBM, tiles_n = (N + TBN - 1) / TBN, tiles = tiles_m * tiles_n;
     const int64_t slots = int64_t(sm_count > 0 ? sm_count : 1) * per_sm[dev];
     const int n_groups = int((K + G::kGroupK - 1) / G::kGroupK);
     int64_t tail = 0;
+    int ks = 2;
     if (n_groups >= 2) {
-        if (tiles > slots && 2 * (tiles % slots) <= slots) tail = tiles % slots;
-        else if (2 * tiles <= slots) tail = tiles;
+        if (tiles > slots && 2 * (tiles % slots) <= slots) {
+            tail = tiles % slots;
+        } else if (n_groups >= 4 && 4 * tiles <= slots) {
+            tail = tiles;
+            ks = 4;
+        } else if (2 * tiles <= slots) {
+            tail = tiles;
+        }
     }
     p.tiles_m = int(tiles_m);
-    p.g_split = n_groups / 2;
     if (tiles - tail > 0) {
         p.tile_base = 0;
         p.split = 0;
@@ -741,15 +798,15 @@ cudaError_t launch_fmt(TcParams& p, const uint8_t* W, int64_t N, const int8_t* x
     }
     if (tail > 0) {
         p.tile_base = int(tiles - tail);
-        p.split = 1;
+        p.split = ks;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(unsigned(2 * tail));
+        cfg.gridDim = dim3(unsigned(ks * tail));
         cfg.blockDim = dim3(kTcThreads);
         cfg.dynamicSmemBytes = tc_smem_bytes<FMT>();
         cfg.stream = s;
         cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.x = unsigned(ks);
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         // beside the first launch (which lets it start at its own start, so
@@ -771,7 +828,7 @@ bool prefill_tc_serves(int fmt, int64_t N, int64_t K, int64_t M, int64_t row_byt
     const int64_t limit = (int64_t(1) << 31) - 4096;
     const int64_t tiles_n = (N + TBN - 1) / TBN;
     const int64_t tiles = tiles_n * ((M + TBM - 1) / TBM);
-    return M <= INT32_MAX && N <= INT32_MAX && K <= INT32_MAX && 2 * tiles <= INT32_MAX &&
+    return M <= INT32_MAX && N <= INT32_MAX && K <= INT32_MAX && 4 * tiles <= INT32_MAX &&
            tiles_n * TBN * row_bytes < limit;
 }
 

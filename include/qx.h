@@ -191,13 +191,15 @@ qx_status qx_gemm_prefill(qx_fmt fmt, const void* W, int64_t rows, int64_t cols,
  *       rows) leave a last wave over the SMs at most half full, that wave's
  *       tiles are split in two along K (a second launch, started beside the
  *       first by programmatic dependent launch; Y = the first half's sum plus
- *       the second's), and when all the tiles fill at most half a wave, every
- *       tile is; so results depend on the shape and the GPU's SM count but not
- *       on the run.  No workspace: the call allocates nothing, may
+ *       the second's); when all the tiles fill at most half a wave, every
+ *       tile is, and when they fill at most a quarter (K of 1024 columns or
+ *       more; 512 for Q8_0) every tile is split in four (Y = (a0 + a1) +
+ *       (a2 + a3)); so results depend on the shape and the GPU's SM count but
+ *       not on the run.  No workspace: the call allocates nothing, may
  *       be captured in a CUDA graph on its first use and may run concurrently
  *       on several streams.  Shapes whose weights span 2 GiB or more (the
- *       copy engine's 32-bit coordinates) or need more than 65535 weight
- *       tiles return QX_ERR_SHAPE; path 0 takes path 1 for them.
+ *       copy engine's 32-bit coordinates) or more than 2^29 - 1 tiles
+ *       return QX_ERR_SHAPE; path 0 takes path 1 for them.
  *   4 = small-batch GEMV (decode of several tokens at once: speculative or
  *       batched decode), every format, the weights streamed once per group
  *       of rows of X: groups of eight while five or more rows remain, then
