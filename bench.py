@@ -55,7 +55,7 @@ def measured_peaks():
 
 CHAIN_SOURCES = ["qx_chain.cu", "qx_lanes.cuh", "qx_device.cuh", "qx_api.cu", "qx_internal.h"]
 CHAIN_PROFILE_NAME = "profiles/gemv_chain_llama8b.md"
-GEMV_SOURCES = ["qx_gemv.cu", "qx_lanes.cuh", "qx_device.cuh", "qx_api.cu", "qx_internal.h"]
+GEMV_SOURCES = ["qx_gemv.cu", "qx_stage.cuh", "qx_lanes.cuh", "qx_device.cuh", "qx_api.cu", "qx_internal.h"]
 GATEUP_PROFILE_NAME = "profiles/gemv_q4k_w4a8_gateup_llama8b.md"
 
 

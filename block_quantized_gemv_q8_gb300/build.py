@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libqx.so")
-SOURCES = ["qx_api.cu", "qx_actq8.cu", "qx_gemv.cu", "qx_chain.cu", "qx_prefill.cu", "qx_tc.cu", "qx_repack.cu", "qx_mma_rate.cu"]
+SOURCES = ["qx_api.cu", "qx_actq8.cu", "qx_gemv.cu", "qx_f32mma.cu", "qx_chain.cu", "qx_prefill.cu", "qx_tc.cu", "qx_repack.cu", "qx_mma_rate.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"] + ARCH
 # Extra defines for measurement sweeps of the launch geometry (e.g.

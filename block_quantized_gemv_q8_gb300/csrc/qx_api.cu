@@ -386,6 +386,48 @@ qx_status chain_geometry(const DeviceInfo& dev, ChainParams& p, size_t& smem) {
 
 // One streaming-GEMV launch over `n` matrices of the same format.  `mode` is
 // the public mode (flags already removed).
+// Whether the f32-mode tensor-pipe kernel (gemv_f32_mma_kernel) serves the
+// shape: Q6_K rows (either layout) of 2048 or 4096 columns, where both
+// layouts are served alike (GGUF rows are then a 16-byte multiple), so their
+// outputs stay bit-identical.
+bool f32_mma_serves(int fmt, int64_t cols) {
+    return (fmt == QX_Q6_K || fmt == QX_Q6_K_SOA) && (cols == 2048 || cols == 4096);
+}
+
+// f32 mode on the tensor pipe: stages of 16 P gq rows (P = 16 / units per
+// row warps per unit, each taking gq 16-row groups a stage) at a padded
+// stride of row_bytes + 16, per stage the consumers' partials [P gq][units][16]
+// floats.  One group a warp and stage: four stages of 16 rows of 4096
+// columns ran the lm_head faster than two stages of 32 rows (80.5 against
+// 88.8 us, repacked layout), which halve the per-stage overhead per output.
+qx_status run_gemv_f32_mma(int fmt, GemvParams& p, int64_t cols, const DeviceInfo& dev, bool pdl, cudaStream_t s) {
+    const int nsb = static_cast<int>(cols / 256), P = 16 / nsb, gq = 1;
+    const int64_t rb = row_bytes_of(fmt, cols);
+    const size_t slot = (size_t(16 * P * gq) * size_t(rb + 16) + 127) / 128 * 128;
+    const size_t red_stage = size_t(P * gq) * nsb * 16 * 4;
+    const size_t budget = 224 * 1024;
+    int stages = 2;
+    while (stages < 8 && size_t(stages + 1) * (slot + red_stage + 24) + 32 <= budget) ++stages;
+    p.red_off = static_cast<int>(size_t(stages) * slot);
+    p.bar_off = static_cast<int>(size_t(p.red_off) + size_t(stages) * red_stage);
+    const size_t smem = size_t(p.bar_off) + 24 * size_t(stages);
+    if (smem > 227 * 1024) return QX_ERR_SHAPE;
+    p.cols = cols;
+    p.row_bytes = rb;
+    p.quantum = 16;
+    p.G = 16 * P * gq;
+    p.gq = gq;
+    p.stages = stages;
+    p.slot_bytes = static_cast<int>(slot);
+    int64_t groups = 0;  // 16-row groups over the entries
+    for (int k = 0; k < p.n_entries; ++k) groups += (p.e[k].rows + 15) / 16;
+    p.n_cta = static_cast<int>(groups < dev.sm_count ? groups : dev.sm_count);
+    p.err = dev.err_word;
+    p.wait_ns = kDefaultWaitNs;
+    const cudaError_t e = launch_gemv_f32_mma(fmt, p, smem, s, pdl);
+    return e == cudaSuccess ? QX_OK : cuda_fail(e, "gemv (f32, tensor) launch");
+}
+
 qx_status run_gemv(int fmt, int n, const void* const* W, const int64_t* rows, int64_t cols, const void* x,
                    float* const* y, int32_t* P, int mode, bool pdl, cudaStream_t s) {
     DeviceInfo* dev = nullptr;
@@ -408,6 +450,7 @@ qx_status run_gemv(int fmt, int n, const void* const* W, const int64_t* rows, in
     if (mode == QX_MODE_F32) {
         p.x = static_cast<const float*>(x);
         kmode = QX_MODE_F32;
+        if (P == nullptr && y != nullptr && f32_mma_serves(fmt, cols)) return run_gemv_f32_mma(fmt, p, cols, *dev, pdl, s);
     } else if (mode == QX_MODE_W4A8_FUSED) {
         p.xf = static_cast<const float*>(x);
     } else {

@@ -1,0 +1,391 @@
+// qx_f32mma.cu -- f32-mode GEMV of Q6_K rows (GGUF blocks or the repacked
+// QX_Q6_K_SOA layout) with the products on the tensor pipe, sm_103a.
+//
+// f32 mode is the dequantise-and-FMA GEMV (llambda.lisp README, "Features &
+// Architecture"): y_r = sum_k w_rk x_k with the f32 activation and the Q6_K
+// weights w = d sc (q - 32) (one int8 scale sc per 16 weights, one f16 d per
+// 256).  The lanes of gemv_kernel spend about 4.5 instructions per weight on
+// it, mostly converting quants to f32; here the multiplications run as
+// mma.sync m16n8k16 with bf16 operands and f32 accumulation:
+//
+//   * A = 16 weight rows x 16 columns: the quants q - 32 (-32..31), which
+//     are exact bf16 values -- a byte q becomes the bf16 128 + q by one byte
+//     permute (0x43 above the byte), and one bf16x2 subtraction of 160 leaves
+//     q - 32, two values per instruction;
+//   * B = the activation of the warp's 256-column super-block, scaled by a
+//     power of two 2^e that brings its largest magnitude into [1, 2), and
+//     split into two bf16 terms: x 2^e = hi + lo + r, |r| <= 2^-18 |x 2^e|;
+//   * the eight B columns are four pairs (hi, lo), one pair per 16-column
+//     group and zero outside it, so one accumulator holds, per weight row,
+//     the hi and lo sums of four groups; per group the f32 epilogue adds
+//     sc (D_hi + D_lo), per super-block d 2^-e, and the reducer warp adds the
+//     super-blocks of each row in a fixed order.
+//
+// Error: each product (q - 32) hi, (q - 32) lo is exact (6 x 8 significant
+// bits); the split drops at most 2^-18 of each |x| (for every element within
+// 2^-100 of its super-block's largest, whose terms stay normal); the f32 sums
+// (the tensor pipe's, the epilogue's, the reduction's) add a few units of
+// 2^-24 of the sum of |terms|.  So |y - y_exact| is below about 2^-17 of
+// sum_k |w_rk x_k|, well inside the f32-mode tolerance of 1e-4 of that sum.
+// Both layouts hold the same values and run the same arithmetic in the same
+// order, so their outputs are bit-identical.
+//
+// Structure: the row-group kernel of the small-batch tensor path -- one CTA
+// per SM, a producer warp copying each row of a stage of 16 P gq rows to a
+// padded stride (qx_stage.cuh), 16 consumer warps (warp w owns super-block
+// w % nsb of row groups w / nsb, w / nsb + P, ... of every stage, P = 16 /
+// nsb, so its B fragments stay in registers), and a reducer warp.  Rows of 2048 or 4096 columns (GGUF Q6_K
+// rows are then a 16-byte multiple).
+#include <cuda_runtime.h>
+
+#include "qx_device.cuh"
+#include "qx_internal.h"
+#include "qx_stage.cuh"
+
+namespace qx {
+
+namespace {
+
+constexpr int kF32MmaWarps = 16;
+
+// bf16x2 (hi half = b, lo half = a), rounded to nearest even.
+__device__ __forceinline__ uint32_t bf16x2_rn(float a, float b) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+    return r;
+}
+
+__device__ __forceinline__ float bf16_rn_f32(float v) {
+    return __uint_as_float(bf16x2_rn(v, 0.0f) << 16);
+}
+
+// The bf16 pair (q0 - 32, q1 - 32) of bytes k, k + 1 (k = 0 or 2) of a word
+// of 6-bit quants: 0x43 above each byte is the bf16 128 + q; minus 160, exact.
+template <int K>
+__device__ __forceinline__ uint32_t q6_pair_bf16(uint32_t w) {
+    const uint32_t biased = __byte_perm(w, 0x43u, K == 0 ? 0x4140u : 0x4342u);
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(biased), "r"(0x43204320u));
+    return r;
+}
+
+// Byte sel & 3 of w, sign-extended (prmt with the sign-replicate selectors).
+__device__ __forceinline__ int sext_byte(uint32_t w, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(w), "r"(sel));
+    return static_cast<int>(r);
+}
+
+// D += A B, m16n8k16, bf16 operands, f32 accumulators.
+__device__ __forceinline__ void mma_bf16_k16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// 8 or 16 bytes of shared memory at a 2-byte-aligned address, from the
+// aligned words around them (funnel shifts).
+__device__ __forceinline__ uint2 lds_u64_a2(const uint8_t* p) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
+    const uint32_t sh = static_cast<uint32_t>(a & 3u) * 8u;
+    const uint32_t w0 = w[0], w1 = w[1], w2 = w[2];
+    return make_uint2(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh));
+}
+__device__ __forceinline__ uint4 lds_u128_a2(const uint8_t* p) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
+    const uint32_t sh = static_cast<uint32_t>(a & 3u) * 8u;
+    const uint32_t w0 = w[0], w1 = w[1], w2 = w[2], w3 = w[3], w4 = w[4];
+    return make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh), __funnelshift_r(w2, w3, sh),
+                      __funnelshift_r(w3, w4, sh));
+}
+
+// A Q6_K super-block as stored in a stage: ql[128] at 0, qh[64] at 128,
+// scales[16] at 192; GGUF blocks are 210 bytes (d at 208, blocks 2-byte
+// aligned), repacked ones 208 (every field 16-byte aligned, d gathered at
+// the end of the row).
+template <int FMT>
+struct Q6Block {
+    static constexpr bool kSoa = FMT == QX_Q6_K_SOA;
+    static constexpr int kBytes = kSoa ? 208 : 210;
+    __device__ __forceinline__ static uint2 ld8(const uint8_t* p) {
+        if constexpr (kSoa) return *reinterpret_cast<const uint2*>(p);
+        else return lds_u64_a2(p);
+    }
+    __device__ __forceinline__ static uint4 ld16(const uint8_t* p) {
+        if constexpr (kSoa) return *reinterpret_cast<const uint4*>(p);
+        else return lds_u128_a2(p);
+    }
+    // d of super-block sb of the row at `row`
+    __device__ __forceinline__ static float d(const uint8_t* row, int sb, int nsb) {
+        const uint8_t* p = kSoa ? row + 208 * nsb + 2 * sb : row + 210 * sb + 208;
+        return f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(p));
+    }
+};
+
+// MMA index of (half h, quarter tq, step s) within a super-block; its B
+// fragment is bx[2 i], bx[2 i + 1].
+__device__ __forceinline__ constexpr int mma_index(int h, int tq, int s) { return 8 * h + 2 * tq + s; }
+
+// The B fragments of the warp's super-block (its 256 values at xs, times
+// `up`), in the order of mma_index.  MMA (h, tq, s) covers, for thread
+// (gid, t), elements 128 h + 32 tq + 8 t + 4 s + {0, 1} (logical k = 2 t,
+// 2 t + 1) and + {2, 3} (k = 2 t + 8, 2 t + 9); they lie in group (tq, u =
+// t >> 1) of the 32-column quarter, whose (hi, lo) pair is column pair
+// 2 (tq & 1) + u.  Column gid holds them iff gid >> 1 is that pair: hi for
+// even gid, lo for odd; every other B entry is zero.
+__device__ __forceinline__ void load_b_f32(const float* xs, float up, int gid, int t, bool live,
+                                           uint32_t (&bx)[32]) {
+    const bool odd = gid & 1;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int tq = 0; tq < 4; ++tq)
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+                const int i = mma_index(h, tq, s);
+                const bool mine = live && (gid >> 1) == 2 * (tq & 1) + (t >> 1);
+                uint32_t b0 = 0u, b1 = 0u;
+                if (mine) {
+                    const float4 v = __ldg(reinterpret_cast<const float4*>(xs + 128 * h + 32 * tq + 8 * t + 4 * s));
+                    float e[4] = {v.x * up, v.y * up, v.z * up, v.w * up};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float hi = bf16_rn_f32(e[j]);
+                        // non-finite activations: the hi term alone carries them
+                        e[j] = odd ? (isfinite(hi) ? e[j] - hi : 0.0f) : hi;
+                    }
+                    b0 = bf16x2_rn(e[0], e[1]);
+                    b1 = bf16x2_rn(e[2], e[3]);
+                }
+                bx[2 * i] = b0;
+                bx[2 * i + 1] = b1;
+            }
+}
+
+// One super-block of rows gid (ra) and gid + 8 (rb) of a 16-row group:
+// returns, for thread (gid, t), sum over its groups g = 8 h + 4 a + t of
+// sc_g (D_hi + D_lo), rows gid and gid + 8.
+template <int FMT>
+__device__ __forceinline__ void q6_f32_mma(const uint8_t* ra, const uint8_t* rb, int t, uint32_t scsel,
+                                           const uint32_t (&bx)[32], float& ya, float& yb) {
+    using B = Q6Block<FMT>;
+    const uint4 sca = B::ld16(ra + 192), scb = B::ld16(rb + 192);
+    const uint32_t swa[4] = {sca.x, sca.y, sca.z, sca.w}, swb[4] = {scb.x, scb.y, scb.z, scb.w};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        // thread t's 8 bytes of each 32-byte chunk: ql of quarters 0 / 2 and 1 / 3, qh
+        const uint2 l0[2] = {B::ld8(ra + 64 * h + 8 * t), B::ld8(rb + 64 * h + 8 * t)};
+        const uint2 l1[2] = {B::ld8(ra + 64 * h + 32 + 8 * t), B::ld8(rb + 64 * h + 32 + 8 * t)};
+        const uint2 hh[2] = {B::ld8(ra + 128 + 32 * h + 8 * t), B::ld8(rb + 128 + 32 * h + 8 * t)};
+        // qh fields 0, 2 (bits 0-1, 4-5 of each byte) and 1, 3 (bits 2-3, 6-7), each word
+        // masked once: shifted so that the quarter's field lands on bits 4-5, bits 6-7 stay zero
+        uint32_t he[2][2], ho[2][2];  // [row][s]
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            he[r][0] = hh[r].x & 0x33333333u;
+            he[r][1] = hh[r].y & 0x33333333u;
+            ho[r][0] = hh[r].x & 0xCCCCCCCCu;
+            ho[r][1] = hh[r].y & 0xCCCCCCCCu;
+        }
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {  // quarters 2 a, 2 a + 1: low (a = 0) or high nibbles of ql
+            float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int tp = 0; tp < 2; ++tp) {
+                const int tq = 2 * a + tp;
+#pragma unroll
+                for (int s = 0; s < 2; ++s) {
+                    uint32_t w[2];  // rows gid, gid + 8: the 6-bit quants of 4 consecutive elements
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const uint2 lq = tp ? l1[r] : l0[r];
+                        const uint32_t lw = s ? lq.y : lq.x;
+                        const uint32_t lo4 = a ? (lw >> 4) : lw;
+                        const uint32_t hm = tp ? ho[r][s] : he[r][s];
+                        const uint32_t hi2 = tq == 0 ? (hm << 4) : tq == 1 ? (hm << 2) : tq == 2 ? hm : (hm >> 2);
+                        // bits 0-3 from the nibble, 4-7 from the field (bits 6-7 zero): one lop3
+                        w[r] = (lo4 & 0x0F0F0F0Fu) | (hi2 & 0xF0F0F0F0u);
+                    }
+                    const uint32_t A[4] = {q6_pair_bf16<0>(w[0]), q6_pair_bf16<0>(w[1]), q6_pair_bf16<2>(w[0]),
+                                           q6_pair_bf16<2>(w[1])};
+                    const int i = mma_index(h, tq, s);
+                    mma_bf16_k16(d, A, bx[2 * i], bx[2 * i + 1]);
+                }
+            }
+            // column pair t = group 8 h + 4 a + t: its scale is byte t of scale word 2 h + a
+            const float sa = static_cast<float>(sext_byte(swa[2 * h + a], scsel));
+            const float sb = static_cast<float>(sext_byte(swb[2 * h + a], scsel));
+            ya = fmaf(sa, d[0] + d[1], ya);
+            yb = fmaf(sb, d[2] + d[3], yb);
+        }
+    }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kF32MmaThreads, 1) gemv_f32_mma_kernel(const __grid_constant__ GemvParams p) {
+    constexpr int NW = kF32MmaWarps;
+    using B = Q6Block<FMT>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int S = p.stages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
+    uint64_t* empty = full + S;
+    uint64_t* part = empty + S;
+    const int nsb = static_cast<int>(p.cols / 256), P = NW / nsb;  // warps per super-block
+    const int GS = P * p.gq;                                          // 16-row groups per stage
+    float* red = reinterpret_cast<float*>(smem + p.red_off);          // [S][GS][nsb][16]
+    const int red_stage = GS * nsb * 16;
+    const int rstride = static_cast<int>(p.row_bytes) + 16;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t r0 = cta_row_begin(p, blockIdx.x), r1 = cta_row_begin(p, blockIdx.x + 1);
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < S; ++k) {
+            mbar_init(&full[k], 1);
+            mbar_init(&empty[k], NW + 1);
+            mbar_init(&part[k], NW);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    if (warp == NW) {
+        produce_padded_rows(p, r0, r1, full, empty, smem, lane);
+        return;
+    }
+    if (warp == NW + 1) {
+        // ---------------- reducer: y[row] = the nsb partials in a fixed order --
+        pdl_wait_prior_grid();  // y may be read by the previous kernel
+        StageWalker wk{r0, r1, 0};
+        int e, nrows;
+        int64_t lrow;
+        const int row = lane & 15, half = lane >> 4;
+        int slot = 0, lap = 0;
+        for (int k = 0; wk.next(p, e, lrow, nrows); ++k) {
+            if (!warp_wait_all(&part[slot], lap & 1, p.wait_ns, p.err, kErrTimeoutFull)) break;
+            const float* rs = red + size_t(slot) * red_stage;
+            for (int gi = 0; gi < GS && 16 * gi < nrows; ++gi) {
+                float acc = 0.0f;  // super-blocks half, half + 2, ...; then the two halves
+                for (int sb = half; sb < nsb; sb += 2) acc += rs[(gi * nsb + sb) * 16 + row];
+                acc += __shfl_xor_sync(0xffffffffu, acc, 16);
+                if (half == 0 && 16 * gi + row < nrows) p.e[e].y[lrow + 16 * gi + row] = acc;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (++slot == S) {
+                slot = 0;
+                ++lap;
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------------------------------------
+    pdl_wait_prior_grid();  // x may come from the previous kernel
+    const int sb = warp % nsb, gsub = warp / nsb;
+    const bool active = gsub < P;
+    const int gid = lane >> 2, t = lane & 3;
+    // 2^e from the largest magnitude of the super-block's activation (every lane reads 8 values)
+    const float* xs = p.x + 256 * sb;
+    uint32_t amax = 0u;
+    {
+        const float4 v0 = __ldg(reinterpret_cast<const float4*>(xs + 8 * lane));
+        const float4 v1 = __ldg(reinterpret_cast<const float4*>(xs + 8 * lane + 4));
+        const float m = fmaxf(fmaxf(fmaxf(fabsf(v0.x), fabsf(v0.y)), fmaxf(fabsf(v0.z), fabsf(v0.w))),
+                              fmaxf(fmaxf(fabsf(v1.x), fabsf(v1.y)), fmaxf(fabsf(v1.z), fabsf(v1.w))));
+        amax = __float_as_uint(m);
+        // a NaN anywhere: the exponent field 255, like inf (fmaxf drops NaN operands)
+        if (isnan(v0.x) || isnan(v0.y) || isnan(v0.z) || isnan(v0.w) || isnan(v1.x) || isnan(v1.y) ||
+            isnan(v1.z) || isnan(v1.w))
+            amax = 0x7F800000u;
+    }
+    amax = __reduce_max_sync(0xffffffffu, amax);
+    int ex = static_cast<int>(amax >> 23);  // biased exponent of the largest magnitude (0: zero or subnormal)
+    if (ex == 255) ex = 127;                // inf or NaN: unscaled
+    const float up = ldexpf(1.0f, 127 - ex), down = ldexpf(1.0f, ex - 127);
+    uint32_t bx[32];
+    load_b_f32(xs, up, gid, t, active, bx);
+    // byte t of a scale word, sign-extended
+    const uint32_t tt = static_cast<uint32_t>(t);
+    const uint32_t scsel = tt | ((tt | 8u) << 4) | ((tt | 8u) << 8) | ((tt | 8u) << 12);
+
+    StageWalker wk{r0, r1, 0};
+    int e, nrows;
+    int64_t lrow;
+    int slot = 0, lap = 0;  // ring position of stage k: k % S, k / S
+    for (int k = 0; wk.next(p, e, lrow, nrows); ++k) {
+        if (!warp_wait_all(&full[slot], lap & 1, p.wait_ns, p.err, kErrTimeoutFull)) break;
+        const uint8_t* stage = smem + size_t(slot) * p.slot_bytes;
+        float* rs = red + size_t(slot) * red_stage + sb * 16;
+        if (active) {
+            for (int gi = gsub; gi < GS && 16 * gi < nrows; gi += P) {  // warp-uniform
+                const uint8_t* rowa = stage + (16 * gi + gid) * rstride;
+                const uint8_t* rowb = rowa + 8 * rstride;
+                float ya = 0.0f, yb = 0.0f;
+                q6_f32_mma<FMT>(rowa + B::kBytes * sb, rowb + B::kBytes * sb, t, scsel, bx, ya, yb);
+                ya += __shfl_xor_sync(0xffffffffu, ya, 1);
+                yb += __shfl_xor_sync(0xffffffffu, yb, 1);
+                ya += __shfl_xor_sync(0xffffffffu, ya, 2);
+                yb += __shfl_xor_sync(0xffffffffu, yb, 2);
+                if (t == 0) {
+                    rs[gi * nsb * 16 + gid] = (ya * B::d(rowa, sb, nsb)) * down;
+                    rs[gi * nsb * 16 + gid + 8] = (yb * B::d(rowb, sb, nsb)) * down;
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(&part[slot]);
+            mbar_arrive(&empty[slot]);
+        }
+        if (++slot == S) {
+            slot = 0;
+            ++lap;
+        }
+    }
+}
+
+// Largest shared memory (static + dynamic) a CTA may use on sm_103a.
+constexpr int kMaxDynamicSmem = 227 * 1024;
+
+template <int FMT>
+cudaError_t launch_f32_mma_one(const GemvParams& p, size_t smem, cudaStream_t s, bool pdl) {
+    static bool done[64] = {false};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!done[dev]) {
+        cudaFuncAttributes fa;
+        if ((err = cudaFuncGetAttributes(&fa, gemv_f32_mma_kernel<FMT>)) != cudaSuccess) return err;
+        err = cudaFuncSetAttribute(gemv_f32_mma_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   kMaxDynamicSmem - static_cast<int>(fa.sharedSizeBytes));
+        if (err != cudaSuccess) return err;
+        done[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_cta);
+    cfg.blockDim = dim3(kF32MmaThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_f32_mma_kernel<FMT>, p);
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_f32_mma(int fmt, const GemvParams& p, size_t smem, cudaStream_t s, bool pdl) {
+    switch (fmt) {
+        case QX_Q6_K: return launch_f32_mma_one<QX_Q6_K>(p, smem, s, pdl);
+        case QX_Q6_K_SOA: return launch_f32_mma_one<QX_Q6_K_SOA>(p, smem, s, pdl);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace qx

@@ -30,6 +30,7 @@
 #include "qx_device.cuh"
 #include "qx_internal.h"
 #include "qx_lanes.cuh"
+#include "qx_stage.cuh"
 
 namespace qx {
 
@@ -39,38 +40,8 @@ using namespace lanes;
 
 
 // ----------------------------------------------------------------------------
-// Work distribution
+// Work distribution (the row split and the stage walk: qx_stage.cuh)
 // ----------------------------------------------------------------------------
-
-// First row (in the concatenated row space) of CTA i: an even split of the
-// rows, rounded down within its entry to a multiple of the alignment quantum.
-__device__ __forceinline__ int64_t cta_row_begin(const GemvParams& p, int i) {
-    if (i >= p.n_cta) return p.total_rows;
-    const int64_t raw = p.total_rows * int64_t(i) / p.n_cta;
-    int e = 0;
-    while (e + 1 < p.n_entries && raw >= p.e[e + 1].row0) ++e;
-    const int64_t local = raw - p.e[e].row0;
-    return p.e[e].row0 + (local - local % p.quantum);
-}
-
-// Walks one CTA's rows as a sequence of stages: at most G rows, never
-// crossing an entry boundary.
-struct StageWalker {
-    int64_t g, gend;
-    int e;
-    __device__ __forceinline__ bool next(const GemvParams& p, int& entry, int64_t& lrow, int& nrows) {
-        if (g >= gend) return false;
-        while (g >= p.e[e].row0 + p.e[e].rows) ++e;
-        const int64_t entry_end = p.e[e].row0 + p.e[e].rows;
-        const int64_t stop = gend < entry_end ? gend : entry_end;
-        const int64_t n = stop - g < p.G ? stop - g : p.G;
-        entry = e;
-        lrow = g - p.e[e].row0;
-        nrows = static_cast<int>(n);
-        g += n;
-        return true;
-    }
-};
 
 // W4A8 kernels and Q8_0 kernels fit two CTAs per SM (<= 112 registers), so
 // that with programmatic dependent launch the next GEMV's CTA can be resident
@@ -507,12 +478,6 @@ __global__ void __launch_bounds__(kBatchThreads, 1) gemv_batch_kernel(const __gr
 // rows of X.
 // ----------------------------------------------------------------------------
 constexpr int kMmaBatchWarps = 16;
-
-// Every lane waits on the barrier itself; the outcome is made warp-uniform.
-__device__ __forceinline__ bool warp_wait_all(uint64_t* bar, uint32_t parity, uint64_t ns, unsigned* err,
-                                              unsigned code) {
-    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, ns, err, code));
-}
 
 __device__ __forceinline__ void mma_s8s8_k32(int (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm("mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "

@@ -83,6 +83,9 @@ struct GemvParams {
     int mb;
     int m_valid;
     int64_t y_stride;
+    // Row-group kernels (gemv_f32_mma_kernel): 16-row groups each consumer
+    // warp takes per stage (the stage holds 16 P gq rows).
+    int gq;
 };
 
 // Small-batch GEMV (one weight stream for several activation rows): rows of
@@ -103,6 +106,9 @@ __host__ __device__ constexpr int batch_cols_per_lane(int fmt, int mb) {
 constexpr int kMmaBatchRows = 8;
 constexpr int kMmaBatchMaxSuperBlocks = 16;
 constexpr int kMmaBatchThreads = 32 * (16 + 2);
+// f32-mode GEMV of Q6_K rows on the tensor pipe (gemv_f32_mma_kernel): the
+// same geometry, rows of 2048 or 4096 columns.
+constexpr int kF32MmaThreads = 32 * (16 + 2);
 
 // Columns owned by one lane, per (format, mode).
 __host__ __device__ constexpr int gemv_cols_per_lane(int fmt, int mode) {
@@ -163,6 +169,7 @@ cudaError_t launch_gemv(int fmt, int mode, bool partials, const GemvParams& p, s
 cudaError_t gemv_max_ctas_per_sm(int fmt, int mode, bool partials, bool merged, bool fused, size_t smem, int* out);
 cudaError_t launch_gemv_batch(int fmt, const GemvParams& p, size_t smem, cudaStream_t s);
 cudaError_t launch_gemv_batch_mma(int fmt, const GemvParams& p, size_t smem, cudaStream_t s);
+cudaError_t launch_gemv_f32_mma(int fmt, const GemvParams& p, size_t smem, cudaStream_t s, bool pdl);
 // Q6_K <-> QX_Q6_K_SOA (qx_repack.cu); row bytes of each side.
 cudaError_t launch_repack_q6k(bool to_soa, const uint8_t* src, int64_t rows, int64_t nsb, int64_t src_row_bytes,
                               uint8_t* dst, int64_t dst_row_bytes, cudaStream_t s);
