@@ -449,7 +449,9 @@ def measure_config(name: str, qx, torch, stream, hbm: float, bf16: float, peak_k
             us = graph_time_ms(torch, lambda: qx.qx_gemv(f, Wm, rows, cols, x, y=y, mode=mode, stream=stream),
                                50, stream) * 1e3
             out[mname] = {"GB_per_s": nbytes / (us * 1e-6) / 1e9, "us": us, "frac_of_hbm": nbytes / (us * 1e-6) / 1e9 / hbm,
-                          "roofline": gemv_roofline(nbytes, us, hbm, peak_kind, f"gemv_kernel lm_head {mname}")}
+                          "roofline": gemv_roofline(nbytes, us, hbm, peak_kind,
+                                                    ("gemv_f32_mma_kernel" if mname.startswith("f32") else "gemv_kernel")
+                                                    + f" lm_head {mname}")}
         out["weight_bytes"] = nbytes
         del W, Ws
     elif name == "qwen05b":

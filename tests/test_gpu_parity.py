@@ -448,6 +448,37 @@ def test_prefill_tcgen05_split_last_wave(fmt, cols):
     assert qx.qx_device_check() == qx.QX_OK
 
 
+@pytest.mark.parametrize("fmt,cols", [(synth.Q4_K, 1280), (synth.Q6_K, 1792), (synth.Q8_0, 512), (synth.Q8_0, 384)])
+def test_prefill_tcgen05_split_small_grid(fmt, cols):
+    """Twenty tiles (ragged M: 300 rows; ragged N: the last tile has 57 rows),
+    at most a quarter of a wave: every tile runs as a cluster of four CTAs
+    with shares of 1, 1, 1, 2 (Q4_K, five K groups), 1, 2, 2, 2 (Q6_K, seven)
+    and 1 each (Q8_0, four groups), the sums meeting as (a0 + a1) +
+    (a2 + a3); with three K groups (Q8_0, 384 columns) as clusters of two.
+    Sampled rows and the last tile against the oracle; a CUDA graph of the
+    call gives the eager bits."""
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert 20 * 4 <= sm
+    m, rows = 300, 9 * 128 + 57
+    W = synth.weights(fmt, rows, cols, seed=90 + cols)
+    X = synth.activation(m, cols, seed=91 + cols)
+    a, q, d, s = quantize_both(X)
+    Wd = dev(W)
+    Y = host(qx.qx_gemm_prefill_ex(fmt, Wd, rows, cols, a, path=3))
+    rng = np.random.default_rng(92)
+    wr = np.sort(np.concatenate([np.arange(9 * 128, rows), rng.choice(9 * 128, 120, replace=False)]))
+    ref, absdot = oracle.gemm_w4a8(fmt, np.ascontiguousarray(W[wr]), len(wr), cols, q, d)
+    assert_close(Y[:, wr].reshape(-1), ref.reshape(-1), absdot.reshape(-1), f"small grid {synth.NAMES[fmt]}")
+    stream = torch.cuda.Stream()
+    Yg = torch.full((m, rows), float("nan"), device="cuda")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        qx.qx_gemm_prefill_ex(fmt, Wd, rows, cols, a, Y=Yg, path=3, stream=stream)
+    g.replay()
+    assert np.array_equal(host(Yg).view(np.uint32), Y.view(np.uint32))
+    assert qx.qx_device_check() == qx.QX_OK
+
+
 @pytest.mark.parametrize("path", [2, 3])
 def test_prefill_full_size_sampled(path):
     """X [512, 4096] against Q4_K [14336, 4096]: sampled rows of X and of W against the oracle."""
