@@ -256,7 +256,12 @@ qx_status gemv_geometry(int fmt, int kmode, bool partials, bool fused, bool pdl,
     // following launches under PDL, costs the Llama-3.1-8B decode step more
     // than it saves on its 48 MB down projections: long launches only.
     const int64_t rb = row_bytes_of(fmt, cols);
-    bool merged = gemv_has_merged(fmt, kmode, partials) && p.total_rows * rb >= kMergedMinBytes;
+    // f32 K-quants: the merged variant for small launches under programmatic
+    // dependent launch (the launch then runs one CTA per SM, below, and the
+    // next launch's CTA fits beside it)
+    const bool small_bytes = p.total_rows * rb <= kOneCtaPerSmBytes * int64_t(dev.sm_count);
+    bool merged = gemv_has_merged(fmt, kmode, partials) &&
+                  (kmode == QX_MODE_F32 ? (pdl && small_bytes) : p.total_rows * rb >= kMergedMinBytes);
     TeamGeom g;
     // the merged variant's seven consumer warps cover rows of up to 28672
     // columns; wider rows take the standard kernel
@@ -265,7 +270,7 @@ qx_status gemv_geometry(int fmt, int kmode, bool partials, bool fused, bool pdl,
     p.merged = merged ? 1 : 0;
     qx_status st = team_geometry(fmt, kmode, partials, cols, gemv_consumer_warps(fmt, kmode, merged), g);
     if (st != QX_OK) return st;
-    const bool half_sm = (kmode == QX_MODE_W4A8 || fmt == QX_Q8_0);
+    const bool half_sm = (kmode == QX_MODE_W4A8 || fmt == QX_Q8_0 || merged);
     const size_t budget = half_sm ? kHalfSmBytes : 200 * 1024;
     const size_t act = fused ? (size_t(cols) + size_t(cols / 32) * 8 + 15) / 16 * 16 : 0;
     // per stage: the slot, three mbarriers and (for y outputs) the per-lane partial sums

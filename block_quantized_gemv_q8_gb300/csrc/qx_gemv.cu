@@ -46,14 +46,14 @@ using namespace lanes;
 // W4A8 kernels and Q8_0 kernels fit two CTAs per SM (<= 112 registers), so
 // that with programmatic dependent launch the next GEMV's CTA can be resident
 // next to this one and stream its weights while this one finishes.
-template <int FMT, int MODE>
+template <int FMT, int MODE, bool MERGED>
 constexpr int gemv_min_blocks() {
-    return (MODE == QX_MODE_W4A8 || FMT == QX_Q8_0) ? 2 : 1;
+    return (MODE == QX_MODE_W4A8 || FMT == QX_Q8_0 || MERGED) ? 2 : 1;
 }
 
 // FUSED: W4A8 with the activation quantised in-kernel (p.xf set).
 template <int FMT, int MODE, bool PART, bool MERGED, bool FUSED>
-__global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_min_blocks<FMT, MODE>())
+__global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_min_blocks<FMT, MODE, MERGED>())
     gemv_kernel(const __grid_constant__ GemvParams p) {
     using LaneT = Lane<FMT, MODE>;
     constexpr int NW = gemv_consumer_warps(FMT, MODE, MERGED);
@@ -262,6 +262,8 @@ __global__ void __launch_bounds__(gemv_threads(FMT, MODE, PART, MERGED), gemv_mi
             // so that the warp never sits in two different waits at once.
             __syncwarp();
             if constexpr (FUSED) quantise_share();
+            else pdl_wait_prior_grid();  // y may be read by the previous kernel (a small launch fetches
+                                         // its whole ring before this wait in issue_first_stages)
             StageWalker rw{r0, r1, 0};
             int e, nrows;
             int64_t lrow;
@@ -939,6 +941,11 @@ cudaError_t launch_gemv(int fmt, int mode, bool partials, const GemvParams& p, s
         if (fmt == QX_Q6_K_SOA && mode == QX_MODE_W4A8 && !partials)
             return fused ? launch_one<QX_Q6_K_SOA, QX_MODE_W4A8, false, true, true>(p, smem, s, pdl)
                          : launch_one<QX_Q6_K_SOA, QX_MODE_W4A8, false, true, false>(p, smem, s, pdl);
+        if (mode == QX_MODE_F32 && !partials && !fused) {
+            if (fmt == QX_Q4_K) return launch_one<QX_Q4_K, QX_MODE_F32, false, true, false>(p, smem, s, pdl);
+            if (fmt == QX_Q6_K) return launch_one<QX_Q6_K, QX_MODE_F32, false, true, false>(p, smem, s, pdl);
+            if (fmt == QX_Q6_K_SOA) return launch_one<QX_Q6_K_SOA, QX_MODE_F32, false, true, false>(p, smem, s, pdl);
+        }
         return cudaErrorInvalidValue;
     }
     switch (fmt * 8 + mode * 4 + (partials ? 2 : 0) + (fused ? 1 : 0)) {
@@ -971,6 +978,11 @@ cudaError_t gemv_max_ctas_per_sm(int fmt, int mode, bool partials, bool merged, 
         if (fmt == QX_Q6_K_SOA && mode == QX_MODE_W4A8 && !partials)
             return fused ? occupancy_one<QX_Q6_K_SOA, QX_MODE_W4A8, false, true, true>(smem, out)
                          : occupancy_one<QX_Q6_K_SOA, QX_MODE_W4A8, false, true, false>(smem, out);
+        if (mode == QX_MODE_F32 && !partials && !fused) {
+            if (fmt == QX_Q4_K) return occupancy_one<QX_Q4_K, QX_MODE_F32, false, true, false>(smem, out);
+            if (fmt == QX_Q6_K) return occupancy_one<QX_Q6_K, QX_MODE_F32, false, true, false>(smem, out);
+            if (fmt == QX_Q6_K_SOA) return occupancy_one<QX_Q6_K_SOA, QX_MODE_F32, false, true, false>(smem, out);
+        }
         return cudaErrorInvalidValue;
     }
     switch (fmt * 8 + mode * 4 + (partials ? 2 : 0) + (fused ? 1 : 0)) {

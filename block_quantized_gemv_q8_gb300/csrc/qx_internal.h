@@ -23,11 +23,16 @@ namespace qx {
 // reduces, 16 warps per SM and so 128 registers (the standard Q6_K W4A8
 // kernel is held to 96 and spills); rows of 14336 columns are then exactly
 // two teams of 112 lanes.
+// The f32-mode K-quant kernels have a merged variant too, for small launches
+// under programmatic dependent launch: 8 warps of at most 128 registers, so
+// that the next launch's CTA fits on the SM beside it (the standard f32
+// kernel's 14 warps of 128 registers leave no room).
 __host__ __device__ constexpr bool gemv_has_merged(int fmt, int mode, bool partials) {
-    return !partials && mode == QX_MODE_W4A8 && (fmt == QX_Q6_K || fmt == QX_Q6_K_SOA);
+    return !partials && ((mode == QX_MODE_W4A8 && (fmt == QX_Q6_K || fmt == QX_Q6_K_SOA)) ||
+                         (mode == QX_MODE_F32 && fmt != QX_Q8_0));
 }
 __host__ __device__ constexpr int gemv_consumer_warps(int fmt, int mode, bool merged) {
-    return (mode == QX_MODE_F32 && fmt != QX_Q8_0) ? 12 : (merged ? 7 : 8);
+    return merged ? 7 : ((mode == QX_MODE_F32 && fmt != QX_Q8_0) ? 12 : 8);
 }
 // Integer partials need no reducer warp; the merged variant has none either.
 __host__ __device__ constexpr int gemv_threads(int fmt, int mode, bool partials, bool merged) {

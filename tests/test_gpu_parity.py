@@ -267,6 +267,27 @@ def test_two_step_chain_reads_after_the_producer():
     assert qx.qx_device_check() == qx.QX_OK
 
 
+@pytest.mark.parametrize("fmt,rows,cols", [(synth.Q4_K, 1024, 1024), (synth.Q4_K, 77, 4096), (synth.Q6_K, 65, 14336),
+                                           (synth.Q6_K, 300, 1024), (qx.QX_Q6_K_SOA, 129, 1024)])
+def test_gemv_f32_small_pdl_launch(fmt, rows, cols):
+    """Small f32 launches under programmatic dependent launch run the merged
+    variant (8 warps, so that the next launch's CTA fits beside it): the
+    same lanes and reduction as the standard kernel, bit for bit, and the
+    oracle's tolerance."""
+    base = synth.Q6_K if fmt == qx.QX_Q6_K_SOA else fmt
+    W = synth.weights(base, rows, cols, seed=rows + 3 * cols)
+    x = synth.activation(1, cols, seed=cols + 19)[0]
+    Wd = dev(W)
+    if fmt == qx.QX_Q6_K_SOA:
+        Wd = qx.qx_repack(synth.Q6_K, qx.QX_Q6_K_SOA, Wd, rows, cols)
+    y0 = host(qx.qx_gemv(fmt, Wd, rows, cols, dev(x), mode=qx.QX_MODE_F32))
+    y1 = host(qx.qx_gemv(fmt, Wd, rows, cols, dev(x), mode=qx.QX_MODE_F32 | qx.QX_FLAG_PDL))
+    assert np.array_equal(y0.view(np.uint32), y1.view(np.uint32))
+    ref, absdot = oracle.gemv_f32(base, W, rows, cols, x)
+    assert_close(y1, ref, absdot, f"f32 pdl {fmt} {rows}x{cols}")
+    assert qx.qx_device_check() == qx.QX_OK
+
+
 def test_gemv_zero_and_edge_values():
     """All-zero weights, all-zero activation, a zero-scale super-block."""
     rows, cols = 16, 1024
