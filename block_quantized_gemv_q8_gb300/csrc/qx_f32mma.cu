@@ -84,39 +84,45 @@ __device__ __forceinline__ void mma_bf16_k16(float (&d)[4], const uint32_t (&a)[
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// 8 or 16 bytes of shared memory at a 2-byte-aligned address, from the
-// aligned words around them (funnel shifts).
-__device__ __forceinline__ uint2 lds_u64_a2(const uint8_t* p) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-    const uint32_t sh = static_cast<uint32_t>(a & 3u) * 8u;
-    const uint32_t w0 = w[0], w1 = w[1], w2 = w[2];
-    return make_uint2(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh));
-}
-__device__ __forceinline__ uint4 lds_u128_a2(const uint8_t* p) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-    const uint32_t sh = static_cast<uint32_t>(a & 3u) * 8u;
-    const uint32_t w0 = w[0], w1 = w[1], w2 = w[2], w3 = w[3], w4 = w[4];
-    return make_uint4(__funnelshift_r(w0, w1, sh), __funnelshift_r(w1, w2, sh), __funnelshift_r(w2, w3, sh),
-                      __funnelshift_r(w3, w4, sh));
+// (w0 >> 16) | (w1 << 16) with two multiplies (the FMA pipe; the ALU pipe is
+// this kernel's busiest): m = 65536, passed as a run-time value.
+__device__ __forceinline__ uint32_t join16(uint32_t w0, uint32_t w1, uint32_t m) {
+    return __umulhi(w0, m) + w1 * m;
 }
 
 // A Q6_K super-block as stored in a stage: ql[128] at 0, qh[64] at 128,
-// scales[16] at 192; GGUF blocks are 210 bytes (d at 208, blocks 2-byte
-// aligned), repacked ones 208 (every field 16-byte aligned, d gathered at
-// the end of the row).
-template <int FMT>
+// scales[16] at 192; GGUF blocks are 210 bytes (d at 208), repacked ones
+// 208 (every field 16-byte aligned, d gathered at the end of the row).  A
+// GGUF super-block sb starts at byte 210 sb of a 16-byte-aligned row: on a
+// 4-byte boundary for even sb (MIS = 0), 2 bytes past one for odd sb
+// (MIS = 2), the same for every field a thread reads.
+template <int FMT, int MIS = 0>
 struct Q6Block {
     static constexpr bool kSoa = FMT == QX_Q6_K_SOA;
     static constexpr int kBytes = kSoa ? 208 : 210;
-    __device__ __forceinline__ static uint2 ld8(const uint8_t* p) {
-        if constexpr (kSoa) return *reinterpret_cast<const uint2*>(p);
-        else return lds_u64_a2(p);
+    __device__ __forceinline__ static uint2 ld8(const uint8_t* p, uint32_t m) {
+        if constexpr (kSoa) {
+            return *reinterpret_cast<const uint2*>(p);
+        } else if constexpr (MIS == 0) {
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(p);
+            return make_uint2(w[0], w[1]);
+        } else {
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(p - 2);
+            const uint32_t w0 = w[0], w1 = w[1], w2 = w[2];
+            return make_uint2(join16(w0, w1, m), join16(w1, w2, m));
+        }
     }
-    __device__ __forceinline__ static uint4 ld16(const uint8_t* p) {
-        if constexpr (kSoa) return *reinterpret_cast<const uint4*>(p);
-        else return lds_u128_a2(p);
+    __device__ __forceinline__ static uint4 ld16(const uint8_t* p, uint32_t m) {
+        if constexpr (kSoa) {
+            return *reinterpret_cast<const uint4*>(p);
+        } else if constexpr (MIS == 0) {
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(p);
+            return make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(p - 2);
+            const uint32_t w0 = w[0], w1 = w[1], w2 = w[2], w3 = w[3], w4 = w[4];
+            return make_uint4(join16(w0, w1, m), join16(w1, w2, m), join16(w2, w3, m), join16(w3, w4, m));
+        }
     }
     // d of super-block sb of the row at `row`
     __device__ __forceinline__ static float d(const uint8_t* row, int sb, int nsb) {
@@ -168,18 +174,18 @@ __device__ __forceinline__ void load_b_f32(const float* xs, float up, int gid, i
 // One super-block of rows gid (ra) and gid + 8 (rb) of a 16-row group:
 // returns, for thread (gid, t), sum over its groups g = 8 h + 4 a + t of
 // sc_g (D_hi + D_lo), rows gid and gid + 8.
-template <int FMT>
-__device__ __forceinline__ void q6_f32_mma(const uint8_t* ra, const uint8_t* rb, int t, uint32_t scsel,
+template <int FMT, int MIS>
+__device__ __forceinline__ void q6_f32_mma(const uint8_t* ra, const uint8_t* rb, int t, uint32_t scsel, uint32_t m,
                                            const uint32_t (&bx)[32], float& ya, float& yb) {
-    using B = Q6Block<FMT>;
-    const uint4 sca = B::ld16(ra + 192), scb = B::ld16(rb + 192);
+    using B = Q6Block<FMT, MIS>;
+    const uint4 sca = B::ld16(ra + 192, m), scb = B::ld16(rb + 192, m);
     const uint32_t swa[4] = {sca.x, sca.y, sca.z, sca.w}, swb[4] = {scb.x, scb.y, scb.z, scb.w};
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         // thread t's 8 bytes of each 32-byte chunk: ql of quarters 0 / 2 and 1 / 3, qh
-        const uint2 l0[2] = {B::ld8(ra + 64 * h + 8 * t), B::ld8(rb + 64 * h + 8 * t)};
-        const uint2 l1[2] = {B::ld8(ra + 64 * h + 32 + 8 * t), B::ld8(rb + 64 * h + 32 + 8 * t)};
-        const uint2 hh[2] = {B::ld8(ra + 128 + 32 * h + 8 * t), B::ld8(rb + 128 + 32 * h + 8 * t)};
+        const uint2 l0[2] = {B::ld8(ra + 64 * h + 8 * t, m), B::ld8(rb + 64 * h + 8 * t, m)};
+        const uint2 l1[2] = {B::ld8(ra + 64 * h + 32 + 8 * t, m), B::ld8(rb + 64 * h + 32 + 8 * t, m)};
+        const uint2 hh[2] = {B::ld8(ra + 128 + 32 * h + 8 * t, m), B::ld8(rb + 128 + 32 * h + 8 * t, m)};
         // qh fields 0, 2 (bits 0-1, 4-5 of each byte) and 1, 3 (bits 2-3, 6-7), each word
         // masked once: shifted so that the quarter's field lands on bits 4-5, bits 6-7 stay zero
         uint32_t he[2][2], ho[2][2];  // [row][s]
@@ -310,6 +316,8 @@ __global__ void __launch_bounds__(kF32MmaThreads, 1) gemv_f32_mma_kernel(const _
     // byte t of a scale word, sign-extended
     const uint32_t tt = static_cast<uint32_t>(t);
     const uint32_t scsel = tt | ((tt | 8u) << 4) | ((tt | 8u) << 8) | ((tt | 8u) << 12);
+    // 65536 for the GGUF layout's 2-byte joins, from a value the compiler cannot fold
+    const uint32_t jm = 65536u * static_cast<uint32_t>(p.stages > 0);
 
     StageWalker wk{r0, r1, 0};
     int e, nrows;
@@ -324,7 +332,10 @@ __global__ void __launch_bounds__(kF32MmaThreads, 1) gemv_f32_mma_kernel(const _
                 const uint8_t* rowa = stage + (16 * gi + gid) * rstride;
                 const uint8_t* rowb = rowa + 8 * rstride;
                 float ya = 0.0f, yb = 0.0f;
-                q6_f32_mma<FMT>(rowa + B::kBytes * sb, rowb + B::kBytes * sb, t, scsel, bx, ya, yb);
+                if (FMT == QX_Q6_K && (sb & 1))  // warp-uniform
+                    q6_f32_mma<FMT, 2>(rowa + B::kBytes * sb, rowb + B::kBytes * sb, t, scsel, jm, bx, ya, yb);
+                else
+                    q6_f32_mma<FMT, 0>(rowa + B::kBytes * sb, rowb + B::kBytes * sb, t, scsel, jm, bx, ya, yb);
                 ya += __shfl_xor_sync(0xffffffffu, ya, 1);
                 yb += __shfl_xor_sync(0xffffffffu, yb, 1);
                 ya += __shfl_xor_sync(0xffffffffu, ya, 2);
