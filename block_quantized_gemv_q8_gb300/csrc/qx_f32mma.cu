@@ -319,11 +319,22 @@ __global__ void __launch_bounds__(kF32MmaThreads, 1) gemv_f32_mma_kernel(const _
     // 65536 for the GGUF layout's 2-byte joins, from a value the compiler cannot fold
     const uint32_t jm = 65536u * static_cast<uint32_t>(p.stages > 0);
 
+    // The consumers need only each stage's row count: for one matrix, the
+    // CTA's rows in stages of p.G (32-bit); otherwise the full stage walk.
     StageWalker wk{r0, r1, 0};
     int e, nrows;
     int64_t lrow;
+    const bool one = p.n_entries == 1;
+    int left = static_cast<int>(r1 - r0);
     int slot = 0, lap = 0;  // ring position of stage k: k % S, k / S
-    for (int k = 0; wk.next(p, e, lrow, nrows); ++k) {
+    for (;;) {
+        if (one) {
+            if (left <= 0) break;
+            nrows = left < p.G ? left : p.G;
+            left -= nrows;
+        } else if (!wk.next(p, e, lrow, nrows)) {
+            break;
+        }
         if (!warp_wait_all(&full[slot], lap & 1, p.wait_ns, p.err, kErrTimeoutFull)) break;
         const uint8_t* stage = smem + size_t(slot) * p.slot_bytes;
         float* rs = red + size_t(slot) * red_stage + sb * 16;
