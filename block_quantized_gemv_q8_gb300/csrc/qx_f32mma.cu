@@ -34,8 +34,8 @@
 // per SM, a producer warp copying each row of a stage of 16 P gq rows to a
 // padded stride (qx_stage.cuh), 16 consumer warps (warp w owns super-block
 // w % nsb of row groups w / nsb, w / nsb + P, ... of every stage, P = 16 /
-// nsb, so its B fragments stay in registers), and a reducer warp.  Rows of 2048 or 4096 columns (GGUF Q6_K
-// rows are then a 16-byte multiple).
+// nsb, so its B fragments stay in registers), and a reducer warp.  Rows of
+// 2048 or 4096 columns (GGUF Q6_K rows are then a 16-byte multiple).
 #include <cuda_runtime.h>
 
 #include "qx_device.cuh"
