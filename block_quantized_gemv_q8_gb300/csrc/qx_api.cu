@@ -394,9 +394,13 @@ qx_status chain_geometry(const DeviceInfo& dev, ChainParams& p, size_t& smem) {
 // Whether the f32-mode tensor-pipe kernel (gemv_f32_mma_kernel) serves the
 // shape: Q6_K rows (either layout) of 2048 or 4096 columns, where both
 // layouts are served alike (GGUF rows are then a 16-byte multiple), so their
-// outputs stay bit-identical.
-bool f32_mma_serves(int fmt, int64_t cols) {
-    return (fmt == QX_Q6_K || fmt == QX_Q6_K_SOA) && (cols == 2048 || cols == 4096);
+// outputs stay bit-identical; Q4_K rows of 256 to 4096 columns, except small
+// launches under programmatic dependent launch, which take the merged f32
+// lanes (half an SM, so the next launch's CTA fits beside them).
+bool f32_mma_serves(int fmt, int64_t cols, bool pdl_small) {
+    if (fmt == QX_Q6_K || fmt == QX_Q6_K_SOA) return cols == 2048 || cols == 4096;
+    if (fmt == QX_Q4_K) return !pdl_small && cols % 256 == 0 && cols / 256 >= 1 && cols / 256 <= 16;
+    return false;
 }
 
 // f32 mode on the tensor pipe: stages of 16 P gq rows (P = 16 / units per
@@ -455,7 +459,9 @@ qx_status run_gemv(int fmt, int n, const void* const* W, const int64_t* rows, in
     if (mode == QX_MODE_F32) {
         p.x = static_cast<const float*>(x);
         kmode = QX_MODE_F32;
-        if (P == nullptr && y != nullptr && f32_mma_serves(fmt, cols)) return run_gemv_f32_mma(fmt, p, cols, *dev, pdl, s);
+        const bool pdl_small = pdl && total * row_bytes_of(fmt, cols) <= kOneCtaPerSmBytes * int64_t(dev->sm_count);
+        if (P == nullptr && y != nullptr && f32_mma_serves(fmt, cols, pdl_small))
+            return run_gemv_f32_mma(fmt, p, cols, *dev, pdl, s);
     } else if (mode == QX_MODE_W4A8_FUSED) {
         p.xf = static_cast<const float*>(x);
     } else {

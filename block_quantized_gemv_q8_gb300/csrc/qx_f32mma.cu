@@ -1,5 +1,6 @@
 // qx_f32mma.cu -- f32-mode GEMV of Q6_K rows (GGUF blocks or the repacked
-// QX_Q6_K_SOA layout) with the products on the tensor pipe, sm_103a.
+// QX_Q6_K_SOA layout) and Q4_K rows with the products on the tensor pipe,
+// sm_103a.  (Q6_K below; Q4_K differs in its unit, see q4k_f32_mma.)
 //
 // f32 mode is the dequantise-and-FMA GEMV (llambda.lisp README, "Features &
 // Architecture"): y_r = sum_k w_rk x_k with the f32 activation and the Q6_K
@@ -230,10 +231,116 @@ __device__ __forceinline__ void q6_f32_mma(const uint8_t* ra, const uint8_t* rb,
     }
 }
 
+// ---------------------------------------------------------------------------
+// Q4_K (d, dmin f16; twelve bytes of 6-bit scales sc and mins m; 128 bytes of
+// nibbles: chunk j = bytes 16 + 32 j .. + 31 holds sub-block 2 j in its low
+// nibbles and 2 j + 1 in its high ones).  w = d sc_s q - dmin m_s, so a
+// sub-block s adds d sc_s sum q x - dmin m_s sum x: the first on the tensor
+// pipe (q exact in bf16: the nibble under the exponent pattern 0x43 is the
+// bf16 128 + q, one lop3 for two of them, minus 128 exactly), the second from
+// the sub-block's sum of x.  MMA (s, f), f = 0, 1, covers sub-block s alone:
+// thread (gid, t) holds elements 32 s + 8 t + 4 f + {0, 2} (logical k = 2 t,
+// 2 t + 1) and + {1, 3} (k = 2 t + 8, 2 t + 9), so that a word's bytes 0, 2 and
+// 1, 3 are its pairs; column pair s & 3 holds the sub-block's (hi, lo), and
+// an accumulator holds the four sub-blocks 4 a .. 4 a + 3 (a = 0, 1).
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void load_b_q4k(const float* xs, float up, int gid, int t, bool live,
+                                           uint32_t (&bx)[32]) {
+    const bool odd = gid & 1;
+#pragma unroll
+    for (int sbk = 0; sbk < 8; ++sbk)
+#pragma unroll
+        for (int f = 0; f < 2; ++f) {
+            const int i = 2 * sbk + f;
+            const bool mine = live && (gid >> 1) == (sbk & 3);
+            uint32_t b0 = 0u, b1 = 0u;
+            if (mine) {
+                const float4 v = __ldg(reinterpret_cast<const float4*>(xs + 32 * sbk + 8 * t + 4 * f));
+                float e[4] = {v.x * up, v.y * up, v.z * up, v.w * up};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float hi = bf16_rn_f32(e[j]);
+                    e[j] = odd ? (isfinite(hi) ? e[j] - hi : 0.0f) : hi;
+                }
+                b0 = bf16x2_rn(e[0], e[2]);
+                b1 = bf16x2_rn(e[1], e[3]);
+            }
+            bx[2 * i] = b0;
+            bx[2 * i + 1] = b1;
+        }
+}
+
+// The bf16 pair (q0, q2) of the nibbles at bits 0-3 and 16-19 of w: 0x43 over
+// each nibble is the bf16 128 + q; one subtraction of 128 gives q, exactly.
+__device__ __forceinline__ uint32_t q4_pair_bf16(uint32_t w) {
+    const uint32_t biased = (w & 0x000F000Fu) | 0x43004300u;
+    uint32_t r;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(biased), "r"(0x43004300u));
+    return r;
+}
+
+// One super-block of rows gid (ra) and gid + 8 (rb): returns, for thread
+// (gid, t), the sum over its sub-blocks s = t, t + 4 of d sc_s (D_hi + D_lo) -
+// dmin m_s S_s (S_s: the sub-block's sum of the scaled activation), rows gid
+// and gid + 8.  bsel = 0x7650 + t selects byte t of a scale word as 2^23 + byte.
+__device__ __forceinline__ void q4k_f32_mma(const uint8_t* ra, const uint8_t* rb, uint32_t bsel, float s_lo,
+                                            float s_hi, const uint32_t (&bx)[32], int t, float& ya, float& yb) {
+    const uint8_t* rows[2] = {ra, rb};
+    float dd[2], ndd[2], dm[2], ndm[2];
+    uint32_t scw[2][2], mw[2][2];
+    uint2 qw[2][4];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const uint4 h = *reinterpret_cast<const uint4*>(rows[r]);
+        dd[r] = f16_bits_to_f32(h.x & 0xFFFFu);
+        dm[r] = f16_bits_to_f32(h.x >> 16);
+        ndd[r] = dd[r] * -8388608.0f;
+        ndm[r] = dm[r] * -8388608.0f;
+        scw[r][0] = h.y & 0x3F3F3F3Fu;
+        mw[r][0] = h.z & 0x3F3F3F3Fu;
+        scw[r][1] = (h.w & 0x0F0F0F0Fu) | ((h.y >> 2) & 0x30303030u);
+        mw[r][1] = ((h.w >> 4) & 0x0F0F0F0Fu) | ((h.z >> 2) & 0x30303030u);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) qw[r][j] = *reinterpret_cast<const uint2*>(rows[r] + 16 + 32 * j + 8 * t);
+    }
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+        float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int sbk = 4 * a + k, j = sbk >> 1;
+#pragma unroll
+            for (int f = 0; f < 2; ++f) {
+                uint32_t w[2];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const uint32_t word = f ? qw[r][j].y : qw[r][j].x;
+                    w[r] = (sbk & 1) ? (word >> 4) : word;
+                }
+                const uint32_t A[4] = {q4_pair_bf16(w[0]), q4_pair_bf16(w[1]), q4_pair_bf16(w[0] >> 8),
+                                       q4_pair_bf16(w[1] >> 8)};
+                const int i = 2 * sbk + f;
+                mma_bf16_k16(d, A, bx[2 * i], bx[2 * i + 1]);
+            }
+        }
+        // column pair t = sub-block 4 a + t: d sc and dmin m exactly (an f16 times a 6-bit integer)
+        const float sx = a ? s_hi : s_lo;
+        const float sca = fmaf(dd[0], __int_as_float(__byte_perm(scw[0][a], 0x4B000000u, bsel)), ndd[0]);
+        const float ma = fmaf(dm[0], __int_as_float(__byte_perm(mw[0][a], 0x4B000000u, bsel)), ndm[0]);
+        const float scb = fmaf(dd[1], __int_as_float(__byte_perm(scw[1][a], 0x4B000000u, bsel)), ndd[1]);
+        const float mb = fmaf(dm[1], __int_as_float(__byte_perm(mw[1][a], 0x4B000000u, bsel)), ndm[1]);
+        ya = fmaf(-ma, sx, fmaf(sca, d[0] + d[1], ya));
+        yb = fmaf(-mb, sx, fmaf(scb, d[2] + d[3], yb));
+    }
+}
+
 template <int FMT>
 __global__ void __launch_bounds__(kF32MmaThreads, 1) gemv_f32_mma_kernel(const __grid_constant__ GemvParams p) {
     constexpr int NW = kF32MmaWarps;
-    using B = Q6Block<FMT>;
+    constexpr bool kQ4 = FMT == QX_Q4_K;
+    using B = Q6Block<kQ4 ? QX_Q6_K : FMT>;  // Q6_K layouts only
+    constexpr int kBytes = kQ4 ? 144 : B::kBytes;
     extern __shared__ __align__(128) uint8_t smem[];
     const int S = p.stages;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
@@ -312,7 +419,22 @@ __global__ void __launch_bounds__(kF32MmaThreads, 1) gemv_f32_mma_kernel(const _
     if (ex == 255) ex = 127;                // inf or NaN: unscaled
     const float up = ldexpf(1.0f, 127 - ex), down = ldexpf(1.0f, ex - 127);
     uint32_t bx[32];
-    load_b_f32(xs, up, gid, t, active, bx);
+    float s_lo = 0.0f, s_hi = 0.0f;  // Q4_K: sums of the scaled activation over sub-blocks t and t + 4
+    if constexpr (kQ4) {
+        load_b_q4k(xs, up, gid, t, active, bx);
+        // lane L holds x[8 L .. 8 L + 7] of the super-block: sub-block L / 4
+        const float4 v0 = __ldg(reinterpret_cast<const float4*>(xs + 8 * lane));
+        const float4 v1 = __ldg(reinterpret_cast<const float4*>(xs + 8 * lane + 4));
+        float sum = ((v0.x * up + v0.y * up) + (v0.z * up + v0.w * up)) +
+                    ((v1.x * up + v1.y * up) + (v1.z * up + v1.w * up));
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        s_lo = __shfl_sync(0xffffffffu, sum, 4 * t);
+        s_hi = __shfl_sync(0xffffffffu, sum, 4 * t + 16);
+    } else {
+        load_b_f32(xs, up, gid, t, active, bx);
+    }
+    const uint32_t bsel = 0x7650u + static_cast<uint32_t>(t);
     // byte t of a scale word, sign-extended
     const uint32_t tt = static_cast<uint32_t>(t);
     const uint32_t scsel = tt | ((tt | 8u) << 4) | ((tt | 8u) << 8) | ((tt | 8u) << 12);
@@ -343,17 +465,26 @@ __global__ void __launch_bounds__(kF32MmaThreads, 1) gemv_f32_mma_kernel(const _
                 const uint8_t* rowa = stage + (16 * gi + gid) * rstride;
                 const uint8_t* rowb = rowa + 8 * rstride;
                 float ya = 0.0f, yb = 0.0f;
-                if (FMT == QX_Q6_K && (sb & 1))  // warp-uniform
-                    q6_f32_mma<FMT, 2>(rowa + B::kBytes * sb, rowb + B::kBytes * sb, t, scsel, jm, bx, ya, yb);
-                else
-                    q6_f32_mma<FMT, 0>(rowa + B::kBytes * sb, rowb + B::kBytes * sb, t, scsel, jm, bx, ya, yb);
+                if constexpr (kQ4) {
+                    q4k_f32_mma(rowa + kBytes * sb, rowb + kBytes * sb, bsel, s_lo, s_hi, bx, t, ya, yb);
+                } else {
+                    if (FMT == QX_Q6_K && (sb & 1))  // warp-uniform
+                        q6_f32_mma<FMT, 2>(rowa + kBytes * sb, rowb + kBytes * sb, t, scsel, jm, bx, ya, yb);
+                    else
+                        q6_f32_mma<FMT, 0>(rowa + kBytes * sb, rowb + kBytes * sb, t, scsel, jm, bx, ya, yb);
+                }
                 ya += __shfl_xor_sync(0xffffffffu, ya, 1);
                 yb += __shfl_xor_sync(0xffffffffu, yb, 1);
                 ya += __shfl_xor_sync(0xffffffffu, ya, 2);
                 yb += __shfl_xor_sync(0xffffffffu, yb, 2);
                 if (t == 0) {
-                    rs[gi * nsb * 16 + gid] = (ya * B::d(rowa, sb, nsb)) * down;
-                    rs[gi * nsb * 16 + gid + 8] = (yb * B::d(rowb, sb, nsb)) * down;
+                    if constexpr (kQ4) {  // d and dmin are inside
+                        rs[gi * nsb * 16 + gid] = ya * down;
+                        rs[gi * nsb * 16 + gid + 8] = yb * down;
+                    } else {
+                        rs[gi * nsb * 16 + gid] = (ya * B::d(rowa, sb, nsb)) * down;
+                        rs[gi * nsb * 16 + gid + 8] = (yb * B::d(rowb, sb, nsb)) * down;
+                    }
                 }
             }
         }
@@ -406,6 +537,7 @@ cudaError_t launch_gemv_f32_mma(int fmt, const GemvParams& p, size_t smem, cudaS
     switch (fmt) {
         case QX_Q6_K: return launch_f32_mma_one<QX_Q6_K>(p, smem, s, pdl);
         case QX_Q6_K_SOA: return launch_f32_mma_one<QX_Q6_K_SOA>(p, smem, s, pdl);
+        case QX_Q4_K: return launch_f32_mma_one<QX_Q4_K>(p, smem, s, pdl);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -1,7 +1,9 @@
 """f32 mode on the tensor pipe: Q6_K rows (GGUF blocks and QX_Q6_K_SOA) of
-2048 and 4096 columns, whose f32-mode GEMV runs as bf16 mma.sync over the
-exact quants q - 32 and the activation split into hi + lo bf16 terms
-(scaled per 256-column super-block by a power of two).
+2048 and 4096 columns and Q4_K rows of 256 to 4096 columns, whose
+f32-mode GEMV runs as bf16 mma.sync over the exact quants (q - 32; q) and
+the activation split into hi + lo bf16 terms (scaled per 256-column
+super-block by a power of two); the Q4_K min term from each sub-block's sum
+of the activation.
 
 Gates: the f32-mode tolerance |y - y_ref| <= 1e-4 * sum_i |w_i x_i| per row
 against the oracle, and the kernel's own error bound (2^-16 of the same sum,
@@ -137,6 +139,81 @@ def test_f32_tensor_multi_and_graph():
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         qx.qx_gemv_multi([Q6, Q6], Wg, rows, cols, x, ys=yg, mode=F | qx.QX_FLAG_PDL, stream=stream)
+    g.replay()
+    for a, b in zip(yg, ys):
+        assert np.array_equal(bits(a), bits(b))
+    assert qx.qx_device_check() == qx.QX_OK
+
+
+# ----------------------------------------------------------------- Q4_K ----
+Q4 = synth.Q4_K
+# Q4_K: w = d sc q - dmin m; the two terms of a sub-block may cancel, so the
+# kernel's own bound is looser relative to sum |w x| than for Q6_K
+TIGHT_Q4 = 2.0 ** -13
+
+
+def check_q4(y, ref, absdot, what):
+    err = np.abs(np.asarray(y, dtype=np.float64) - ref)
+    bad = np.nonzero(~(err <= TOL * absdot))[0]
+    assert bad.size == 0, f"{what}: row {bad[0]} err {err[bad[0]]} bound {TOL * absdot[bad[0]]}"
+    bad = np.nonzero(~(err <= TIGHT_Q4 * absdot))[0]
+    assert bad.size == 0, f"{what}: row {bad[0]} err {err[bad[0]]} above 2^-13 of {absdot[bad[0]]}"
+
+
+@pytest.mark.parametrize("rows,cols", [(1, 256), (37, 768), (300, 1024), (1005, 4096), (14336, 4096)])
+def test_f32_tensor_q4k_parity(rows, cols):
+    """Ragged rows, one to sixteen super-blocks a row (three: 15 of 16 warps
+    in use); a large launch under programmatic dependent launch gives the
+    same bits (small ones take the merged lanes, checked elsewhere)."""
+    W = synth.weights(Q4, rows, cols, seed=11 * rows + cols)
+    x = synth.activation(1, cols, seed=cols + 23)[0]
+    Wd, xd = dev(W), dev(x)
+    y = host(qx.qx_gemv(Q4, Wd, rows, cols, xd, mode=qx.QX_MODE_F32))
+    ref, absdot = oracle.gemv_f32(Q4, W, rows, cols, x)
+    check_q4(y, ref, absdot, f"q4_k {rows}x{cols}")
+    if rows * cols >= 14336 * 4096:  # more than 192 KB a SM: the tensor pipe under PDL too
+        yp = host(qx.qx_gemv(Q4, Wd, rows, cols, xd, mode=qx.QX_MODE_F32 | qx.QX_FLAG_PDL))
+        assert np.array_equal(yp.view(np.uint32), y.view(np.uint32))
+    assert qx.qx_device_check() == qx.QX_OK
+
+
+@pytest.mark.parametrize("k", [-130, -100, 60, 100])
+def test_f32_tensor_q4k_activation_scale(k):
+    rows, cols = 200, 4096
+    W = synth.weights(Q4, rows, cols, seed=56)
+    x = (synth.activation(1, cols, seed=57)[0].astype(np.float64) * 2.0 ** k).astype(np.float32)
+    y = host(qx.qx_gemv(Q4, dev(W), rows, cols, dev(x), mode=qx.QX_MODE_F32))
+    ref, absdot = oracle.gemv_f32(Q4, W, rows, cols, x)
+    assert np.all(np.isfinite(y))
+    if k > -130:
+        check_q4(y, ref, absdot, f"q4_k 2^{k}")
+    else:  # y among the f32 subnormals: the f32-mode tolerance only
+        err = np.abs(y.astype(np.float64) - ref)
+        assert np.all(err <= TOL * absdot)
+
+
+def test_f32_tensor_q4k_zero_cases_and_multi():
+    """Zero weights or activation give exact zeros; two Q4_K matrices in one
+    launch equal the separate launches; a CUDA graph replays the eager bits."""
+    rows, cols = 40, 1024
+    W = synth.weights(Q4, rows, cols, seed=58)
+    x = synth.activation(1, cols, seed=59)[0]
+    assert np.all(host(qx.qx_gemv(Q4, dev(np.zeros_like(W)), rows, cols, dev(x), mode=qx.QX_MODE_F32)) == 0)
+    assert np.all(host(qx.qx_gemv(Q4, dev(W), rows, cols, dev(np.zeros_like(x)), mode=qx.QX_MODE_F32)) == 0)
+    cols = 4096
+    rows2 = [3000, 77]
+    Wh = [synth.weights(Q4, r, cols, seed=70 + r) for r in rows2]
+    Wg = [dev(w) for w in Wh]
+    xg = dev(synth.activation(1, cols, seed=71)[0])
+    F = qx.QX_MODE_F32
+    ys = qx.qx_gemv_multi([Q4, Q4], Wg, rows2, cols, xg, mode=F)
+    for Wd, r, y in zip(Wg, rows2, ys):
+        assert np.array_equal(bits(y), bits(qx.qx_gemv(Q4, Wd, r, cols, xg, mode=F)))
+    stream = torch.cuda.Stream()
+    yg = [torch.full((r,), float("nan"), device="cuda") for r in rows2]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        qx.qx_gemv_multi([Q4, Q4], Wg, rows2, cols, xg, ys=yg, mode=F, stream=stream)
     g.replay()
     for a, b in zip(yg, ys):
         assert np.array_equal(bits(a), bits(b))
