@@ -273,9 +273,12 @@ __device__ __forceinline__ void load_b_q4k(const float* xs, float up, int gid, i
 
 // The bf16 pair (q0, q2) of the nibbles at bits 0-3 and 16-19 of w: 0x43 over
 // each nibble is the bf16 128 + q; one subtraction of 128 gives q, exactly.
-__device__ __forceinline__ uint32_t q4_pair_bf16(uint32_t w) {
-    const uint32_t biased = (w & 0x000F000Fu) | 0x43004300u;
-    uint32_t r;
+// (w & mask) | 0x43004300 is one lop3 with the mask in a register (`mask` =
+// 0x000F000F, passed in: with both constants as immediates the compiler
+// emits two instructions).
+__device__ __forceinline__ uint32_t q4_pair_bf16(uint32_t w, uint32_t mask) {
+    uint32_t biased, r;
+    asm("lop3.b32 %0, %1, %2, 0x43004300, 0xEA;" : "=r"(biased) : "r"(w), "r"(mask));
     asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(biased), "r"(0x43004300u));
     return r;
 }
@@ -284,8 +287,9 @@ __device__ __forceinline__ uint32_t q4_pair_bf16(uint32_t w) {
 // (gid, t), the sum over its sub-blocks s = t, t + 4 of d sc_s (D_hi + D_lo) -
 // dmin m_s S_s (S_s: the sub-block's sum of the scaled activation), rows gid
 // and gid + 8.  bsel = 0x7650 + t selects byte t of a scale word as 2^23 + byte.
-__device__ __forceinline__ void q4k_f32_mma(const uint8_t* ra, const uint8_t* rb, uint32_t bsel, float s_lo,
-                                            float s_hi, const uint32_t (&bx)[32], int t, float& ya, float& yb) {
+__device__ __forceinline__ void q4k_f32_mma(const uint8_t* ra, const uint8_t* rb, uint32_t bsel, uint32_t nmask,
+                                            float s_lo, float s_hi, const uint32_t (&bx)[32], int t, float& ya,
+                                            float& yb) {
     const uint8_t* rows[2] = {ra, rb};
     float dd[2], ndd[2], dm[2], ndm[2];
     uint32_t scw[2][2], mw[2][2];
@@ -318,8 +322,8 @@ __device__ __forceinline__ void q4k_f32_mma(const uint8_t* ra, const uint8_t* rb
                     const uint32_t word = f ? qw[r][j].y : qw[r][j].x;
                     w[r] = (sbk & 1) ? (word >> 4) : word;
                 }
-                const uint32_t A[4] = {q4_pair_bf16(w[0]), q4_pair_bf16(w[1]), q4_pair_bf16(w[0] >> 8),
-                                       q4_pair_bf16(w[1] >> 8)};
+                const uint32_t A[4] = {q4_pair_bf16(w[0], nmask), q4_pair_bf16(w[1], nmask),
+                                       q4_pair_bf16(w[0] >> 8, nmask), q4_pair_bf16(w[1] >> 8, nmask)};
                 const int i = 2 * sbk + f;
                 mma_bf16_k16(d, A, bx[2 * i], bx[2 * i + 1]);
             }
@@ -435,6 +439,7 @@ __global__ void __launch_bounds__(kF32MmaThreads, 1) gemv_f32_mma_kernel(const _
         load_b_f32(xs, up, gid, t, active, bx);
     }
     const uint32_t bsel = 0x7650u + static_cast<uint32_t>(t);
+    const uint32_t nmask = 0x000F000Fu * static_cast<uint32_t>(p.stages > 0);  // a register, not an immediate
     // byte t of a scale word, sign-extended
     const uint32_t tt = static_cast<uint32_t>(t);
     const uint32_t scsel = tt | ((tt | 8u) << 4) | ((tt | 8u) << 8) | ((tt | 8u) << 12);
@@ -466,7 +471,7 @@ __global__ void __launch_bounds__(kF32MmaThreads, 1) gemv_f32_mma_kernel(const _
                 const uint8_t* rowb = rowa + 8 * rstride;
                 float ya = 0.0f, yb = 0.0f;
                 if constexpr (kQ4) {
-                    q4k_f32_mma(rowa + kBytes * sb, rowb + kBytes * sb, bsel, s_lo, s_hi, bx, t, ya, yb);
+                    q4k_f32_mma(rowa + kBytes * sb, rowb + kBytes * sb, bsel, nmask, s_lo, s_hi, bx, t, ya, yb);
                 } else {
                     if (FMT == QX_Q6_K && (sb & 1))  // warp-uniform
                         q6_f32_mma<FMT, 2>(rowa + kBytes * sb, rowb + kBytes * sb, t, scsel, jm, bx, ya, yb);
