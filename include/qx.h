@@ -132,14 +132,18 @@ qx_status qx_quantize_act_q8(const float* x, int64_t m, int64_t cols, qx_act_q8*
  * y[r] = sum_i w[r, i] * x[i] for r in [0, rows)  (device y, f32 [rows]).
  *   mode QX_MODE_F32 : x is `const float*`, device, f32 [cols]; y is within
  *                      1e-4 * sum_i |w[r, i] * x[i]| of the exact sum.  Q6_K
- *                      and QX_Q6_K_SOA rows of 2048 or 4096 columns run the
- *                      products on the tensor pipe (the quants q - 32 exact
- *                      in bf16, x scaled per 256 columns by a power of two
- *                      and split into bf16 hi + lo; error below about 2^-17
- *                      of that sum for every x within 2^-100 of its
- *                      256-column block's largest magnitude); both layouts
- *                      give bit-identical y.  The others dequantise each
- *                      quant to f32 and use one FMA per weight.
+ *                      and QX_Q6_K_SOA rows of 2048 or 4096 columns, and
+ *                      Q4_K rows of 256 to 4096 columns (except launches of
+ *                      at most 192 KB per SM with QX_FLAG_PDL), run the
+ *                      products on the tensor pipe: the quants exact in
+ *                      bf16, x scaled per 256 columns by a power of two and
+ *                      split into bf16 hi + lo, so each product carries at
+ *                      most 2^-17 of its magnitude for every x within 2^-100
+ *                      of its 256-column block's largest (Q4_K's min term
+ *                      d_min m sum(x) is taken per 32 columns in f32); both
+ *                      Q6_K layouts give bit-identical y.  The others
+ *                      dequantise each quant to f32 and use one FMA per
+ *                      weight.
  *   mode QX_MODE_W4A8: x is `const qx_act_q8*` (host struct) with m == 1 and
  *                      cols == cols, produced by qx_quantize_act_q8; y is the
  *                      per-block-scaled sum of exact integer partial sums.
