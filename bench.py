@@ -339,6 +339,15 @@ def job_throughput(world_size: int, bytes_per_step: int, steps: int, max_ms: flo
     return world_size * bytes_per_step * steps / (max_ms * 1e-3) / 1e9
 
 
+def reference_step_budget(steps: int) -> float:
+    """Seconds of oracle work per timed step of the reference arm: about 2 s,
+    less when there are many steps, so that the whole --steps K --warmup W run
+    stays near a minute and a half (each step still runs at least one
+    repetition of layer 0, about 40 ms on 16 host cores)."""
+    return min(float(os.environ.get("QX_REF_STEP_S", "2.0")),
+               float(os.environ.get("QX_REF_TOTAL_S", "90")) / max(1, steps))
+
+
 def run_reference(args):
     """Time the CPU oracle itself on bounded samples of the workload (rank 0 only)."""
     ws, rank, _ = dist_env()
@@ -352,11 +361,7 @@ def run_reference(args):
                       for j, (n, (f, r, c)) in enumerate(wl.shapes.items())}
     wl.xcols = [4096, 4096, 4096, 14336]
     wl.x_host = synth.activation(1, sum(wl.xcols), seed=synth.seed_for(1, 0, 100))[0]
-    # each step a bounded sample: about 2 s, less when there are many steps, so
-    # that the whole --steps K --warmup W run stays near a minute and a half
-    # (one repetition of layer 0 takes about 40 ms on 16 host cores)
-    per_step_budget = min(float(os.environ.get("QX_REF_STEP_S", "2.0")),
-                          float(os.environ.get("QX_REF_TOTAL_S", "90")) / max(1, args.steps))
+    per_step_budget = reference_step_budget(args.steps)
     for _ in range(args.warmup):
         wl.cpu_sample(oracle, budget_s=0.0)
     vals, t0 = [], time.perf_counter()

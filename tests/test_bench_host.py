@@ -1,6 +1,7 @@
 """Host-side pieces of bench.py on CPU: the clock-sample summary that flags
-throttling, and the profile lookups that feed `roofline.traffic` (valid only
-while the kernel sources hash as they did when the counters were taken)."""
+throttling, the profile lookups that feed `roofline.traffic` (valid only
+while the kernel sources hash as they did when the counters were taken), and
+the reference arm's per-step sample budget."""
 import os
 import sys
 
@@ -57,3 +58,13 @@ def test_job_throughput_counts_every_rank():
     # 2 ranks x 4.41 GB x 10 steps in 11.66 ms (the slowest rank)
     v = bench.job_throughput(2, 4_410_310_656, 10, 11.66)
     assert abs(v - 2 * 4_410_310_656 * 10 / 11.66e-3 / 1e9) < 1e-6
+
+
+def test_reference_step_budget_bounds_the_whole_run(monkeypatch):
+    monkeypatch.delenv("QX_REF_STEP_S", raising=False)
+    monkeypatch.delenv("QX_REF_TOTAL_S", raising=False)
+    assert bench.reference_step_budget(1) == 2.0 and bench.reference_step_budget(45) == 2.0
+    for steps in (46, 100, 500, 10000):
+        b = bench.reference_step_budget(steps)
+        assert b < 2.0 and abs(b * steps - 90.0) < 1e-9
+    assert bench.reference_step_budget(0) == 2.0
